@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for the decoder-step attention path.
+
+This module only draws random numbers and lays them out; it holds none of the
+path's arithmetic.  The same bytes feed the CUDA library and the CPU oracle.
+
+Workloads (shapes of the pages' models; no weights or audio are needed):
+
+* ``whisper_tiny_b1``      -- Whisper-tiny (d=384, 6 heads x 64, 4 decoder
+  layers), one sequence, self cache of 448 slots filled to t=223 so the new
+  token sits at 224 (225 keys), cross K/V of 1500 encoder frames.
+* ``whisper_tiny_b64_beam5`` -- the same model, 64 sequences in 5-beam groups
+  (group of sequence b is b // 5, so 13 groups, the last of 4 beams), self
+  lengths uniform in [1, 448], cross K/V shared per group, a random beam
+  permutation drawn within each group.
+* ``whisper_large_b32``    -- Large-Whisper shape (d=1280, 20 heads x 64, 32
+  decoder layers), 32 sequences, self lengths uniform in [1, 448], cross K/V of
+  1500 frames per sequence.
+* ``qwen3_asr_gqa_b16``    -- Qwen3-ASR decoder (28 layers, 16 Q / 8 KV heads of
+  128), 16 sequences, n_past uniform in [1024, 4096], cache of 4224 slots,
+  RMSNorm weights N(1, 0.1).
+* ``qwen3_asr_prefill_b8`` -- the same decoder prefilling 8 prompts of 1536
+  tokens (16 prefix + 1500 audio frames + 20 suffix).
+
+Values: activations and caches N(0, 1); caches are stored as f16 (the fp32
+draw rounded to nearest even).  Host draws use numpy's PCG64; device draws use
+torch's generator for that device.
+"""
+import numpy as np
+
+WORKLOADS = {
+    "whisper_tiny_b1": dict(kind="whisper", B=1, d=384, heads=6, head_dim=64, layers=4,
+                            capacity=448, frames=1500, beam=1, lens="fixed", fixed_len=225),
+    "whisper_tiny_b64_beam5": dict(kind="whisper", B=64, d=384, heads=6, head_dim=64, layers=4,
+                                   capacity=448, frames=1500, beam=5, lens="uniform",
+                                   len_lo=1, len_hi=448, rearrange=True),
+    "whisper_large_b32": dict(kind="whisper", B=32, d=1280, heads=20, head_dim=64, layers=32,
+                              capacity=448, frames=1500, beam=1, lens="uniform",
+                              len_lo=1, len_hi=448),
+    "qwen3_asr_gqa_b16": dict(kind="gqa", B=16, layers=28, q_heads=16, kv_heads=8, head_dim=128,
+                              capacity=4224, n_past_lo=1024, n_past_hi=4096, eps=1e-6,
+                              rope_base=1e6, w_mean=1.0, w_std=0.1),
+    "qwen3_asr_prefill_b8": dict(kind="prefill", B=8, T=1536, prefix=16, audio=1500, suffix=20,
+                                 q_heads=16, kv_heads=8, head_dim=128, capacity=1536, eps=1e-6,
+                                 rope_base=1e6, w_mean=1.0, w_std=0.1),
+}
+
+
+def seed_for(workload_index, tensor_id):
+    """Seed of tensor ``tensor_id`` of workload ``workload_index``."""
+    return 1000 * int(workload_index) + int(tensor_id)
+
+
+# ------------------------------------------------------------------ host --
+
+def rng(seed):
+    return np.random.Generator(np.random.PCG64(int(seed)))
+
+
+def host_normal_f32(shape, seed, mean=0.0, std=1.0):
+    """float32 N(mean, std) array."""
+    x = rng(seed).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0 or mean != 0.0:
+        x = (x * np.float32(std) + np.float32(mean)).astype(np.float32)
+    return x
+
+
+def host_normal_f16bits(shape, seed):
+    """f16 N(0, 1) values as their binary16 bit patterns (uint16)."""
+    return host_normal_f32(shape, seed).astype(np.float16).view(np.uint16)
+
+
+def lens_uniform(B, lo, hi, seed):
+    """int32 [B] drawn uniformly from the integers lo..hi inclusive."""
+    return rng(seed).integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+
+
+def beam_groups(B, beam):
+    """Group (encoder source) of each sequence: consecutive runs of ``beam``."""
+    return (np.arange(B, dtype=np.int32) // np.int32(beam)).astype(np.int32)
+
+
+def beam_permutation(B, beam, seed):
+    """A random permutation of the sequences that stays inside each beam group."""
+    r = rng(seed)
+    idx = np.arange(B, dtype=np.int32)
+    for g0 in range(0, B, beam):
+        g1 = min(g0 + beam, B)
+        idx[g0:g1] = g0 + r.permutation(g1 - g0).astype(np.int32)
+    return idx
+
+
+# ---------------------------------------------------------------- device --
+
+def dev_normal(shape, seed, device, dtype=None, mean=0.0, std=1.0):
+    """torch tensor N(mean, std) drawn on ``device`` (fp32 draw, then cast)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0 or mean != 0.0:
+        x.mul_(std).add_(mean)
+    if dtype is not None and dtype != torch.float32:
+        x = x.to(dtype)
+    return x
+
+
+def dev_fill_normal_(t, seed, chunk_elems=1 << 28):
+    """Fill an existing f16 (or f32) device tensor with N(0,1), in bounded chunks."""
+    import torch
+    flat = t.view(-1)
+    g = torch.Generator(device=t.device)
+    g.manual_seed(int(seed))
+    for s in range(0, flat.numel(), chunk_elems):
+        e = min(s + chunk_elems, flat.numel())
+        flat[s:e] = torch.randn(e - s, generator=g, device=t.device, dtype=torch.float32).to(t.dtype)
+    return t

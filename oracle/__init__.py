@@ -1,0 +1,299 @@
+"""Double-precision CPU oracle for the decoder-step attention path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg import this package; the CUDA library never
+does, and the two share no code.  It wraps ``liboracle.so`` (oracle.c) with
+numpy arrays in and out.  Every function returns float64 results computed
+from the same f16 bytes the GPU reads.
+
+Parity pins: every function here is pinned by the ``-m "not gpu"`` tests in
+tests/test_oracle_pins.py (closed forms, brute force on tiny inputs, numpy's
+independent binary16 conversion, invariants such as step == prefill row and
+GQA == MHA with duplicated KV heads).  No function is left unpinned.
+
+Layout: a cache row holds 2*Hkv*hd f16 (K of every KV head, then V of every
+KV head); caches are C-contiguous ``uint16`` arrays whose leading axis is the
+sequence (or source) axis.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_dbl = ctypes.c_double
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        sig = {
+            "orc_set_threads": (_int, [_int]),
+            "orc_get_threads": (_int, []),
+            "orc_f16_to_f64": (_dbl, [ctypes.c_uint16]),
+            "orc_f64_to_f16": (ctypes.c_uint16, [_dbl]),
+            "orc_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
+            "orc_f16_decode_array": (None, [_u16p, _f64p, _i64]),
+            "orc_f32_encode_array": (None, [_f32p, _u16p, _i64]),
+            "orc_f64_encode_array": (None, [_f64p, _u16p, _i64]),
+            "orc_attend_one": (None, [_f64p, _u16p, _u16p, _i64, _int, _int, _dbl, _f64p, _f64p]),
+            "orc_kv_append": (_int, [_f32p, _f32p, _i64, _u16p, _i64, _i32p, _int, _int, _int, _int]),
+            "orc_self_attn_step": (_int, [_f32p, _i64, _u16p, _i64, _i32p, _int, _int, _int, _int,
+                                          _dbl, _f64p]),
+            "orc_cross_attn_step": (_int, [_f32p, _i64, _u16p, _i64, _i32p, _int, _int, _int, _int,
+                                           _int, _dbl, _f64p]),
+            "orc_rmsnorm": (None, [_f64p, _f64p, _dbl, _int, _f64p]),
+            "orc_rope_neox": (None, [_f64p, _int, _dbl, _dbl, _f64p]),
+            "orc_gqa_step": (_int, [_f32p, _f32p, _f32p, _f32p, _f32p, _dbl, _dbl, _i32p, _u16p,
+                                    _i64, _int, _int, _int, _int, _int, _dbl, _f64p]),
+            "orc_kv_rearrange": (_int, [_u16p, _u16p, _i64, _i64, _int, _int, _int, _i32p, _i32p,
+                                        _i32p, _int]),
+            "orc_prefill_attn": (_int, [_u16p, _u16p, _u16p, _f32p, _f32p, _dbl, _dbl, _int, _int,
+                                        _int, _int, _int, _dbl, _u16p, _i64, _int, _f64p, _u16p]),
+            "orc_prefill_attn_rows": (None, [_u16p, _i32p, _int, _u16p, _int, _int, _int, _int,
+                                             _dbl, _f64p]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _p(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _c(a, dtype):
+    a = np.asarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    if not a.flags.c_contiguous:
+        raise ValueError("array must be C-contiguous")
+    return a
+
+
+def set_threads(n):
+    """Number of host threads the attention loops may use (independent items)."""
+    return _lib().orc_set_threads(int(n))
+
+
+def get_threads():
+    return _lib().orc_get_threads()
+
+
+# ---------------------------------------------------------------- binary16 --
+
+def f16_to_f64(bits):
+    """binary16 bit patterns (uint16) -> exact float64 values."""
+    bits = _c(np.ascontiguousarray(bits), np.uint16)
+    out = np.empty(bits.shape, np.float64)
+    _lib().orc_f16_decode_array(_p(bits, ctypes.c_uint16), _p(out, ctypes.c_double), bits.size)
+    return out
+
+
+def f32_to_f16(x):
+    """float32 -> binary16 bits, IEEE round to nearest even, overflow to inf."""
+    x = _c(np.ascontiguousarray(x), np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _lib().orc_f32_encode_array(_p(x, ctypes.c_float), _p(out, ctypes.c_uint16), x.size)
+    return out
+
+
+def f64_to_f16(x):
+    """float64 -> binary16 bits, one IEEE round to nearest even."""
+    x = _c(np.ascontiguousarray(x), np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _lib().orc_f64_encode_array(_p(x, ctypes.c_double), _p(out, ctypes.c_uint16), x.size)
+    return out
+
+
+# ------------------------------------------------------------- primitives --
+
+def attend_one(q, k_rows, v_rows, scale):
+    """softmax(scale * k_rows @ q) @ v_rows with k/v given as f16 [L, hd] rows."""
+    q = np.ascontiguousarray(q, np.float64)
+    k_rows = _c(np.ascontiguousarray(k_rows), np.uint16)
+    v_rows = _c(np.ascontiguousarray(v_rows), np.uint16)
+    L, hd = k_rows.shape
+    both = np.concatenate([k_rows, v_rows], axis=1)  # one row = K then V
+    z = np.empty(max(L, 1), np.float64)
+    out = np.empty(hd, np.float64)
+    _lib().orc_attend_one(_p(q, ctypes.c_double), _p(both, ctypes.c_uint16),
+                          both[:, hd:].ctypes.data_as(_u16p), 2 * hd, L, hd, float(scale),
+                          _p(z, ctypes.c_double), _p(out, ctypes.c_double))
+    return out
+
+
+def rmsnorm(x, w, eps):
+    x = np.ascontiguousarray(x, np.float64)
+    w = np.ascontiguousarray(w, np.float64)
+    y = np.empty_like(x)
+    _lib().orc_rmsnorm(_p(x, ctypes.c_double), _p(w, ctypes.c_double), float(eps), x.size,
+                       _p(y, ctypes.c_double))
+    return y
+
+
+def rope_neox(x, pos, base):
+    x = np.ascontiguousarray(x, np.float64)
+    y = np.empty_like(x)
+    _lib().orc_rope_neox(_p(x, ctypes.c_double), x.size, float(pos), float(base),
+                         _p(y, ctypes.c_double))
+    return y
+
+
+# -------------------------------------------------------------- the steps --
+
+def kv_append(k, v, cache, slot, kv_heads, head_dim, src_row_stride=None):
+    """Write f16(k_b) || f16(v_b) into row slot[b] of cache[b] (in place).
+
+    k, v: float32 arrays whose rows are sequences (row stride src_row_stride
+    floats, default the row length); cache: uint16 [B, capacity, row].
+    Returns the number of sequences skipped for an out-of-range slot."""
+    k = _c(k, np.float32)
+    v = _c(v, np.float32)
+    cache = _c(cache, np.uint16)
+    slot = _c(np.ascontiguousarray(slot, np.int32), np.int32)
+    B, cap = cache.shape[0], cache.shape[1]
+    stride = src_row_stride if src_row_stride is not None else kv_heads * head_dim
+    return _lib().orc_kv_append(_p(k, ctypes.c_float), _p(v, ctypes.c_float), stride,
+                                _p(cache, ctypes.c_uint16), cache[0].size, _p(slot, ctypes.c_int32),
+                                B, kv_heads, head_dim, cap)
+
+
+def self_attn_step(q, cache, lens, heads, head_dim, scale, q_stride=None):
+    """Causal one-token self-attention; q float32 [B, >=H*hd], cache uint16
+    [B, capacity, 2*H*hd], lens int32 [B] (keys incl. the new one).
+    Returns (out float64 [B, H*hd], n_skipped)."""
+    q = _c(q, np.float32)
+    cache = _c(cache, np.uint16)
+    lens = _c(np.ascontiguousarray(lens, np.int32), np.int32)
+    B, cap = cache.shape[0], cache.shape[1]
+    out = np.empty((B, heads * head_dim), np.float64)
+    qs = q_stride if q_stride is not None else q.shape[-1]
+    n = _lib().orc_self_attn_step(_p(q, ctypes.c_float), qs, _p(cache, ctypes.c_uint16),
+                                  cache[0].size, _p(lens, ctypes.c_int32), B, heads, head_dim, cap,
+                                  float(scale), _p(out, ctypes.c_double))
+    return out, n
+
+
+def cross_attn_step(q, cross, group, heads, head_dim, scale, q_stride=None):
+    """Unmasked one-token cross-attention; cross uint16 [G, frames, 2*H*hd],
+    group int32 [B] (source of each sequence).  Returns (out, n_skipped)."""
+    q = _c(q, np.float32)
+    cross = _c(cross, np.uint16)
+    group = _c(np.ascontiguousarray(group, np.int32), np.int32)
+    G, frames = cross.shape[0], cross.shape[1]
+    B = group.shape[0]
+    out = np.empty((B, heads * head_dim), np.float64)
+    qs = q_stride if q_stride is not None else q.shape[-1]
+    n = _lib().orc_cross_attn_step(_p(q, ctypes.c_float), qs, _p(cross, ctypes.c_uint16),
+                                   cross[0].size, _p(group, ctypes.c_int32), B, G, heads, head_dim,
+                                   frames, float(scale), _p(out, ctypes.c_double))
+    return out, n
+
+
+def gqa_step(q, k_new, v_new, q_norm_w, k_norm_w, eps, rope_base, n_past, cache, q_heads,
+             kv_heads, head_dim, scale):
+    """Fused RMSNorm + NeoX RoPE + append + GQA attention step (cache updated
+    in place).  Returns (out float64 [B, Hq*hd], n_skipped)."""
+    q = _c(q, np.float32)
+    k_new = _c(k_new, np.float32)
+    v_new = _c(v_new, np.float32)
+    wq = _c(np.ascontiguousarray(q_norm_w, np.float32), np.float32)
+    wk = _c(np.ascontiguousarray(k_norm_w, np.float32), np.float32)
+    n_past = _c(np.ascontiguousarray(n_past, np.int32), np.int32)
+    cache = _c(cache, np.uint16)
+    B, cap = cache.shape[0], cache.shape[1]
+    out = np.empty((B, q_heads * head_dim), np.float64)
+    n = _lib().orc_gqa_step(_p(q, ctypes.c_float), _p(k_new, ctypes.c_float),
+                            _p(v_new, ctypes.c_float), _p(wq, ctypes.c_float),
+                            _p(wk, ctypes.c_float), float(eps), float(rope_base),
+                            _p(n_past, ctypes.c_int32), _p(cache, ctypes.c_uint16), cache[0].size,
+                            cap, B, q_heads, kv_heads, head_dim, float(scale),
+                            _p(out, ctypes.c_double))
+    return out, n
+
+
+def kv_rearrange(src, dst, idx, lens_src, capacity):
+    """Beam reorder.  src/dst uint16 [B, n_layers, capacity, row] (dst updated
+    in place).  Returns (lens_dst int32 [B], n_skipped)."""
+    src = _c(src, np.uint16)
+    dst = _c(dst, np.uint16)
+    idx = _c(np.ascontiguousarray(idx, np.int32), np.int32)
+    lens_src = _c(np.ascontiguousarray(lens_src, np.int32), np.int32)
+    B, n_layers, cap, row = src.shape
+    lens_dst = np.zeros(B, np.int32)
+    n = _lib().orc_kv_rearrange(_p(src, ctypes.c_uint16), _p(dst, ctypes.c_uint16), src[0].size,
+                                src[0, 0].size, n_layers, row, capacity,
+                                _p(idx, ctypes.c_int32), _p(lens_src, ctypes.c_int32),
+                                _p(lens_dst, ctypes.c_int32), B)
+    return lens_dst, n
+
+
+def prefill_attn(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_heads, head_dim, scale,
+                 cache):
+    """Batched causal prefill.  q uint16 [B, T, Hq*hd], k/v uint16 [B, T, Hkv*hd];
+    cache uint16 [B, capacity, 2*Hkv*hd] (rows [0,T) written in place).
+    Returns (out float64 [B, T, Hq*hd], qhat uint16 [B, T, Hq*hd])."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    wq = _c(np.ascontiguousarray(q_norm_w, np.float32), np.float32)
+    wk = _c(np.ascontiguousarray(k_norm_w, np.float32), np.float32)
+    cache = _c(cache, np.uint16)
+    B, T = q.shape[0], q.shape[1]
+    cap = cache.shape[1]
+    out = np.empty((B, T, q_heads * head_dim), np.float64)
+    qhat = np.empty((B, T, q_heads * head_dim), np.uint16)
+    rc = _lib().orc_prefill_attn(_p(q, ctypes.c_uint16), _p(k, ctypes.c_uint16),
+                                 _p(v, ctypes.c_uint16), _p(wq, ctypes.c_float),
+                                 _p(wk, ctypes.c_float), float(eps), float(rope_base), B, T,
+                                 q_heads, kv_heads, head_dim, float(scale),
+                                 _p(cache, ctypes.c_uint16), cache[0].size, cap,
+                                 _p(out, ctypes.c_double), _p(qhat, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError("T exceeds the cache capacity")
+    return out, qhat
+
+
+def prefill_attn_rows(qhat_rows, t_of_row, seq_cache, q_heads, kv_heads, head_dim, head, scale):
+    """Causal attention for selected query rows of one (sequence, head):
+    qhat_rows uint16 [n, hd] (normed+roped f16 queries), t_of_row int32 [n],
+    seq_cache uint16 [capacity, row] of that sequence.  Returns float64 [n, hd]."""
+    qhat_rows = _c(np.ascontiguousarray(qhat_rows), np.uint16)
+    t_of_row = _c(np.ascontiguousarray(t_of_row, np.int32), np.int32)
+    seq_cache = _c(np.ascontiguousarray(seq_cache), np.uint16)
+    n = t_of_row.shape[0]
+    out = np.empty((n, head_dim), np.float64)
+    _lib().orc_prefill_attn_rows(_p(qhat_rows, ctypes.c_uint16), _p(t_of_row, ctypes.c_int32), n,
+                                 _p(seq_cache, ctypes.c_uint16), q_heads, kv_heads, head_dim, head,
+                                 float(scale), _p(out, ctypes.c_double))
+    return out
+
+
+def build():
+    """Compile liboracle.so (the checker) if it is missing or stale."""
+    return _build.build()
+
+
+__all__ = [
+    "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
+    "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
+    "kv_rearrange", "prefill_attn", "prefill_attn_rows", "build",
+]
+
+if os.environ.get("ORACLE_THREADS"):
+    set_threads(int(os.environ["ORACLE_THREADS"]))

@@ -1,0 +1,440 @@
+"""Pins of the CPU oracle to facts fixed outside it (CPU only).
+
+Each test checks the oracle against something other than itself: IEEE 754
+worked cases, numpy's independent binary16 conversion, closed forms of the
+softmax, hand-worked RoPE/RMSNorm examples, and invariants the definition
+implies (one key returns its value row, key-shift invariance, relative
+positions of RoPE, step == row of the causal prefill, GQA == MHA with the KV
+heads repeated).  The cases are chosen so that a dropped term, a swapped
+operand, a wrong head offset or an off-by-one length fails at least one.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+from kv_cache_decode_asr_gb300 import synthetic as syn
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f16(x):
+    """float values -> binary16 bits via numpy (independent of the oracle)."""
+    return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+
+def dec(bits):
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+
+
+# ------------------------------------------------------------ binary16 ----
+
+def test_f16_decode_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = oracle_mod.f16_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    # signs of zeros survive
+    assert math.copysign(1.0, mine[0x8000]) == -1.0
+
+
+def test_f16_encode_golden_cases(oracle_mod):
+    rows = []
+    with open(os.path.join(GOLDEN, "f16_rne_cases.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            x = float(parts[0]) if "inf" in parts[0] else float.fromhex(parts[0])
+            rows.append((x, int(parts[1], 16)))
+    assert len(rows) >= 17
+    xs = np.array([r[0] for r in rows], np.float32)
+    assert np.array_equal(xs.astype(np.float64), np.array([r[0] for r in rows]))  # exact f32
+    got = oracle_mod.f32_to_f16(xs)
+    for (x, want), g in zip(rows, got):
+        assert int(g) == want, f"{x!r}: got {int(g):#06x} want {want:#06x}"
+    got64 = oracle_mod.f64_to_f16(xs.astype(np.float64))
+    assert np.array_equal(got64, got)
+
+
+def test_f16_encode_matches_numpy_random(oracle_mod):
+    r = syn.rng(7)
+    # a million values over the whole binary16 range and beyond: normals,
+    # subnormals, overflow, random signs; plus exact ties.
+    e = r.uniform(-27.0, 17.0, size=1_000_000)
+    x = (np.sign(r.standard_normal(e.size)) * np.exp2(e)).astype(np.float32)
+    ties = (dec(r.integers(0, 0x7bff, 20000).astype(np.uint16)) +
+            dec(r.integers(0, 0x7bff, 20000).astype(np.uint16))) / 2.0
+    x = np.concatenate([x, ties.astype(np.float32), np.float32([0.0, -0.0, np.inf, -np.inf])])
+    mine = oracle_mod.f32_to_f16(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(mine, ref)
+    # double inputs take one rounding straight to binary16 (numpy does too)
+    xd = r.standard_normal(200_000) * np.exp2(r.uniform(-26, 16, 200_000))
+    with np.errstate(over="ignore"):
+        ref64 = xd.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle_mod.f64_to_f16(xd), ref64)
+
+
+# ------------------------------------------------------------ attention ---
+
+def _cache(B, cap, heads, hd, k, v):
+    """Assemble rows K(all heads) || V(all heads) from k/v float [B, cap, heads, hd]."""
+    c = np.zeros((B, cap, 2 * heads * hd), np.uint16)
+    c[:, :, : heads * hd] = f16(k).reshape(B, cap, heads * hd)
+    c[:, :, heads * hd:] = f16(v).reshape(B, cap, heads * hd)
+    return c
+
+
+def test_one_key_returns_its_value_row(oracle_mod):
+    r = syn.rng(1)
+    hd = 64
+    k = r.standard_normal((1, 4, 2, hd))
+    v = r.standard_normal((1, 4, 2, hd))
+    cache = _cache(1, 4, 2, hd, k, v)
+    q = r.standard_normal((1, 2 * hd)).astype(np.float32) * 10
+    out, bad = oracle_mod.self_attn_step(q, cache, [1], 2, hd, hd ** -0.5)
+    assert bad == 0
+    want = dec(cache[0, 0, 2 * hd:])
+    assert np.array_equal(out[0], want)
+
+
+def test_worked_example_two_keys(oracle_mod):
+    """hd=64, scale 1/8: q = (8 ln 3, 0...), k0 = e0, k1 = 0 gives scores
+    (ln 3, 0), weights (3/4, 1/4); with v0 = 1, v1 = -1 the output is 0.5."""
+    hd = 64
+    k = np.zeros((1, 3, 1, hd))
+    v = np.zeros((1, 3, 1, hd))
+    k[0, 0, 0, 0] = 1.0
+    v[0, 0, 0, :] = 1.0
+    v[0, 1, 0, :] = -1.0
+    k[0, 2, 0, 0] = 100.0   # row 2 is beyond the length: must be ignored
+    v[0, 2, 0, :] = 7.0
+    cache = _cache(1, 3, 1, hd, k, v)
+    q = np.zeros((1, hd), np.float32)
+    q[0, 0] = 8.0 * math.log(3.0)
+    out, _ = oracle_mod.self_attn_step(q, cache, [2], 1, hd, 0.125)
+    assert np.allclose(out[0], 0.5, atol=1e-6)
+    # L = 3 includes row 2, whose score 8 ln3 * 100 / 8 dominates
+    out3, _ = oracle_mod.self_attn_step(q, cache, [3], 1, hd, 0.125)
+    assert np.allclose(out3[0], 7.0, atol=1e-9)
+
+
+def test_two_key_sigmoid_closed_form(oracle_mod):
+    r = syn.rng(2)
+    hd = 64
+    for trial in range(20):
+        z = r.uniform(-6, 6, size=2)
+        # q = 8 e0 * scale^-1 ... pick k_j = z_j e0 exactly representable
+        zq = np.round(z * 64) / 64           # dyadic, exact in f16
+        k = np.zeros((1, 2, 1, hd))
+        k[0, :, 0, 0] = zq
+        v = r.standard_normal((1, 2, 1, hd))
+        cache = _cache(1, 2, 1, hd, k, v)
+        q = np.zeros((1, hd), np.float32)
+        q[0, 0] = 8.0                        # scores = zq
+        out, _ = oracle_mod.self_attn_step(q, cache, [2], 1, hd, 0.125)
+        sig = 1.0 / (1.0 + math.exp(-(zq[0] - zq[1])))
+        vv = dec(cache[0, :, hd:])
+        assert np.allclose(out[0], sig * vv[0] + (1 - sig) * vv[1], atol=1e-12)
+
+
+def test_equal_scores_give_mean_of_values(oracle_mod):
+    r = syn.rng(3)
+    hd, L = 64, 1500
+    kk = np.tile(r.standard_normal((1, 1, 1, hd)), (1, L, 1, 1))   # all keys equal
+    v = r.standard_normal((1, L, 1, hd))
+    cache = _cache(1, L, 1, hd, kk, v)
+    q = r.standard_normal((1, hd)).astype(np.float32)
+    out, _ = oracle_mod.cross_attn_step(q, cache, [0], 1, hd, hd ** -0.5)
+    assert np.allclose(out[0], dec(cache[0, :, hd:]).mean(axis=0), atol=1e-12)
+    # q = 0 gives equal scores for any keys
+    k2 = r.standard_normal((1, L, 1, hd))
+    cache2 = _cache(1, L, 1, hd, k2, v)
+    out0, _ = oracle_mod.cross_attn_step(np.zeros((1, hd), np.float32), cache2, [0], 1, hd, 0.125)
+    assert np.allclose(out0[0], dec(cache2[0, :, hd:]).mean(axis=0), atol=1e-12)
+
+
+def test_heads_read_their_own_segments(oracle_mod):
+    """Head h's query selects row h+1 by a huge score; the V segments of the
+    heads are different constants, so a wrong K or V offset shows."""
+    H, hd, L = 3, 64, 5
+    k = np.zeros((1, L, H, hd))
+    v = np.zeros((1, L, H, hd))
+    for h in range(H):
+        k[0, h + 1, h, h] = 50.0
+        for j in range(L):
+            v[0, j, h, :] = 10 * h + j
+    cache = _cache(1, L, H, hd, k, v)
+    q = np.zeros((1, H * hd), np.float32)
+    for h in range(H):
+        q[0, h * hd + h] = 8.0
+    out, _ = oracle_mod.self_attn_step(q, cache, [L], H, hd, 0.125)
+    for h in range(H):
+        assert np.allclose(out[0, h * hd:(h + 1) * hd], 10 * h + h + 1, atol=1e-9)
+
+
+def test_key_shift_invariance(oracle_mod):
+    """Adding one vector c to every key adds q.c to every score, which the
+    softmax ignores (keys and c are small dyadics, so k + c is exact in f16)."""
+    r = syn.rng(4)
+    H, hd, L = 2, 64, 37
+    k = r.integers(-8, 9, size=(1, L, H, hd)) / 4.0
+    c = r.integers(-4, 5, size=(1, 1, H, hd)) / 4.0
+    v = r.standard_normal((1, L, H, hd))
+    q = r.standard_normal((1, H * hd)).astype(np.float32)
+    a, _ = oracle_mod.self_attn_step(q, _cache(1, L, H, hd, k, v), [L], H, hd, hd ** -0.5)
+    b, _ = oracle_mod.self_attn_step(q, _cache(1, L, H, hd, k + c, v), [L], H, hd, hd ** -0.5)
+    assert np.allclose(a, b, atol=1e-12)
+
+
+def test_cross_group_mapping(oracle_mod):
+    G, H, hd, F = 3, 2, 64, 11
+    r = syn.rng(5)
+    k = r.standard_normal((G, F, H, hd))
+    v = np.zeros((G, F, H, hd))
+    for g in range(G):
+        v[g] = g + 1
+    cross = _cache(G, F, H, hd, k, v)
+    group = np.array([2, 0, 1, 2, 2], np.int32)
+    q = r.standard_normal((5, H * hd)).astype(np.float32)
+    out, bad = oracle_mod.cross_attn_step(q, cross, group, H, hd, hd ** -0.5)
+    assert bad == 0
+    for b in range(5):
+        assert np.allclose(out[b], group[b] + 1, atol=1e-12)
+    out, bad = oracle_mod.cross_attn_step(q, cross, [0, 3, -1, 1, 2], H, hd, 0.125)
+    assert bad == 2 and np.all(out[1] == 0) and np.all(out[2] == 0)
+
+
+def test_self_lengths_out_of_range_are_skipped(oracle_mod):
+    r = syn.rng(6)
+    cache = _cache(3, 4, 1, 64, r.standard_normal((3, 4, 1, 64)), r.standard_normal((3, 4, 1, 64)))
+    q = r.standard_normal((3, 64)).astype(np.float32)
+    out, bad = oracle_mod.self_attn_step(q, cache, [0, 4, 5], 1, 64, 0.125)
+    assert bad == 2 and np.all(out[0] == 0) and np.all(out[2] == 0) and np.any(out[1] != 0)
+
+
+# ------------------------------------------------------------- append ----
+
+def test_append_matches_numpy_rounding(oracle_mod):
+    r = syn.rng(8)
+    B, H, hd, cap = 3, 2, 64, 6
+    qkv = (r.standard_normal((B, 3 * H * hd)) * 100).astype(np.float32)
+    cache = np.full((B, cap, 2 * H * hd), 0xAAAA, np.uint16)
+    slot = np.array([0, 5, 6], np.int32)
+    before = cache.copy()
+    # k and v are views into the [q|k|v] rows (row stride 3*H*hd floats)
+    kv = np.ascontiguousarray(qkv)
+    k_view = kv[:, H * hd:]
+    v_view = kv[:, 2 * H * hd:]
+    skipped = oracle_mod._lib().orc_kv_append(
+        k_view.ctypes.data_as(oracle_mod._f32p), v_view.ctypes.data_as(oracle_mod._f32p),
+        3 * H * hd, cache.ctypes.data_as(oracle_mod._u16p), cap * 2 * H * hd,
+        slot.ctypes.data_as(oracle_mod._i32p), B, H, hd, cap)
+    assert skipped == 1
+    for b in range(2):
+        want = np.concatenate([f16(qkv[b, H * hd:2 * H * hd]), f16(qkv[b, 2 * H * hd:])])
+        assert np.array_equal(cache[b, slot[b]], want)
+        others = [s for s in range(cap) if s != slot[b]]
+        assert np.array_equal(cache[b, others], before[b, others])
+    assert np.array_equal(cache[2], before[2])
+
+
+# ------------------------------------------------------------ rearrange --
+
+def test_rearrange_is_a_row_gather(oracle_mod):
+    r = syn.rng(9)
+    B, nl, cap, row = 7, 3, 10, 16
+    src = r.integers(0, 65536, size=(B, nl, cap, row)).astype(np.uint16)
+    lens = r.integers(1, cap + 1, size=B).astype(np.int32)
+    idx = syn.beam_permutation(B, 3, 1)
+    idx[1] = idx[0]                       # repeats are allowed (take semantics)
+    dst = np.full_like(src, 0x1234)
+    lens_dst, bad = oracle_mod.kv_rearrange(src, dst, idx, lens, cap)
+    assert bad == 0
+    taken = np.take(src, idx, axis=0)
+    for b in range(B):
+        n = lens[idx[b]] - 1
+        assert np.array_equal(dst[b, :, :n], taken[b, :, :n])
+        assert np.all(dst[b, :, n:] == 0x1234)          # rows past the history untouched
+    assert np.array_equal(lens_dst, lens[idx])
+    # identity
+    dst2 = np.zeros_like(src)
+    oracle_mod.kv_rearrange(src, dst2, np.arange(B, dtype=np.int32), lens, cap)
+    for b in range(B):
+        assert np.array_equal(dst2[b, :, :lens[b] - 1], src[b, :, :lens[b] - 1])
+    # bad index / bad length are skipped with lens_dst = 0
+    lens_bad = lens.copy()
+    lens_bad[2] = cap + 1
+    dst3 = np.zeros_like(src)
+    ld, bad = oracle_mod.kv_rearrange(src, dst3, np.array([B, 2, 0, 1, 3, 4, -1], np.int32),
+                                      lens_bad, cap)
+    assert bad == 3 and ld[0] == 0 and ld[1] == 0 and ld[6] == 0 and ld[2] == lens[0]
+
+
+# --------------------------------------------------------- RMSNorm, RoPE --
+
+def test_rmsnorm_worked_example(oracle_mod):
+    y = oracle_mod.rmsnorm([3.0, 4.0], [1.0, 1.0], 0.0)
+    assert np.allclose(y, np.array([3.0, 4.0]) / math.sqrt(12.5), atol=1e-15)
+    y = oracle_mod.rmsnorm([3.0, 4.0], [2.0, -1.0], 1e-6)
+    assert np.allclose(y, np.array([6.0, -4.0]) / math.sqrt(12.5 + 1e-6), atol=1e-15)
+    r = syn.rng(10)
+    x = r.standard_normal(128)
+    y = oracle_mod.rmsnorm(x, np.ones(128), 0.0)
+    assert abs(np.mean(y * y) - 1.0) < 1e-12
+    assert np.allclose(oracle_mod.rmsnorm(7.5 * x, np.ones(128), 0.0), y, atol=1e-12)
+
+
+def test_rope_worked_example_hd4():
+    """hd=4, base 1e6, position 1: theta = (1, 1e-3); pairs (0,2) and (1,3)."""
+    import oracle
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    y = oracle.rope_neox(x, 1, 1e6)
+    c1, s1 = math.cos(1.0), math.sin(1.0)
+    c2, s2 = math.cos(1e-3), math.sin(1e-3)
+    want = [1 * c1 - 3 * s1, 2 * c2 - 4 * s2, 3 * c1 + 1 * s1, 4 * c2 + 2 * s2]
+    assert np.allclose(y, want, atol=1e-15)
+
+
+def test_rope_properties(oracle_mod):
+    r = syn.rng(11)
+    hd = 128
+    x = r.standard_normal(hd)
+    k = r.standard_normal(hd)
+    assert np.array_equal(oracle_mod.rope_neox(x, 0, 1e6), x)
+    y = oracle_mod.rope_neox(x, 4093, 1e6)
+    # norm of every (i, i + hd/2) pair is preserved (NeoX pairing)
+    assert np.allclose(y[:64] ** 2 + y[64:] ** 2, x[:64] ** 2 + x[64:] ** 2, atol=1e-12)
+    # the score depends on the position difference only
+    d1 = oracle_mod.rope_neox(x, 3000, 1e6) @ oracle_mod.rope_neox(k, 1000, 1e6)
+    d2 = oracle_mod.rope_neox(x, 2100, 1e6) @ oracle_mod.rope_neox(k, 100, 1e6)
+    d3 = oracle_mod.rope_neox(x, 2000, 1e6) @ k
+    assert abs(d1 - d2) < 1e-9 and abs(d1 - d3) < 1e-9
+    # rotations compose
+    assert np.allclose(oracle_mod.rope_neox(oracle_mod.rope_neox(x, 17, 1e6), 25, 1e6),
+                       oracle_mod.rope_neox(x, 42, 1e6), atol=1e-12)
+
+
+# ---------------------------------------------------- GQA step, prefill --
+
+def _gqa_inputs(B, Hq, Hkv, hd, cap, seed):
+    r = syn.rng(seed)
+    q = r.standard_normal((B, Hq * hd)).astype(np.float32)
+    kn = r.standard_normal((B, Hkv * hd)).astype(np.float32)
+    vn = r.standard_normal((B, Hkv * hd)).astype(np.float32)
+    wq = (1 + 0.1 * r.standard_normal(hd)).astype(np.float32)
+    wk = (1 + 0.1 * r.standard_normal(hd)).astype(np.float32)
+    cache = syn.host_normal_f16bits((B, cap, 2 * Hkv * hd), seed + 1)
+    return q, kn, vn, wq, wk, cache
+
+
+def test_gqa_step_equals_mha_with_repeated_kv_heads(oracle_mod):
+    B, Hq, Hkv, hd, cap = 3, 4, 2, 128, 40
+    q, kn, vn, wq, wk, cache = _gqa_inputs(B, Hq, Hkv, hd, cap, 12)
+    n_past = np.array([0, 17, 39], np.int32)
+    out, bad = oracle_mod.gqa_step(q, kn, vn, wq, wk, 1e-6, 1e6, n_past, cache, Hq, Hkv, hd,
+                                   hd ** -0.5)
+    assert bad == 0
+    # the appended row: f16 of the normed + roped key, f16 of v
+    for b in range(B):
+        p = n_past[b]
+        for h in range(Hkv):
+            kh = oracle_mod.rope_neox(
+                oracle_mod.rmsnorm(kn[b, h * hd:(h + 1) * hd].astype(np.float64), wk, 1e-6), p, 1e6)
+            assert np.array_equal(cache[b, p, h * hd:(h + 1) * hd], kh.astype(np.float16).view(np.uint16))
+        assert np.array_equal(cache[b, p, Hkv * hd:], f16(vn[b]))
+    # MHA over the same cache with each KV head repeated for its query group
+    rep = Hq // Hkv
+    kpart = cache[:, :, :Hkv * hd].reshape(B, cap, Hkv, hd)
+    vpart = cache[:, :, Hkv * hd:].reshape(B, cap, Hkv, hd)
+    mha = np.concatenate([np.repeat(kpart, rep, axis=2).reshape(B, cap, Hq * hd),
+                          np.repeat(vpart, rep, axis=2).reshape(B, cap, Hq * hd)], axis=2)
+    qhat = np.zeros((B, Hq * hd), np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            qhat[b, h * hd:(h + 1) * hd] = oracle_mod.rope_neox(
+                oracle_mod.rmsnorm(q[b, h * hd:(h + 1) * hd].astype(np.float64), wq, 1e-6),
+                n_past[b], 1e6)
+    ref, _ = oracle_mod.self_attn_step(qhat.astype(np.float32), np.ascontiguousarray(mha),
+                                       n_past + 1, Hq, hd, hd ** -0.5)
+    assert np.allclose(out, ref, atol=2e-6)   # q^ rounded to float32 on the MHA side
+    # n_past == 0: the only key is the new one, so the output is f16(v)
+    for h in range(Hq):
+        assert np.array_equal(out[0, h * hd:(h + 1) * hd],
+                              dec(f16(vn[0, (h // rep) * hd:(h // rep + 1) * hd])))
+
+
+def test_gqa_step_bad_position_skipped(oracle_mod):
+    B, Hq, Hkv, hd, cap = 2, 2, 1, 64, 8
+    q, kn, vn, wq, wk, cache = _gqa_inputs(B, Hq, Hkv, hd, cap, 13)
+    before = cache.copy()
+    out, bad = oracle_mod.gqa_step(q, kn, vn, wq, wk, 1e-6, 1e6, [8, -1], cache, Hq, Hkv, hd, 0.125)
+    assert bad == 2 and np.all(out == 0) and np.array_equal(cache, before)
+
+
+def test_prefill_rows_equal_steps(oracle_mod):
+    """Row t of the causal prefill equals a one-token step at position t over
+    rows [0, t] of the cache the prefill wrote (GQA via repeated KV heads)."""
+    B, T, Hq, Hkv, hd, cap = 2, 9, 4, 2, 64, 12
+    q = syn.host_normal_f16bits((B, T, Hq * hd), 20)
+    k = syn.host_normal_f16bits((B, T, Hkv * hd), 21)
+    v = syn.host_normal_f16bits((B, T, Hkv * hd), 22)
+    wq = syn.host_normal_f32(hd, 23, 1.0, 0.1)
+    wk = syn.host_normal_f32(hd, 24, 1.0, 0.1)
+    cache = np.zeros((B, cap, 2 * Hkv * hd), np.uint16)
+    out, qhat = oracle_mod.prefill_attn(q, k, v, wq, wk, 1e-6, 1e6, Hq, Hkv, hd, hd ** -0.5, cache)
+    assert np.array_equal(cache[:, :T, Hkv * hd:], v)          # V copied bitwise
+    assert np.all(cache[:, T:] == 0)                          # nothing past T
+    rep = Hq // Hkv
+    kpart = cache[:, :, :Hkv * hd].reshape(B, cap, Hkv, hd)
+    vpart = cache[:, :, Hkv * hd:].reshape(B, cap, Hkv, hd)
+    mha = np.ascontiguousarray(np.concatenate(
+        [np.repeat(kpart, rep, axis=2).reshape(B, cap, Hq * hd),
+         np.repeat(vpart, rep, axis=2).reshape(B, cap, Hq * hd)], axis=2))
+    for t in range(T):
+        qt = dec(qhat[:, t]).astype(np.float32)
+        ref, _ = oracle_mod.self_attn_step(qt, mha, np.full(B, t + 1, np.int32), Hq, hd, hd ** -0.5)
+        assert np.allclose(out[:, t], ref, atol=1e-12)
+    # the first position has one key: its output is that V row
+    for h in range(Hq):
+        assert np.array_equal(out[:, 0, h * hd:(h + 1) * hd], dec(v[:, 0, (h // rep) * hd:(h // rep + 1) * hd]))
+    # causality: changing later keys does not move earlier rows
+    k2 = k.copy()
+    k2[:, 5:] = syn.host_normal_f16bits(k2[:, 5:].shape, 25)
+    out2, _ = oracle_mod.prefill_attn(q, k2, v, wq, wk, 1e-6, 1e6, Hq, Hkv, hd, hd ** -0.5,
+                                      np.zeros_like(cache))
+    assert np.array_equal(out2[:, :5], out[:, :5])
+    assert not np.allclose(out2[:, 5:], out[:, 5:])
+    # sampled rows through the per-row entry point agree
+    ts = np.array([0, 3, 8], np.int32)
+    rows = oracle_mod.prefill_attn_rows(qhat[1, ts, 3 * hd:4 * hd], ts, cache[1], Hq, Hkv, hd, 3,
+                                        hd ** -0.5)
+    assert np.array_equal(rows, out[1, ts, 3 * hd:4 * hd])
+
+
+def test_step_key_equals_prefill_key(oracle_mod):
+    """A key appended by the step at n_past = p is bit-identical to the key the
+    prefill writes at row p from the same input values."""
+    B, T, Hq, Hkv, hd, cap = 1, 6, 2, 2, 128, 8
+    q = syn.host_normal_f16bits((B, T, Hq * hd), 30)
+    k = syn.host_normal_f16bits((B, T, Hkv * hd), 31)
+    v = syn.host_normal_f16bits((B, T, Hkv * hd), 32)
+    wq = syn.host_normal_f32(hd, 33, 1.0, 0.1)
+    wk = syn.host_normal_f32(hd, 34, 1.0, 0.1)
+    pre = np.zeros((B, cap, 2 * Hkv * hd), np.uint16)
+    outp, _ = oracle_mod.prefill_attn(q, k, v, wq, wk, 1e-6, 1e6, Hq, Hkv, hd, hd ** -0.5, pre)
+    step = pre.copy()
+    step[:, T - 1] = 0
+    outs, _ = oracle_mod.gqa_step(dec(q[:, T - 1]).astype(np.float32),
+                                  dec(k[:, T - 1]).astype(np.float32),
+                                  dec(v[:, T - 1]).astype(np.float32), wq, wk, 1e-6, 1e6,
+                                  [T - 1], step, Hq, Hkv, hd, hd ** -0.5)
+    assert np.array_equal(step, pre)
+    # outputs differ only by the f16 rounding of the prefill's query
+    assert np.allclose(outs[0], outp[0, T - 1], atol=2e-2)
