@@ -1,0 +1,199 @@
+/*
+ * asrkv.h -- C ABI of libasrkv.so: GB300 (sm_103a) kernels for the per-token
+ * decoder step of encoder-decoder speech recognisers (Whisper-style MHA and a
+ * Qwen3-ASR-style GQA decoder) over f16 K/V caches.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    keeps no pointer after a call returns and allocates no device memory.
+ *  - f16 data are IEEE binary16 bit patterns passed as uint16_t*.
+ *  - A cache ROW holds 2*Hkv*hd f16: the K vectors of KV heads 0..Hkv-1, then
+ *    the V vectors of KV heads 0..Hkv-1; head h sits at offset h*hd inside its
+ *    half ("wavo 0.1.0, src/whisper/decoder.rs", doc of `Buffers`: a cache row
+ *    is K then V of all heads, as f16).  Rows of one sequence are contiguous.
+ *  - Query head h reads KV head h / (Hq/Hkv) (contiguous GQA groups).
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream), never synchronises, and returns an asr_status.  All argument
+ *    checks happen on the host before anything is enqueued; a call that
+ *    returns an error has enqueued nothing.
+ *  - Data errors found on the device (a length or index out of range) never
+ *    trap: the affected sequence is skipped (its output row is set to 0 where
+ *    the call has one) and an ASR_DEVERR_* bit is OR-ed into *dev_err when
+ *    dev_err is not NULL.  The caller zeroes *dev_err and reads it back.
+ *  - Per-step scalars (lengths, positions, slots, indices) live in device
+ *    arrays, so a whole decode step can be captured once in a CUDA graph and
+ *    replayed; the graph's shape depends only on capacities ("transcribe.cpp,
+ *    src/arch/qwen3_asr/decoder.h", comment of build_step_graph: a static step
+ *    graph reused across steps).
+ *  - Attention scores are scale * (q . k) in fp32, softmax in fp32, output
+ *    fp32.  The caller passes `scale`; the pages use (D/H)^-0.5 = hd^-0.5
+ *    ("Nest whisper-tiny, src/lib.linnet", Attention.attend: rsqrt(D/Heads)).
+ *
+ * Workspace: the attention entry points split long key ranges over many CTAs
+ * and merge the pieces (flash-decoding with a log-sum-exp combine).  They
+ * need a caller-provided workspace of at least asr_workspace_size(...) bytes,
+ * 256-byte aligned, ZERO-FILLED before its first use (cudaMemsetAsync).  Each
+ * call leaves the workspace's counters at zero again, so one zeroing at
+ * allocation time is enough; a workspace must not be shared by calls that can
+ * run concurrently (different streams without ordering).
+ */
+#ifndef ASRKV_H
+#define ASRKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* asr_stream_t;
+
+/* Return codes. */
+enum asr_status {
+  ASR_OK = 0,
+  ASR_ERR_INVALID_ARG = 1, /* NULL pointer, size out of range, stride too small */
+  ASR_ERR_UNSUPPORTED = 2, /* head_dim not 64/128, Hq % Hkv != 0, too many heads/beams/sequences */
+  ASR_ERR_MISALIGNED = 3,  /* a pointer or stride is not 16-byte aligned */
+  ASR_ERR_ALIAS = 4,       /* rearrange source and destination overlap */
+  ASR_ERR_WORKSPACE = 5,   /* workspace NULL, too small or not 256-byte aligned */
+  ASR_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+};
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define ASR_DEVERR_LEN 0x1     /* a length / position / slot outside its range */
+#define ASR_DEVERR_INDEX 0x2   /* a beam index or group id outside its range, or groups not sorted */
+#define ASR_DEVERR_BEAMS 0x4   /* a group has more sequences than max_beams */
+#define ASR_DEVERR_TIMEOUT 0x8 /* a bounded wait inside a kernel gave up (never expected) */
+
+/* Operation ids for asr_workspace_size. */
+enum asr_op {
+  ASR_OP_SELF_ATTN = 1,
+  ASR_OP_CROSS_ATTN = 2,
+  ASR_OP_GQA_STEP = 3,
+  ASR_OP_PREFILL_ATTN = 4,
+};
+
+/* Limits checked on the host. */
+#define ASR_MAX_BATCH 2048 /* sequences (and groups) per call */
+#define ASR_MAX_BEAMS 8    /* sequences sharing one cross source; also max Hq/Hkv */
+#define ASR_MAX_KV_HEADS 64
+
+/* a1 -- K/V append.
+ * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step (k and v
+ * of the new token packed as f16 into cache row `pos`); "Nest whisper-tiny,
+ * src/lib.linnet", DecoderLayer.step (write_at(self_k/self_v, ..., pos)).
+ *   cache[b*seq_stride + slot[b]*row + i] = f16_rne(k[b*src_row_stride + i])      i < Hkv*hd
+ *   cache[b*seq_stride + slot[b]*row + Hkv*hd + i] = f16_rne(v[b*src_row_stride + i])
+ * with row = 2*kv_heads*head_dim; f16_rne is IEEE round to nearest even with
+ * overflow to infinity.  k, v: fp32 [B][src_row_stride] (e.g. the k and v
+ * parts of a [q|k|v] projection row, src_row_stride = 3*d); slot: int32 [B],
+ * device.  A slot outside [0, capacity) skips that sequence (ASR_DEVERR_LEN).
+ * Alignment: k, v, cache 16-byte aligned; src_row_stride % 4 == 0;
+ * seq_stride % 8 == 0 and >= capacity*row.  head_dim % 8 == 0. */
+int asr_kv_append(const float* k, const float* v, int64_t src_row_stride, uint16_t* cache,
+                  int64_t seq_stride, const int32_t* slot, int B, int kv_heads, int head_dim,
+                  int capacity, int32_t* dev_err, asr_stream_t stream);
+
+/* a2 (+ a4) -- causal self-attention of one new token per sequence.
+ * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
+ * (attend(q, own, pos+1)); "Nest whisper-tiny, src/lib.linnet",
+ * DecoderLayer.step (mask: slots <= pos); "mlx-bun whisper.ts", #attention
+ * (additive causal mask, precise softmax).
+ *   For sequence b and head h, with L = lens[b] keys (the new token's own key,
+ *   appended before this call, is row L-1):
+ *   z_j = scale * q_bh . K_bj,h  (j < L);  out_bh = sum_j softmax(z)_j V_bj,h
+ * q: fp32 [B][q_stride] (head h at h*head_dim); cache: f16 [B][seq_stride]
+ * rows as above with Hkv = heads; lens: int32 [B], device, each in
+ * [1, capacity] (else the row of out is zeroed, ASR_DEVERR_LEN); out: fp32
+ * [B][heads*head_dim], contiguous.  head_dim in {64, 128}; heads <= 64;
+ * B <= ASR_MAX_BATCH.  q_stride % 4 == 0; seq_stride % 8 == 0.
+ * ws: workspace of asr_workspace_size(ASR_OP_SELF_ATTN, B, B, 1, heads, head_dim, 0) bytes. */
+int asr_self_attn_step(const float* q, int64_t q_stride, const uint16_t* cache,
+                       int64_t seq_stride, const int32_t* lens, int B, int heads, int head_dim,
+                       int capacity, float scale, float* out, void* ws, size_t ws_bytes,
+                       int32_t* dev_err, asr_stream_t stream);
+
+/* a3 (+ a4) -- cross-attention of one token per sequence over the encoder's
+ * cached K/V, shared by the beams of one audio.
+ * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
+ * (attend(q, cross, frames)); "Nest whisper-tiny, src/lib.linnet",
+ * DecoderLayer.cross (no mask); "mlx-bun whisper.ts", #attention (k/v keep
+ * their own batch: beams attend one broadcast encoder output).
+ *   Sequence b attends all `frames` rows of source group[b]:
+ *   out_bh = sum_j softmax_j(scale * q_bh . K_{group[b]} j,h) V_{group[b]} j,h
+ * cross: f16 [G][group_stride] rows with Hkv = heads; group: int32 [B],
+ * device, NON-DECREASING (the beams of one audio are consecutive), each in
+ * [0, G) (else the output row is zeroed, ASR_DEVERR_INDEX); at most
+ * max_beams (<= ASR_MAX_BEAMS) sequences per group (extra ones are zeroed,
+ * ASR_DEVERR_BEAMS).  Each group's K/V is read once for all its beams.
+ * ws: asr_workspace_size(ASR_OP_CROSS_ATTN, B, G, max_beams, heads, head_dim, 0) bytes. */
+int asr_cross_attn_step(const float* q, int64_t q_stride, const uint16_t* cross,
+                        int64_t group_stride, const int32_t* group, int B, int G, int max_beams,
+                        int heads, int head_dim, int frames, float scale, float* out, void* ws,
+                        size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+
+/* a5 -- Qwen3-ASR-style GQA decode step, fused: per-head Q/K RMSNorm, NeoX
+ * RoPE, K/V append and grouped-query attention.
+ * Defines: "transcribe.cpp, src/arch/qwen3_asr/decoder.h", header comment
+ * (RMSNorm weight*rsqrt(mean(x^2)+eps)*x; per-head Q/K RMSNorm over head_dim
+ * after projection and before RoPE; NeoX rotate_half RoPE at freq_base 1e6;
+ * GQA 16 Q / 8 KV heads of 128) and StepBuildBatched (position = n_past, K/V
+ * written at row n_past, positions > n_past masked).
+ *   For sequence b at p = n_past[b]:
+ *   k^_h = RoPE_p(RMSNorm(k_new_bh) * k_norm_w);  q^_h = RoPE_p(RMSNorm(q_bh) * q_norm_w)
+ *   cache row p = f16(k^) || f16(v_new_b)                    (written by this call)
+ *   out_bh = attention of q^_h over rows [0, p] of KV head h / (Hq/Hkv)
+ *   RoPE_p turns the pair (i, i + hd/2) by p * rope_base^(-2i/hd).
+ * q: fp32 [B][q_heads*hd]; k_new, v_new: fp32 [B][kv_heads*hd]; q_norm_w,
+ * k_norm_w: fp32 [hd] (shared by all heads); n_past: int32 [B], device, in
+ * [0, capacity) (else output zeroed, cache untouched, ASR_DEVERR_LEN);
+ * out: fp32 [B][q_heads*hd].  head_dim in {64, 128}; q_heads % kv_heads == 0;
+ * q_heads/kv_heads <= ASR_MAX_BEAMS.
+ * ws: asr_workspace_size(ASR_OP_GQA_STEP, B, B, 1, q_heads, head_dim, 0) bytes. */
+int asr_gqa_step(const float* q, const float* k_new, const float* v_new, const float* q_norm_w,
+                 const float* k_norm_w, float eps, float rope_base, const int32_t* n_past,
+                 uint16_t* cache, int64_t seq_stride, int capacity, int B, int q_heads,
+                 int kv_heads, int head_dim, float scale, float* out, void* ws, size_t ws_bytes,
+                 int32_t* dev_err, asr_stream_t stream);
+
+/* a6 -- beam reorder of the self caches of n_layers layers.
+ * Defines: "mlx-bun whisper.ts", WhisperKvCache.rearrange (take along the batch
+ * axis of every layer's self k/v; cross k/v broadcast from one audio are left
+ * alone).
+ *   For each beam b with s = idx[b]: the n = lens_src[s] - 1 history rows
+ *   (the rows written before the coming step's token) of every layer l are
+ *   copied, dst[b*seq_stride + l*layer_stride + 0 .. n*row_elems) =
+ *              src[s*seq_stride + l*layer_stride + 0 .. n*row_elems),
+ *   and lens_dst[b] = lens_src[s].  Rows past n are left untouched.
+ * idx, lens_src, lens_dst: int32 [B], device.  idx outside [0, B) or
+ * lens_src[s] outside [1, capacity] skips the beam with lens_dst[b] = 0
+ * (ASR_DEVERR_INDEX / ASR_DEVERR_LEN).  src and dst must not overlap
+ * (ASR_ERR_ALIAS).  row_elems % 8 == 0; strides % 8 == 0; pointers 16-byte
+ * aligned; B * n_layers <= 65535.  Copies are bitwise. */
+int asr_kv_rearrange(const uint16_t* src, uint16_t* dst, int64_t seq_stride, int64_t layer_stride,
+                     int n_layers, int row_elems, int capacity, const int32_t* idx,
+                     const int32_t* lens_src, int32_t* lens_dst, int B, int32_t* dev_err,
+                     asr_stream_t stream);
+
+/* Workspace bytes needed by an attention entry point on the CURRENT device
+ * (its SM count sets the number of key-range pieces).  op: asr_op;
+ * n_sources: sequences (self, GQA) or groups (cross); max_beams: 1 except for
+ * cross; T: prompt length (prefill only).  Returns 0 for invalid arguments
+ * or when no CUDA device is usable. */
+size_t asr_workspace_size(int op, int B, int n_sources, int max_beams, int q_heads, int head_dim,
+                          int T);
+
+/* Static description of a status code. */
+const char* asr_status_string(int status);
+
+/* ABI version (major*100 + minor). */
+int asr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASRKV_H */

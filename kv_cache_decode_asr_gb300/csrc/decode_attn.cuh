@@ -1,0 +1,79 @@
+// decode_attn.cuh -- shared definitions of the split-K decode-attention kernel
+// (kernel in decode_attn.cu, workspace sizing in abi.cu).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace asrkv {
+
+enum DecodeMode { kModeSelf = 0, kModeCross = 1, kModeGqa = 2 };
+
+// Most persistent CTAs per SM any decode launch uses; bounds the number of
+// partial results a workspace must hold.
+constexpr int kMaxCtasPerSm = 4;
+
+struct DecodeArgs {
+  // queries: fp32, sequence b at q + b*q_stride, head h at h*HD
+  const float* q;
+  int64_t q_stride;
+  // keys/values: f16 rows (K of all KV heads, then V), source g at kv + g*src_stride
+  const uint16_t* kv;
+  int64_t src_stride;
+  int row_elems;
+  int n_src;  // sources: sequences (self, GQA) or groups (cross)
+  int B;      // query sequences
+  const int32_t* lens;   // self: keys per sequence; GQA: n_past per sequence
+  const int32_t* group;  // cross: source of each sequence (non-decreasing)
+  int fixed_len;         // cross: frames per source
+  int capacity;          // self / GQA: rows per sequence cache
+  int Hq, Hkv, rep;      // rep = Hq / Hkv
+  int max_members;       // cross: max sequences per group; else 1
+  float qscale;          // scale * log2(e): scores are kept in the log2 domain
+  float* out;            // fp32 [B][Hq*HD]
+  // workspace
+  int* counters;   // [n_src], zero between calls
+  float* part_ml;  // [(P + n_src) * max_members * Hq][2]  (max, sum) per partial
+  float* part_o;   // [(P + n_src) * max_members * Hq][HD] unnormalised output per partial
+  int32_t* dev_err;
+  // tiling
+  int R;            // row slots (groups of the same head working on different rows)
+  int tile_rows;    // rows per pipeline stage (R * rows per slot)
+  int stages;       // pipeline depth
+  int stage_elems;  // f16 elements per stage buffer (128-byte multiple)
+  int mode;         // DecodeMode
+  // GQA only
+  const float* k_new;
+  const float* v_new;
+  const float* wq;
+  const float* wk;
+  float eps;
+  uint16_t* cache_w;  // the cache, writable (row n_past is appended)
+  double theta[64];   // rope_base^(-2i/HD), i < HD/2, computed on the host in double
+};
+
+// Shared-memory layout of one CTA (bytes from the dynamic smem base).
+struct DecodeSmem {
+  int bars, ctl, off, mstart, rope, merge, stage, total;
+};
+
+__host__ __device__ inline int dsm_align(int x, int a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, int R, int Hkv,
+                                                         int NQ, int HD, int stage_elems) {
+  DecodeSmem s;
+  s.bars = 0;
+  s.ctl = dsm_align(s.bars + 2 * stages * 8, 16);
+  s.off = dsm_align(s.ctl + 16 * 4, 16);
+  s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
+  s.rope = dsm_align(s.mstart + (n_src + 1) * 4, 16);
+  s.merge = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
+  s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 2) * 4, 128);
+  s.total = s.stage + stages * stage_elems * 2;
+  return s;
+}
+
+// Workspace bytes of a decode call with n_src sources on a device with `sms` SMs.
+size_t decode_ws_bytes(int n_src, int max_members, int Hq, int HD, int sms);
+
+}  // namespace asrkv
