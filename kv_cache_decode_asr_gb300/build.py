@@ -74,7 +74,7 @@ def build(force=False, verbose=False):
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
     tmp = LIB + ".tmp"
-    subprocess.check_call([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+    subprocess.check_call([cc, *ARCH, "-shared", "--cudart", "static", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     return LIB
 

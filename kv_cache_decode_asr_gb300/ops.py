@@ -1,0 +1,199 @@
+"""ctypes binding of libasrkv.so: the C entry points under the same names.
+
+Each function takes torch tensors (device memory owned by the caller),
+checks dtype/device/contiguity, and passes raw pointers, sizes and the
+current CUDA stream to the C ABI.  All arithmetic happens in the library's
+kernels; this module only marshals arguments.  A non-zero status raises
+AsrError.  If libasrkv.so has not been built, every call raises: there is no
+CPU fallback.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libasrkv.so")
+
+ASR_OK = 0
+STATUS = {0: "ASR_OK", 1: "ASR_ERR_INVALID_ARG", 2: "ASR_ERR_UNSUPPORTED",
+          3: "ASR_ERR_MISALIGNED", 4: "ASR_ERR_ALIAS", 5: "ASR_ERR_WORKSPACE", 6: "ASR_ERR_CUDA"}
+DEVERR_LEN, DEVERR_INDEX, DEVERR_BEAMS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+OP_SELF_ATTN, OP_CROSS_ATTN, OP_GQA_STEP, OP_PREFILL_ATTN = 1, 2, 3, 4
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+SIGNATURES = {
+    "asr_kv_append": (_int, [_p, _p, _i64, _p, _i64, _p, _int, _int, _int, _int, _p, _p]),
+    "asr_self_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _f, _p, _p, _sz,
+                                  _p, _p]),
+    "asr_cross_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _int, _int, _f,
+                                   _p, _p, _sz, _p, _p]),
+    "asr_gqa_step": (_int, [_p, _p, _p, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int, _int, _int,
+                            _f, _p, _p, _sz, _p, _p]),
+    "asr_kv_rearrange": (_int, [_p, _p, _i64, _i64, _int, _int, _int, _p, _p, _p, _int, _p, _p]),
+    "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
+    "asr_status_string": (ctypes.c_char_p, [_int]),
+    "asr_version": (_int, []),
+}
+
+_LIB = None
+
+
+class AsrError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+
+
+def load():
+    """Load libasrkv.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def _check(fn, st):
+    if st != ASR_OK:
+        raise AsrError(fn, st)
+
+
+def asr_status_string(status):
+    return load().asr_status_string(int(status)).decode()
+
+
+def asr_version():
+    return load().asr_version()
+
+
+def asr_workspace_size(op, B, n_sources, max_beams, q_heads, head_dim, T=0):
+    return load().asr_workspace_size(op, B, n_sources, max_beams, q_heads, head_dim, T)
+
+
+def workspace(op, B, n_sources, max_beams, q_heads, head_dim, T=0, device=None):
+    """A zero-filled, 256-byte-aligned workspace tensor for one entry point."""
+    import torch
+    n = asr_workspace_size(op, B, n_sources, max_beams, q_heads, head_dim, T)
+    if n == 0:
+        raise AsrError("asr_workspace_size", 1)
+    return torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws_ptr(ws):
+    """Pointer into ws rounded up to 256 bytes, and the bytes left."""
+    base = ws.data_ptr()
+    al = (base + 255) // 256 * 256
+    return ctypes.c_void_p(al), ws.numel() - (al - base)
+
+
+def asr_kv_append(k, v, cache, slot, kv_heads, head_dim, capacity, dev_err=None,
+                  src_row_stride=None, stream=None):
+    """k, v: f32 [B, >=Hkv*hd] views (row stride src_row_stride); cache: f16
+    [B, seq_stride]-strided; slot: int32 [B]."""
+    import torch
+    _need(k, torch.float32, "k")
+    _need(v, torch.float32, "v")
+    _need(cache, torch.float16, "cache")
+    _need(slot, torch.int32, "slot")
+    B = slot.shape[0]
+    stride = src_row_stride if src_row_stride is not None else k.stride(0)
+    st = load().asr_kv_append(_ptr(k), _ptr(v), stride, _ptr(cache), cache.stride(0), _ptr(slot),
+                              B, kv_heads, head_dim, capacity, _ptr(dev_err), _stream(stream))
+    _check("asr_kv_append", st)
+
+
+def asr_self_attn_step(q, cache, lens, heads, head_dim, capacity, scale, out, ws, dev_err=None,
+                       stream=None):
+    """q: f32 [B, >=H*hd] (row stride q.stride(0)); cache: f16 [B, ...] with
+    seq stride cache.stride(0); lens: int32 [B]; out: f32 [B, H*hd]."""
+    import torch
+    _need(q, torch.float32, "q")
+    _need(cache, torch.float16, "cache")
+    _need(lens, torch.int32, "lens")
+    _need(out, torch.float32, "out")
+    B = lens.shape[0]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_self_attn_step(_ptr(q), q.stride(0), _ptr(cache), cache.stride(0), _ptr(lens),
+                                   B, heads, head_dim, capacity, float(scale), _ptr(out), wp, wn,
+                                   _ptr(dev_err), _stream(stream))
+    _check("asr_self_attn_step", st)
+
+
+def asr_cross_attn_step(q, cross, group, G, max_beams, heads, head_dim, frames, scale, out, ws,
+                        dev_err=None, stream=None):
+    import torch
+    _need(q, torch.float32, "q")
+    _need(cross, torch.float16, "cross")
+    _need(group, torch.int32, "group")
+    _need(out, torch.float32, "out")
+    B = group.shape[0]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_cross_attn_step(_ptr(q), q.stride(0), _ptr(cross), cross.stride(0),
+                                    _ptr(group), B, G, max_beams, heads, head_dim, frames,
+                                    float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_cross_attn_step", st)
+
+
+def asr_gqa_step(q, k_new, v_new, q_norm_w, k_norm_w, eps, rope_base, n_past, cache, capacity,
+                 q_heads, kv_heads, head_dim, scale, out, ws, dev_err=None, stream=None):
+    import torch
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (q_norm_w, "q_norm_w"),
+                 (k_norm_w, "k_norm_w"), (out, "out")):
+        _need(t, torch.float32, n)
+    _need(n_past, torch.int32, "n_past")
+    _need(cache, torch.float16, "cache")
+    B = n_past.shape[0]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_gqa_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w),
+                             float(eps), float(rope_base), _ptr(n_past), _ptr(cache),
+                             cache.stride(0), capacity, B, q_heads, kv_heads, head_dim,
+                             float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_gqa_step", st)
+
+
+def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,
+                     layer_stride=None, dev_err=None, stream=None):
+    """src, dst: f16 [B, n_layers, capacity, row] (or strided alike); idx,
+    lens_src, lens_dst: int32 [B]."""
+    import torch
+    _need(src, torch.float16, "src")
+    _need(dst, torch.float16, "dst")
+    for t, n in ((idx, "idx"), (lens_src, "lens_src"), (lens_dst, "lens_dst")):
+        _need(t, torch.int32, n)
+    if src.stride(0) != dst.stride(0):
+        raise ValueError("src and dst must share the sequence stride")
+    B = idx.shape[0]
+    ls = layer_stride if layer_stride is not None else (src.stride(1) if src.dim() > 2 else 0)
+    st = load().asr_kv_rearrange(_ptr(src), _ptr(dst), src.stride(0), ls, n_layers, row_elems,
+                                 capacity, _ptr(idx), _ptr(lens_src), _ptr(lens_dst), B,
+                                 _ptr(dev_err), _stream(stream))
+    _check("asr_kv_rearrange", st)

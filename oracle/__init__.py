@@ -159,15 +159,20 @@ def rope_neox(x, pos, base):
 def kv_append(k, v, cache, slot, kv_heads, head_dim, src_row_stride=None):
     """Write f16(k_b) || f16(v_b) into row slot[b] of cache[b] (in place).
 
-    k, v: float32 arrays whose rows are sequences (row stride src_row_stride
-    floats, default the row length); cache: uint16 [B, capacity, row].
+    k, v: float32 [B, >=Hkv*hd] row-strided views (for example the k and v
+    columns of [q|k|v] rows; row stride in floats = src_row_stride, default
+    the view's own); cache: uint16 [B, capacity, row].
     Returns the number of sequences skipped for an out-of-range slot."""
-    k = _c(k, np.float32)
-    v = _c(v, np.float32)
+    k = np.asarray(k)
+    v = np.asarray(v)
+    if k.dtype != np.float32 or v.dtype != np.float32:
+        raise TypeError("k and v must be float32")
+    if k.ndim != 2 or k.strides[1] != 4 or v.strides != k.strides:
+        raise ValueError("k and v must be row-strided 2-D views with unit inner stride")
     cache = _c(cache, np.uint16)
     slot = _c(np.ascontiguousarray(slot, np.int32), np.int32)
     B, cap = cache.shape[0], cache.shape[1]
-    stride = src_row_stride if src_row_stride is not None else kv_heads * head_dim
+    stride = src_row_stride if src_row_stride is not None else k.strides[0] // 4
     return _lib().orc_kv_append(_p(k, ctypes.c_float), _p(v, ctypes.c_float), stride,
                                 _p(cache, ctypes.c_uint16), cache[0].size, _p(slot, ctypes.c_int32),
                                 B, kv_heads, head_dim, cap)
