@@ -186,8 +186,9 @@ def test_self_attn_repeat_calls_identical():
     a = _run_self(qkv, cache, lens, H, hd, cap, ws=ws)
     b = _run_self(qkv, cache, lens, H, hd, cap, ws=ws)
     assert np.array_equal(a, b)
-    cnt = torch.frombuffer(bytearray(host(ws[:B * 4 + 256]).tobytes()), dtype=torch.int32)
-    assert int(cnt.abs().sum()) == 0
+    start = (ws.data_ptr() + 255) // 256 * 256 - ws.data_ptr()   # the pointer the call used
+    cnt = np.frombuffer(host(ws[start:start + 4 * B]).tobytes(), dtype=np.int32)
+    assert np.all(cnt == 0)
 
 
 # ------------------------------------------------------ cross-attention --
@@ -255,6 +256,10 @@ def test_cross_attn_bad_groups():
 
 # ----------------------------------------------------------- GQA step ----
 
+# fp32 evaluation error of the normed + roped key before its f16 rounding:
+# a few float32 roundings of terms of magnitude <= ~4 (8 * 2^-24 * 4 ~ 2e-6).
+K_FP32_SLACK = 2e-6
+
 GQA_CASES = [
     # B, Hq, Hkv, hd, cap, n_past (None = uniform in [1024, 4096])
     (4, 16, 8, 128, 300, [0, 1, 150, 299]),
@@ -309,7 +314,13 @@ def test_gqa_step_matches_oracle(B, Hq, Hkv, hd, cap, n_past):
         assert np.array_equal(cache_gpu[b, p, half:], ref_cache[b, p, half:])  # V bitwise
         kg = cache_gpu[b, p, :half].view(np.float16).astype(np.float64)
         kr = ref_cache[b, p, :half].view(np.float16).astype(np.float64)
-        assert np.all(np.abs(kg - kr) <= f16_ulp(ref_cache[b, p, :half]))  # K within 1 ulp
+        # K within 1 f16 ulp of the oracle's rounding plus the fp32 evaluation
+        # error of RMSNorm + rotation (absolute: it scales with the operands,
+        # |x^| <= ~4, not with a result that cancellation made small)
+        excess = np.abs(kg - kr) - f16_ulp(ref_cache[b, p, :half])
+        worst = int(np.argmax(excess))
+        assert excess[worst] <= K_FP32_SLACK, (f"b={b} p={p} K elem {worst}: gpu {kg[worst]!r} "
+                                               f"ref {kr[worst]!r}")
 
 
 def test_gqa_bad_positions():
