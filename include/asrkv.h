@@ -116,6 +116,23 @@ int asr_self_attn_step(const float* q, int64_t q_stride, const uint16_t* cache,
                        int capacity, float scale, float* out, void* ws, size_t ws_bytes,
                        int32_t* dev_err, asr_stream_t stream);
 
+/* a1 + a2 (+ a4) fused -- append the new token's K/V and attend, in one launch.
+ * Same definitions as asr_kv_append followed by asr_self_attn_step: row
+ * lens[b]-1 of sequence b becomes f16_rne(k_new_b) || f16_rne(v_new_b) and the
+ * token attends rows [0, lens[b]) ("wavo 0.1.0, src/whisper/decoder.rs",
+ * Decoder::record_step: pack k,v into row pos, then attend over pos+1 rows).
+ * The cache bytes written are identical to those of asr_kv_append; the key
+ * of the new row is taken from the rounded k_new rather than re-read.
+ * k_new, v_new: fp32 [B][kv_stride] (the k and v parts of [q|k|v] rows:
+ * kv_stride = 3*d, v_new = k_new + d); kv_stride % 4 == 0.  Other arguments
+ * and errors as asr_self_attn_step (lens outside [1, capacity]: output
+ * zeroed, nothing written).  ws: the ASR_OP_SELF_ATTN size. */
+int asr_self_attn_append_step(const float* q, int64_t q_stride, const float* k_new,
+                              const float* v_new, int64_t kv_stride, uint16_t* cache,
+                              int64_t seq_stride, const int32_t* lens, int B, int heads,
+                              int head_dim, int capacity, float scale, float* out, void* ws,
+                              size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+
 /* a3 (+ a4) -- cross-attention of one token per sequence over the encoder's
  * cached K/V, shared by the beams of one audio.
  * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step

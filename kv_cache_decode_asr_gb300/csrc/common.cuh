@@ -144,7 +144,7 @@ __device__ __forceinline__ void set_dev_err(int32_t* dev_err, int bits) {
 }
 
 // 8 consecutive f16 (one 16-byte vector) -> 8 floats.
-__device__ __forceinline__ void h8_to_f8(const uint4& u, float* f) {
+__device__ __forceinline__ void h8_to_f8(const uint4 u, float* f) {
   const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

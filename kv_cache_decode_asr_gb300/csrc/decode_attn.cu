@@ -24,6 +24,9 @@
 // src/arch/qwen3_asr/decoder.h" (per-head Q/K RMSNorm, NeoX RoPE, GQA,
 // StepBuildBatched: K/V written at row n_past, keys up to n_past attended).
 #include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 #include <mutex>
@@ -35,7 +38,6 @@ namespace asrkv {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kRowsPerSlot = 2;
 
 // In-place exclusive scan of data[0..n) over the whole block; data[n] gets
 // the total.  tmp: 32 ints of shared memory.  All threads must call it.
@@ -118,36 +120,138 @@ struct TileIter {
   }
 };
 
-template <int HD>
+// ---- packed fp32 pairs and the fast base-2 exponential ---------------------
+
+// d = a * b + c on two fp32 lanes at once (sm_100+ packed FMA).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// d = a * b on two fp32 lanes at once.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 8 f16 held in registers -> 4 float pairs.  Takes the vector by value: a
+// reference into shared memory would make the conversion re-read it as four
+// 32-bit loads.
+__device__ __forceinline__ void h8_to_f2x4(const uint4 u, float2* f) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = __half22float2(h[i]);
+}
+
+template <int G>
 __device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int o = 1; o < HD / 8; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  for (int o = 1; o < G; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
 }
 
-// Per-head RMSNorm (weight * x * rsqrt(mean(x^2) + eps)) followed by NeoX
-// RoPE on the 8 dims this lane holds (lane li of its group holds dims
-// li*8 .. li*8+7).  Pair (i, i + HD/2) lives in lanes li and li ^ (G/2).
-// rope: cos[HD/2] then sin[HD/2] for the current position.  Warp-uniform.
-template <int HD>
-__device__ __forceinline__ void norm_rope8(float* x, const float* __restrict__ w, float eps,
-                                           const float* rope, int li) {
-  constexpr int G = HD / 8;
+// Lane layout of one head vector: a group of G = HD/DPL lanes covers the
+// head; lane li holds NCH = DPL/8 chunks of 8 dims.  Register slot j holds
+// chunk li + (j ^ sw)*G, i.e. dims (li + (j^sw)*G)*8 .. +8, as 4 float pairs
+// (pair t: slot t/4, dims 2*(t%4), 2*(t%4)+1 of the chunk).  With two chunks
+// per lane the NeoX RoPE partner (i, i + HD/2) of every dim is in the same
+// lane.  sw (0/1) swaps the slots of odd groups when a quarter-warp holds two
+// groups (G = 4), so its 8 lanes cover all 32 shared-memory banks per load.
+template <int HD, int DPL>
+struct LaneLayout {
+  static constexpr int NCH = DPL / 8;
+  static constexpr int G = HD / DPL;
+  static constexpr int NP = DPL / 2;
+  static constexpr bool kSwap = NCH == 2 && G < 8;
+  static __device__ __forceinline__ int chunk_off(int li, int j, int sw) {
+    return (li + (j ^ sw) * G) * 8;
+  }
+  static __device__ __forceinline__ int dim(int li, int t, int sw) {
+    return chunk_off(li, t / 4, sw) + 2 * (t % 4);
+  }
+};
+
+// Load one head vector (fp32) into the lane layout.
+template <int HD, int DPL>
+__device__ __forceinline__ void load_head_f32(const float* __restrict__ src, int li, int sw,
+                                              float2* x) {
+  using LL = LaneLayout<HD, DPL>;
+#pragma unroll
+  for (int j = 0; j < LL::NCH; ++j) {
+    const float* p = src + LL::chunk_off(li, j, sw);
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    x[4 * j + 0] = make_float2(a.x, a.y);
+    x[4 * j + 1] = make_float2(a.z, a.w);
+    x[4 * j + 2] = make_float2(b.x, b.y);
+    x[4 * j + 3] = make_float2(b.z, b.w);
+  }
+}
+
+// Per-head RMSNorm (weight * x * rsqrt(mean(x^2) + eps)) then NeoX RoPE, in
+// place, on a head vector in the lane layout.  rope: cos[HD/2], sin[HD/2].
+// Warp-uniform (it shuffles).
+template <int HD, int DPL>
+__device__ __forceinline__ void norm_rope(float2* x, const float* __restrict__ w, float eps,
+                                          const float* rope, int li, int sw) {
+  using LL = LaneLayout<HD, DPL>;
+  constexpr int NP = LL::NP, G = LL::G;
   float ss = 0.f;
 #pragma unroll
-  for (int d = 0; d < 8; ++d) ss = fmaf(x[d], x[d], ss);
-  ss = group_sum<HD>(ss);
+  for (int t = 0; t < NP; ++t) ss = fmaf(x[t].y, x[t].y, fmaf(x[t].x, x[t].x, ss));
+  ss = group_sum<G>(ss);
   const float rinv = 1.0f / sqrtf(ss / (float)HD + eps);
-  float xn[8];
+  float2 xn[NP];
 #pragma unroll
-  for (int d = 0; d < 8; ++d) xn[d] = w[li * 8 + d] * (x[d] * rinv);
-  const bool lower = li < G / 2;
-  const int i0 = (lower ? li : li - G / 2) * 8;
+  for (int t = 0; t < NP; ++t) {
+    const int d0 = LL::dim(li, t, sw);
+    xn[t] = make_float2(w[d0] * (x[t].x * rinv), w[d0 + 1] * (x[t].y * rinv));
+  }
+  if constexpr (LL::NCH == 2) {
+    // chunk li holds dims i < HD/2 (slot sw), chunk li + G their partners
+    // i + HD/2 (slot 1 - sw)
 #pragma unroll
-  for (int d = 0; d < 8; ++d) {
-    const float partner = __shfl_xor_sync(kFull, xn[d], G / 2);
-    const float c = rope[i0 + d], s = rope[HD / 2 + i0 + d];
-    x[d] = lower ? (xn[d] * c - partner * s) : (xn[d] * c + partner * s);
+    for (int p = 0; p < 4; ++p) {
+      const int i0 = li * 8 + 2 * p;
+      const float c0 = rope[i0], s0 = rope[HD / 2 + i0];
+      const float c1 = rope[i0 + 1], s1 = rope[HD / 2 + i0 + 1];
+      const float2 lo = sw ? xn[4 + p] : xn[p], hi = sw ? xn[p] : xn[4 + p];
+      const float2 ylo = make_float2(lo.x * c0 - hi.x * s0, lo.y * c1 - hi.y * s1);
+      const float2 yhi = make_float2(hi.x * c0 + lo.x * s0, hi.y * c1 + lo.y * s1);
+      x[p] = sw ? yhi : ylo;
+      x[4 + p] = sw ? ylo : yhi;
+    }
+  } else {
+    // one chunk per lane: the partner chunk lives in lane li ^ (G/2)
+    const bool lower = li < G / 2;
+    const int ib = (lower ? li : li - G / 2) * 8;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float px = __shfl_xor_sync(kFull, xn[p].x, G / 2);
+      const float py = __shfl_xor_sync(kFull, xn[p].y, G / 2);
+      const int i0 = ib + 2 * p;
+      const float c0 = rope[i0], s0 = rope[HD / 2 + i0];
+      const float c1 = rope[i0 + 1], s1 = rope[HD / 2 + i0 + 1];
+      x[p] = lower ? make_float2(xn[p].x * c0 - px * s0, xn[p].y * c1 - py * s1)
+                   : make_float2(xn[p].x * c0 + px * s0, xn[p].y * c1 + py * s1);
+    }
   }
 }
 
@@ -158,8 +262,8 @@ template <int HD>
 __device__ __forceinline__ void rope_table(float* rope, const double* theta, int p, int tid) {
   if (tid < HD / 2) {
     const double ang = (double)p * theta[tid];
-    const double two_pi_hi = 6.283185307179586;       // 2*pi rounded to double
-    const double two_pi_lo = 2.4492935982947064e-16;  // 2*pi - two_pi_hi
+    const double two_pi_hi = 6.283185307179586;        // 2*pi rounded to double
+    const double two_pi_lo = 2.4492935982947064e-16;   // 2*pi - two_pi_hi
     const double kq = rint(ang * 0.15915494309189535);  // ang / (2*pi)
     double r = fma(-kq, two_pi_hi, ang);
     r = fma(-kq, two_pi_lo, r);
@@ -170,10 +274,68 @@ __device__ __forceinline__ void rope_table(float* rope, const double* theta, int
   }
 }
 
-template <int HD, int NQ, int MAXT>
+// Merge the (max, sum, output) states of row slots 1..R-1 into row slot 0
+// through shared memory.  Called by all consumer threads.
+template <int HD, int NQ, int DPL>
+__device__ __forceinline__ void merge_row_slots(float (&M)[NQ], float (&Ls)[NQ],
+                                                float2 (&O)[NQ][DPL / 2], float* merge, int r,
+                                                int R, int h, int Hkv, int li, int sw, int nq,
+                                                int n_cons) {
+  using LL = LaneLayout<HD, DPL>;
+  named_bar(1, n_cons);
+  if (r > 0) {
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+      if (qi < nq) {
+        float* mb = merge + (((r - 1) * Hkv + h) * NQ + qi) * (HD + 4);
+#pragma unroll
+        for (int j = 0; j < LL::NCH; ++j) {
+          float4* dst = reinterpret_cast<float4*>(mb + LL::chunk_off(li, j, sw));
+          dst[0] = make_float4(O[qi][4 * j].x, O[qi][4 * j].y, O[qi][4 * j + 1].x, O[qi][4 * j + 1].y);
+          dst[1] = make_float4(O[qi][4 * j + 2].x, O[qi][4 * j + 2].y, O[qi][4 * j + 3].x,
+                               O[qi][4 * j + 3].y);
+        }
+        if (li == 0) {
+          mb[HD] = M[qi];
+          mb[HD + 1] = Ls[qi];
+        }
+      }
+    }
+  }
+  named_bar(1, n_cons);
+  if (r == 0) {
+    for (int r2 = 1; r2 < R; ++r2) {
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) {
+        if (qi < nq) {
+          const float* mb = merge + (((r2 - 1) * Hkv + h) * NQ + qi) * (HD + 4);
+          const float m2 = mb[HD], l2 = mb[HD + 1];
+          const float mn = fmaxf(M[qi], m2);
+          if (mn != -INFINITY) {
+            const float ca = ex2(M[qi] - mn), cb = ex2(m2 - mn);
+            Ls[qi] = Ls[qi] * ca + l2 * cb;
+#pragma unroll
+            for (int j = 0; j < LL::NCH; ++j) {
+              const float4* src = reinterpret_cast<const float4*>(mb + LL::chunk_off(li, j, sw));
+              const float4 u0 = src[0], u1 = src[1];
+              const float2 cb2 = make_float2(cb, cb), ca2 = make_float2(ca, ca);
+              O[qi][4 * j] = ffma2(cb2, make_float2(u0.x, u0.y), fmul2(O[qi][4 * j], ca2));
+              O[qi][4 * j + 1] = ffma2(cb2, make_float2(u0.z, u0.w), fmul2(O[qi][4 * j + 1], ca2));
+              O[qi][4 * j + 2] = ffma2(cb2, make_float2(u1.x, u1.y), fmul2(O[qi][4 * j + 2], ca2));
+              O[qi][4 * j + 3] = ffma2(cb2, make_float2(u1.z, u1.w), fmul2(O[qi][4 * j + 3], ca2));
+            }
+            M[qi] = mn;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int HD, int NQ, int DPL, int RS, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_constant__ DecodeArgs a) {
-  constexpr int G = HD / 8;
-  constexpr int RS = kRowsPerSlot;
+  using LL = LaneLayout<HD, DPL>;
+  constexpr int G = LL::G, NP = LL::NP, NCH = LL::NCH;
   extern __shared__ __align__(128) unsigned char smem[];
   const DecodeSmem lay = decode_smem_layout(a.stages, a.n_src, a.R, a.Hkv, NQ, HD, a.stage_elems);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
@@ -219,7 +381,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     for (int g = tid; g < S; g += blockDim.x) {
       const int v = a.lens[g];
       int keys;
-      if (a.mode == kModeSelf) keys = (v >= 1 && v <= a.capacity) ? v : 0;
+      if (a.mode == kModeSelf) keys = (v >= 1 && v <= a.capacity) ? v - a.append : 0;
       else keys = (v >= 0 && v < a.capacity) ? v : 0;  // rows cached before the new one
       off[g] = keys;
       mst[g] = 1;
@@ -262,7 +424,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   const int64_t total = off[S];
   const int P = gridDim.x;
   int64_t share = (total + P - 1) / P;
-  if (share < a.tile_rows) share = a.tile_rows;
+  if (share < a.min_share) share = a.min_share;
   const int64_t k0 = (int64_t)blockIdx.x * share;
   const int64_t k1 = min(k0 + share, total);
 
@@ -295,20 +457,22 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   const int grp = tid / G, li = tid % G;
   const int h = grp % a.Hkv, r = grp / a.Hkv;
   const int rep = a.rep;
+  const int R = a.R;
+  const int sw = LL::kSwap ? (grp & 1) : 0;
+  const int hoff = h * HD;  // element offset of this group's head in a K (or V) half
 
-  float qv[NQ][8], o[NQ][8], m[NQ], l[NQ];
+  float2 qv[NQ][NP], o[NQ][NP];
+  float m[NQ], l[NQ], snew[NQ];
+  float2 vn[NP];
   int nq = 0, mbase = 0;
-  // New-token K/V of the GQA step (f16-rounded, as floats) and its scores.
-  float kn[8], vn[8], snew[NQ];
-#pragma unroll
-  for (int d = 0; d < 8; ++d) kn[d] = vn[d] = 0.f;
 #pragma unroll
   for (int qi = 0; qi < NQ; ++qi) snew[qi] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NP; ++t) vn[t] = make_float2(0.f, 0.f);
 
   auto seg_begin = [&](int g) {
-    const int cnt = mst[g + 1] - mst[g];
     mbase = mst[g];
-    nq = min(cnt, a.max_members) * rep;
+    nq = min(mst[g + 1] - mst[g], a.max_members) * rep;
     if (a.mode == kModeGqa) {
       named_bar(1, n_cons);
       rope_table<HD>(rope, a.theta, a.lens[g], tid);
@@ -319,112 +483,86 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       m[qi] = -INFINITY;
       l[qi] = 0.f;
 #pragma unroll
-      for (int d = 0; d < 8; ++d) o[qi][d] = 0.f;
+      for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
       if (qi < nq) {
         const int b = mbase + qi / rep;
         const int hq = h * rep + qi % rep;
-        const float* src = a.q + (int64_t)b * a.q_stride + hq * HD + li * 8;
-        const float4 x0 = *reinterpret_cast<const float4*>(src);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-        float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        if (a.mode == kModeGqa) norm_rope8<HD>(x, a.wq, a.eps, rope, li);
+        load_head_f32<HD, DPL>(a.q + (int64_t)b * a.q_stride + hq * HD, li, sw, qv[qi]);
+        if (a.mode == kModeGqa) norm_rope<HD, DPL>(qv[qi], a.wq, a.eps, rope, li, sw);
+        const float2 s2 = make_float2(a.qscale, a.qscale);
 #pragma unroll
-        for (int d = 0; d < 8; ++d) qv[qi][d] = x[d] * a.qscale;
+        for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
       } else {
 #pragma unroll
-        for (int d = 0; d < 8; ++d) qv[qi][d] = 0.f;
+        for (int t = 0; t < NP; ++t) qv[qi][t] = make_float2(0.f, 0.f);
       }
     }
   };
 
-  // Fold the new token (GQA) into (M, Ls, O) and write the normalised
-  // output of query qi.  Contains no shuffles: callable per group.
-  auto finalize = [&](int qi, float M, float Ls, float* O) {
-    if (a.mode == kModeGqa) {
+  // Fold the new token (append) into (M, Ls, O) and write the normalised
+  // output of query qi.  No shuffles: callable per group.
+  auto finalize = [&](int qi, float M, float Ls, float2* O) {
+    if (a.append) {
       const float mn = fmaxf(M, snew[qi]);
-      const float ca = exp2f(M - mn), cb = exp2f(snew[qi] - mn);
+      const float ca = ex2(M - mn), cb = ex2(snew[qi] - mn);
       Ls = Ls * ca + cb;
 #pragma unroll
-      for (int d = 0; d < 8; ++d) O[d] = fmaf(cb, vn[d], O[d] * ca);
+      for (int t = 0; t < NP; ++t)
+        O[t] = ffma2(make_float2(cb, cb), vn[t], fmul2(O[t], make_float2(ca, ca)));
     }
     const int b = mbase + qi / rep;
     const int hq = h * rep + qi % rep;
     const float inv = 1.0f / Ls;
-    float* dst = a.out + (int64_t)b * qw + hq * HD + li * 8;
-    *reinterpret_cast<float4*>(dst) = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-    *reinterpret_cast<float4*>(dst + 4) =
-        make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
+    float* dst = a.out + (int64_t)b * qw + hq * HD;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      float4* p = reinterpret_cast<float4*>(dst + LL::chunk_off(li, j, sw));
+      p[0] = make_float4(O[4 * j].x * inv, O[4 * j].y * inv, O[4 * j + 1].x * inv, O[4 * j + 1].y * inv);
+      p[1] = make_float4(O[4 * j + 2].x * inv, O[4 * j + 2].y * inv, O[4 * j + 3].x * inv,
+                         O[4 * j + 3].y * inv);
+    }
   };
 
   auto seg_end = [&](int g) {
-    // GQA: the new token's key/value, computed by every group (warp-uniform
-    // code: it shuffles), appended to the cache by row slot 0.
-    if (a.mode == kModeGqa) {
-      const int p = a.lens[g];
-      const float* ks = a.k_new + (int64_t)g * a.Hkv * HD + h * HD + li * 8;
-      const float* vs = a.v_new + (int64_t)g * a.Hkv * HD + h * HD + li * 8;
-      const float4 x0 = *reinterpret_cast<const float4*>(ks);
-      const float4 x1 = *reinterpret_cast<const float4*>(ks + 4);
-      const float4 v0 = *reinterpret_cast<const float4*>(vs);
-      const float4 v1 = *reinterpret_cast<const float4*>(vs + 4);
-      float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      norm_rope8<HD>(x, a.wk, a.eps, rope, li);
-      const uint4 kh = f8_to_h8(x);
-      const uint4 vh = f8_to_h8(vv);
-      h8_to_f8(kh, kn);
-      h8_to_f8(vh, vn);
-      if (r == 0) {
-        uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
-        *reinterpret_cast<uint4*>(row + h * HD + li * 8) = kh;
-        *reinterpret_cast<uint4*>(row + a.Hkv * HD + h * HD + li * 8) = vh;
+    // Append: the new token's key/value (GQA: normed and roped), computed by
+    // every group (warp-uniform code: it may shuffle), written to the cache
+    // by row slot 0 and scored against this group's queries.
+    if (a.append) {
+      const int p = a.mode == kModeGqa ? a.lens[g] : a.lens[g] - 1;
+      float2 kx[NP];
+      load_head_f32<HD, DPL>(a.k_new + (int64_t)g * a.kv_stride + h * HD, li, sw, kx);
+      load_head_f32<HD, DPL>(a.v_new + (int64_t)g * a.kv_stride + h * HD, li, sw, vn);
+      if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, a.wk, a.eps, rope, li, sw);
+      uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        float kf[8], vf[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kf[2 * e] = kx[4 * j + e].x;
+          kf[2 * e + 1] = kx[4 * j + e].y;
+          vf[2 * e] = vn[4 * j + e].x;
+          vf[2 * e + 1] = vn[4 * j + e].y;
+        }
+        const uint4 kh = f8_to_h8(kf), vh = f8_to_h8(vf);
+        h8_to_f2x4(kh, kx + 4 * j);  // the key as the cache holds it
+        h8_to_f2x4(vh, vn + 4 * j);
+        if (r == 0) {
+          *reinterpret_cast<uint4*>(row + hoff + LL::chunk_off(li, j, sw)) = kh;
+          *reinterpret_cast<uint4*>(row + a.Hkv * HD + hoff + LL::chunk_off(li, j, sw)) = vh;
+        }
       }
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
         if (qi < nq) {
-          float sdot = 0.f;
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int d = 0; d < 8; ++d) sdot = fmaf(qv[qi][d], kn[d], sdot);
-          snew[qi] = group_sum<HD>(sdot);
+          for (int t = 0; t < NP; ++t) acc = ffma2(qv[qi][t], kx[t], acc);
+          snew[qi] = group_sum<G>(acc.x + acc.y);
         }
       }
     }
-    // merge the row slots of each head into slot 0
-    named_bar(1, n_cons);
-    if (r > 0) {
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          float* mb = merge + (((r - 1) * a.Hkv + h) * NQ + qi) * (HD + 2);
-#pragma unroll
-          for (int d = 0; d < 8; ++d) mb[li * 8 + d] = o[qi][d];
-          if (li == 0) {
-            mb[HD] = m[qi];
-            mb[HD + 1] = l[qi];
-          }
-        }
-      }
-    }
-    named_bar(1, n_cons);
-    if (r == 0) {
-      for (int r2 = 1; r2 < a.R; ++r2) {
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
-            const float* mb = merge + (((r2 - 1) * a.Hkv + h) * NQ + qi) * (HD + 2);
-            const float m2 = mb[HD], l2 = mb[HD + 1];
-            const float mn = fmaxf(m[qi], m2);
-            if (mn != -INFINITY) {
-              const float ca = exp2f(m[qi] - mn), cb = exp2f(m2 - mn);
-              l[qi] = l[qi] * ca + l2 * cb;
-#pragma unroll
-              for (int d = 0; d < 8; ++d) o[qi][d] = fmaf(cb, mb[li * 8 + d], o[qi][d] * ca);
-              m[qi] = mn;
-            }
-          }
-        }
-      }
-    }
+    merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
     // pieces of this source over the grid
     const int64_t go = off[g], gl = (int64_t)off[g + 1] - off[g];
     const int first = gl > 0 ? (int)(go / share) : 0;
@@ -444,9 +582,14 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       for (int qi = 0; qi < NQ; ++qi) {
         if (qi < nq) {
           const int64_t pidx = (slot * a.max_members + qi / rep) * a.Hq + h * rep + qi % rep;
-          float* po = a.part_o + pidx * HD + li * 8;
-          *reinterpret_cast<float4*>(po) = make_float4(o[qi][0], o[qi][1], o[qi][2], o[qi][3]);
-          *reinterpret_cast<float4*>(po + 4) = make_float4(o[qi][4], o[qi][5], o[qi][6], o[qi][7]);
+          float* po = a.part_o + pidx * HD;
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            float4* p = reinterpret_cast<float4*>(po + LL::chunk_off(li, j, sw));
+            p[0] = make_float4(o[qi][4 * j].x, o[qi][4 * j].y, o[qi][4 * j + 1].x, o[qi][4 * j + 1].y);
+            p[1] = make_float4(o[qi][4 * j + 2].x, o[qi][4 * j + 2].y, o[qi][4 * j + 3].x,
+                               o[qi][4 * j + 3].y);
+          }
           if (li == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(m[qi], l[qi]);
         }
       }
@@ -462,24 +605,47 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     named_bar(1, n_cons);
     if (ctl[1]) {
       __threadfence();
-      for (int qi = r; qi < nq; qi += a.R) {
-        float M = -INFINITY, Ls = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int kp = first; kp <= lastp; ++kp) {
-          const int64_t slot = (int64_t)kp + g;
-          const int64_t pidx = (slot * a.max_members + qi / rep) * a.Hq + h * rep + qi % rep;
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
-          const float4 p0 = ld_cg_f4(a.part_o + pidx * HD + li * 8);
-          const float4 p1 = ld_cg_f4(a.part_o + pidx * HD + li * 8 + 4);
-          const float mn = fmaxf(M, ml.x);
-          if (mn == -INFINITY) continue;
-          const float ca = exp2f(M - mn), cb = exp2f(ml.x - mn);
-          Ls = Ls * ca + ml.y * cb;
-          const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      // row slot r merges pieces first + r, first + r + R, ...; then the
+      // slots are merged like a tile's rows.  The running state registers are
+      // reused: this CTA's own piece is already among the partials.
 #pragma unroll
-          for (int d = 0; d < 8; ++d) O[d] = fmaf(cb, pv[d], O[d] * ca);
-          M = mn;
+      for (int qi = 0; qi < NQ; ++qi) {
+        m[qi] = -INFINITY;
+        l[qi] = 0.f;
+#pragma unroll
+        for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
+      }
+      for (int kp = first + r; kp <= lastp; kp += R) {
+        const int64_t slot = (int64_t)kp + g;
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          if (qi < nq) {
+            const int64_t pidx = (slot * a.max_members + qi / rep) * a.Hq + h * rep + qi % rep;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
+            const float mn = fmaxf(m[qi], ml.x);
+            if (mn != -INFINITY) {
+              const float ca = ex2(m[qi] - mn), cb = ex2(ml.x - mn);
+              l[qi] = l[qi] * ca + ml.y * cb;
+              const float2 ca2 = make_float2(ca, ca), cb2 = make_float2(cb, cb);
+#pragma unroll
+              for (int j = 0; j < NCH; ++j) {
+                const float* src = a.part_o + pidx * HD + LL::chunk_off(li, j, sw);
+                const float4 u0 = ld_cg_f4(src), u1 = ld_cg_f4(src + 4);
+                o[qi][4 * j] = ffma2(cb2, make_float2(u0.x, u0.y), fmul2(o[qi][4 * j], ca2));
+                o[qi][4 * j + 1] = ffma2(cb2, make_float2(u0.z, u0.w), fmul2(o[qi][4 * j + 1], ca2));
+                o[qi][4 * j + 2] = ffma2(cb2, make_float2(u1.x, u1.y), fmul2(o[qi][4 * j + 2], ca2));
+                o[qi][4 * j + 3] = ffma2(cb2, make_float2(u1.z, u1.w), fmul2(o[qi][4 * j + 3], ca2));
+              }
+              m[qi] = mn;
+            }
+          }
         }
-        finalize(qi, M, Ls, O);
+      }
+      merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
+      if (r == 0) {
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi)
+          if (qi < nq) finalize(qi, m[qi], l[qi], o[qi]);
       }
     }
   };
@@ -494,77 +660,105 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
         break;
       }
-      const uint16_t* tb = stage + (size_t)s * a.stage_elems;
-      float kf[RS][8], vf[RS][8];
+      const uint16_t* tb = stage + (size_t)s * a.stage_elems + hoff;
+      // scores of this group's rows (row r + i*R of the tile)
+      float sc[NQ][RS];
       bool val[RS];
 #pragma unroll
       for (int i = 0; i < RS; ++i) {
-        const int row = r + i * a.R;
+        const int row = r + i * R;  // < tile_rows: always inside the stage buffer
         val[i] = row < tl.nr;
-        if (val[i]) {
-          const uint16_t* rp = tb + row * a.row_elems + h * HD + li * 8;
-          const uint4 ku = *reinterpret_cast<const uint4*>(rp);
-          const uint4 vu = *reinterpret_cast<const uint4*>(rp + a.Hkv * HD);
-          h8_to_f8(ku, kf[i]);
-          h8_to_f8(vu, vf[i]);
-        } else {
+        float2 kf[NP];
 #pragma unroll
-          for (int d = 0; d < 8; ++d) kf[i][d] = vf[i][d] = 0.f;
+        for (int j = 0; j < NCH; ++j) {
+          const uint4 u = *reinterpret_cast<const uint4*>(tb + row * a.row_elems + LL::chunk_off(li, j, sw));
+          h8_to_f2x4(u, kf + 4 * j);
+        }
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          if (qi < nq) {
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < NP; t += 2) {
+              a0 = ffma2(qv[qi][t], kf[t], a0);
+              a1 = ffma2(qv[qi][t + 1], kf[t + 1], a1);
+            }
+            sc[qi][i] = (a0.x + a0.y) + (a1.x + a1.y);
+          }
         }
       }
-      // the stage is in registers now: hand it back to the producer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+      for (int o2 = 1; o2 < G; o2 <<= 1) {
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          if (qi < nq) {
+#pragma unroll
+            for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
+          }
+        }
+      }
+      // online softmax over the RS rows, one rescale per tile
+      float pr[NQ][RS];
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
+#pragma unroll
+        for (int i = 0; i < RS; ++i) pr[qi][i] = 0.f;
         if (qi < nq) {
-          float sc[RS];
-#pragma unroll
-          for (int i = 0; i < RS; ++i) {
-            float dsum = 0.f;
-#pragma unroll
-            for (int d = 0; d < 8; ++d) dsum = fmaf(qv[qi][d], kf[i][d], dsum);
-            sc[i] = dsum;
-          }
-#pragma unroll
-          for (int o2 = 1; o2 < G; o2 <<= 1) {
-#pragma unroll
-            for (int i = 0; i < RS; ++i) sc[i] += __shfl_xor_sync(kFull, sc[i], o2);
-          }
           float mt = -INFINITY;
 #pragma unroll
           for (int i = 0; i < RS; ++i)
-            if (val[i]) mt = fmaxf(mt, sc[i]);
+            if (val[i]) mt = fmaxf(mt, sc[qi][i]);
           if (mt != -INFINITY) {
             const float mn = fmaxf(m[qi], mt);
-            const float alpha = exp2f(m[qi] - mn);
-            float p[RS], psum = 0.f;
+            const float alpha = ex2(m[qi] - mn);
+            float psum = 0.f;
 #pragma unroll
             for (int i = 0; i < RS; ++i) {
-              p[i] = val[i] ? exp2f(sc[i] - mn) : 0.f;
-              psum += p[i];
+              pr[qi][i] = val[i] ? ex2(sc[qi][i] - mn) : 0.f;
+              psum += pr[qi][i];
             }
             l[qi] = fmaf(l[qi], alpha, psum);
-#pragma unroll
-            for (int d = 0; d < 8; ++d) {
-              float acc = o[qi][d] * alpha;
-#pragma unroll
-              for (int i = 0; i < RS; ++i) acc = fmaf(p[i], vf[i][d], acc);
-              o[qi][d] = acc;
-            }
             m[qi] = mn;
+            const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int t = 0; t < NP; ++t) o[qi][t] = fmul2(o[qi][t], al2);
           }
         }
       }
+      // weighted values
+#pragma unroll
+      for (int i = 0; i < RS; ++i) {
+        if (val[i]) {
+          const int row = r + i * R;
+          float2 vf[NP];
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(tb + row * a.row_elems + a.Hkv * HD +
+                                                            LL::chunk_off(li, j, sw));
+            h8_to_f2x4(u, vf + 4 * j);
+          }
+#pragma unroll
+          for (int qi = 0; qi < NQ; ++qi) {
+            if (qi < nq) {
+              const float2 p2 = make_float2(pr[qi][i], pr[qi][i]);
+#pragma unroll
+              for (int t = 0; t < NP; ++t) o[qi][t] = ffma2(p2, vf[t], o[qi][t]);
+            }
+          }
+        }
+      }
+      // the stage is consumed: hand it back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
       if (tl.last) seg_end(tl.g);
     }
   }
 
-  // GQA sources with no cached rows (n_past == 0): only the new token; CTA
-  // g % P handles source g.
-  if (a.mode == kModeGqa) {
+  // Appending sources with no cached rows (GQA n_past == 0, self lens == 1):
+  // only the new token; CTA g % P handles source g.
+  if (a.append) {
     for (int g = blockIdx.x; g < S; g += P) {
-      if (a.lens[g] == 0) {
+      if (a.lens[g] == (a.mode == kModeGqa ? 0 : 1)) {
         seg_begin(g);
         seg_end(g);
       }
@@ -575,67 +769,118 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 
 // ---------------------------------------------------------------- host ----
 
-struct DecodePlan {
-  int R, tile_rows, stages, stage_elems, threads, smem, grid;
+// Per query-count bucket: dims per lane, rows per slot per tile, thread cap.
+struct Variant {
+  int NQ, DPL, RS, MAXT;
 };
+static constexpr int kNumVariants = 6;
+static constexpr Variant kVariants[kNumVariants] = {
+    {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256},
+    {1, 16, 2, 384}, {2, 16, 2, 384}};  // the last two: 2 rows per slot (tuning)
 
-static int max_threads_for(int NQ) { return NQ <= 2 ? 640 : (NQ <= 4 ? 512 : 256); }
+static int variant_index(int nq, int rs) {
+  if (nq <= 1) return rs == 2 ? 4 : 0;
+  if (nq <= 2) return rs == 2 ? 5 : 1;
+  if (nq <= 4) return 2;
+  if (nq <= 8) return 3;
+  return -1;
+}
 
-template <int HD, int NQ>
+template <int HD, int VI>
 static void* kernel_ptr() {
-  return (void*)decode_attn_kernel<HD, NQ, (NQ <= 2 ? 640 : (NQ <= 4 ? 512 : 256))>;
+  constexpr Variant v = kVariants[VI];
+  return (void*)decode_attn_kernel<HD, v.NQ, v.DPL, v.RS, v.MAXT>;
 }
 
-static int nq_bucket(int nq) {
-  if (nq <= 1) return 1;
-  if (nq <= 2) return 2;
-  if (nq <= 4) return 4;
-  if (nq <= 8) return 8;
-  return 0;
-}
-
-static void* kernel_for(int HD, int NQ) {
+static void* kernel_for(int HD, int vi) {
   if (HD == 64) {
-    switch (NQ) {
+    switch (vi) {
+      case 0: return kernel_ptr<64, 0>();
       case 1: return kernel_ptr<64, 1>();
       case 2: return kernel_ptr<64, 2>();
+      case 3: return kernel_ptr<64, 3>();
       case 4: return kernel_ptr<64, 4>();
-      case 8: return kernel_ptr<64, 8>();
+      case 5: return kernel_ptr<64, 5>();
     }
   } else if (HD == 128) {
-    switch (NQ) {
+    switch (vi) {
+      case 0: return kernel_ptr<128, 0>();
       case 1: return kernel_ptr<128, 1>();
       case 2: return kernel_ptr<128, 2>();
+      case 3: return kernel_ptr<128, 3>();
       case 4: return kernel_ptr<128, 4>();
-      case 8: return kernel_ptr<128, 8>();
+      case 5: return kernel_ptr<128, 5>();
     }
   }
   return nullptr;
 }
 
-// Row slots R: as many as fit the thread budget (at most 512 consumer
-// threads), with the consumer count a multiple of 32.  Stages: as many as fit
-// 200 KB of shared memory, 2..8.
-static bool plan_decode(int HD, int NQ, int Hkv, int row_elems, int n_src, DecodePlan& p) {
-  const int G = HD / 8;
+// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=36,smem_kb=110,ctas=0,R=0,rs=4"
+// overrides them (ctas / R = 0: chosen automatically; rs: rows per slot).
+struct DecodeTune {
+  int tile_kb = 36, smem_kb = 110, ctas = 0, R = 0, rs = 4;
+};
+
+static DecodeTune decode_tune() {
+  static DecodeTune t = [] {
+    DecodeTune d;
+    const char* e = getenv("ASRKV_DECODE_TUNE");
+    if (e) {
+      char key[32];
+      int val, n;
+      while (sscanf(e, " %31[A-Za-z_]=%d%n", key, &val, &n) == 2) {
+        if (!strcmp(key, "tile_kb")) d.tile_kb = val;
+        else if (!strcmp(key, "smem_kb")) d.smem_kb = val;
+        else if (!strcmp(key, "ctas")) d.ctas = val;
+        else if (!strcmp(key, "R")) d.R = val;
+        else if (!strcmp(key, "rs")) d.rs = val;
+        e += n;
+        if (*e == ',') ++e;
+      }
+    }
+    return d;
+  }();
+  return t;
+}
+
+struct DecodePlan {
+  int R, tile_rows, stages, stage_elems, threads, smem, min_share;
+};
+
+// Row slots R: the consumer count R * Hkv * G must be a multiple of 32 and
+// fit the variant's thread cap; among those, the largest R whose tile fits
+// tile_kb (else the smallest valid R).  Stages: as many as fit smem_kb, 2..8.
+// One CTA takes at least 64 KB of rows, so a source splits into a bounded
+// number of partial results.
+static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_src,
+                        DecodePlan& p) {
+  const DecodeTune tune = decode_tune();
+  const int G = HD / v.DPL;
   const int per_slot = Hkv * G;
-  const int budget = std::min(max_threads_for(NQ) - 32, 512);
-  int best = 0;
-  for (int R = 1; R * per_slot <= budget; ++R)
-    if ((R * per_slot) % 32 == 0) best = R;
-  if (best == 0) return false;
+  const int budget = std::min(v.MAXT - 32, 512);
+  const int row_bytes = row_elems * 2;
+  int best = 0, smallest = 0;
+  for (int R = 1; R * per_slot <= budget; ++R) {
+    if ((R * per_slot) % 32 != 0) continue;
+    if (!smallest) smallest = R;
+    if (R * v.RS * row_bytes <= tune.tile_kb * 1024) best = R;
+  }
+  if (tune.R > 0 && tune.R * per_slot <= budget && (tune.R * per_slot) % 32 == 0) best = tune.R;
+  if (!best) best = smallest;
+  if (!best) return false;
   p.R = best;
   p.threads = best * per_slot + 32;
-  p.tile_rows = best * kRowsPerSlot;
+  p.tile_rows = best * v.RS;
   p.stage_elems = dsm_align(p.tile_rows * row_elems, 64);
-  const int smem_cap = 200 * 1024;
+  const int cap = std::max(tune.smem_kb, 16) * 1024;
   int stages = 8;
   while (stages > 2 &&
-         decode_smem_layout(stages, n_src, p.R, Hkv, NQ, HD, p.stage_elems).total > smem_cap)
+         decode_smem_layout(stages, n_src, p.R, Hkv, v.NQ, HD, p.stage_elems).total > cap)
     --stages;
   p.stages = stages;
-  p.smem = decode_smem_layout(stages, n_src, p.R, Hkv, NQ, HD, p.stage_elems).total;
+  p.smem = decode_smem_layout(stages, n_src, p.R, Hkv, v.NQ, HD, p.stage_elems).total;
   if (p.smem > 227 * 1024) return false;
+  p.min_share = std::max(p.tile_rows, (65536 + row_bytes - 1) / row_bytes);
   return true;
 }
 
@@ -647,31 +892,54 @@ size_t decode_ws_bytes(int n_src, int max_members, int Hq, int HD, int sms) {
   return counters + ml + o;
 }
 
-static std::once_flag g_attr_once[2][4];
+static std::once_flag g_attr_once[2][kNumVariants];
+
+// CTAs per SM for (kernel, threads, smem) on the current device; the query
+// is slow next to a launch, so results are memoised (small linear table).
+static int occupancy_cached(void* fn, int threads, int smem) {
+  struct Entry {
+    void* fn;
+    int dev, threads, smem, occ;
+  };
+  static Entry table[64];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn && table[i].dev == dev && table[i].threads == threads &&
+        table[i].smem == smem)
+      return table[i].occ;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem) != cudaSuccess)
+    return 0;
+  if (n < 64) table[n++] = {fn, dev, threads, smem, occ};
+  return occ;
+}
 
 static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
-  const int NQ = nq_bucket(nq_needed);
-  if (NQ == 0) return ASR_ERR_UNSUPPORTED;
+  const int vi = variant_index(nq_needed, decode_tune().rs);
+  if (vi < 0) return ASR_ERR_UNSUPPORTED;
+  const Variant& v = kVariants[vi];
   DecodePlan p;
-  if (!plan_decode(HD, NQ, a.Hkv, a.row_elems, a.n_src, p)) return ASR_ERR_UNSUPPORTED;
+  if (!plan_decode(HD, v, a.Hkv, a.row_elems, a.n_src, p)) return ASR_ERR_UNSUPPORTED;
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
   const size_t need = decode_ws_bytes(a.n_src, a.max_members, a.Hq, HD, sms);
   if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < need) return ASR_ERR_WORKSPACE;
-  void* fn = kernel_for(HD, NQ);
-  const int hi = HD == 64 ? 0 : 1;
-  const int ni = NQ == 1 ? 0 : NQ == 2 ? 1 : NQ == 4 ? 2 : 3;
+  void* fn = kernel_for(HD, vi);
   cudaError_t attr_err = cudaSuccess;
-  std::call_once(g_attr_once[hi][ni], [&] {
+  std::call_once(g_attr_once[HD == 64 ? 0 : 1][vi], [&] {
     attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (attr_err != cudaSuccess) return ASR_ERR_CUDA;
-  int occ = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p.threads, p.smem) != cudaSuccess)
-    return ASR_ERR_CUDA;
+  int occ = occupancy_cached(fn, p.threads, p.smem);
+  if (occ <= 0) return ASR_ERR_CUDA;
+  const int want = decode_tune().ctas;
+  if (want > 0) occ = std::min(occ, want);
   occ = std::max(1, std::min(occ, kMaxCtasPerSm));
-  p.grid = sms * occ;
   char* w = static_cast<char*>(ws);
   a.counters = reinterpret_cast<int*>(w);
   w += align_up((size_t)a.n_src * 4, 256);
@@ -681,10 +949,11 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
   a.part_o = reinterpret_cast<float*>(w);
   a.R = p.R;
   a.tile_rows = p.tile_rows;
+  a.min_share = p.min_share;
   a.stages = p.stages;
   a.stage_elems = p.stage_elems;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
+  cfg.gridDim = dim3(sms * occ);
   cfg.blockDim = dim3(p.threads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
@@ -737,6 +1006,50 @@ extern "C" int asr_self_attn_step(const float* q, int64_t q_stride, const uint16
   a.out = out;
   a.dev_err = dev_err;
   a.mode = kModeSelf;
+  return launch_decode(a, head_dim, 1, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int asr_self_attn_append_step(const float* q, int64_t q_stride, const float* k_new,
+                                         const float* v_new, int64_t kv_stride, uint16_t* cache,
+                                         int64_t seq_stride, const int32_t* lens, int B, int heads,
+                                         int head_dim, int capacity, float scale, float* out,
+                                         void* ws, size_t ws_bytes, int32_t* dev_err,
+                                         asr_stream_t stream) {
+  if (B < 0 || B > ASR_MAX_BATCH || heads < 1 || capacity < 1) return ASR_ERR_INVALID_ARG;
+  if ((head_dim != 64 && head_dim != 128) || heads > ASR_MAX_KV_HEADS) return ASR_ERR_UNSUPPORTED;
+  if (B == 0) return ASR_OK;
+  if (!q || !k_new || !v_new || !cache || !lens || !out) return ASR_ERR_INVALID_ARG;
+  const int64_t row = 2LL * heads * head_dim;
+  if (q_stride < (int64_t)heads * head_dim || kv_stride < (int64_t)heads * head_dim ||
+      seq_stride < (int64_t)capacity * row)
+    return ASR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cache) ||
+      !aligned16(out) || q_stride % 4 != 0 || kv_stride % 4 != 0 || seq_stride % 8 != 0)
+    return ASR_ERR_MISALIGNED;
+  if (!rows_fit_int(B, capacity)) return ASR_ERR_UNSUPPORTED;
+  DecodeArgs a = {};
+  a.q = q;
+  a.q_stride = q_stride;
+  a.kv = cache;
+  a.cache_w = cache;
+  a.src_stride = seq_stride;
+  a.row_elems = (int)row;
+  a.n_src = B;
+  a.B = B;
+  a.lens = lens;
+  a.capacity = capacity;
+  a.Hq = heads;
+  a.Hkv = heads;
+  a.rep = 1;
+  a.max_members = 1;
+  a.qscale = scale * kLog2e;
+  a.out = out;
+  a.dev_err = dev_err;
+  a.mode = kModeSelf;
+  a.append = 1;
+  a.kv_stride = kv_stride;
+  a.k_new = k_new;
+  a.v_new = v_new;
   return launch_decode(a, head_dim, 1, ws, ws_bytes, (cudaStream_t)stream);
 }
 
@@ -820,6 +1133,8 @@ extern "C" int asr_gqa_step(const float* q, const float* k_new, const float* v_n
   a.out = out;
   a.dev_err = dev_err;
   a.mode = kModeGqa;
+  a.append = 1;
+  a.kv_stride = (int64_t)kv_heads * head_dim;
   a.k_new = k_new;
   a.v_new = v_new;
   a.wq = q_norm_w;

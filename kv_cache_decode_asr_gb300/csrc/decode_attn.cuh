@@ -39,16 +39,21 @@ struct DecodeArgs {
   // tiling
   int R;            // row slots (groups of the same head working on different rows)
   int tile_rows;    // rows per pipeline stage (R * rows per slot)
+  int min_share;    // fewest rows one CTA takes (bounds the partials per source)
   int stages;       // pipeline depth
   int stage_elems;  // f16 elements per stage buffer (128-byte multiple)
   int mode;         // DecodeMode
-  // GQA only
+  // new-token append (GQA step, fused self step): the call writes row p and
+  // folds that key in; p = n_past (GQA) or lens - 1 (self)
+  int append;
+  int64_t kv_stride;  // floats between sequences of k_new / v_new
   const float* k_new;
   const float* v_new;
+  // GQA only
   const float* wq;
   const float* wk;
   float eps;
-  uint16_t* cache_w;  // the cache, writable (row n_past is appended)
+  uint16_t* cache_w;  // the cache, writable (row p is appended)
   double theta[64];   // rope_base^(-2i/HD), i < HD/2, computed on the host in double
 };
 
@@ -68,7 +73,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
   s.rope = dsm_align(s.mstart + (n_src + 1) * 4, 16);
   s.merge = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
-  s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 2) * 4, 128);
+  s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 4) * 4, 128);
   s.total = s.stage + stages * stage_elems * 2;
   return s;
 }

@@ -29,6 +29,8 @@ SIGNATURES = {
     "asr_kv_append": (_int, [_p, _p, _i64, _p, _i64, _p, _int, _int, _int, _int, _p, _p]),
     "asr_self_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _f, _p, _p, _sz,
                                   _p, _p]),
+    "asr_self_attn_append_step": (_int, [_p, _i64, _p, _p, _i64, _p, _i64, _p, _int, _int, _int,
+                                         _int, _f, _p, _p, _sz, _p, _p]),
     "asr_cross_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _int, _int, _f,
                                    _p, _p, _sz, _p, _p]),
     "asr_gqa_step": (_int, [_p, _p, _p, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int, _int, _int,
@@ -146,6 +148,27 @@ def asr_self_attn_step(q, cache, lens, heads, head_dim, capacity, scale, out, ws
                                    B, heads, head_dim, capacity, float(scale), _ptr(out), wp, wn,
                                    _ptr(dev_err), _stream(stream))
     _check("asr_self_attn_step", st)
+
+
+def asr_self_attn_append_step(q, k_new, v_new, cache, lens, heads, head_dim, capacity, scale,
+                              out, ws, dev_err=None, stream=None):
+    """Fused append + self-attention.  q, k_new, v_new: f32 [B, >=H*hd] row
+    views (k_new and v_new share one row stride); cache: f16, sequence stride
+    cache.stride(0); lens: int32 [B]; out: f32 [B, H*hd]."""
+    import torch
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (out, "out")):
+        _need(t, torch.float32, n)
+    _need(cache, torch.float16, "cache")
+    _need(lens, torch.int32, "lens")
+    if k_new.stride(0) != v_new.stride(0):
+        raise ValueError("k_new and v_new must share the row stride")
+    B = lens.shape[0]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_self_attn_append_step(_ptr(q), q.stride(0), _ptr(k_new), _ptr(v_new),
+                                          k_new.stride(0), _ptr(cache), cache.stride(0),
+                                          _ptr(lens), B, heads, head_dim, capacity, float(scale),
+                                          _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_self_attn_append_step", st)
 
 
 def asr_cross_attn_step(q, cross, group, G, max_beams, heads, head_dim, frames, scale, out, ws,

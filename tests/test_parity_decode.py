@@ -191,6 +191,50 @@ def test_self_attn_repeat_calls_identical():
     assert np.all(cnt == 0)
 
 
+@pytest.mark.parametrize("B,H,hd,cap,lens", SELF_CASES + [(4, 2, 64, 30, [1, 2, 29, 30])])
+def test_self_attn_append_step_matches_oracle(B, H, hd, cap, lens):
+    """Fused append + attend: the cache bytes equal the oracle's append, the
+    output the oracle's attention over rows [0, lens)."""
+    qkv, cache0, lens = _self_case(B, H, hd, cap, lens, 260 + B + H)
+    d = H * hd
+    ref_cache = cache0.copy()
+    oracle.kv_append(qkv[:, d:2 * d], qkv[:, 2 * d:], ref_cache, lens - 1, H, hd)
+    ref, bad = oracle.self_attn_step(qkv, ref_cache, lens, H, hd, hd ** -0.5, q_stride=3 * d)
+    assert bad == 0
+    q = dev(qkv)
+    cache = dev(cache0)
+    out = torch.full((B, d), float("nan"), device="cuda")
+    ws = ops.workspace(ops.OP_SELF_ATTN, B, B, 1, H, hd)
+    err = new_err()
+    for _ in range(2):   # a repeat rewrites the same row and returns the same output
+        ops.asr_self_attn_append_step(q[:, :d], q[:, d:2 * d], q[:, 2 * d:], cache, dev(lens), H,
+                                      hd, cap, hd ** -0.5, out, ws, dev_err=err)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_u16(cache), ref_cache)
+        assert_attn_close(host(out), ref, f"self+append B={B} H={H} hd={hd}")
+    assert int(err.item()) == 0
+
+
+def test_self_attn_append_bad_lengths():
+    B, H, hd, cap = 3, 2, 64, 20
+    qkv, cache0, _ = _self_case(B, H, hd, cap, [1] * B, 270)
+    lens = np.array([0, 21, 5], np.int32)
+    d = H * hd
+    q = dev(qkv)
+    cache = dev(cache0)
+    out = torch.full((B, d), float("nan"), device="cuda")
+    ws = ops.workspace(ops.OP_SELF_ATTN, B, B, 1, H, hd)
+    err = new_err()
+    ops.asr_self_attn_append_step(q[:, :d], q[:, d:2 * d], q[:, 2 * d:], cache, dev(lens), H, hd,
+                                  cap, hd ** -0.5, out, ws, dev_err=err)
+    torch.cuda.synchronize()
+    got = host(out)
+    assert np.all(got[:2] == 0) and int(err.item()) == ops.DEVERR_LEN
+    ref_cache = cache0.copy()
+    oracle.kv_append(qkv[2:, d:2 * d], qkv[2:, 2 * d:], ref_cache[2:], lens[2:] - 1, H, hd)
+    assert np.array_equal(host_u16(cache), ref_cache)      # rows of bad sequences untouched
+
+
 # ------------------------------------------------------ cross-attention --
 
 CROSS_CASES = [
