@@ -60,6 +60,7 @@ enum asr_status {
   ASR_ERR_ALIAS = 4,       /* rearrange source and destination overlap */
   ASR_ERR_WORKSPACE = 5,   /* workspace NULL, too small or not 256-byte aligned */
   ASR_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+  ASR_ERR_SCRATCH_LIMIT = 7, /* the problem needs more scratch than the library's fixed array */
 };
 
 /* Bits OR-ed into *dev_err by the kernels. */
@@ -194,6 +195,30 @@ int asr_kv_rearrange(const uint16_t* src, uint16_t* dst, int64_t seq_stride, int
                      int n_layers, int row_elems, int capacity, const int32_t* idx,
                      const int32_t* lens_src, int32_t* lens_dst, int B, int32_t* dev_err,
                      asr_stream_t stream);
+
+/* Self-attention without a caller workspace (no counterpart in the pages: it
+ * is a convenience of this library).  For callers that cannot allocate device
+ * memory for a workspace -- a plugin whose host owns every allocation and
+ * forbids allocating while it enqueues work, a real-time audio thread that
+ * must not wait on an allocator, or a small C program that would rather not
+ * size a buffer.  Same arguments, result and errors as asr_self_attn_step,
+ * minus ws/ws_bytes: the scratch is a fixed array of
+ * asr_noalloc_scratch_bytes() (8 MiB) bytes in device memory, held by every
+ * GPU that loads the library until the process exits.  A problem whose
+ * workspace (asr_workspace_size(ASR_OP_SELF_ATTN, B, B, 1, heads, head_dim, 0))
+ * exceeds it is rejected with ASR_ERR_SCRATCH_LIMIT.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Each call
+ * enqueues a small memset (the counters) and the kernel, and allocates
+ * nothing.  All calls on a device share the array: calls that can overlap on
+ * the GPU (unordered streams) race and give wrong results. */
+int asr_self_attn_step_noalloc(const float* q, int64_t q_stride, const uint16_t* cache,
+                               int64_t seq_stride, const int32_t* lens, int B, int heads,
+                               int head_dim, int capacity, float scale, float* out,
+                               int32_t* dev_err, asr_stream_t stream);
+
+/* Size in bytes of the fixed scratch array of asr_self_attn_step_noalloc. */
+size_t asr_noalloc_scratch_bytes(void);
 
 /* Workspace bytes needed by an attention entry point on the CURRENT device
  * (its SM count sets the number of key-range pieces).  op: asr_op;

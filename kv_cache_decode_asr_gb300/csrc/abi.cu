@@ -61,6 +61,7 @@ extern "C" const char* asr_status_string(int status) {
     case ASR_ERR_ALIAS: return "source and destination overlap";
     case ASR_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case ASR_ERR_CUDA: return "CUDA error";
+    case ASR_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed scratch array";
     default: return "unknown status";
   }
 }

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(HERE, "libasrkv.so")
 
 ASR_OK = 0
 STATUS = {0: "ASR_OK", 1: "ASR_ERR_INVALID_ARG", 2: "ASR_ERR_UNSUPPORTED",
-          3: "ASR_ERR_MISALIGNED", 4: "ASR_ERR_ALIAS", 5: "ASR_ERR_WORKSPACE", 6: "ASR_ERR_CUDA"}
+          3: "ASR_ERR_MISALIGNED", 4: "ASR_ERR_ALIAS", 5: "ASR_ERR_WORKSPACE", 6: "ASR_ERR_CUDA",
+          7: "ASR_ERR_SCRATCH_LIMIT"}
 DEVERR_LEN, DEVERR_INDEX, DEVERR_BEAMS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 OP_SELF_ATTN, OP_CROSS_ATTN, OP_GQA_STEP, OP_PREFILL_ATTN = 1, 2, 3, 4
 
@@ -36,6 +37,9 @@ SIGNATURES = {
     "asr_gqa_step": (_int, [_p, _p, _p, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int, _int, _int,
                             _f, _p, _p, _sz, _p, _p]),
     "asr_kv_rearrange": (_int, [_p, _p, _i64, _i64, _int, _int, _int, _p, _p, _p, _int, _p, _p]),
+    "asr_self_attn_step_noalloc": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _f, _p,
+                                          _p, _p]),
+    "asr_noalloc_scratch_bytes": (_sz, []),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -169,6 +173,28 @@ def asr_self_attn_append_step(q, k_new, v_new, cache, lens, heads, head_dim, cap
                                           _ptr(lens), B, heads, head_dim, capacity, float(scale),
                                           _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
     _check("asr_self_attn_append_step", st)
+
+
+def asr_self_attn_step_noalloc(q, cache, lens, heads, head_dim, capacity, scale, out,
+                               dev_err=None, stream=None):
+    """Self-attention with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate one); arguments as
+    asr_self_attn_step without ws."""
+    import torch
+    _need(q, torch.float32, "q")
+    _need(cache, torch.float16, "cache")
+    _need(lens, torch.int32, "lens")
+    _need(out, torch.float32, "out")
+    B = lens.shape[0]
+    st = load().asr_self_attn_step_noalloc(_ptr(q), q.stride(0), _ptr(cache), cache.stride(0),
+                                           _ptr(lens), B, heads, head_dim, capacity,
+                                           float(scale), _ptr(out), _ptr(dev_err),
+                                           _stream(stream))
+    _check("asr_self_attn_step_noalloc", st)
+
+
+def asr_noalloc_scratch_bytes():
+    return load().asr_noalloc_scratch_bytes()
 
 
 def asr_cross_attn_step(q, cross, group, G, max_beams, heads, head_dim, frames, scale, out, ws,

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     assert lib.asr_version() >= 100
-    for s in range(7):
+    for s in range(8):
         assert lib.asr_status_string(s)
     assert lib.asr_status_string(0) == b"ok"
     assert lib.asr_status_string(99) == b"unknown status"
