@@ -181,6 +181,7 @@ class WhisperStep:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
     separate_append = False
+    profile_kernel = "cross"
 
     # kernels launched by one step
     def launches(self):
@@ -240,10 +241,19 @@ class WhisperStep:
     kernel_file = "kv_cache_decode_asr_gb300/csrc/decode_attn.cu"
 
     def dominant_bytes_per_launch(self):
-        return self.bytes_per_layer()["cross"]
+        b = self.bytes_per_layer()
+        return b["self"] + b["append"] if self.profile_kernel == "self" else b["cross"]
 
     def dominant_call(self, l, stream=None):
-        self.cross_call(l, stream)
+        if self.profile_kernel == "self":
+            ops, d = self.ops, self.d
+            qkv = self.qkv[l]
+            ops.asr_self_attn_append_step(qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:],
+                                          self.cache[:, l], self.lens, self.H, self.hd, self.cap,
+                                          self.scale, self.out_self[l], self.ws_self,
+                                          dev_err=self.err, stream=stream)
+        else:
+            self.cross_call(l, stream)
 
     # per-step inputs and outputs for the end-to-end figure
     def host_io(self):
@@ -481,6 +491,9 @@ def run_ours(args):
     wl = make_workload(args.workload, device, rank, args.layers)
     if args.separate_append:
         wl.separate_append = True
+    if args.roofline_kernel != "default":
+        wl.profile_kernel = args.roofline_kernel
+        wl.dominant_kernel = f"roofline of the {args.roofline_kernel} kernel"
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
 
@@ -687,6 +700,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate-append", action="store_true",
                     help="Whisper: launch the K/V append and the self-attention separately")
+    ap.add_argument("--roofline-kernel", default="default", choices=["default", "cross", "self"],
+                    help="Whisper: which kernel the roofline object times (default: cross)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run fewer layers than the model has (small cases for profiling)")
     args = ap.parse_args()

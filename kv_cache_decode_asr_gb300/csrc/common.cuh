@@ -164,6 +164,17 @@ __device__ __forceinline__ uint4 f8_to_h8(const float* f) {
   return u;
 }
 
+// Atomic add with acquire-release semantics at GPU scope.  Preceded by a
+// CTA barrier, it publishes every write the CTA made before the barrier
+// (barriers are cumulative); followed by one, it makes other CTAs' published
+// writes visible to the whole CTA.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   return __ldcg(reinterpret_cast<const float4*>(p));
 }

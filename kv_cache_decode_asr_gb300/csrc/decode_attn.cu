@@ -361,6 +361,10 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     for (int i = 0; i < 16; ++i) ctl[i] = 0;
     fence_barrier_init();
   }
+  // Let the next kernel on the stream launch now: its CTAs take SMs as ours
+  // leave and wait (griddepcontrol.wait) for this grid to finish before they
+  // touch memory, so only its launch latency overlaps with our tail.
+  grid_launch_dependents();
   grid_dependency_wait();
 
   // ---- keys per source (off) and sequences per source (mst), then scans
@@ -593,18 +597,18 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
           if (li == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(m[qi], l[qi]);
         }
       }
-      __threadfence();
     }
+    // ticket: the barrier orders the CTA's partial writes before thread 0's
+    // release; the acquire side lets the last CTA read everyone's partials
     named_bar(1, n_cons);
     if (tid == 0) {
-      const int old = atomicAdd(&a.counters[g], 1);
+      const int old = atomic_add_acq_rel_gpu(&a.counters[g], 1);
       const int is_last = old == parts - 1;
-      if (is_last) atomicExch(&a.counters[g], 0);
+      if (is_last) a.counters[g] = 0;  // no other CTA touches it again in this launch
       ctl[1] = is_last;
     }
     named_bar(1, n_cons);
     if (ctl[1]) {
-      __threadfence();
       // row slot r merges pieces first + r, first + r + R, ...; then the
       // slots are merged like a tile's rows.  The running state registers are
       // reused: this CTA's own piece is already among the partials.
@@ -615,26 +619,49 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 #pragma unroll
         for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
       }
-      for (int kp = first + r; kp <= lastp; kp += R) {
-        const int64_t slot = (int64_t)kp + g;
+      // each round loads two pieces before merging them (one L2 round trip)
+      for (int kp = first + r; kp <= lastp; kp += 2 * R) {
+        const bool two = kp + R <= lastp;
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
           if (qi < nq) {
-            const int64_t pidx = (slot * a.max_members + qi / rep) * a.Hq + h * rep + qi % rep;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
-            const float mn = fmaxf(m[qi], ml.x);
+            const int64_t qoff = (int64_t)(qi / rep) * a.Hq + h * rep + qi % rep;
+            const int64_t p0 = ((int64_t)(kp + g) * a.max_members) * a.Hq + qoff;
+            const int64_t p1 = two ? ((int64_t)(kp + R + g) * a.max_members) * a.Hq + qoff : p0;
+            const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + p0 * 2));
+            const float2 ml1 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + p1 * 2));
+            float4 u[2][NCH][2];
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              const float* s0 = a.part_o + p0 * HD + LL::chunk_off(li, j, sw);
+              const float* s1 = a.part_o + p1 * HD + LL::chunk_off(li, j, sw);
+              u[0][j][0] = ld_cg_f4(s0);
+              u[0][j][1] = ld_cg_f4(s0 + 4);
+              u[1][j][0] = ld_cg_f4(s1);
+              u[1][j][1] = ld_cg_f4(s1 + 4);
+            }
+            const float m1 = two ? ml1.x : -INFINITY;
+            const float mn = fmaxf(m[qi], fmaxf(ml0.x, m1));
             if (mn != -INFINITY) {
-              const float ca = ex2(m[qi] - mn), cb = ex2(ml.x - mn);
-              l[qi] = l[qi] * ca + ml.y * cb;
-              const float2 ca2 = make_float2(ca, ca), cb2 = make_float2(cb, cb);
+              const float ca = ex2(m[qi] - mn), c0 = ex2(ml0.x - mn), c1 = ex2(m1 - mn);
+              l[qi] = l[qi] * ca + ml0.y * c0 + (two ? ml1.y * c1 : 0.f);
+              const float2 ca2 = make_float2(ca, ca), c02 = make_float2(c0, c0),
+                           c12 = make_float2(c1, c1);
 #pragma unroll
               for (int j = 0; j < NCH; ++j) {
-                const float* src = a.part_o + pidx * HD + LL::chunk_off(li, j, sw);
-                const float4 u0 = ld_cg_f4(src), u1 = ld_cg_f4(src + 4);
-                o[qi][4 * j] = ffma2(cb2, make_float2(u0.x, u0.y), fmul2(o[qi][4 * j], ca2));
-                o[qi][4 * j + 1] = ffma2(cb2, make_float2(u0.z, u0.w), fmul2(o[qi][4 * j + 1], ca2));
-                o[qi][4 * j + 2] = ffma2(cb2, make_float2(u1.x, u1.y), fmul2(o[qi][4 * j + 2], ca2));
-                o[qi][4 * j + 3] = ffma2(cb2, make_float2(u1.z, u1.w), fmul2(o[qi][4 * j + 3], ca2));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  float2 x0 = fmul2(o[qi][4 * j + 2 * e], ca2);
+                  float2 x1 = fmul2(o[qi][4 * j + 2 * e + 1], ca2);
+                  x0 = ffma2(c02, make_float2(u[0][j][e].x, u[0][j][e].y), x0);
+                  x1 = ffma2(c02, make_float2(u[0][j][e].z, u[0][j][e].w), x1);
+                  if (two) {
+                    x0 = ffma2(c12, make_float2(u[1][j][e].x, u[1][j][e].y), x0);
+                    x1 = ffma2(c12, make_float2(u[1][j][e].z, u[1][j][e].w), x1);
+                  }
+                  o[qi][4 * j + 2 * e] = x0;
+                  o[qi][4 * j + 2 * e + 1] = x1;
+                }
               }
               m[qi] = mn;
             }
@@ -815,10 +842,13 @@ static void* kernel_for(int HD, int vi) {
   return nullptr;
 }
 
-// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=36,smem_kb=110,ctas=0,R=0,rs=4"
-// overrides them (ctas / R = 0: chosen automatically; rs: rows per slot).
+// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64"
+// overrides them (ctas / R = 0: chosen automatically; rs: rows per slot;
+// min_kb: fewest K/V bytes one CTA takes).
+// Defaults (measured on GB300): one CTA per SM with about ten consumer
+// warps and two or more stages of large tiles.
 struct DecodeTune {
-  int tile_kb = 36, smem_kb = 110, ctas = 0, R = 0, rs = 4;
+  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64;
 };
 
 static DecodeTune decode_tune() {
@@ -834,6 +864,7 @@ static DecodeTune decode_tune() {
         else if (!strcmp(key, "ctas")) d.ctas = val;
         else if (!strcmp(key, "R")) d.R = val;
         else if (!strcmp(key, "rs")) d.rs = val;
+        else if (!strcmp(key, "min_kb")) d.min_kb = val;
         e += n;
         if (*e == ',') ++e;
       }
@@ -848,16 +879,16 @@ struct DecodePlan {
 };
 
 // Row slots R: the consumer count R * Hkv * G must be a multiple of 32 and
-// fit the variant's thread cap; among those, the largest R whose tile fits
-// tile_kb (else the smallest valid R).  Stages: as many as fit smem_kb, 2..8.
-// One CTA takes at least 64 KB of rows, so a source splits into a bounded
-// number of partial results.
+// fit the variant's thread cap (at most 320 consumers); among those, the
+// largest R whose tile fits tile_kb (else the smallest valid R).  Stages: as many as fit smem_kb, 2..8.
+// One CTA takes at least min_kb (64 KB) of rows, so a source splits into a
+// bounded number of partial results.
 static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_src,
                         DecodePlan& p) {
   const DecodeTune tune = decode_tune();
   const int G = HD / v.DPL;
   const int per_slot = Hkv * G;
-  const int budget = std::min(v.MAXT - 32, 512);
+  const int budget = std::min(v.MAXT - 32, 320);
   const int row_bytes = row_elems * 2;
   int best = 0, smallest = 0;
   for (int R = 1; R * per_slot <= budget; ++R) {
@@ -880,7 +911,8 @@ static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_
   p.stages = stages;
   p.smem = decode_smem_layout(stages, n_src, p.R, Hkv, v.NQ, HD, p.stage_elems).total;
   if (p.smem > 227 * 1024) return false;
-  p.min_share = std::max(p.tile_rows, (65536 + row_bytes - 1) / row_bytes);
+  const int min_bytes = std::max(tune.min_kb, 1) * 1024;
+  p.min_share = std::max(p.tile_rows, (min_bytes + row_bytes - 1) / row_bytes);
   return true;
 }
 

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const float* __restrict__ k, const float* __restrict__ v, int64_t src_row_stride,
     uint16_t* __restrict__ cache, int64_t seq_stride, const int32_t* __restrict__ slot, int B,
     int half_elems, int capacity, int32_t* dev_err) {
+  grid_launch_dependents();  // the next kernel may launch; it waits for our completion
   grid_dependency_wait();
   const int vec_per_half = half_elems >> 3;  // 8 f16 per 16-byte vector
   const int64_t total = (int64_t)B * 2 * vec_per_half;
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kRearrangeThreads) kv_rearrange_kernel(
     int64_t layer_stride, int n_layers, int row_elems, int capacity,
     const int32_t* __restrict__ idx, const int32_t* __restrict__ lens_src,
     int32_t* __restrict__ lens_dst, int B, int32_t* dev_err) {
+  grid_launch_dependents();  // the next kernel may launch; it waits for our completion
   grid_dependency_wait();
   const int b = blockIdx.y / n_layers;
   const int l = blockIdx.y % n_layers;
