@@ -61,6 +61,8 @@ def _lib():
                                         _i32p, _int]),
             "orc_prefill_attn": (_int, [_u16p, _u16p, _u16p, _f32p, _f32p, _dbl, _dbl, _int, _int,
                                         _int, _int, _int, _dbl, _u16p, _i64, _int, _f64p, _u16p]),
+            "orc_prefill_prep": (_int, [_u16p, _u16p, _u16p, _f32p, _f32p, _dbl, _dbl, _int, _int,
+                                        _int, _int, _int, _u16p, _i64, _int, _u16p]),
             "orc_prefill_attn_rows": (None, [_u16p, _i32p, _int, _u16p, _int, _int, _int, _int,
                                              _dbl, _f64p]),
         }
@@ -274,6 +276,28 @@ def prefill_attn(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_heads,
     return out, qhat
 
 
+def prefill_prep(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_heads, head_dim,
+                 cache):
+    """Prefill preparation only: cache rows [0,T) written in place (normed and
+    roped K, V copied); returns qhat uint16 [B, T, Hq*hd]."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    wq = _c(np.ascontiguousarray(q_norm_w, np.float32), np.float32)
+    wk = _c(np.ascontiguousarray(k_norm_w, np.float32), np.float32)
+    cache = _c(cache, np.uint16)
+    B, T = q.shape[0], q.shape[1]
+    qhat = np.empty((B, T, q_heads * head_dim), np.uint16)
+    rc = _lib().orc_prefill_prep(_p(q, ctypes.c_uint16), _p(k, ctypes.c_uint16),
+                                 _p(v, ctypes.c_uint16), _p(wq, ctypes.c_float),
+                                 _p(wk, ctypes.c_float), float(eps), float(rope_base), B, T,
+                                 q_heads, kv_heads, head_dim, _p(cache, ctypes.c_uint16),
+                                 cache[0].size, cache.shape[1], _p(qhat, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError("T exceeds the cache capacity")
+    return qhat
+
+
 def prefill_attn_rows(qhat_rows, t_of_row, seq_cache, q_heads, kv_heads, head_dim, head, scale):
     """Causal attention for selected query rows of one (sequence, head):
     qhat_rows uint16 [n, hd] (normed+roped f16 queries), t_of_row int32 [n],
@@ -297,7 +321,7 @@ def build():
 __all__ = [
     "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
     "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
-    "kv_rearrange", "prefill_attn", "prefill_attn_rows", "build",
+    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "build",
 ]
 
 if os.environ.get("ORACLE_THREADS"):

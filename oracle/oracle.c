@@ -498,22 +498,20 @@ static void orc_prefill_item(void* vctx, int64_t item) {
   free(z);
 }
 
-/* Batched prefill (decoder.h build_prefill_graph_batched; lib.linnet
- * DecoderLayer.prefill): every prompt position t in [0,T) of every sequence
- * gets q^ = f16(RoPE(RMSNorm(q, w_q), t)) and k^ = f16(RoPE(RMSNorm(k, w_k), t));
- * cache row t = k^ || v (v copied as given), then causal attention of q^ over
- * rows [0, t].  q, k, v are f16 [B][T][H*hd].  The f16 rounding of q^ and k^
- * is part of the definition here because they are the f16 matrix operands.
- * qhat_out (may be NULL) receives q^.  Returns 0, or -1 if T > capacity. */
-int orc_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+/* Prefill preparation (decoder.h build_prefill_graph_batched: positions
+ * 0..T-1, K/V into rows [0, T)): every prompt position t in [0,T) of every
+ * sequence gets q^ = f16(RoPE(RMSNorm(q, w_q), t)) and
+ * k^ = f16(RoPE(RMSNorm(k, w_k), t)); cache row t = k^ || v (v copied as
+ * given).  q, k, v are f16 [B][T][H*hd]; qhat receives q^ [B][T][Hq*hd].
+ * The f16 rounding of q^ and k^ is part of the definition here because they
+ * are the f16 matrix operands.  Returns 0, or -1 if T > capacity. */
+int orc_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      const float* q_norm_w, const float* k_norm_w, double eps, double rope_base,
-                     int B, int T, int q_heads, int kv_heads, int head_dim, double scale,
-                     uint16_t* cache, int64_t seq_stride, int capacity, double* out,
-                     uint16_t* qhat_out) {
+                     int B, int T, int q_heads, int kv_heads, int head_dim, uint16_t* cache,
+                     int64_t seq_stride, int capacity, uint16_t* qhat) {
   if (T > capacity) return -1;
   int hd = head_dim;
   int64_t qw = (int64_t)q_heads * hd, kw = (int64_t)kv_heads * hd;
-  uint16_t* qhat = qhat_out ? qhat_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * T * qw);
   double* wq = (double*)malloc(sizeof(double) * hd);
   double* wk = (double*)malloc(sizeof(double) * hd);
   double* x = (double*)malloc(sizeof(double) * hd);
@@ -545,14 +543,31 @@ int orc_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
       for (int64_t i = 0; i < kw; ++i) row[kw + i] = vs[i];
     }
   }
-  orc_prefill_ctx c = {qhat, cache, seq_stride, B, T, q_heads, kv_heads, hd, scale, out};
-  orc_parallel_for((int64_t)B * q_heads, orc_prefill_item, &c);
-  if (!qhat_out) free(qhat);
   free(wq);
   free(wk);
   free(x);
   free(xn);
   free(xr);
+  return 0;
+}
+
+/* Batched prefill (decoder.h build_prefill_graph_batched; lib.linnet
+ * DecoderLayer.prefill): orc_prefill_prep, then causal attention of q^ at
+ * position t over cache rows [0, t] for every t, sequence and query head.
+ * qhat_out (may be NULL) receives q^.  Returns 0, or -1 if T > capacity. */
+int orc_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* q_norm_w, const float* k_norm_w, double eps, double rope_base,
+                     int B, int T, int q_heads, int kv_heads, int head_dim, double scale,
+                     uint16_t* cache, int64_t seq_stride, int capacity, double* out,
+                     uint16_t* qhat_out) {
+  if (T > capacity) return -1;
+  int64_t qw = (int64_t)q_heads * head_dim;
+  uint16_t* qhat = qhat_out ? qhat_out : (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * T * qw);
+  orc_prefill_prep(q, k, v, q_norm_w, k_norm_w, eps, rope_base, B, T, q_heads, kv_heads,
+                   head_dim, cache, seq_stride, capacity, qhat);
+  orc_prefill_ctx c = {qhat, cache, seq_stride, B, T, q_heads, kv_heads, head_dim, scale, out};
+  orc_parallel_for((int64_t)B * q_heads, orc_prefill_item, &c);
+  if (!qhat_out) free(qhat);
   return 0;
 }
 

@@ -411,6 +411,10 @@ def test_prefill_rows_equal_steps(oracle_mod):
                                       np.zeros_like(cache))
     assert np.array_equal(out2[:, :5], out[:, :5])
     assert not np.allclose(out2[:, 5:], out[:, 5:])
+    # the preparation alone writes the same cache and queries
+    cache_p = np.zeros_like(cache)
+    qhat_p = oracle_mod.prefill_prep(q, k, v, wq, wk, 1e-6, 1e6, Hq, Hkv, hd, cache_p)
+    assert np.array_equal(cache_p, cache) and np.array_equal(qhat_p, qhat)
     # sampled rows through the per-row entry point agree
     ts = np.array([0, 3, 8], np.int32)
     rows = oracle_mod.prefill_attn_rows(qhat[1, ts, 3 * hd:4 * hd], ts, cache[1], Hq, Hkv, hd, 3,
