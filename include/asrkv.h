@@ -196,6 +196,31 @@ int asr_kv_rearrange(const uint16_t* src, uint16_t* dst, int64_t seq_stride, int
                      const int32_t* lens_src, int32_t* lens_dst, int B, int32_t* dev_err,
                      asr_stream_t stream);
 
+/* a7 + a8 -- batched causal prefill of a Qwen3-ASR-style decoder.
+ * Defines: "transcribe.cpp, src/arch/qwen3_asr/decoder.h", header comment
+ * (per-head Q/K RMSNorm after projection and before RoPE; NeoX RoPE at
+ * freq_base 1e6; GQA) and PrefillBuildBatched (positions shared 0..T-1, K/V
+ * written to cache rows [0, T), shared causal mask); "Nest whisper-tiny,
+ * src/lib.linnet", DecoderLayer.prefill (write_span at 0, causal mask).
+ *   For every sequence b and position t < T:
+ *   q^_t,h = f16(RoPE_t(RMSNorm(q_t,h) * q_norm_w)), k^_t,h likewise with k_norm_w;
+ *   cache row t = k^_t || v_t  (v copied bitwise);
+ *   out_t,h = sum_{j<=t} softmax_j(scale * q^_t,h . k^_j,kvh(h)) v_j,kvh(h)
+ * The f16 rounding of q^ and k^ is part of the operation (they are the
+ * tensor-core operands); the softmax weights enter the P.V product as f16.
+ * q: f16 [B][T][q_heads*128]; k, v: f16 [B][T][kv_heads*128]; q_norm_w,
+ * k_norm_w: fp32 [128]; cache: f16 [B][seq_stride] (rows of 2*kv_heads*128);
+ * out: fp32 [B][T][q_heads*128].  head_dim must be 128; kv_heads <= 16;
+ * q_heads % kv_heads == 0; T <= capacity.  Runs on the tensor cores
+ * (tcgen05); needs an sm_100-family GPU.
+ * ws: asr_workspace_size(ASR_OP_PREFILL_ATTN, B, kv_heads, 1, q_heads, 128, T)
+ * bytes (n_sources = kv_heads for this op); need not be zeroed. */
+int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* q_norm_w, const float* k_norm_w, float eps, float rope_base,
+                     int B, int T, int q_heads, int kv_heads, int head_dim, float scale,
+                     uint16_t* cache, int64_t seq_stride, int capacity, float* out, void* ws,
+                     size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device
  * memory for a workspace -- a plugin whose host owns every allocation and
@@ -222,8 +247,8 @@ size_t asr_noalloc_scratch_bytes(void);
 
 /* Workspace bytes needed by an attention entry point on the CURRENT device
  * (its SM count sets the number of key-range pieces).  op: asr_op;
- * n_sources: sequences (self, GQA) or groups (cross); max_beams: 1 except for
- * cross; T: prompt length (prefill only).  Returns 0 for invalid arguments
+ * n_sources: sequences (self, GQA), groups (cross) or KV heads (prefill);
+ * max_beams: 1 except for cross; T: prompt length (prefill only).  Returns 0 for invalid arguments
  * or when no CUDA device is usable. */
 size_t asr_workspace_size(int op, int B, int n_sources, int max_beams, int q_heads, int head_dim,
                           int T);

@@ -4,6 +4,7 @@
 
 #include "common.cuh"
 #include "decode_attn.cuh"
+#include "tcgen05.cuh"
 
 namespace asrkv {
 
@@ -34,7 +35,13 @@ using namespace asrkv;
 
 extern "C" size_t asr_workspace_size(int op, int B, int n_sources, int max_beams, int q_heads,
                                      int head_dim, int T) {
-  (void)T;
+  if (op == ASR_OP_PREFILL_ATTN) {
+    // n_sources is the number of KV heads here
+    if (B < 1 || B > ASR_MAX_BATCH || T < 1 || n_sources < 1 || n_sources > 16 || q_heads < 1 ||
+        q_heads % n_sources != 0 || head_dim != 128)
+      return 0;
+    return prefill_ws_bytes(B, T, q_heads, n_sources);
+  }
   if (B < 0 || n_sources < 1 || n_sources > ASR_MAX_BATCH || max_beams < 1 ||
       max_beams > ASR_MAX_BEAMS || q_heads < 1 || (head_dim != 64 && head_dim != 128))
     return 0;

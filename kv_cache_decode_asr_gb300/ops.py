@@ -40,6 +40,8 @@ SIGNATURES = {
     "asr_self_attn_step_noalloc": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _f, _p,
                                           _p, _p]),
     "asr_noalloc_scratch_bytes": (_sz, []),
+    "asr_prefill_attn": (_int, [_p, _p, _p, _p, _p, _f, _f, _int, _int, _int, _int, _int, _f, _p,
+                                _i64, _int, _p, _p, _sz, _p, _p]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -227,6 +229,25 @@ def asr_gqa_step(q, k_new, v_new, q_norm_w, k_norm_w, eps, rope_base, n_past, ca
                              cache.stride(0), capacity, B, q_heads, kv_heads, head_dim,
                              float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
     _check("asr_gqa_step", st)
+
+
+def asr_prefill_attn(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_heads, head_dim,
+                     scale, cache, capacity, out, ws, dev_err=None, stream=None):
+    """q: f16 [B, T, Hq*hd]; k, v: f16 [B, T, Hkv*hd]; cache: f16 with sequence
+    stride cache.stride(0); out: f32 [B, T, Hq*hd]; ws from
+    workspace(OP_PREFILL_ATTN, B, kv_heads, 1, q_heads, head_dim, T)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cache, "cache")):
+        _need(t, torch.float16, n)
+    for t, n in ((q_norm_w, "q_norm_w"), (k_norm_w, "k_norm_w"), (out, "out")):
+        _need(t, torch.float32, n)
+    B, T = q.shape[0], q.shape[1]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_prefill_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
+                                 float(eps), float(rope_base), B, T, q_heads, kv_heads, head_dim,
+                                 float(scale), _ptr(cache), cache.stride(0), capacity, _ptr(out),
+                                 wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_prefill_attn", st)
 
 
 def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["asr_kv_append", "asr_self_attn_step", "asr_self_attn_append_step",
-              "asr_cross_attn_step", "asr_gqa_step",
+              "asr_cross_attn_step", "asr_gqa_step", "asr_prefill_attn",
               "asr_kv_rearrange", "asr_workspace_size", "asr_status_string", "asr_version"]:
         assert n in names
 
