@@ -49,6 +49,19 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def load_all_peaks():
+    """HBM GB/s and dense bf16 TFLOP/s (burst) with where they came from."""
+    hbm, src = load_peaks()
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            tf = float(json.load(f)["bf16_tflops"])
+        tsrc = "measured bf16_tflops (burst)"
+    except Exception:
+        tf, tsrc = 1900.0, "fallback bf16 burst"
+    return {"hbm": (hbm, src), "tensor": (tf, tsrc)}
+
+
 def source_sha(rel):
     with open(os.path.join(ROOT, rel), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -293,6 +306,27 @@ class WhisperStep:
     def gpu_layer_outputs(self, l):
         return {"self": self.out_self[l].cpu().numpy(), "cross": self.out_cross[l].cpu().numpy()}
 
+    def oracle_sample(self, i, oracle):
+        """(oracle seconds, fraction of the step, reference, gpu) for layer i."""
+        dt, ref = self.oracle_layer(i, oracle)
+        return dt, 1.0 / self.L, ref, self.gpu_layer_outputs(i), f"layer {i}"
+
+    def n_samples(self):
+        return self.L
+
+    metric = "decode-attn tokens/s (K/V HBM GB/s and fraction of HBM peak alongside)"
+
+    def tokens_per_step(self):
+        return self.B
+
+    def roofline(self, launch_ms, peaks):
+        peak, src = peaks["hbm"]
+        b = self.dominant_bytes_per_launch()
+        achieved = b / (launch_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "bytes_per_launch": b,
+                "peak_source": f"{src} hbm_gbs"}
+
     # one small reference-arm unit: one sequence of one layer
     def oracle_unit(self, i, oracle, cache):
         l = i % self.L
@@ -404,6 +438,20 @@ class GqaStep:
     def gpu_layer_outputs(self, l):
         return {"gqa": self.out[l].cpu().numpy()}
 
+    def oracle_sample(self, i, oracle):
+        dt, ref = self.oracle_layer(i, oracle)
+        return dt, 1.0 / self.L, ref, self.gpu_layer_outputs(i), f"layer {i}"
+
+    def n_samples(self):
+        return self.L
+
+    metric = WhisperStep.metric
+
+    def tokens_per_step(self):
+        return self.B
+
+    roofline = WhisperStep.roofline
+
     def oracle_unit(self, i, oracle, cache):
         import torch
         l = i % self.L
@@ -427,6 +475,120 @@ class GqaStep:
         return self.B * self.L
 
 
+class PrefillStep:
+    """Qwen3-ASR batched prefill: RMSNorm + RoPE + cache write (a7) and the
+    causal tensor-core attention (a8) of B prompts of T tokens, one layer."""
+
+    dominant = "prefill_attention"
+    dominant_kernel = "prefill_attn_kernel (tcgen05, asr_prefill_attention)"
+    kernel_file = "kv_cache_decode_asr_gb300/csrc/prefill.cu"
+    metric = "prefill tokens/s (tensor-core TFLOP/s and fraction of the f16 peak alongside)"
+
+    def __init__(self, name, cfg, device, rank=0):
+        import torch
+        from kv_cache_decode_asr_gb300 import ops
+        self.name, self.cfg, self.ops = name, cfg, ops
+        wi = WORKLOAD_INDEX[name] + 100 * rank
+        B, T, Hq, Hkv, hd = cfg["B"], cfg["T"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
+        self.B, self.T, self.Hq, self.Hkv, self.hd, self.cap = B, T, Hq, Hkv, hd, cfg["capacity"]
+        self.L = 1
+        self.row = 2 * Hkv * hd
+        self.scale = hd ** -0.5
+        self.eps, self.base = cfg["eps"], cfg["rope_base"]
+        f16 = torch.float16
+        self.q = syn.dev_normal((B, T, Hq * hd), syn.seed_for(wi, 1), device, dtype=f16)
+        self.k = syn.dev_normal((B, T, Hkv * hd), syn.seed_for(wi, 2), device, dtype=f16)
+        self.v = syn.dev_normal((B, T, Hkv * hd), syn.seed_for(wi, 3), device, dtype=f16)
+        self.wq = syn.dev_normal((hd,), syn.seed_for(wi, 4), device, mean=cfg["w_mean"],
+                                 std=cfg["w_std"])
+        self.wk = syn.dev_normal((hd,), syn.seed_for(wi, 5), device, mean=cfg["w_mean"],
+                                 std=cfg["w_std"])
+        self.cache = torch.zeros(B, self.cap, self.row, dtype=f16, device=device)
+        self.out = torch.zeros(B, T, Hq * hd, device=device)
+        self.ws = ops.workspace(ops.OP_PREFILL_ATTN, B, Hkv, 1, Hq, hd, T, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def launches(self):
+        return 2
+
+    def step(self, stream=None):
+        self.ops.asr_prefill_attn(self.q, self.k, self.v, self.wq, self.wk, self.eps, self.base,
+                                  self.Hq, self.Hkv, self.hd, self.scale, self.cache, self.cap,
+                                  self.out, self.ws, dev_err=self.err, stream=stream)
+
+    def dominant_call(self, l, stream=None):
+        self.ops.asr_prefill_attention(self.B, self.T, self.Hq, self.Hkv, self.hd, self.scale,
+                                       self.cache, self.cap, self.out, self.ws, dev_err=self.err,
+                                       stream=stream)
+
+    def flops(self):
+        """Causal attention FLOPs: QK^T and PV over the keys at or below each query."""
+        return 4 * self.B * self.Hq * self.hd * self.T * (self.T + 1) // 2
+
+    def kv_bytes_per_step(self):
+        """Bytes the prefill must move: q, k, v in (f16), cache rows written,
+        output written (fp32)."""
+        return (self.B * self.T * (self.Hq + 2 * self.Hkv) * self.hd * 2
+                + self.B * self.T * self.row * 2 + self.B * self.T * self.Hq * self.hd * 4)
+
+    def tokens_per_step(self):
+        return self.B * self.T
+
+    def roofline(self, launch_ms, peaks):
+        peak, src = peaks["tensor"]
+        f = self.flops()
+        achieved = f / (launch_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "flops_per_launch": f,
+                "peak_source": f"{src} (dense f16 taken equal to bf16, the nominal ratio 1:1)"}
+
+    def host_io(self):
+        return [self.q, self.k, self.v], [self.out]
+
+    def n_samples(self):
+        return self.B
+
+    def oracle_sample(self, i, oracle):
+        """The whole prefill of sequence i (all heads and positions)."""
+        import torch
+        h16 = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        q, k, v = h16(self.q[i:i + 1]), h16(self.k[i:i + 1]), h16(self.v[i:i + 1])
+        wq, wk = self.wq.cpu().numpy(), self.wk.cpu().numpy()
+        cache = np.zeros((1, self.cap, self.row), np.uint16)
+        t0 = time.perf_counter()
+        ref, _ = oracle.prefill_attn(q, k, v, wq, wk, self.eps, self.base, self.Hq, self.Hkv,
+                                     self.hd, self.scale, cache)
+        dt = time.perf_counter() - t0
+        return dt, 1.0 / self.B, {"out": ref[0]}, {"out": self.out[i].cpu().numpy()}, \
+            f"sequence {i}"
+
+    def oracle_unit(self, i, oracle, cache):
+        """Reference-arm unit: one head of one sequence (its causal attention
+        over all positions, plus its share of the preparation)."""
+        import torch
+        b = (i // self.Hq) % self.B
+        h = i % self.Hq
+        if b not in cache:
+            h16 = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            q, k, v = h16(self.q[b:b + 1]), h16(self.k[b:b + 1]), h16(self.v[b:b + 1])
+            c = np.zeros((1, self.cap, self.row), np.uint16)
+            t0 = time.perf_counter()
+            qhat = oracle.prefill_prep(q, k, v, self.wq.cpu().numpy(), self.wk.cpu().numpy(),
+                                       self.eps, self.base, self.Hq, self.Hkv, self.hd, c)
+            prep_s = time.perf_counter() - t0
+            cache.clear()
+            cache[b] = (qhat, c, prep_s)
+        qhat, c, prep_s = cache[b]
+        ts = np.arange(self.T, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill_attn_rows(qhat[0, :, h * self.hd:(h + 1) * self.hd], ts, c[0], self.Hq,
+                                 self.Hkv, self.hd, h, self.scale)
+        return time.perf_counter() - t0 + prep_s / self.Hq
+
+    def units_per_step(self):
+        return self.B * self.Hq
+
+
 def make_workload(name, device, rank=0, layers=0):
     cfg = dict(syn.WORKLOADS[name])
     if layers:
@@ -435,6 +597,8 @@ def make_workload(name, device, rank=0, layers=0):
         return WhisperStep(name, cfg, device, rank)
     if cfg["kind"] == "gqa":
         return GqaStep(name, cfg, device, rank)
+    if cfg["kind"] == "prefill":
+        return PrefillStep(name, cfg, device, rank)
     raise SystemExit(f"workload {name}: not a decode-step bench line")
 
 
@@ -530,7 +694,7 @@ def run_ours(args):
     ms_total = ev0.elapsed_time(ev1)
     ms_total = max_over_ranks(ms_total, world, device)
     ms_step = ms_total / args.steps
-    tokens = wl.B * world
+    tokens = wl.tokens_per_step() * world
     value = tokens / (ms_step / 1e3)
     kv_bytes = wl.kv_bytes_per_step()
     kv_gbs = kv_bytes * world / (ms_step / 1e3) / 1e9
@@ -538,12 +702,12 @@ def run_ours(args):
     # ---- dominant kernel: a CUDA graph of back-to-back launches of it, one
     # per layer (each on its own layer's data, together larger than L2),
     # timed with CUDA events on the launching stream; average per launch
-    peak, peak_src = load_peaks()
+    peaks = load_all_peaks()
     dom_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(dom_graph, stream=stream):
         for l in range(wl.L):
             wl.dominant_call(l)
-    reps = max(3, 2000 // max(wl.L, 1))
+    reps = max(3, min(200, 2000 // max(wl.L, 1)))
     with torch.cuda.stream(stream):
         for _ in range(3):
             dom_graph.replay()
@@ -555,9 +719,9 @@ def run_ours(args):
         d1.record(stream)
     d1.synchronize()
     launch_ms = d0.elapsed_time(d1) / (reps * wl.L)
-    dom_bytes = wl.dominant_bytes_per_launch()
-    achieved = dom_bytes / (launch_ms / 1e3) / 1e9
-    traffic = recorded_traffic(wl.kernel_file, args.workload)
+    roof = wl.roofline(launch_ms, peaks)
+    roof.update({"traffic": recorded_traffic(wl.kernel_file, args.workload),
+                 "kernel": wl.dominant_kernel, "launch_us": launch_ms * 1e3})
 
     # ---- end to end through host buffers: per step, H2D of the step's
     # activations from pinned memory, the step, D2H of its outputs
@@ -586,32 +750,35 @@ def run_ours(args):
     if int(wl.err.item()) != 0:
         raise RuntimeError(f"device error flags {int(wl.err.item()):#x}")
 
-    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only); its layer
-    # outputs double as a parity check of the timed kernels
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only); its outputs
+    # double as a parity check of the timed kernels
     cpu = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_count()
         oracle.set_threads(threads)
         budget = args.cpu_seconds
-        spent, layers_done, max_err = 0.0, 0, 0.0
-        while layers_done < wl.L and (layers_done == 0 or spent < budget):
-            dt, ref = wl.oracle_layer(layers_done, oracle)
-            got = wl.gpu_layer_outputs(layers_done)
+        spent, frac, max_err, done = 0.0, 0.0, 0.0, []
+        i = 0
+        while i < wl.n_samples() and (i == 0 or spent < budget):
+            dt, f, ref, got, what = wl.oracle_sample(i, oracle)
             for k in ref:
                 max_err = max(max_err, float(np.abs(got[k] - ref[k]).max()))
             spent += dt
-            layers_done += 1
-        step_s = spent / layers_done * wl.L
-        cpu = {"value": wl.B / step_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{layers_done} of {wl.L} layers, all {wl.B} sequences, "
-                         f"{spent:.1f} s of oracle time, scaled to the {wl.L}-layer step"}
-        parity = {"max_abs_err": max_err, "checked": f"outputs of {layers_done} layers vs oracle",
+            frac += f
+            done.append(what)
+            i += 1
+        step_s = spent / frac
+        cpu = {"value": wl.tokens_per_step() / step_s, "unit": "tokens/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{len(done)} of {wl.n_samples()} units ({done[0]} .. {done[-1]}), "
+                         f"{spent:.1f} s of oracle time, scaled to the whole step"}
+        parity = {"max_abs_err": max_err, "checked": f"outputs of {len(done)} units vs oracle",
                   "tolerance": 2e-3}
 
     if rank == 0:
         line = {
-            "metric": "decode-attn tokens/s (K/V HBM GB/s and fraction of HBM peak alongside)",
+            "metric": wl.metric,
             "value": value,
             "unit": "tokens/s",
             "n_gpus": world,
@@ -628,12 +795,9 @@ def run_ours(args):
                              f"vs {L2_BYTES / 1e6:.0f} MB L2)",
                        "parallelism": f"replicas x{world} (batch per GPU fixed)"},
             "kv_gbs": kv_gbs,
-            "kv_frac_of_hbm": kv_gbs / world / peak,
+            "kv_frac_of_hbm": kv_gbs / world / peaks["hbm"][0],
             "kv_bytes_per_step": kv_bytes,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": wl.dominant_kernel, "bytes_per_launch": dom_bytes,
-                         "launch_us": launch_ms * 1e3, "peak_source": f"{peak_src} hbm_gbs"},
+            "roofline": roof,
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -671,18 +835,18 @@ def run_reference(args):
     times = [wl.oracle_unit(args.warmup + i, oracle, cache) for i in range(args.steps)]
     unit_s = sum(times) / len(times)
     step_s = unit_s * wl.units_per_step()
-    value = wl.B / step_s
+    value = wl.tokens_per_step() / step_s
     line = {
         "impl": "reference",
-        "metric": "decode-attn tokens/s (K/V HBM GB/s and fraction of HBM peak alongside)",
+        "metric": wl.metric,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded N(0,1); no weights or audio)",
         "config": {"workload": args.workload, **wl.cfg},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: one sequence of one layer, "
-                                   f"x{wl.units_per_step()} for the whole step"},
+                         "sample": f"each step: one unit ({wl.units_per_step()} per "
+                                   f"workload step), scaled to the whole step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

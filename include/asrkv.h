@@ -221,6 +221,22 @@ int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      uint16_t* cache, int64_t seq_stride, int capacity, float* out, void* ws,
                      size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
+/* a7 alone -- the prefill preparation of asr_prefill_attn: cache rows [0, T)
+ * (roped K, V) and, in the workspace, q^ and V transposed for the tensor
+ * cores.  Same arguments and definitions as asr_prefill_attn. */
+int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* q_norm_w, const float* k_norm_w, float eps, float rope_base,
+                     int B, int T, int q_heads, int kv_heads, int head_dim, uint16_t* cache,
+                     int64_t seq_stride, int capacity, void* ws, size_t ws_bytes,
+                     asr_stream_t stream);
+
+/* a8 alone -- the causal attention of asr_prefill_attn, reading what
+ * asr_prefill_prep left in the cache and the workspace (same workspace,
+ * unchanged in between). */
+int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, int head_dim, float scale,
+                          const uint16_t* cache, int64_t seq_stride, int capacity, float* out,
+                          void* ws, size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device
  * memory for a workspace -- a plugin whose host owns every allocation and

@@ -13,15 +13,17 @@
 //   row t and also written transposed (keys contiguous, zero-padded to a
 //   multiple of 128) to the workspace, so both matrix products below read
 //   K-major operands.
-// a8 attention (5th-generation tensor cores): one CTA per (128-query tile,
-//   sequence, query head), heaviest tiles first.  Q, K and V^T tiles arrive by
-//   tiled TMA with the 128-byte swizzle; S = Q K^T and O += P V are
-//   tcgen05.mma kind::f16 (f16 operands, fp32 accumulators in tensor memory,
-//   256 columns: S then O).  128 threads own one query row each: they read S
-//   from TMEM, run the online softmax in fp32 (log2 domain), rescale O in TMEM
-//   when the row maximum grows, and write P (f16) to shared memory in the
-//   swizzled K-major layout the next MMA reads.  Only key tiles at or below
-//   the diagonal are visited (causal), the diagonal tile is masked.
+// a8 attention (5th-generation tensor cores): one CTA per (pair of 128-query
+//   tiles, sequence, query head), warp-specialised.  Q, K and V^T tiles
+//   arrive by tiled TMA with the 128-byte swizzle; S = Q K^T (128 x 64 per
+//   key tile) and O += P V are tcgen05.mma kind::f16 (f16 operands, fp32
+//   accumulators in tensor memory).  Two softmax warpgroups (one per query
+//   tile, one thread per query row) read S from TMEM, run the online softmax
+//   in fp32 (log2 domain), rescale O in TMEM only when a row maximum grows by
+//   more than 2^8 (the normalisation at the end is exact either way), and
+//   write P (f16) to shared memory in the swizzled K-major layout the next MMA
+//   reads, so the tensor core works on one tile while the other is softmaxed.
+//   Only key tiles at or below the diagonal are visited (causal).
 #include <math.h>
 
 #include <mutex>
@@ -144,46 +146,78 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
 // ------------------------------------------------------------- attention --
 
 struct PrefillAttnArgs {
-  int B, T, Hq, Hkv, n_qt;
+  int B, T, Hq, Hkv, n_qt, n_pairs;
   float sl2e;   // scale * log2(e)
   float* out;   // [B][T][Hq*128] fp32
   int32_t* dev_err;
 };
 
-constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 f16 operand tile
-constexpr int kAttnSmem = 6 * kTileBytes + 1024 + 1024;
+constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16
+constexpr int kKTile = 64 * 128 * 2;      // 64 keys x 128 dims
+constexpr int kVTile = 128 * 64 * 2;      // V^T: 128 dims x 64 keys
+constexpr int kPTile = 128 * 64 * 2;      // P: 128 queries x 64 keys
+constexpr int kKVStages = 3;
+constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + 2 * kPTile + 1024 + 1024;
+constexpr int kAttnThreads = 320;         // warps 0-3, 4-7: softmax of tiles A, B; 8: TMA; 9: MMA
+constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two query tiles of one (sequence, head) per CTA: tile A = pair p and tile
+// B = n_qt-1-p, so every CTA sees n_qt+1 tiles of 128 keys (a lone middle
+// tile when n_qt is odd).  Roles: warpgroups 0 and 1 (warps 0-7) run the
+// softmax of tiles A and B (warp w reads TMEM lanes 32*(w%4)..+31), warp 8
+// owns the TMEM allocation and its lane 0 issues the TMA loads (Q once, K and
+// V^T per 64-key tile through a 3-stage ring), warp 9 lane 0 issues the MMAs.  While one warpgroup turns its S into P, the tensor core
+// works on the other tile's S or PV.
+__global__ void __launch_bounds__(kAttnThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1024-byte alignment for the swizzled tiles
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;                    // [2 K-halves][128 rows][128 B]
-  unsigned char* sK = smem + kTileBytes;       // 2 stages
-  unsigned char* sV = smem + 3 * kTileBytes;   // 2 stages (V^T: rows = dims, K = keys)
-  unsigned char* sP = smem + 5 * kTileBytes;   // P: rows = queries, K = keys
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * kTileBytes);  // q, kv0, kv1, mma
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
-  int* abort_flag = reinterpret_cast<int*>(tslot + 1);
+  unsigned char* sQ = smem;                                  // [A, B] x 32 KB
+  unsigned char* sK = sQ + 2 * kQTile;                       // stages x 16 KB
+  unsigned char* sV = sK + kKVStages * kKTile;               // stages x 16 KB
+  unsigned char* sP = sV + kKVStages * kVTile;               // [A, B] x 16 KB
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + 2 * kPTile);
+  uint64_t* q_full = bar;                  // 1
+  uint64_t* kv_full = bar + 1;             // kKVStages
+  uint64_t* kv_empty = kv_full + kKVStages;
+  uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of tile i, buffer j % 2
+  uint64_t* p_full = s_full + 4;            // [A, B]
+  uint64_t* o_done = p_full + 2;            // [A, B]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 2);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int BH = a.B * a.Hq;
-  const int qt = a.n_qt - 1 - (int)(blockIdx.x / BH);  // longest rows of tiles first
-  const int rem = (int)(blockIdx.x % BH);
-  const int b = rem / a.Hq, h = rem % a.Hq;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pair = (int)(blockIdx.x % a.n_pairs);
+  const int bh = (int)(blockIdx.x / a.n_pairs);
+  const int b = bh / a.Hq, h = bh % a.Hq;
   const int kvh = h / (a.Hq / a.Hkv);
-  const int q0 = qt * 128;
-  const int n_kv = qt + 1;  // causal: key tiles 0 .. qt
-  const int qidx = q0 + tid;  // this thread's query row
+  const int qt_a = pair, qt_b = a.n_qt - 1 - pair;
+  const bool two = qt_b != qt_a;
+  // 64-key tiles each query tile visits (causal: up to its last row)
+  const int nA = 2 * (qt_a + 1), nB = two ? 2 * (qt_b + 1) : 0;
+  const int n = nA > nB ? nA : nB;
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
-    *abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kKVStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&o_done[i], 1);
+    }
     fence_barrier_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tslot, 256);
+  if (warp == 8) {
+    tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
   grid_launch_dependents();
@@ -192,145 +226,202 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tO = tbase + 128;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  constexpr uint32_t kIdesc = mma_idesc_f16_f32(128, 128);
-  const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV), aP = smem_addr(sP);
+  // TMEM columns: S of tile i, buffer u at 64*(2i+u) (0..255), O_A 256..383,
+  // O_B 384..511.  S is double-buffered so the tensor core computes S(j+1)
+  // while the softmax works on S(j).
+  auto tS = [&](int i, int u) { return tbase + 64u * (2 * i + u); };
+  auto tO = [&](int i) { return tbase + 256u + 128u * i; };
 
-  auto load_kv = [&](int j, int s) {
-    mbar_arrive_expect_tx(&bars[1 + s], 2 * kTileBytes);
-    tma_load_3d(sK + s * kTileBytes, &tk, kvh * 128, j * 128, b, &bars[1 + s]);
-    tma_load_3d(sK + s * kTileBytes + kTileBytes / 2, &tk, kvh * 128 + 64, j * 128, b, &bars[1 + s]);
-    tma_load_3d(sV + s * kTileBytes, &tv, j * 128, 0, b * a.Hkv + kvh, &bars[1 + s]);
-    tma_load_3d(sV + s * kTileBytes + kTileBytes / 2, &tv, j * 128 + 64, 0, b * a.Hkv + kvh,
-                &bars[1 + s]);
-  };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bars[0], kTileBytes);
-    tma_load_3d(sQ, &tq, h * 128, q0, b, &bars[0]);
-    tma_load_3d(sQ + kTileBytes / 2, &tq, h * 128 + 64, q0, b, &bars[0]);
-    load_kv(0, 0);
-    if (n_kv > 1) load_kv(1, 1);
-  }
-
-  float m_i = -INFINITY, l_i = 0.f;
-  uint32_t mma_phase = 0;
-  float v[32];
-  for (int j = 0; j < n_kv; ++j) {
-    const int s = j & 1;
-    // ---- S = Q K^T
-    if (tid == 0) {
-      bool ok = (j > 0 || mbar_wait(&bars[0], 0)) && mbar_wait(&bars[1 + s], (j >> 1) & 1);
-      if (!ok) {
-        set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      } else {
-        tc_fence_after_sync();
+  if (warp == 8) {
+    // ======================================================= TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, two ? 2 * kQTile : kQTile);
+      tma_load_3d(sQ, &tq, h * 128, qt_a * 128, b, q_full);
+      tma_load_3d(sQ + kQTile / 2, &tq, h * 128 + 64, qt_a * 128, b, q_full);
+      if (two) {
+        tma_load_3d(sQ + kQTile, &tq, h * 128, qt_b * 128, b, q_full);
+        tma_load_3d(sQ + kQTile + kQTile / 2, &tq, h * 128 + 64, qt_b * 128, b, q_full);
+      }
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kKVStages;
+        if (j >= kKVStages && !mbar_wait(&kv_empty[s], ((j / kKVStages) - 1) & 1)) {
+          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[s], kKTile + kVTile);
+        tma_load_3d(sK + s * kKTile, &tk, kvh * 128, j * 64, b, &kv_full[s]);
+        tma_load_3d(sK + s * kKTile + kKTile / 2, &tk, kvh * 128 + 64, j * 64, b, &kv_full[s]);
+        tma_load_3d(sV + s * kVTile, &tv, j * 64, 0, b * a.Hkv + kvh, &kv_full[s]);
+      }
+    }
+  } else if (warp == 9) {
+    // ======================================================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
+      constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
+      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV),
+                     aP = smem_addr(sP);
+      bool ok = mbar_wait(q_full, 0) && mbar_wait(&kv_full[0], 0);
+      auto issue_s = [&](int i, int j) {
+        const int s = j % kKVStages;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_f16(tS, sw128_kmajor_desc(aQ + off), sw128_kmajor_desc(aK + s * kTileBytes + off),
-                  kIdesc, kk > 0);
+          const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
+          mma_f16(tS(i, j & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
+                  sw128_kmajor_desc(aK + s * kKTile + koff), kIdS, kk > 0);
+        }
+        mma_commit(&s_full[2 * i + (j & 1)]);
+      };
+      auto issue_pv = [&](int i, int j) {
+        const int s = j % kKVStages;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tO(i), sw128_kmajor_desc(aP + i * kPTile + kk * 32),
+                  sw128_kmajor_desc(aV + s * kVTile + kk * 32), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&o_done[i]);
+      };
+      if (ok) {
+        // S runs two tiles ahead of PV: S(j+2) reuses S buffer j%2, free once
+        // the softmax of tile j has signalled P(j)
+        tc_fence_after_sync();
+        issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
+        if (n > 1) {
+          ok = mbar_wait(&kv_full[1 % kKVStages], 0);
+          tc_fence_after_sync();
+          if (ok && 1 < nA) issue_s(0, 1);
+          if (ok && 1 < nB) issue_s(1, 1);
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const bool next2 = j + 2 < n;
+          if (next2) {
+            ok = mbar_wait(&kv_full[(j + 2) % kKVStages], ((j + 2) / kKVStages) & 1);
+            tc_fence_after_sync();
+          }
+          if (ok && j < nA) {
+            ok = mbar_wait(&p_full[0], j & 1);
+            tc_fence_after_sync();
+            if (ok) issue_pv(0, j);
+            if (ok && j + 2 < nA) issue_s(0, j + 2);
+          }
+          if (ok && j < nB) {
+            ok = mbar_wait(&p_full[1], j & 1);
+            tc_fence_after_sync();
+            if (ok) issue_pv(1, j);
+          }
+          mma_commit(&kv_empty[j % kKVStages]);  // stage free once these MMAs finish
+          if (ok && j + 2 < nB) issue_s(1, j + 2);
         }
       }
-      mma_commit(&bars[3]);
+      if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
     }
-    if (!mbar_wait(&bars[3], mma_phase)) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-    mma_phase ^= 1u;
-    tc_fence_after_sync();
-    const int kbase = j * 128;
-    // ---- row maximum of this tile (causal mask: key <= query)
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      tmem_ld32(tS + lane_off + c * 32, v);
+  } else {
+    // ======================================================= softmax
+    const int i = warp >> 2;                  // 0: tile A, 1: tile B
+    const int ni = i == 0 ? nA : nB;
+    const int row = tid - i * 128;            // 0..127: TMEM lane = query row
+    const int q0 = (i == 0 ? qt_a : qt_b) * 128;
+    const int qidx = q0 + row;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    unsigned char* prow = sP + i * kPTile + row * 128;
+    float m = -INFINITY, l = 0.f;
+    float v[32], w[32];
+    bool ok = true;
+    for (int j = 0; j < ni && ok; ++j) {
+      ok = mbar_wait(&s_full[2 * i + (j & 1)], (j >> 1) & 1);
+      // MMAs of one issuer complete in issue order and S(j) is issued after
+      // PV(j-1): this wait is normally already satisfied.  After it, O and
+      // the P buffer are free.
+      if (j > 0) ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
+      tc_fence_after_sync();
+      tmem_ld32(tS(i, j & 1) + lane_off, v);
+      tmem_ld32(tS(i, j & 1) + lane_off + 32, w);
       tmem_wait_ld();
+      const int key0 = j * 64;
+      const bool edge = key0 + 63 > q0;  // some keys of this tile lie past some rows
+      if (edge) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (kbase + c * 32 + i <= qidx) tmax = fmaxf(tmax, v[i] * a.sl2e);
+        for (int c = 0; c < 32; ++c) {
+          if (key0 + c > qidx) v[c] = -INFINITY;
+          if (key0 + 32 + c > qidx) w[c] = -INFINITY;
+        }
+      }
+      // row max as a tree (independent partial maxima)
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(w[e], w[e + 8]));
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        mx[e] = fmaxf(mx[e], fmaxf(fmaxf(v[e + 16], v[e + 24]), fmaxf(w[e + 16], w[e + 24])));
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      tmax *= a.sl2e;
+      // rescale O only when the row max grew by more than 2^8
+      const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
+      const bool grow = j > 0 && m_new != m;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float alpha = grow ? ex2f(m - m_new) : 1.0f;
+        float o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tO(i) + lane_off + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tO(i) + lane_off + c * 32, o);
+        }
+        tmem_wait_st();
+        l *= alpha;
+      }
+      m = m_new;
+      // P = 2^(S*c - m) (masked entries are -inf, so 0), as eight swizzled
+      // 16-byte chunks; the row sum in four independent partial sums
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float* src = c < 4 ? v + 8 * c : w + 8 * (c - 4);
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float p0 = ex2f(fmaf(src[e], a.sl2e, -m));
+          const float p1 = ex2f(fmaf(src[e + 1], a.sl2e, -m));
+          ls[e / 2] += p0 + p1;
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      fence_async_shared();
+      tc_fence_before_sync();
+      named_bar(1 + i, 128);
+      if (row == 0) mbar_arrive(&p_full[i]);
     }
-    const float m_new = fmaxf(m_i, tmax);
-    // ---- rescale O when the maximum grew (warp-collective TMEM access)
-    const bool grow = j > 0 && m_new > m_i;
-    const float alpha = grow ? exp2f(m_i - m_new) : 1.0f;
-    if (__any_sync(0xffffffffu, grow)) {
+    if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    // ---- O / l to global memory once the last PV is done
+    if (ni > 0 && ok && mbar_wait(&o_done[i], (ni - 1) & 1)) {
+      tc_fence_after_sync();
+      const float inv = 1.0f / l;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tO + lane_off + c * 32, v);
+        tmem_ld32(tO(i) + lane_off + c * 32, v);
         tmem_wait_ld();
+        if (qidx < a.T) {
+          float* dst = a.out + (((int64_t)b * a.T + qidx) * a.Hq + h) * kPrefillHD + c * 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(tO + lane_off + c * 32, v);
-      }
-      tmem_wait_st();
-    }
-    l_i *= alpha;
-    // ---- P = exp2(S - m) as f16, written K-major with the 128-byte swizzle
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      tmem_ld32(tS + lane_off + c * 32, v);
-      tmem_wait_ld();
-      uint32_t packed[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float p0 = (kbase + c * 32 + i <= qidx) ? exp2f(v[i] * a.sl2e - m_new) : 0.f;
-        const float p1 = (kbase + c * 32 + i + 1 <= qidx) ? exp2f(v[i + 1] * a.sl2e - m_new) : 0.f;
-        l_i += p0 + p1;
-        const __half2 hp = __halves2half2(__float2half_rn(p0), __float2half_rn(p1));
-        packed[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-      }
-      // keys c*32 .. c*32+31: K-half c/2, 16-byte chunks 4*(c%2) .. 4*(c%2)+3 of the row
-      unsigned char* rowp = sP + (c >> 1) * (kTileBytes / 2) + tid * 128;
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        const int chunk = ((c & 1) * 4 + qd) ^ (tid & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-            make_uint4(packed[4 * qd], packed[4 * qd + 1], packed[4 * qd + 2], packed[4 * qd + 3]);
-      }
-    }
-    m_i = m_new;
-    fence_async_shared();
-    tc_fence_before_sync();
-    __syncthreads();
-    // ---- O += P V
-    if (tid == 0) {
-      tc_fence_after_sync();
-      if (!*abort_flag) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_f16(tO, sw128_kmajor_desc(aP + off), sw128_kmajor_desc(aV + s * kTileBytes + off),
-                  kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) =
+                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
         }
       }
-      mma_commit(&bars[3]);
-    }
-    if (!mbar_wait(&bars[3], mma_phase)) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-    mma_phase ^= 1u;
-    tc_fence_after_sync();
-    // stage s is free again (both products that read it are done)
-    if (tid == 0 && j + 2 < n_kv && !*abort_flag) load_kv(j + 2, s);
-  }
-
-  // ---- O / l to global memory (rows past T are not written)
-  const float inv = 1.0f / l_i;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    tmem_ld32(tO + lane_off + c * 32, v);
-    tmem_wait_ld();
-    if (qidx < a.T) {
-      float* dst = a.out + (((int64_t)b * a.T + qidx) * a.Hq + h) * kPrefillHD + c * 32;
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(dst + i) =
-            make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
     }
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 8) {
     tc_fence_after_sync();
-    tmem_dealloc(tbase, 256);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -383,53 +474,53 @@ static std::once_flag g_prefill_attr;
 
 using namespace asrkv;
 
-extern "C" int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                const float* q_norm_w, const float* k_norm_w, float eps,
-                                float rope_base, int B, int T, int q_heads, int kv_heads,
-                                int head_dim, float scale, uint16_t* cache, int64_t seq_stride,
-                                int capacity, float* out, void* ws, size_t ws_bytes,
-                                int32_t* dev_err, asr_stream_t stream) {
-  if (B < 0 || B > ASR_MAX_BATCH || T < 1 || q_heads < 1 || kv_heads < 1 || capacity < 1 ||
-      !(eps >= 0.f) || !(rope_base > 0.f))
+// Checks shared by the prefill entry points (host only, before any launch).
+static int prefill_check(int B, int T, int q_heads, int kv_heads, int head_dim, int capacity,
+                         const void* cache, int64_t seq_stride, void* ws, size_t ws_bytes) {
+  if (B < 0 || B > ASR_MAX_BATCH || T < 1 || q_heads < 1 || kv_heads < 1 || capacity < 1)
     return ASR_ERR_INVALID_ARG;
   if (head_dim != kPrefillHD || q_heads % kv_heads != 0 || kv_heads > 16 || q_heads > 64)
     return ASR_ERR_UNSUPPORTED;
   if (T > capacity) return ASR_ERR_INVALID_ARG;
   if (B == 0) return ASR_OK;
-  if (!q || !k || !v || !q_norm_w || !k_norm_w || !cache || !out) return ASR_ERR_INVALID_ARG;
-  const int64_t row = 2LL * kv_heads * head_dim;
-  if (seq_stride < (int64_t)capacity * row) return ASR_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cache) || !aligned16(out) ||
-      seq_stride % 8 != 0)
-    return ASR_ERR_MISALIGNED;
-  if ((int64_t)B * T * q_heads * head_dim >= (1LL << 40)) return ASR_ERR_UNSUPPORTED;
+  if (!cache) return ASR_ERR_INVALID_ARG;
+  if (seq_stride < (int64_t)capacity * 2 * kv_heads * head_dim) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(cache) || seq_stride % 8 != 0) return ASR_ERR_MISALIGNED;
   if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < prefill_ws_bytes(B, T, q_heads, kv_heads))
     return ASR_ERR_WORKSPACE;
-  const int Tpad = round_up(T, 128);
-  uint16_t* qhat = static_cast<uint16_t*>(ws);
-  uint16_t* vt = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) +
-                                             align_up((size_t)B * T * q_heads * kPrefillHD * 2, 1024));
-  cudaError_t attr = cudaSuccess;
-  std::call_once(g_prefill_attr, [&] {
+  return ASR_OK;
+}
+
+static cudaError_t prefill_attrs() {
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(g_prefill_attr, [] {
     attr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kAttnSmem);
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   100 * 1024);
   });
-  if (attr != cudaSuccess) return ASR_ERR_CUDA;
+  return attr;
+}
 
-  // tensor maps: q^ (dims: Hq*128, T, B), cache (row, capacity, B), V^T (Tpad, 128, B*Hkv)
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_f16_3d(&tq, qhat, (uint64_t)q_heads * kPrefillHD, T, B,
-                        (uint64_t)q_heads * kPrefillHD * 2, (uint64_t)T * q_heads * kPrefillHD * 2,
-                        64, 128) ||
-      !make_tmap_f16_3d(&tk, cache, (uint64_t)row, capacity, B, (uint64_t)row * 2,
-                        (uint64_t)seq_stride * 2, 64, 128) ||
-      !make_tmap_f16_3d(&tv, vt, Tpad, kPrefillHD, (uint64_t)B * kv_heads, (uint64_t)Tpad * 2,
-                        (uint64_t)Tpad * kPrefillHD * 2, 64, 128))
-    return ASR_ERR_CUDA;
+static uint16_t* ws_vt(void* ws, int B, int T, int q_heads) {
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) +
+                                     align_up((size_t)B * T * q_heads * kPrefillHD * 2, 1024));
+}
 
+extern "C" int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const float* q_norm_w, const float* k_norm_w, float eps,
+                                float rope_base, int B, int T, int q_heads, int kv_heads,
+                                int head_dim, uint16_t* cache, int64_t seq_stride, int capacity,
+                                void* ws, size_t ws_bytes, asr_stream_t stream) {
+  if (!(eps >= 0.f) || !(rope_base > 0.f)) return ASR_ERR_INVALID_ARG;
+  int st = prefill_check(B, T, q_heads, kv_heads, head_dim, capacity, cache, seq_stride, ws,
+                         ws_bytes);
+  if (st != ASR_OK || B == 0) return st;
+  if (!q || !k || !v || !q_norm_w || !k_norm_w) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return ASR_ERR_MISALIGNED;
+  if (prefill_attrs() != cudaSuccess) return ASR_ERR_CUDA;
+  const int Tpad = round_up(T, 128);
   PrepArgs pa = {};
   pa.q = q;
   pa.k = k;
@@ -444,26 +535,71 @@ extern "C" int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint
   pa.Hkv = kv_heads;
   pa.cache = cache;
   pa.seq_stride = seq_stride;
-  pa.qhat = qhat;
-  pa.vt = vt;
+  pa.qhat = static_cast<uint16_t*>(ws);
+  pa.vt = ws_vt(ws, B, T, q_heads);
   for (int i = 0; i < kPrefillHD / 2; ++i)
     pa.theta[i] = pow((double)rope_base, -2.0 * i / kPrefillHD);
   const size_t prep_smem =
       2 * kPrepT * (kPrefillHD / 2) * sizeof(float) + (size_t)kPrepT * kv_heads * kPrefillHD * 2;
   cudaError_t e = launch_pdl(prefill_prep_kernel, dim3(Tpad / kPrepT, B), dim3(256), prep_smem,
                              (cudaStream_t)stream, pa);
-  if (e != cudaSuccess) return ASR_ERR_CUDA;
+  return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
+}
 
+extern "C" int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, int head_dim,
+                                     float scale, const uint16_t* cache, int64_t seq_stride,
+                                     int capacity, float* out, void* ws, size_t ws_bytes,
+                                     int32_t* dev_err, asr_stream_t stream) {
+  int st = prefill_check(B, T, q_heads, kv_heads, head_dim, capacity, cache, seq_stride, ws,
+                         ws_bytes);
+  if (st != ASR_OK || B == 0) return st;
+  if (!out) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(out)) return ASR_ERR_MISALIGNED;
+  if (prefill_attrs() != cudaSuccess) return ASR_ERR_CUDA;
+  const int Tpad = round_up(T, 128);
+  const int64_t row = 2LL * kv_heads * kPrefillHD;
+  // tensor maps: q^ (dims: Hq*128, T, B), cache (row, capacity, B), V^T (Tpad, 128, B*Hkv)
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_f16_3d(&tq, ws, (uint64_t)q_heads * kPrefillHD, T, B,
+                        (uint64_t)q_heads * kPrefillHD * 2, (uint64_t)T * q_heads * kPrefillHD * 2,
+                        64, 128) ||
+      !make_tmap_f16_3d(&tk, cache, (uint64_t)row, capacity, B, (uint64_t)row * 2,
+                        (uint64_t)seq_stride * 2, 64, 64) ||
+      !make_tmap_f16_3d(&tv, ws_vt(ws, B, T, q_heads), Tpad, kPrefillHD, (uint64_t)B * kv_heads,
+                        (uint64_t)Tpad * 2, (uint64_t)Tpad * kPrefillHD * 2, 64, 128))
+    return ASR_ERR_CUDA;
   PrefillAttnArgs aa = {};
   aa.B = B;
   aa.T = T;
   aa.Hq = q_heads;
   aa.Hkv = kv_heads;
   aa.n_qt = (T + 127) / 128;
+  aa.n_pairs = (aa.n_qt + 1) / 2;
   aa.sl2e = scale * kLog2eP;
   aa.out = out;
   aa.dev_err = dev_err;
-  e = launch_pdl(prefill_attn_kernel, dim3(aa.n_qt * B * q_heads), dim3(128), (size_t)kAttnSmem,
-                 (cudaStream_t)stream, tq, tk, tv, aa);
+  cudaError_t e = launch_pdl(prefill_attn_kernel, dim3(aa.n_pairs * B * q_heads),
+                             dim3(kAttnThreads), (size_t)kAttnSmem, (cudaStream_t)stream, tq, tk,
+                             tv, aa);
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
+}
+
+extern "C" int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const float* q_norm_w, const float* k_norm_w, float eps,
+                                float rope_base, int B, int T, int q_heads, int kv_heads,
+                                int head_dim, float scale, uint16_t* cache, int64_t seq_stride,
+                                int capacity, float* out, void* ws, size_t ws_bytes,
+                                int32_t* dev_err, asr_stream_t stream) {
+  // every check of both stages first, so that a rejected call enqueues nothing
+  if (!(eps >= 0.f) || !(rope_base > 0.f)) return ASR_ERR_INVALID_ARG;
+  int st = prefill_check(B, T, q_heads, kv_heads, head_dim, capacity, cache, seq_stride, ws,
+                         ws_bytes);
+  if (st != ASR_OK || B == 0) return st;
+  if (!q || !k || !v || !q_norm_w || !k_norm_w || !out) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ASR_ERR_MISALIGNED;
+  st = asr_prefill_prep(q, k, v, q_norm_w, k_norm_w, eps, rope_base, B, T, q_heads, kv_heads,
+                        head_dim, cache, seq_stride, capacity, ws, ws_bytes, stream);
+  if (st != ASR_OK) return st;
+  return asr_prefill_attention(B, T, q_heads, kv_heads, head_dim, scale, cache, seq_stride,
+                               capacity, out, ws, ws_bytes, dev_err, stream);
 }

@@ -42,6 +42,10 @@ SIGNATURES = {
     "asr_noalloc_scratch_bytes": (_sz, []),
     "asr_prefill_attn": (_int, [_p, _p, _p, _p, _p, _f, _f, _int, _int, _int, _int, _int, _f, _p,
                                 _i64, _int, _p, _p, _sz, _p, _p]),
+    "asr_prefill_prep": (_int, [_p, _p, _p, _p, _p, _f, _f, _int, _int, _int, _int, _int, _p,
+                                _i64, _int, _p, _sz, _p]),
+    "asr_prefill_attention": (_int, [_int, _int, _int, _int, _int, _f, _p, _i64, _int, _p, _p,
+                                     _sz, _p, _p]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -248,6 +252,31 @@ def asr_prefill_attn(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_he
                                  float(scale), _ptr(cache), cache.stride(0), capacity, _ptr(out),
                                  wp, wn, _ptr(dev_err), _stream(stream))
     _check("asr_prefill_attn", st)
+
+
+def asr_prefill_prep(q, k, v, q_norm_w, k_norm_w, eps, rope_base, q_heads, kv_heads, head_dim,
+                     cache, capacity, ws, stream=None):
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cache, "cache")):
+        _need(t, torch.float16, n)
+    B, T = q.shape[0], q.shape[1]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_prefill_prep(_ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
+                                 float(eps), float(rope_base), B, T, q_heads, kv_heads, head_dim,
+                                 _ptr(cache), cache.stride(0), capacity, wp, wn, _stream(stream))
+    _check("asr_prefill_prep", st)
+
+
+def asr_prefill_attention(B, T, q_heads, kv_heads, head_dim, scale, cache, capacity, out, ws,
+                          dev_err=None, stream=None):
+    import torch
+    _need(cache, torch.float16, "cache")
+    _need(out, torch.float32, "out")
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_prefill_attention(B, T, q_heads, kv_heads, head_dim, float(scale), _ptr(cache),
+                                      cache.stride(0), capacity, _ptr(out), wp, wn, _ptr(dev_err),
+                                      _stream(stream))
+    _check("asr_prefill_attention", st)
 
 
 def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["asr_kv_append", "asr_self_attn_step", "asr_self_attn_append_step",
-              "asr_cross_attn_step", "asr_gqa_step", "asr_prefill_attn",
+              "asr_cross_attn_step", "asr_gqa_step", "asr_prefill_attn", "asr_prefill_prep",
+              "asr_prefill_attention",
               "asr_kv_rearrange", "asr_workspace_size", "asr_status_string", "asr_version"]:
         assert n in names
 
@@ -143,3 +144,20 @@ def test_rearrange_rejects(lib):
     assert f(*base(row=4)) == INVALID
     assert f(*base(B=0)) == OK
     assert f(*base(nl=1100)) in (INVALID, UNSUP)
+
+
+def test_prefill_rejects(lib):
+    f = lib.asr_prefill_attn
+    row = 2 * 8 * 128
+    args = lambda **kw: [A16, A16, A16, A16, A16, ctypes.c_float(1e-6), ctypes.c_float(1e6),
+                         kw.get("B", 8), kw.get("T", 1536), 16, kw.get("hkv", 8), kw.get("hd", 128),
+                         ctypes.c_float(0.088), A16b, kw.get("ss", 1536 * row),
+                         kw.get("cap", 1536), P(0x40000), P(0x50000), ctypes.c_size_t(1 << 30),
+                         None, None]
+    assert f(*args(hd=64)) == UNSUP
+    assert f(*args(hkv=32)) == UNSUP
+    assert f(*args(T=1537)) == INVALID          # T beyond the capacity
+    assert f(*args(T=0)) == INVALID
+    assert f(*args(ss=1536 * row - 8)) == INVALID
+    assert f(*args(ss=1536 * row + 4)) == MISAL
+    assert f(*args(B=0)) == OK
