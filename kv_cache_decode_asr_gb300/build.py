@@ -16,6 +16,9 @@ ROOT = os.path.dirname(HERE)
 HEADERS = [os.path.join(ROOT, "include", "asrkv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# per-file flags: the prefill attention kernel runs 576 threads per CTA, so its
+# registers are capped to keep 576 x regs within one SM's 65536
+EXTRA = {"prefill.cu": ["-maxrregcount=112"]}
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]
 
@@ -59,7 +62,8 @@ def build(force=False, verbose=False):
         log = obj + ".log"
         objs.append(obj)
         fh = open(log, "w")
-        p = subprocess.Popen([cc, *ARCH, *FLAGS, "-c", src, "-o", obj], stdout=fh,
+        extra = EXTRA.get(os.path.basename(src), [])
+        p = subprocess.Popen([cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj], stdout=fh,
                              stderr=subprocess.STDOUT)
         procs.append((p, fh, log, src))
     failed = []

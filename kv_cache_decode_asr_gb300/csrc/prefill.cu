@@ -21,8 +21,9 @@
 //   tile, one thread per query row) read S from TMEM, run the online softmax
 //   in fp32 (log2 domain), rescale O in TMEM only when a row maximum grows by
 //   more than 2^8 (the normalisation at the end is exact either way), and
-//   write P (f16) to shared memory in the swizzled K-major layout the next MMA
-//   reads, so the tensor core works on one tile while the other is softmaxed.
+//   write P (f16) back into tensor memory over its S buffer, where the PV MMA
+//   reads it as its A operand; S/P are double-buffered, so the tensor core
+//   works on one tile while the other is softmaxed.
 //   Only key tiles at or below the diagonal are visited (causal).
 #include <math.h>
 
@@ -155,10 +156,9 @@ struct PrefillAttnArgs {
 constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16
 constexpr int kKTile = 64 * 128 * 2;      // 64 keys x 128 dims
 constexpr int kVTile = 128 * 64 * 2;      // V^T: 128 dims x 64 keys
-constexpr int kPTile = 128 * 64 * 2;      // P: 128 queries x 64 keys
 constexpr int kKVStages = 3;
-constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + 2 * kPTile + 1024 + 1024;
-constexpr int kAttnThreads = 320;         // warps 0-3, 4-7: softmax of tiles A, B; 8: TMA; 9: MMA
+constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + 4096 + 1024 + 1024;
+constexpr int kAttnThreads = 576;  // warps 0-7, 8-15: softmax of tiles A, B; 16: TMA; 17: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -169,28 +169,32 @@ __device__ __forceinline__ float ex2f(float x) {
 
 // Two query tiles of one (sequence, head) per CTA: tile A = pair p and tile
 // B = n_qt-1-p, so every CTA sees n_qt+1 tiles of 128 keys (a lone middle
-// tile when n_qt is odd).  Roles: warpgroups 0 and 1 (warps 0-7) run the
-// softmax of tiles A and B (warp w reads TMEM lanes 32*(w%4)..+31), warp 8
-// owns the TMEM allocation and its lane 0 issues the TMA loads (Q once, K and
-// V^T per 64-key tile through a 3-stage ring), warp 9 lane 0 issues the MMAs.  While one warpgroup turns its S into P, the tensor core
+// tile when n_qt is odd).  Roles: warps 0-7 and 8-15 run the softmax of
+// tiles A and B, two threads per query row (warp w reads TMEM lanes
+// 32*(w%4)..+31; warps w and w+4 take the two halves of the row's keys and of
+// its O columns, and exchange their partial row maxima through shared
+// memory); warp 16 owns the TMEM allocation and its lane 0 issues the TMA
+// loads (Q once, K and V^T per 64-key tile through a 3-stage ring); warp 17
+// lane 0 issues the MMAs.  While one warpgroup turns its S into P, the tensor core
 // works on the other tile's S or PV.
-__global__ void __launch_bounds__(kAttnThreads, 1)
-    prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+// Launched with kAttnThreads threads; prefill.cu is compiled with a register
+// cap (build.py) that keeps kAttnThreads x registers within one SM's file.
+__global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char* sQ = smem;                                  // [A, B] x 32 KB
   unsigned char* sK = sQ + 2 * kQTile;                       // stages x 16 KB
   unsigned char* sV = sK + kKVStages * kKTile;               // stages x 16 KB
-  unsigned char* sP = sV + kKVStages * kVTile;               // [A, B] x 16 KB
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + 2 * kPTile);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile);
   uint64_t* q_full = bar;                  // 1
   uint64_t* kv_full = bar + 1;             // kKVStages
   uint64_t* kv_empty = kv_full + kKVStages;
   uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of tile i, buffer j % 2
-  uint64_t* p_full = s_full + 4;            // [A, B]
-  uint64_t* o_done = p_full + 2;            // [A, B]
+  uint64_t* p_full = s_full + 4;            // [A0, A1, B0, B1]: P of tile i, buffer j % 2
+  uint64_t* o_done = p_full + 4;            // [A, B]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 2);
+  float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + 1024);  // partials
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = (int)(blockIdx.x % a.n_pairs);
@@ -209,14 +213,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&s_full[i], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 1);
-      mbar_init(&o_done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
     fence_barrier_init();
   }
-  if (warp == 8) {
+  if (warp == 16) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto tS = [&](int i, int u) { return tbase + 64u * (2 * i + u); };
   auto tO = [&](int i) { return tbase + 256u + 128u * i; };
 
-  if (warp == 8) {
+  if (warp == 16) {
     // ======================================================= TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, two ? 2 * kQTile : kQTile);
@@ -254,13 +258,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_3d(sV + s * kVTile, &tv, j * 64, 0, b * a.Hkv + kvh, &kv_full[s]);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     // ======================================================= MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
       constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV),
-                     aP = smem_addr(sP);
+      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
       bool ok = mbar_wait(q_full, 0) && mbar_wait(&kv_full[0], 0);
       auto issue_s = [&](int i, int j) {
         const int s = j % kKVStages;
@@ -273,12 +276,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&s_full[2 * i + (j & 1)]);
       };
+      // P(j) sits in TMEM over its S buffer: 64 keys packed two per column
       auto issue_pv = [&](int i, int j) {
         const int s = j % kKVStages;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tO(i), sw128_kmajor_desc(aP + i * kPTile + kk * 32),
-                  sw128_kmajor_desc(aV + s * kVTile + kk * 32), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tO(i), tS(i, j & 1) + kk * 8, sw128_kmajor_desc(aV + s * kVTile + kk * 32),
+                     kIdO, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&o_done[i]);
       };
       if (ok) {
@@ -300,13 +304,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after_sync();
           }
           if (ok && j < nA) {
-            ok = mbar_wait(&p_full[0], j & 1);
+            ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
             tc_fence_after_sync();
             if (ok) issue_pv(0, j);
             if (ok && j + 2 < nA) issue_s(0, j + 2);
           }
           if (ok && j < nB) {
-            ok = mbar_wait(&p_full[1], j & 1);
+            ok = mbar_wait(&p_full[2 + (j & 1)], (j >> 1) & 1);
             tc_fence_after_sync();
             if (ok) issue_pv(1, j);
           }
@@ -318,97 +322,105 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ======================================================= softmax
-    const int i = warp >> 2;                  // 0: tile A, 1: tile B
+    const int i = warp >> 3;                  // 0: tile A, 1: tile B
+    const int hh = (warp >> 2) & 1;           // which half of the keys / O columns
     const int ni = i == 0 ? nA : nB;
-    const int row = tid - i * 128;            // 0..127: TMEM lane = query row
+    const int row = (warp & 3) * 32 + lane;   // 0..127: TMEM lane = query row
     const int q0 = (i == 0 ? qt_a : qt_b) * 128;
     const int qidx = q0 + row;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    unsigned char* prow = sP + i * kPTile + row * 128;
+    float* my_x = xch + (i * 2 + hh) * 128 + row;
+    const float* other_x = xch + (i * 2 + (hh ^ 1)) * 128 + row;
     float m = -INFINITY, l = 0.f;
-    float v[32], w[32];
+    float v[32];
     bool ok = true;
     for (int j = 0; j < ni && ok; ++j) {
       ok = mbar_wait(&s_full[2 * i + (j & 1)], (j >> 1) & 1);
-      // MMAs of one issuer complete in issue order and S(j) is issued after
-      // PV(j-1): this wait is normally already satisfied.  After it, O and
-      // the P buffer are free.
-      if (j > 0) ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
       tc_fence_after_sync();
-      tmem_ld32(tS(i, j & 1) + lane_off, v);
-      tmem_ld32(tS(i, j & 1) + lane_off + 32, w);
+      tmem_ld32(tS(i, j & 1) + lane_off + 32 * hh, v);
       tmem_wait_ld();
-      const int key0 = j * 64;
-      const bool edge = key0 + 63 > q0;  // some keys of this tile lie past some rows
-      if (edge) {
+      const int key0 = j * 64 + 32 * hh;
+      if (key0 + 31 > q0) {  // some keys of this half lie past some rows
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 32; ++c)
           if (key0 + c > qidx) v[c] = -INFINITY;
-          if (key0 + 32 + c > qidx) w[c] = -INFINITY;
-        }
       }
-      // row max as a tree (independent partial maxima)
       float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(w[e], w[e + 8]));
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        mx[e] = fmaxf(mx[e], fmaxf(fmaxf(v[e + 16], v[e + 24]), fmaxf(w[e + 16], w[e + 24])));
-      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(v[e + 16], v[e + 24]));
+      float pmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      tmax *= a.sl2e;
-      // rescale O only when the row max grew by more than 2^8
+      // the row max needs both halves; the barrier also orders both halves'
+      // TMEM reads of S before either overwrites part of it with P
+      *my_x = pmax;
+      tc_fence_before_sync();
+      named_bar(1 + i, 256);
+      tc_fence_after_sync();
+      const float tmax = fmaxf(pmax, *other_x) * a.sl2e;
+      // rescale O only when the row max grew by more than 2^8 (both halves
+      // decide alike: same inputs)
       const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
       const bool grow = j > 0 && m_new != m;
       if (__any_sync(0xffffffffu, grow)) {
+        // O may be touched only once PV(j-1) is done
+        ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
+        tc_fence_after_sync();
         const float alpha = grow ? ex2f(m - m_new) : 1.0f;
-        float o[32];
+        float o[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tO(i) + lane_off + c * 32, o);
+          tmem_ld16(tO(i) + lane_off + 64 * hh + c * 16, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tO(i) + lane_off + c * 32, o);
+          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          tmem_st16(tO(i) + lane_off + 64 * hh + c * 16, o);
         }
         tmem_wait_st();
         l *= alpha;
       }
       m = m_new;
-      // P = 2^(S*c - m) (masked entries are -inf, so 0), as eight swizzled
-      // 16-byte chunks; the row sum in four independent partial sums
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into TMEM
+      // columns 16*hh .. 16*hh+15 of this S buffer (both halves have read
+      // their S columns before the exchange barrier above)
+      const float2 c2 = make_float2(a.sl2e, a.sl2e), nm2 = make_float2(-m, -m);
+      float2 ls = make_float2(0.f, 0.f);
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float* src = c < 4 ? v + 8 * c : w + 8 * (c - 4);
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float p0 = ex2f(fmaf(src[e], a.sl2e, -m));
-          const float p1 = ex2f(fmaf(src[e + 1], a.sl2e, -m));
-          ls[e / 2] += p0 + p1;
-          const __half2 hp = __floats2half2_rn(p0, p1);
-          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-        }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int e = 0; e < 32; e += 2) {
+        const float2 x = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
+        const float2 pe = make_float2(ex2f(x.x), ex2f(x.y));
+        ls = make_float2(ls.x + pe.x, ls.y + pe.y);
+        const __half2 hp = __floats2half2_rn(pe.x, pe.y);
+        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      fence_async_shared();
+      l += ls.x + ls.y;
+      // Observe PV(j-1) before publishing P(j).  A parity wait is unambiguous
+      // only while the barrier is at most one phase behind; here it has seen
+      // j-1 or j completions (S(j) done implies PV(j-2) done, and PV(j) needs
+      // P(j)), and keeping to one observation per tile holds that invariant
+      // for the next tile and the epilogue.  PV(j-1) ran during this softmax.
+      if (j > 0) ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
+      tmem_st16u(tS(i, j & 1) + lane_off + 16 * hh, pk);
+      tmem_wait_st();
       tc_fence_before_sync();
-      named_bar(1 + i, 128);
-      if (row == 0) mbar_arrive(&p_full[i]);
+      named_bar(1 + i, 256);
+      if (hh == 0 && row == 0) mbar_arrive(&p_full[2 * i + (j & 1)]);
     }
     if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-    // ---- O / l to global memory once the last PV is done
+    // ---- O / l to global memory once the last PV is done (l: both halves)
+    *my_x = l;
+    named_bar(1 + i, 256);
+    const float ltot = l + *other_x;
+    // each tile observed PV(j-1), so the barrier is at most one phase behind
     if (ni > 0 && ok && mbar_wait(&o_done[i], (ni - 1) & 1)) {
       tc_fence_after_sync();
-      const float inv = 1.0f / l;
+      const float inv = 1.0f / ltot;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tO(i) + lane_off + c * 32, v);
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(tO(i) + lane_off + 64 * hh + c * 32, v);
         tmem_wait_ld();
         if (qidx < a.T) {
-          float* dst = a.out + (((int64_t)b * a.T + qidx) * a.Hq + h) * kPrefillHD + c * 32;
+          float* dst = a.out + (((int64_t)b * a.T + qidx) * a.Hq + h) * kPrefillHD + 64 * hh + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + e) =
@@ -419,7 +431,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 16) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, 512);
   }
