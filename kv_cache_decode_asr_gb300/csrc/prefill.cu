@@ -156,7 +156,7 @@ struct PrefillAttnArgs {
 constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16
 constexpr int kKTile = 64 * 128 * 2;      // 64 keys x 128 dims
 constexpr int kVTile = 128 * 64 * 2;      // V^T: 128 dims x 64 keys
-constexpr int kKVStages = 3;
+constexpr int kKVStages = 4;
 constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + 4096 + 1024 + 1024;
 constexpr int kAttnThreads = 576;  // warps 0-7, 8-15: softmax of tiles A, B; 16: TMA; 17: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
@@ -167,9 +167,10 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// Two query tiles of one (sequence, head) per CTA: tile A = pair p and tile
-// B = n_qt-1-p, so every CTA sees n_qt+1 tiles of 128 keys (a lone middle
-// tile when n_qt is odd).  Roles: warps 0-7 and 8-15 run the softmax of
+// Two adjacent query tiles of one (sequence, head) per CTA: tile A = 2p and
+// tile B = 2p+1 (a lone last tile when n_qt is odd).  Their causal lengths
+// differ by one 128-key tile, so the two softmax warpgroups stay busy side by
+// side, and both read the same K/V stream.  The longest pairs go first.  Roles: warps 0-7 and 8-15 run the softmax of
 // tiles A and B, two threads per query row (warp w reads TMEM lanes
 // 32*(w%4)..+31; warps w and w+4 take the two halves of the row's keys and of
 // its O columns, and exchange their partial row maxima through shared
@@ -197,12 +198,13 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
   float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + 1024);  // partials
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pair = (int)(blockIdx.x % a.n_pairs);
-  const int bh = (int)(blockIdx.x / a.n_pairs);
+  const int BH = a.B * a.Hq;
+  const int pair = a.n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int kvh = h / (a.Hq / a.Hkv);
-  const int qt_a = pair, qt_b = a.n_qt - 1 - pair;
-  const bool two = qt_b != qt_a;
+  const int qt_a = 2 * pair, qt_b = 2 * pair + 1;
+  const bool two = qt_b < a.n_qt;
   // 64-key tiles each query tile visits (causal: up to its last row)
   const int nA = 2 * (qt_a + 1), nB = two ? 2 * (qt_b + 1) : 0;
   const int n = nA > nB ? nA : nB;
