@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -37,6 +38,9 @@ DEFAULT_WORKLOAD = "whisper_large_b32"
 WORKLOAD_INDEX = {n: i + 1 for i, n in enumerate(syn.WORKLOADS)}
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+CSRC = "kv_cache_decode_asr_gb300/csrc/"
+DECODE_SOURCES = [CSRC + f for f in ("decode_attn.cu", "decode_attn.cuh", "common.cuh")]
+PREFILL_SOURCES = [CSRC + f for f in ("prefill.cu", "tcgen05.cuh", "common.cuh")]
 
 
 def load_peaks():
@@ -62,23 +66,43 @@ def load_all_peaks():
     return {"hbm": (hbm, src), "tensor": (tf, tsrc)}
 
 
-def source_sha(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def code_sha(rels):
+    """Hash of the code in the given sources with comments and whitespace
+    removed, so a comment edit does not orphan a counter record."""
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_file, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel; else None."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
+def recorded_traffic(kernel_sources, workload, kernel):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu summary table, if its row for this workload and
+    kernel was taken on the current code of the kernel; else None."""
     try:
-        with open(path) as f:
-            rec = json.load(f)
-    except Exception:
+        with open(TRAFFIC_TABLE) as f:
+            lines = f.read().splitlines()
+    except OSError:
         return None
-    if rec.get("source_sha") != source_sha(kernel_file):
-        return None
-    return rec.get("dram_bytes_per_launch")
+    sha = code_sha(kernel_sources)
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) < 4 or cells[0] != workload or cells[1] != kernel:
+            continue
+        if cells[2] != sha:
+            return None
+        try:
+            return int(cells[3].replace(",", ""))
+        except ValueError:
+            return None
+    return None
 
 
 # --------------------------------------------------------------- clocks ----
@@ -150,7 +174,7 @@ class WhisperStep:
         import torch
         from kv_cache_decode_asr_gb300 import ops
         self.name, self.cfg, self.ops = name, cfg, ops
-        wi = WORKLOAD_INDEX[name] + 100 * rank
+        wi = rank_seed_base(name, rank)
         B, H, hd, Lyr = cfg["B"], cfg["heads"], cfg["head_dim"], cfg["layers"]
         cap, F, beam = cfg["capacity"], cfg["frames"], cfg["beam"]
         self.B, self.H, self.hd, self.L, self.cap, self.F = B, H, hd, Lyr, cap, F
@@ -251,11 +275,14 @@ class WhisperStep:
 
     dominant = "cross"
     dominant_kernel = "decode_attn_kernel<64,1> (asr_cross_attn_step)"
-    kernel_file = "kv_cache_decode_asr_gb300/csrc/decode_attn.cu"
+    kernel_sources = DECODE_SOURCES
 
     def dominant_bytes_per_launch(self):
         b = self.bytes_per_layer()
         return b["self"] + b["append"] if self.profile_kernel == "self" else b["cross"]
+
+    def traffic_key(self):
+        return "self+append" if self.profile_kernel == "self" else "cross"
 
     def dominant_call(self, l, stream=None):
         if self.profile_kernel == "self":
@@ -367,13 +394,13 @@ class GqaStep:
 
     dominant = "gqa"
     dominant_kernel = "decode_attn_kernel<128,2> (asr_gqa_step)"
-    kernel_file = "kv_cache_decode_asr_gb300/csrc/decode_attn.cu"
+    kernel_sources = DECODE_SOURCES
 
     def __init__(self, name, cfg, device, rank=0):
         import torch
         from kv_cache_decode_asr_gb300 import ops
         self.name, self.cfg, self.ops = name, cfg, ops
-        wi = WORKLOAD_INDEX[name] + 100 * rank
+        wi = rank_seed_base(name, rank)
         B, Hq, Hkv, hd = cfg["B"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
         Lyr, cap = cfg["layers"], cfg["capacity"]
         self.B, self.Hq, self.Hkv, self.hd, self.L, self.cap = B, Hq, Hkv, hd, Lyr, cap
@@ -419,6 +446,9 @@ class GqaStep:
 
     def dominant_bytes_per_launch(self):
         return self.bytes_per_layer()["gqa"]
+
+    def traffic_key(self):
+        return "gqa"
 
     def dominant_call(self, l, stream=None):
         self.layer_call(l, stream)
@@ -481,14 +511,14 @@ class PrefillStep:
 
     dominant = "prefill_attention"
     dominant_kernel = "prefill_attn_kernel (tcgen05, asr_prefill_attention)"
-    kernel_file = "kv_cache_decode_asr_gb300/csrc/prefill.cu"
+    kernel_sources = PREFILL_SOURCES
     metric = "prefill tokens/s (tensor-core TFLOP/s and fraction of the f16 peak alongside)"
 
     def __init__(self, name, cfg, device, rank=0):
         import torch
         from kv_cache_decode_asr_gb300 import ops
         self.name, self.cfg, self.ops = name, cfg, ops
-        wi = WORKLOAD_INDEX[name] + 100 * rank
+        wi = rank_seed_base(name, rank)
         B, T, Hq, Hkv, hd = cfg["B"], cfg["T"], cfg["q_heads"], cfg["kv_heads"], cfg["head_dim"]
         self.B, self.T, self.Hq, self.Hkv, self.hd, self.cap = B, T, Hq, Hkv, hd, cfg["capacity"]
         self.L = 1
@@ -515,6 +545,9 @@ class PrefillStep:
         self.ops.asr_prefill_attn(self.q, self.k, self.v, self.wq, self.wk, self.eps, self.base,
                                   self.Hq, self.Hkv, self.hd, self.scale, self.cache, self.cap,
                                   self.out, self.ws, dev_err=self.err, stream=stream)
+
+    def traffic_key(self):
+        return "prefill_attn"
 
     def dominant_call(self, l, stream=None):
         self.ops.asr_prefill_attention(self.B, self.T, self.Hq, self.Hkv, self.hd, self.scale,
@@ -628,6 +661,21 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def rank_seed_base(name, rank):
+    """Seed base of one rank's synthetic batch.  Weak scaling shards nothing:
+    every rank draws its own batch of the workload's full per-GPU size from
+    seeds no other rank uses (ranks 100 apart, workloads 1 apart)."""
+    return WORKLOAD_INDEX[name] + 100 * rank
+
+
+def job_throughput(ms_total_rank, steps, tokens_per_rank_step, world, device):
+    """The slowest rank's timed region sets the step time; the job's value is
+    the tokens all ranks processed per second of it."""
+    ms_total = max_over_ranks(ms_total_rank, world, device)
+    ms_step = ms_total / steps
+    return ms_step, tokens_per_rank_step * world / (ms_step / 1e3)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -692,10 +740,8 @@ def run_ours(args):
         barrier(world)
         torch.cuda.synchronize()
     ms_total = ev0.elapsed_time(ev1)
-    ms_total = max_over_ranks(ms_total, world, device)
-    ms_step = ms_total / args.steps
+    ms_step, value = job_throughput(ms_total, args.steps, wl.tokens_per_step(), world, device)
     tokens = wl.tokens_per_step() * world
-    value = tokens / (ms_step / 1e3)
     kv_bytes = wl.kv_bytes_per_step()
     kv_gbs = kv_bytes * world / (ms_step / 1e3) / 1e9
 
@@ -720,7 +766,8 @@ def run_ours(args):
     d1.synchronize()
     launch_ms = d0.elapsed_time(d1) / (reps * wl.L)
     roof = wl.roofline(launch_ms, peaks)
-    roof.update({"traffic": recorded_traffic(wl.kernel_file, args.workload),
+    roof.update({"traffic": recorded_traffic(wl.kernel_sources, args.workload,
+                                             wl.traffic_key()),
                  "kernel": wl.dominant_kernel, "launch_us": launch_ms * 1e3})
 
     # ---- end to end through host buffers: per step, H2D of the step's

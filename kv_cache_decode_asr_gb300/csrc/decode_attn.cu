@@ -8,10 +8,11 @@
 // streams its share as tiles of whole cache rows (K and V of every head are
 // contiguous in a row) with one bulk TMA copy per tile into a multi-stage
 // shared-memory ring (mbarrier full/empty pairs, one producer warp).  The
-// consumer threads form groups of HD/8 lanes; a group owns one KV head and
-// 8 dims per lane, keeps its queries (all beams of the group x all query
-// heads of the KV head) in registers, and runs an online softmax in the log2
-// domain over the rows it is given.  At the end of a source's piece the row
+// consumer threads form groups of G = HD/DPL lanes (DPL = 16 dims per lane
+// for one or two queries, 8 for four or eight); a group owns one KV head,
+// keeps its queries (all beams of the group x all query heads of the KV
+// head) in registers, and runs an online softmax in the log2 domain over the
+// rows it is given.  At the end of a source's piece the row
 // slots are merged in shared memory; a source split over several CTAs leaves
 // (max, sum, unnormalised output) partials in the workspace and the last CTA
 // to finish it (atomic ticket, no waiting) merges them and writes the output.
