@@ -13,12 +13,13 @@
 //   row t and also written transposed (keys contiguous, zero-padded to a
 //   multiple of 128) to the workspace, so both matrix products below read
 //   K-major operands.
-// a8 attention (5th-generation tensor cores): one CTA per (pair of 128-query
-//   tiles, sequence, query head), warp-specialised.  Q, K and V^T tiles
+// a8 attention (5th-generation tensor cores): one CTA per (pair of adjacent
+//   128-query tiles, sequence, query head), warp-specialised.  Q, K and V^T tiles
 //   arrive by tiled TMA with the 128-byte swizzle; S = Q K^T (128 x 64 per
 //   key tile) and O += P V are tcgen05.mma kind::f16 (f16 operands, fp32
-//   accumulators in tensor memory).  Two softmax warpgroups (one per query
-//   tile, one thread per query row) read S from TMEM, run the online softmax
+//   accumulators in tensor memory).  Two softmax groups of 256 threads (one
+//   per query tile, two threads per query row, each on half of the 64 key
+//   columns) read S from TMEM, run the online softmax
 //   in fp32 (log2 domain), rescale O in TMEM only when a row maximum grows by
 //   more than 2^8 (the normalisation at the end is exact either way), and
 //   write P (f16) back into tensor memory over its S buffer, where the PV MMA
