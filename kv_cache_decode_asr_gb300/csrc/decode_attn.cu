@@ -88,13 +88,16 @@ struct Tile {
 };
 
 // Walks the tiles of the key range [k, k1) in order; the producer and the
-// consumers run identical copies.
+// consumers run identical copies.  Each non-empty source g spans
+// [off[g], off[g+1]) on the flattened axis: a head of `vrows` virtual rows
+// (never loaded; they charge the CTA that enters the source for its
+// per-source work) followed by its real rows.
 struct TileIter {
   const int* off;
-  int S, tile_rows, g, prev_g;
+  int S, tile_rows, vrows, g, prev_g;
   int64_t k, k1;
-  __device__ TileIter(const int* off_, int S_, int64_t k0, int64_t k1_, int tr)
-      : off(off_), S(S_), tile_rows(tr), g(0), prev_g(-1), k(k0), k1(k1_) {
+  __device__ TileIter(const int* off_, int S_, int64_t k0, int64_t k1_, int tr, int vr)
+      : off(off_), S(S_), tile_rows(tr), vrows(vr), g(0), prev_g(-1), k(k0), k1(k1_) {
     if (k0 < k1_) {
       int lo = 0, hi = S_;  // largest g < S with off[g] <= k0
       while (hi - lo > 1) {
@@ -108,10 +111,15 @@ struct TileIter {
   __device__ bool next(Tile& t) {
     if (k >= k1) return false;
     while (off[g + 1] <= k) ++g;
+    const int64_t real0 = (int64_t)off[g] + vrows;  // < off[g + 1]: a source has a real row
+    if (k < real0) {
+      k = real0;
+      if (k >= k1) return false;
+    }
     const int64_t end = min((int64_t)off[g + 1], k1);
     const int nr = (int)min((int64_t)tile_rows, end - k);
     t.g = g;
-    t.row0 = (int)(k - off[g]);
+    t.row0 = (int)(k - real0);
     t.nr = nr;
     t.first = g != prev_g;
     t.last = k + nr == end;
@@ -323,6 +331,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   int* off = reinterpret_cast<int*>(smem + lay.off);
   int* mst = reinterpret_cast<int*>(smem + lay.mstart);
   float* rope = reinterpret_cast<float*>(smem + lay.rope);
+  float* wts = reinterpret_cast<float*>(smem + lay.wts);  // GQA: RMSNorm weights of q, k
   float* merge = reinterpret_cast<float*>(smem + lay.merge);
   uint16_t* stage = reinterpret_cast<uint16_t*>(smem + lay.stage);
 
@@ -351,6 +360,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     off[g] = 0;
     mst[g] = 0;
   }
+  if (a.mode == kModeGqa)
+    for (int i = tid; i < 2 * HD; i += blockDim.x) wts[i] = i < HD ? a.wq[i] : a.wk[i - HD];
   __syncthreads();
   if (a.mode == kModeCross) {
     for (int b = tid; b < a.B; b += blockDim.x) {
@@ -359,14 +370,14 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       if (b > 0 && a.group[b - 1] > gr) ctl[2] = 1;
     }
     __syncthreads();
-    for (int g = tid; g < S; g += blockDim.x) off[g] = mst[g] > 0 ? a.fixed_len : 0;
+    for (int g = tid; g < S; g += blockDim.x) off[g] = mst[g] > 0 ? a.fixed_len + a.seg_rows : 0;
   } else {
     for (int g = tid; g < S; g += blockDim.x) {
       const int v = a.lens[g];
       int keys;
       if (a.mode == kModeSelf) keys = (v >= 1 && v <= a.capacity) ? v - a.append : 0;
       else keys = (v >= 0 && v < a.capacity) ? v : 0;  // rows cached before the new one
-      off[g] = keys;
+      off[g] = keys > 0 ? keys + a.seg_rows : 0;
       mst[g] = 1;
     }
   }
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     // ======================= producer warp: one lane issues bulk copies
     if (lane == 0 && k0 < k1) {
       const uint64_t pol = policy_evict_first();
-      TileIter it(off, S, k0, k1, a.tile_rows);
+      TileIter it(off, S, k0, k1, a.tile_rows, a.seg_rows);
       Tile tl;
       for (int t = 0; it.next(tl); ++t) {
         const int s = t % a.stages;
@@ -456,11 +467,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   auto seg_begin = [&](int g) {
     mbase = mst[g];
     nq = min(mst[g + 1] - mst[g], a.max_members) * rep;
-    if (a.mode == kModeGqa) {
-      named_bar(1, n_cons);
-      rope_table<HD>(rope, a.theta, a.lens[g], tid);
-      named_bar(1, n_cons);
-    }
+    // every query load is issued before the RoPE table is built, so their
+    // latencies overlap it and one another
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
       m[qi] = -INFINITY;
@@ -471,13 +479,23 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         const int b = mbase + qi / rep;
         const int hq = h * rep + qi % rep;
         load_head_f32<HD, DPL>(a.q + (int64_t)b * a.q_stride + hq * HD, li, sw, qv[qi]);
-        if (a.mode == kModeGqa) norm_rope<HD, DPL>(qv[qi], a.wq, a.eps, rope, li, sw);
-        const float2 s2 = make_float2(a.qscale, a.qscale);
-#pragma unroll
-        for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
       } else {
 #pragma unroll
         for (int t = 0; t < NP; ++t) qv[qi][t] = make_float2(0.f, 0.f);
+      }
+    }
+    if (a.mode == kModeGqa) {
+      named_bar(1, n_cons);
+      rope_table<HD>(rope, a.theta, a.lens[g], tid);
+      named_bar(1, n_cons);
+    }
+    const float2 s2 = make_float2(a.qscale, a.qscale);
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+      if (qi < nq) {
+        if (a.mode == kModeGqa) norm_rope<HD, DPL>(qv[qi], wts, a.eps, rope, li, sw);
+#pragma unroll
+        for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
       }
     }
   };
@@ -506,16 +524,17 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
   };
 
-  auto seg_end = [&](int g) {
-    // Append: the new token's key/value (GQA: normed and roped), computed by
-    // every group (warp-uniform code: it may shuffle), written to the cache
-    // by row slot 0 and scored against this group's queries.
+  // Append: the new token's key/value (GQA: normed and roped), computed by
+  // every group (warp-uniform code: it may shuffle), written to the cache by
+  // row slot 0 and scored against this group's queries.  Only the CTA that
+  // writes source g's output runs it.
+  auto append_new = [&](int g) {
     if (a.append) {
       const int p = a.mode == kModeGqa ? a.lens[g] : a.lens[g] - 1;
       float2 kx[NP];
       load_head_f32<HD, DPL>(a.k_new + (int64_t)g * a.kv_stride + h * HD, li, sw, kx);
       load_head_f32<HD, DPL>(a.v_new + (int64_t)g * a.kv_stride + h * HD, li, sw, vn);
-      if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, a.wk, a.eps, rope, li, sw);
+      if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, wts + HD, a.eps, rope, li, sw);
       uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
@@ -545,13 +564,18 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         }
       }
     }
+  };
+
+  auto seg_end = [&](int g) {
     merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
     // pieces of this source over the grid
-    const int64_t go = off[g], gl = (int64_t)off[g + 1] - off[g];
+    // (real rows of g: [off[g] + seg_rows, off[g + 1]))
+    const int64_t go = (int64_t)off[g] + a.seg_rows, gl = (int64_t)off[g + 1] - go;
     const int first = gl > 0 ? (int)(go / share) : 0;
     const int lastp = gl > 0 ? (int)((go + gl - 1) / share) : 0;
     const int parts = gl > 0 ? lastp - first + 1 : 0;
     if (parts <= 1) {
+      append_new(g);
       if (r == 0) {
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi)
@@ -588,6 +612,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
     named_bar(1, n_cons);
     if (ctl[1]) {
+      append_new(g);
       // row slot r merges pieces first + r, first + r + R, ...; then the
       // slots are merged like a tile's rows.  The running state registers are
       // reused: this CTA's own piece is already among the partials.
@@ -657,7 +682,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   };
 
   if (k0 < k1) {
-    TileIter it(off, S, k0, k1, a.tile_rows);
+    TileIter it(off, S, k0, k1, a.tile_rows, a.seg_rows);
     Tile tl;
     for (int t = 0; it.next(tl); ++t) {
       if (tl.first) seg_begin(tl.g);
@@ -821,13 +846,15 @@ static void* kernel_for(int HD, int vi) {
   return nullptr;
 }
 
-// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64"
+// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256"
 // overrides them (ctas / R = 0: chosen automatically; rs: rows per slot;
-// min_kb: fewest K/V bytes one CTA takes).
+// min_kb: fewest K/V bytes one CTA takes; seg_kb: K/V bytes' worth of
+// virtual rows charged to each source, so CTAs that start or finish more
+// sources take fewer rows).
 // Defaults (measured on GB300): one CTA per SM with about ten consumer
 // warps and two or more stages of large tiles.
 struct DecodeTune {
-  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64;
+  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256;
 };
 
 static DecodeTune decode_tune() {
@@ -844,6 +871,8 @@ static DecodeTune decode_tune() {
         else if (!strcmp(key, "R")) d.R = val;
         else if (!strcmp(key, "rs")) d.rs = val;
         else if (!strcmp(key, "min_kb")) d.min_kb = val;
+        else if (!strcmp(key, "seg_kb")) d.seg_kb = val;
+
         e += n;
         if (*e == ',') ++e;
       }
@@ -854,7 +883,7 @@ static DecodeTune decode_tune() {
 }
 
 struct DecodePlan {
-  int R, tile_rows, stages, stage_elems, threads, smem, min_share;
+  int R, tile_rows, stages, stage_elems, threads, smem, min_share, seg_rows;
 };
 
 // Row slots R: the consumer count R * Hkv * G must be a multiple of 32 and
@@ -892,6 +921,7 @@ static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_
   if (p.smem > 227 * 1024) return false;
   const int min_bytes = std::max(tune.min_kb, 1) * 1024;
   p.min_share = std::max(p.tile_rows, (min_bytes + row_bytes - 1) / row_bytes);
+  p.seg_rows = std::max(tune.seg_kb, 0) * 1024 / row_bytes;
   return true;
 }
 
@@ -961,6 +991,7 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
   a.R = p.R;
   a.tile_rows = p.tile_rows;
   a.min_share = p.min_share;
+  a.seg_rows = p.seg_rows;
   a.stages = p.stages;
   a.stage_elems = p.stage_elems;
   cudaLaunchConfig_t cfg = {};

@@ -40,6 +40,7 @@ struct DecodeArgs {
   int R;            // row slots (groups of the same head working on different rows)
   int tile_rows;    // rows per pipeline stage (R * rows per slot)
   int min_share;    // fewest rows one CTA takes (bounds the partials per source)
+  int seg_rows;     // virtual rows charged per source on the flattened key axis
   int stages;       // pipeline depth
   int stage_elems;  // f16 elements per stage buffer (128-byte multiple)
   int mode;         // DecodeMode
@@ -59,7 +60,7 @@ struct DecodeArgs {
 
 // Shared-memory layout of one CTA (bytes from the dynamic smem base).
 struct DecodeSmem {
-  int bars, ctl, off, mstart, rope, merge, stage, total;
+  int bars, ctl, off, mstart, rope, wts, merge, stage, total;
 };
 
 __host__ __device__ inline int dsm_align(int x, int a) { return (x + a - 1) / a * a; }
@@ -72,7 +73,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.off = dsm_align(s.ctl + 16 * 4, 16);
   s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
   s.rope = dsm_align(s.mstart + (n_src + 1) * 4, 16);
-  s.merge = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
+  s.wts = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
+  s.merge = dsm_align(s.wts + 2 * HD * 4, 16);
   s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 4) * 4, 128);
   s.total = s.stage + stages * stage_elems * 2;
   return s;
