@@ -194,8 +194,8 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
   uint64_t* kv_empty = kv_full + kKVStages;
   uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of tile i, buffer j % 2
   uint64_t* p_full = s_full + 4;            // [A0, A1, B0, B1]: P of tile i, buffer j % 2
-  uint64_t* o_done = p_full + 4;            // [A, B]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 2);
+  uint64_t* o_done = p_full + 4;            // [A0, A1, B0, B1]: PV(j) of tile i -> j % 2
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 4);
   float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + 1024);  // partials
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -218,9 +218,9 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 1);
+      mbar_init(&p_full[i], 8);  // one arrival per softmax warp of the tile
+      mbar_init(&o_done[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
     fence_barrier_init();
   }
   if (warp == 16) {
@@ -241,88 +241,87 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
 
   if (warp == 16) {
     // ======================================================= TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, two ? 2 * kQTile : kQTile);
-      tma_load_3d(sQ, &tq, h * 128, qt_a * 128, b, q_full);
-      tma_load_3d(sQ + kQTile / 2, &tq, h * 128 + 64, qt_a * 128, b, q_full);
-      if (two) {
-        tma_load_3d(sQ + kQTile, &tq, h * 128, qt_b * 128, b, q_full);
-        tma_load_3d(sQ + kQTile + kQTile / 2, &tq, h * 128 + 64, qt_b * 128, b, q_full);
+    // The whole warp runs the schedule; one elected lane issues each copy.
+    mbar_arrive_expect_tx_warp(q_full, two ? 2 * kQTile : kQTile);
+    tma_load_3d_warp(sQ, &tq, h * 128, qt_a * 128, b, q_full);
+    tma_load_3d_warp(sQ + kQTile / 2, &tq, h * 128 + 64, qt_a * 128, b, q_full);
+    if (two) {
+      tma_load_3d_warp(sQ + kQTile, &tq, h * 128, qt_b * 128, b, q_full);
+      tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, h * 128 + 64, qt_b * 128, b, q_full);
+    }
+    for (int j = 0; j < n; ++j) {
+      const int s = j % kKVStages;
+      if (j >= kKVStages && !mbar_wait_warp(&kv_empty[s], ((j / kKVStages) - 1) & 1)) {
+        if (lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+        break;
       }
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kKVStages;
-        if (j >= kKVStages && !mbar_wait(&kv_empty[s], ((j / kKVStages) - 1) & 1)) {
-          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&kv_full[s], kKTile + kVTile);
-        tma_load_3d(sK + s * kKTile, &tk, kvh * 128, j * 64, b, &kv_full[s]);
-        tma_load_3d(sK + s * kKTile + kKTile / 2, &tk, kvh * 128 + 64, j * 64, b, &kv_full[s]);
-        tma_load_3d(sV + s * kVTile, &tv, j * 64, 0, b * a.Hkv + kvh, &kv_full[s]);
-      }
+      mbar_arrive_expect_tx_warp(&kv_full[s], kKTile + kVTile);
+      tma_load_3d_warp(sK + s * kKTile, &tk, kvh * 128, j * 64, b, &kv_full[s]);
+      tma_load_3d_warp(sK + s * kKTile + kKTile / 2, &tk, kvh * 128 + 64, j * 64, b, &kv_full[s]);
+      tma_load_3d_warp(sV + s * kVTile, &tv, j * 64, 0, b * a.Hkv + kvh, &kv_full[s]);
     }
   } else if (warp == 17) {
     // ======================================================= MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
-      constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-      bool ok = mbar_wait(q_full, 0) && mbar_wait(&kv_full[0], 0);
-      auto issue_s = [&](int i, int j) {
-        const int s = j % kKVStages;
+    // The whole warp runs the schedule (operand descriptors stay
+    // warp-uniform); one elected lane issues each tcgen05 operation.
+    constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
+    constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
+    const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
+    bool ok = mbar_wait_warp(q_full, 0) && mbar_wait_warp(&kv_full[0], 0);
+    auto issue_s = [&](int i, int j) {
+      const int s = j % kKVStages;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
-          mma_f16(tS(i, j & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
-                  sw128_kmajor_desc(aK + s * kKTile + koff), kIdS, kk > 0);
-        }
-        mma_commit(&s_full[2 * i + (j & 1)]);
-      };
-      // P(j) sits in TMEM over its S buffer: 64 keys packed two per column
-      auto issue_pv = [&](int i, int j) {
-        const int s = j % kKVStages;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16_ts(tO(i), tS(i, j & 1) + kk * 8, sw128_kmajor_desc(aV + s * kVTile + kk * 32),
-                     kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&o_done[i]);
-      };
-      if (ok) {
-        // S runs two tiles ahead of PV: S(j+2) reuses S buffer j%2, free once
-        // the softmax of tile j has signalled P(j)
-        tc_fence_after_sync();
-        issue_s(0, 0);
-        if (nB > 0) issue_s(1, 0);
-        if (n > 1) {
-          ok = mbar_wait(&kv_full[1 % kKVStages], 0);
-          tc_fence_after_sync();
-          if (ok && 1 < nA) issue_s(0, 1);
-          if (ok && 1 < nB) issue_s(1, 1);
-        }
-        for (int j = 0; j < n && ok; ++j) {
-          const bool next2 = j + 2 < n;
-          if (next2) {
-            ok = mbar_wait(&kv_full[(j + 2) % kKVStages], ((j + 2) / kKVStages) & 1);
-            tc_fence_after_sync();
-          }
-          if (ok && j < nA) {
-            ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
-            tc_fence_after_sync();
-            if (ok) issue_pv(0, j);
-            if (ok && j + 2 < nA) issue_s(0, j + 2);
-          }
-          if (ok && j < nB) {
-            ok = mbar_wait(&p_full[2 + (j & 1)], (j >> 1) & 1);
-            tc_fence_after_sync();
-            if (ok) issue_pv(1, j);
-          }
-          mma_commit(&kv_empty[j % kKVStages]);  // stage free once these MMAs finish
-          if (ok && j + 2 < nB) issue_s(1, j + 2);
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
+        const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
+        mma_f16_warp(tS(i, j & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
+                     sw128_kmajor_desc(aK + s * kKTile + koff), kIdS, kk > 0);
       }
-      if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+      mma_commit_warp(&s_full[2 * i + (j & 1)]);
+    };
+    // P(j) sits in TMEM over its S buffer: 64 keys packed two per column
+    auto issue_pv = [&](int i, int j) {
+      const int s = j % kKVStages;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16_ts_warp(tO(i), tS(i, j & 1) + kk * 8, sw128_kmajor_desc(aV + s * kVTile + kk * 32),
+                        kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_warp(&o_done[2 * i + (j & 1)]);
+    };
+    if (ok) {
+      // S runs two tiles ahead of PV: S(j+2) reuses S buffer j%2, free once
+      // the softmax of tile j has signalled P(j)
+      tc_fence_after_sync();
+      issue_s(0, 0);
+      if (nB > 0) issue_s(1, 0);
+      if (n > 1) {
+        ok = mbar_wait_warp(&kv_full[1 % kKVStages], 0);
+        tc_fence_after_sync();
+        if (ok && 1 < nA) issue_s(0, 1);
+        if (ok && 1 < nB) issue_s(1, 1);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const bool next2 = j + 2 < n;
+        if (next2) {
+          ok = mbar_wait_warp(&kv_full[(j + 2) % kKVStages], ((j + 2) / kKVStages) & 1);
+          tc_fence_after_sync();
+        }
+        if (ok && j < nA) {
+          ok = mbar_wait_warp(&p_full[j & 1], (j >> 1) & 1);
+          tc_fence_after_sync();
+          if (ok) issue_pv(0, j);
+          if (ok && j + 2 < nA) issue_s(0, j + 2);
+        }
+        if (ok && j < nB) {
+          ok = mbar_wait_warp(&p_full[2 + (j & 1)], (j >> 1) & 1);
+          tc_fence_after_sync();
+          if (ok) issue_pv(1, j);
+        }
+        mma_commit_warp(&kv_empty[j % kKVStages]);  // stage free once these MMAs finish
+        if (ok && j + 2 < nB) issue_s(1, j + 2);
+      }
     }
+    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else {
     // ======================================================= softmax
     const int i = warp >> 3;                  // 0: tile A, 1: tile B
@@ -365,8 +364,11 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
       const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
       const bool grow = j > 0 && m_new != m;
       if (__any_sync(0xffffffffu, grow)) {
-        // O may be touched only once PV(j-1) is done
-        ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
+        // O may be touched only once PV(j-1) is done.  PV(j-1) completes
+        // phase (j-1)/2 of o_done[(j-1)%2]; that barrier is at most one phase
+        // behind it (S(j) is done, so PV(j-3) is) and cannot be ahead of it
+        // (PV(j+1) needs P(j+1)), so the parity wait is unambiguous.
+        ok = ok && mbar_wait(&o_done[2 * i + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
         tc_fence_after_sync();
         const float alpha = grow ? ex2f(m - m_new) : 1.0f;
         float o[16];
@@ -397,25 +399,22 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
         pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
       }
       l += ls.x + ls.y;
-      // Observe PV(j-1) before publishing P(j).  A parity wait is unambiguous
-      // only while the barrier is at most one phase behind; here it has seen
-      // j-1 or j completions (S(j) done implies PV(j-2) done, and PV(j) needs
-      // P(j)), and keeping to one observation per tile holds that invariant
-      // for the next tile and the epilogue.  PV(j-1) ran during this softmax.
-      if (j > 0) ok = ok && mbar_wait(&o_done[i], (j - 1) & 1);
+      // P(j) goes over S buffer j % 2, which PV(j-1) does not read; each warp
+      // publishes its rows once its stores are done
       tmem_st16u(tS(i, j & 1) + lane_off + 16 * hh, pk);
       tmem_wait_st();
       tc_fence_before_sync();
-      named_bar(1 + i, 256);
-      if (hh == 0 && row == 0) mbar_arrive(&p_full[2 * i + (j & 1)]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[2 * i + (j & 1)]);
     }
     if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
     // ---- O / l to global memory once the last PV is done (l: both halves)
     *my_x = l;
     named_bar(1 + i, 256);
     const float ltot = l + *other_x;
-    // each tile observed PV(j-1), so the barrier is at most one phase behind
-    if (ni > 0 && ok && mbar_wait(&o_done[i], (ni - 1) & 1)) {
+    // PV(ni-1) is the last; S(ni-1) is done, so PV(ni-3) is and the parity
+    // wait is unambiguous
+    if (ni > 0 && ok && mbar_wait(&o_done[2 * i + ((ni - 1) & 1)], ((ni - 1) >> 1) & 1)) {
       tc_fence_after_sync();
       const float inv = 1.0f / ltot;
 #pragma unroll
