@@ -71,6 +71,21 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
   grid_launch_dependents();
   grid_dependency_wait();
 
+  // V rows of the chunk: every load is issued now, so their latency overlaps
+  // the rotation table below (kPrepV 16-byte vectors per thread)
+  constexpr int kPrepV = 8;
+  const int vec_per_row = kw / 8;
+  const int nv = kPrepT * vec_per_row;
+  uint4 vval[kPrepV];
+#pragma unroll
+  for (int u = 0; u < kPrepV; ++u) {
+    const int idx = tid + u * (int)blockDim.x;
+    const int tt = idx / vec_per_row, c = idx % vec_per_row;
+    vval[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (idx < nv && t0 + tt < a.T)
+      vval[u] = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t0 + tt) * kw + c * 8);
+  }
+
   // rotation table: angle in double, reduced modulo 2*pi, then float sin/cos
   for (int idx = tid; idx < kPrepT * HALF; idx += blockDim.x) {
     const int tt = idx / HALF, i = idx % HALF;
@@ -83,56 +98,97 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
     cs[idx] = c;
     sn[idx] = s;
   }
-  __syncthreads();
-
-  // normed + roped heads: one warp per (position, head); lane l holds dims
-  // 2l, 2l+1 and their RoPE partners 64+2l, 65+2l
-  const int nheads = a.Hq + a.Hkv;
-  for (int item = warp; item < kPrepT * nheads; item += blockDim.x >> 5) {
-    const int tt = item / nheads, hh = item % nheads;
-    const int t = t0 + tt;
-    if (t >= a.T) continue;
-    const bool is_q = hh < a.Hq;
-    const int head = is_q ? hh : hh - a.Hq;
-    const uint16_t* src = (is_q ? a.q + ((int64_t)b * a.T + t) * a.Hq * HD
-                                : a.k + ((int64_t)b * a.T + t) * kw) + head * HD;
-    const __half2 lo = *reinterpret_cast<const __half2*>(src + 2 * lane);
-    const __half2 hi = *reinterpret_cast<const __half2*>(src + HALF + 2 * lane);
-    const float2 xl = __half22float2(lo), xh = __half22float2(hi);
-    float ss = xl.x * xl.x + xl.y * xl.y + xh.x * xh.x + xh.y * xh.y;
+  // V rows: to the cache, and staged for the transpose
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rinv = 1.0f / sqrtf(ss / (float)HD + a.eps);
-    const float* w = is_q ? a.wq : a.wk;
-    const int i0 = 2 * lane;
-    const float l0 = w[i0] * (xl.x * rinv), l1 = w[i0 + 1] * (xl.y * rinv);
-    const float h0 = w[HALF + i0] * (xh.x * rinv), h1 = w[HALF + i0 + 1] * (xh.y * rinv);
-    const float c0 = cs[tt * HALF + i0], s0 = sn[tt * HALF + i0];
-    const float c1 = cs[tt * HALF + i0 + 1], s1 = sn[tt * HALF + i0 + 1];
-    const __half2 ylo = __halves2half2(__float2half_rn(l0 * c0 - h0 * s0),
-                                       __float2half_rn(l1 * c1 - h1 * s1));
-    const __half2 yhi = __halves2half2(__float2half_rn(h0 * c0 + l0 * s0),
-                                       __float2half_rn(h1 * c1 + l1 * s1));
-    uint16_t* dst = is_q ? a.qhat + (((int64_t)b * a.T + t) * a.Hq + head) * HD
-                         : a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * kw + head * HD;
-    *reinterpret_cast<__half2*>(dst + i0) = ylo;
-    *reinterpret_cast<__half2*>(dst + HALF + i0) = yhi;
+  for (int u = 0; u < kPrepV; ++u) {
+    const int idx = tid + u * (int)blockDim.x;
+    if (idx < nv) {
+      const int tt = idx / vec_per_row, c = idx % vec_per_row;
+      if (t0 + tt < a.T)
+        *reinterpret_cast<uint4*>(a.cache + (int64_t)b * a.seq_stride + (int64_t)(t0 + tt) * 2 * kw +
+                                  kw + c * 8) = vval[u];
+      *reinterpret_cast<uint4*>(vsm + tt * kw + c * 8) = vval[u];
+    }
   }
-
-  // V rows: copied to the cache and staged for the transpose
-  const int vec_per_row = kw / 8;
-  for (int idx = tid; idx < kPrepT * vec_per_row; idx += blockDim.x) {
+  // the rows past the first blockDim * kPrepV vectors (more KV heads than
+  // the registers cover) go the plain way
+  for (int idx = tid + kPrepV * (int)blockDim.x; idx < nv; idx += blockDim.x) {
     const int tt = idx / vec_per_row, c = idx % vec_per_row;
-    const int t = t0 + tt;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (t < a.T) {
-      val = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t) * kw + c * 8);
-      *reinterpret_cast<uint4*>(a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * kw + kw +
-                                c * 8) = val;
+    if (t0 + tt < a.T) {
+      val = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t0 + tt) * kw + c * 8);
+      *reinterpret_cast<uint4*>(a.cache + (int64_t)b * a.seq_stride + (int64_t)(t0 + tt) * 2 * kw +
+                                kw + c * 8) = val;
     }
     *reinterpret_cast<uint4*>(vsm + tt * kw + c * 8) = val;
   }
   __syncthreads();
+
+  // normed + roped heads: a half-warp per (position, head) vector; lane hl
+  // of the half-warp holds dims 8*hl .. 8*hl+7, so lanes hl and hl ^ 8 hold
+  // NeoX RoPE partners (i, i + 64).  Each half-warp loads kPrepU vectors
+  // before reducing any of them, so several 16-byte loads per lane are in
+  // flight.
+  constexpr int kPrepU = 4;
+  const int hw = tid >> 4, hl = tid & 15;
+  const bool upper = hl >= 8;
+  const int ib = (hl & 7) * 8;  // frequency index of this lane's first dim
+  float wqr[8], wkr[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    wqr[e] = a.wq[8 * hl + e];
+    wkr[e] = a.wk[8 * hl + e];
+  }
+  const int nheads = a.Hq + a.Hkv;
+  const int items = kPrepT * nheads;
+  const int n_hw = blockDim.x >> 4;
+  for (int base = hw; base < items; base += n_hw * kPrepU) {
+    uint4 x[kPrepU];
+    const uint16_t* srcs[kPrepU];
+#pragma unroll
+    for (int u = 0; u < kPrepU; ++u) {
+      const int item = base + n_hw * u;
+      const int tt = item / nheads, hh = item % nheads, t = t0 + tt;
+      x[u] = make_uint4(0u, 0u, 0u, 0u);
+      srcs[u] = nullptr;
+      if (item < items && t < a.T) {
+        srcs[u] = hh < a.Hq ? a.q + ((int64_t)b * a.T + t) * a.Hq * HD + hh * HD
+                            : a.k + ((int64_t)b * a.T + t) * kw + (hh - a.Hq) * HD;
+        x[u] = *reinterpret_cast<const uint4*>(srcs[u] + 8 * hl);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepU; ++u) {
+      // every lane runs the shuffles (both half-warps of a warp stay converged)
+      const int item = base + n_hw * u;
+      const int tt = min(item / nheads, kPrepT - 1), hh = item % nheads, t = t0 + tt;
+      const bool is_q = hh < a.Hq;
+      float f[8];
+      h8_to_f8(x[u], f);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rinv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+      float xn[8], y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xn[e] = (is_q ? wqr[e] : wkr[e]) * (f[e] * rinv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float pe = __shfl_xor_sync(0xffffffffu, xn[e], 8);
+        const float c = cs[tt * HALF + ib + e], sv = sn[tt * HALF + ib + e];
+        y[e] = upper ? xn[e] * c + pe * sv : xn[e] * c - pe * sv;
+      }
+      if (srcs[u] != nullptr) {
+        uint16_t* dst = is_q ? a.qhat + (((int64_t)b * a.T + t) * a.Hq + hh) * HD
+                             : a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * kw +
+                                   (hh - a.Hq) * HD;
+        *reinterpret_cast<uint4*>(dst + 8 * hl) = f8_to_h8(y);
+      }
+    }
+  }
+
   // V^T[b, kvh, d, t0 .. t0+16): 32 bytes per (kvh, d); zero past T
   for (int idx = tid; idx < kw; idx += blockDim.x) {
     alignas(16) uint16_t col[kPrepT];
