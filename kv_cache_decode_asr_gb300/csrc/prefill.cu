@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
   float* cs = reinterpret_cast<float*>(psm);   // [kPrepT][HALF]
   float* sn = cs + kPrepT * HALF;              // [kPrepT][HALF]
   uint16_t* vsm = reinterpret_cast<uint16_t*>(sn + kPrepT * HALF);  // [kPrepT][Hkv*HD]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int b = blockIdx.y;
   const int t0 = blockIdx.x * kPrepT;
   const int kw = a.Hkv * HD;
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
 // ------------------------------------------------------------- attention --
 
 struct PrefillAttnArgs {
-  int B, T, Hq, Hkv, n_qt, n_pairs;
+  int B, T, Hq, Hkv, n_qt, n_pairs, n_items;
   float sl2e;   // scale * log2(e)
   float* out;   // [B][T][Hq*128] fp32
   int32_t* dev_err;
@@ -214,8 +214,10 @@ constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16
 constexpr int kKTile = 64 * 128 * 2;      // 64 keys x 128 dims
 constexpr int kVTile = 128 * 64 * 2;      // V^T: 128 dims x 64 keys
 constexpr int kKVStages = 4;
-constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + 4096 + 1024 + 1024;
-constexpr int kAttnThreads = 576;  // warps 0-7, 8-15: softmax of tiles A, B; 16: TMA; 17: MMA
+constexpr int kBarBytes = 1024;           // mbarriers and the TMEM address
+constexpr int kXchBytes = 6 * 1024;       // row maxima [tile parity][slot][half][128], row sums [slot][half][128]
+constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + kBarBytes + kXchBytes + 1024;
+constexpr int kAttnThreads = 576;  // warps 0-7, 8-15: softmax of slots A, B; 16: TMA; 17: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -224,17 +226,49 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// Two adjacent query tiles of one (sequence, head) per CTA: tile A = 2p and
-// tile B = 2p+1 (a lone last tile when n_qt is odd).  Their causal lengths
-// differ by one 128-key tile, so the two softmax warpgroups stay busy side by
-// side, and both read the same K/V stream.  The longest pairs go first.  Roles: warps 0-7 and 8-15 run the softmax of
-// tiles A and B, two threads per query row (warp w reads TMEM lanes
-// 32*(w%4)..+31; warps w and w+4 take the two halves of the row's keys and of
-// its O columns, and exchange their partial row maxima through shared
-// memory); warp 16 owns the TMEM allocation and its lane 0 issues the TMA
-// loads (Q once, K and V^T per 64-key tile through a 3-stage ring); warp 17
-// lane 0 issues the MMAs.  While one warpgroup turns its S into P, the tensor core
-// works on the other tile's S or PV.
+// One work item: two adjacent query tiles of one (sequence, head), tile A =
+// 2p in slot A and tile B = 2p+1 in slot B (a lone last tile when n_qt is
+// odd).  Their causal lengths differ by one 128-key tile, so both softmax
+// groups stay busy side by side on the same K/V stream.
+struct PfItem {
+  int b, h, kvh, qt_a, qt_b, nA, nB, n;
+};
+
+__device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
+  const int BH = a.B * a.Hq;
+  const int pair = a.n_pairs - 1 - it / BH;  // items run longest pairs first
+  const int bh = it % BH;
+  PfItem x;
+  x.b = bh / a.Hq;
+  x.h = bh % a.Hq;
+  x.kvh = x.h / (a.Hq / a.Hkv);
+  x.qt_a = 2 * pair;
+  x.qt_b = 2 * pair + 1;
+  x.nA = 2 * (x.qt_a + 1);  // 64-key tiles up to the tile's last row (causal)
+  x.nB = x.qt_b < a.n_qt ? 2 * (x.qt_b + 1) : 0;
+  x.n = x.nA > x.nB ? x.nA : x.nB;
+  return x;
+}
+
+// The k-th item of this CTA, or -1: rounds of gridDim.x items in snake order
+// (even rounds left to right, odd rounds right to left), which with items
+// sorted by length spreads the work evenly over the persistent CTAs.
+__device__ __forceinline__ int pf_item_index(int k, int n_items) {
+  const int P = (int)gridDim.x, c = (int)blockIdx.x;
+  const int it = k * P + ((k & 1) ? P - 1 - c : c);
+  return it < n_items ? it : -1;
+}
+
+// Persistent: one CTA per SM walks its items (pf_item_index) with three
+// roles.  Warps 0-7 and 8-15 run the softmax of slots A and B, two threads
+// per query row (warp w reads TMEM lanes 32*(w%4)..+31; warps w and w+4 take
+// the two halves of the row's keys and of its O columns and exchange their
+// partial row maxima through shared memory).  Warp 16 owns the TMEM
+// allocation and issues the TMA loads (Q per item, K and V^T per 64-key tile
+// through a ring that runs on across items).  Warp 17 issues the MMAs.  Every
+// barrier's phase is counted across items, so the next item's Q and K/V
+// loads and its first S products overlap the end of the current item, and
+// its first PV waits only until the softmax has read the previous O.
 // Launched with kAttnThreads threads; prefill.cu is compiled with a register
 // cap (build.py) that keeps kAttnThreads x registers within one SM's file.
 __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -245,37 +279,36 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
   unsigned char* sK = sQ + 2 * kQTile;                       // stages x 16 KB
   unsigned char* sV = sK + kKVStages * kKTile;               // stages x 16 KB
   uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile);
-  uint64_t* q_full = bar;                  // 1
-  uint64_t* kv_full = bar + 1;             // kKVStages
+  uint64_t* q_full = bar;                   // 1: Q of the item landed
+  uint64_t* q_empty = q_full + 1;           // 1: the item's S products are done with Q
+  uint64_t* kv_full = q_empty + 1;          // kKVStages
   uint64_t* kv_empty = kv_full + kKVStages;
-  uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of tile i, buffer j % 2
-  uint64_t* p_full = s_full + 4;            // [A0, A1, B0, B1]: P of tile i, buffer j % 2
-  uint64_t* o_done = p_full + 4;            // [A0, A1, B0, B1]: PV(j) of tile i -> j % 2
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 4);
-  float* xch = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + 1024);  // partials
+  uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of slot i, buffer g % 2
+  uint64_t* p_full = s_full + 4;            // [A0, A1, B0, B1]: P of slot i, buffer g % 2
+  uint64_t* o_done = p_full + 4;            // [A0, A1, B0, B1]: PV of slot tile g -> g % 2
+  uint64_t* o_free = o_done + 4;            // [A, B]: the softmax has read O of its item
+  uint64_t* xbar = o_free + 2;              // [A, B]: exchange between the two row halves
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 2);
+  float* xmax = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + kBarBytes);
+  float* xsum = xmax + 2 * 2 * 2 * 128;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BH = a.B * a.Hq;
-  const int pair = a.n_pairs - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
-  const int b = bh / a.Hq, h = bh % a.Hq;
-  const int kvh = h / (a.Hq / a.Hkv);
-  const int qt_a = 2 * pair, qt_b = 2 * pair + 1;
-  const bool two = qt_b < a.n_qt;
-  // 64-key tiles each query tile visits (causal: up to its last row)
-  const int nA = 2 * (qt_a + 1), nB = two ? 2 * (qt_b + 1) : 0;
-  const int n = nA > nB ? nA : nB;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kKVStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);  // one arrival per softmax warp of the tile
+      mbar_init(&p_full[i], 8);  // one arrival per softmax warp of the slot
       mbar_init(&o_done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_free[i], 8);
+      mbar_init(&xbar[i], 8);
     }
     fence_barrier_init();
   }
@@ -289,33 +322,42 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tslot;
-  // TMEM columns: S of tile i, buffer u at 64*(2i+u) (0..255), O_A 256..383,
-  // O_B 384..511.  S is double-buffered so the tensor core computes S(j+1)
-  // while the softmax works on S(j).
+  // TMEM columns: S of slot i, buffer u at 64*(2i+u) (0..255), O_A 256..383,
+  // O_B 384..511.  S is double-buffered so the tensor core computes S(g+1)
+  // while the softmax works on S(g).
   auto tS = [&](int i, int u) { return tbase + 64u * (2 * i + u); };
   auto tO = [&](int i) { return tbase + 256u + 128u * i; };
 
   if (warp == 16) {
     // ======================================================= TMA producer
     // The whole warp runs the schedule; one elected lane issues each copy.
-    mbar_arrive_expect_tx_warp(q_full, two ? 2 * kQTile : kQTile);
-    tma_load_3d_warp(sQ, &tq, h * 128, qt_a * 128, b, q_full);
-    tma_load_3d_warp(sQ + kQTile / 2, &tq, h * 128 + 64, qt_a * 128, b, q_full);
-    if (two) {
-      tma_load_3d_warp(sQ + kQTile, &tq, h * 128, qt_b * 128, b, q_full);
-      tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, h * 128 + 64, qt_b * 128, b, q_full);
-    }
-    for (int j = 0; j < n; ++j) {
-      const int s = j % kKVStages;
-      if (j >= kKVStages && !mbar_wait_warp(&kv_empty[s], ((j / kKVStages) - 1) & 1)) {
-        if (lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-        break;
+    int gk = 0;  // K/V tiles loaded so far (ring position)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int it = pf_item_index(k, a.n_items);
+      if (it < 0) break;
+      const PfItem x = pf_item(a, it);
+      // Q is overwritten once the previous item's S products are done
+      if (k > 0 && !(ok = mbar_wait_warp(q_empty, (k - 1) & 1))) break;
+      mbar_arrive_expect_tx_warp(q_full, x.nB > 0 ? 2 * kQTile : kQTile);
+      tma_load_3d_warp(sQ, &tq, x.h * 128, x.qt_a * 128, x.b, q_full);
+      tma_load_3d_warp(sQ + kQTile / 2, &tq, x.h * 128 + 64, x.qt_a * 128, x.b, q_full);
+      if (x.nB > 0) {
+        tma_load_3d_warp(sQ + kQTile, &tq, x.h * 128, x.qt_b * 128, x.b, q_full);
+        tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, x.h * 128 + 64, x.qt_b * 128, x.b, q_full);
       }
-      mbar_arrive_expect_tx_warp(&kv_full[s], kKTile + kVTile);
-      tma_load_3d_warp(sK + s * kKTile, &tk, kvh * 128, j * 64, b, &kv_full[s]);
-      tma_load_3d_warp(sK + s * kKTile + kKTile / 2, &tk, kvh * 128 + 64, j * 64, b, &kv_full[s]);
-      tma_load_3d_warp(sV + s * kVTile, &tv, j * 64, 0, b * a.Hkv + kvh, &kv_full[s]);
+      for (int j = 0; j < x.n; ++j, ++gk) {
+        const int s = gk % kKVStages;
+        if (gk >= kKVStages && !(ok = mbar_wait_warp(&kv_empty[s], ((gk / kKVStages) - 1) & 1)))
+          break;
+        mbar_arrive_expect_tx_warp(&kv_full[s], kKTile + kVTile);
+        tma_load_3d_warp(sK + s * kKTile, &tk, x.kvh * 128, j * 64, x.b, &kv_full[s]);
+        tma_load_3d_warp(sK + s * kKTile + kKTile / 2, &tk, x.kvh * 128 + 64, j * 64, x.b,
+                         &kv_full[s]);
+        tma_load_3d_warp(sV + s * kVTile, &tv, j * 64, 0, x.b * a.Hkv + x.kvh, &kv_full[s]);
+      }
     }
+    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else if (warp == 17) {
     // ======================================================= MMA issuer
     // The whole warp runs the schedule (operand descriptors stay
@@ -323,169 +365,220 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
     constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
     constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
     const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-    bool ok = mbar_wait_warp(q_full, 0) && mbar_wait_warp(&kv_full[0], 0);
-    auto issue_s = [&](int i, int j) {
-      const int s = j % kKVStages;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
-        const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
-        mma_f16_warp(tS(i, j & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
-                     sw128_kmajor_desc(aK + s * kKTile + koff), kIdS, kk > 0);
-      }
-      mma_commit_warp(&s_full[2 * i + (j & 1)]);
-    };
-    // P(j) sits in TMEM over its S buffer: 64 keys packed two per column
-    auto issue_pv = [&](int i, int j) {
-      const int s = j % kKVStages;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16_ts_warp(tO(i), tS(i, j & 1) + kk * 8, sw128_kmajor_desc(aV + s * kVTile + kk * 32),
-                        kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_warp(&o_done[2 * i + (j & 1)]);
-    };
-    if (ok) {
-      // S runs two tiles ahead of PV: S(j+2) reuses S buffer j%2, free once
-      // the softmax of tile j has signalled P(j)
+    int gk = 0;             // K/V tiles consumed so far
+    int gx[2] = {0, 0};     // tiles of slot A / B so far (S, P and PV barrier phases)
+    int ox[2] = {0, 0};     // items whose O slot A / B has accumulated so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int it = pf_item_index(k, a.n_items);
+      if (it < 0) break;
+      const PfItem x = pf_item(a, it);
+      const int nX[2] = {x.nA, x.nB};
+      ok = mbar_wait_warp(q_full, k & 1) &&
+           mbar_wait_warp(&kv_full[gk % kKVStages], (gk / kKVStages) & 1);
+      if (!ok) break;
       tc_fence_after_sync();
+      int s_left = x.nA + x.nB;  // S products of this item still to issue
+      // S(g) of slot i goes to buffer g % 2; that buffer's previous P (tile
+      // g-2) was consumed by a PV issued before this S
+      auto issue_s = [&](int i, int j) {
+        const int st = (gk + j) % kKVStages;
+        const int g = gx[i] + j;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
+          mma_f16_warp(tS(i, g & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
+                       sw128_kmajor_desc(aK + st * kKTile + koff), kIdS, kk > 0);
+        }
+        mma_commit_warp(&s_full[2 * i + (g & 1)]);
+        if (--s_left == 0) mma_commit_warp(q_empty);  // Q free once these finish
+      };
+      // P(g) sits in TMEM over its S buffer: 64 keys packed two per column
+      auto issue_pv = [&](int i, int j) {
+        const int st = (gk + j) % kKVStages;
+        const int g = gx[i] + j;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_ts_warp(tO(i), tS(i, g & 1) + kk * 8,
+                          sw128_kmajor_desc(aV + st * kVTile + kk * 32), kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_warp(&o_done[2 * i + (g & 1)]);
+      };
+      // S runs two tiles ahead of PV within each slot
       issue_s(0, 0);
-      if (nB > 0) issue_s(1, 0);
-      if (n > 1) {
-        ok = mbar_wait_warp(&kv_full[1 % kKVStages], 0);
+      if (x.nB > 0) issue_s(1, 0);
+      if (x.n > 1) {
+        ok = mbar_wait_warp(&kv_full[(gk + 1) % kKVStages], ((gk + 1) / kKVStages) & 1);
         tc_fence_after_sync();
-        if (ok && 1 < nA) issue_s(0, 1);
-        if (ok && 1 < nB) issue_s(1, 1);
+        if (ok && 1 < x.nA) issue_s(0, 1);
+        if (ok && 1 < x.nB) issue_s(1, 1);
       }
-      for (int j = 0; j < n && ok; ++j) {
-        const bool next2 = j + 2 < n;
-        if (next2) {
-          ok = mbar_wait_warp(&kv_full[(j + 2) % kKVStages], ((j + 2) / kKVStages) & 1);
+      for (int j = 0; j < x.n && ok; ++j) {
+        if (j + 2 < x.n) {
+          ok = mbar_wait_warp(&kv_full[(gk + j + 2) % kKVStages], ((gk + j + 2) / kKVStages) & 1);
           tc_fence_after_sync();
         }
-        if (ok && j < nA) {
-          ok = mbar_wait_warp(&p_full[j & 1], (j >> 1) & 1);
-          tc_fence_after_sync();
-          if (ok) issue_pv(0, j);
-          if (ok && j + 2 < nA) issue_s(0, j + 2);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (ok && j < nX[i]) {
+            const int g = gx[i] + j;
+            ok = mbar_wait_warp(&p_full[2 * i + (g & 1)], (g >> 1) & 1);
+            // the first PV of an item overwrites O: the softmax must have
+            // read the previous item's O first
+            if (ok && j == 0 && ox[i] > 0) ok = mbar_wait_warp(&o_free[i], (ox[i] - 1) & 1);
+            tc_fence_after_sync();
+            if (ok) issue_pv(i, j);
+            if (i == 0 && ok && j + 2 < x.nA) issue_s(0, j + 2);
+          }
         }
-        if (ok && j < nB) {
-          ok = mbar_wait_warp(&p_full[2 + (j & 1)], (j >> 1) & 1);
-          tc_fence_after_sync();
-          if (ok) issue_pv(1, j);
-        }
-        mma_commit_warp(&kv_empty[j % kKVStages]);  // stage free once these MMAs finish
-        if (ok && j + 2 < nB) issue_s(1, j + 2);
+        mma_commit_warp(&kv_empty[(gk + j) % kKVStages]);  // stage free once these finish
+        if (ok && j + 2 < x.nB) issue_s(1, j + 2);
       }
+      gx[0] += x.nA;
+      gx[1] += x.nB;
+      ox[0] += x.nA > 0 ? 1 : 0;
+      ox[1] += x.nB > 0 ? 1 : 0;
+      gk += x.n;
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else {
     // ======================================================= softmax
-    const int i = warp >> 3;                  // 0: tile A, 1: tile B
+    const int i = warp >> 3;                  // 0: slot A, 1: slot B
     const int hh = (warp >> 2) & 1;           // which half of the keys / O columns
-    const int ni = i == 0 ? nA : nB;
     const int row = (warp & 3) * 32 + lane;   // 0..127: TMEM lane = query row
-    const int q0 = (i == 0 ? qt_a : qt_b) * 128;
-    const int qidx = q0 + row;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float* my_x = xch + (i * 2 + hh) * 128 + row;
-    const float* other_x = xch + (i * 2 + (hh ^ 1)) * 128 + row;
-    float m = -INFINITY, l = 0.f;
-    float v[32];
-    bool ok = true;
-    for (int j = 0; j < ni && ok; ++j) {
-      ok = mbar_wait(&s_full[2 * i + (j & 1)], (j >> 1) & 1);
-      tc_fence_after_sync();
-      tmem_ld32(tS(i, j & 1) + lane_off + 32 * hh, v);
-      tmem_wait_ld();
-      const int key0 = j * 64 + 32 * hh;
-      if (key0 + 31 > q0) {  // some keys of this half lie past some rows
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (key0 + c > qidx) v[c] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(v[e + 16], v[e + 24]));
-      float pmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // the row max needs both halves; the barrier also orders both halves'
-      // TMEM reads of S before either overwrites part of it with P
-      *my_x = pmax;
-      tc_fence_before_sync();
-      named_bar(1 + i, 256);
-      tc_fence_after_sync();
-      const float tmax = fmaxf(pmax, *other_x) * a.sl2e;
-      // rescale O only when the row max grew by more than 2^8 (both halves
-      // decide alike: same inputs)
-      const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
-      const bool grow = j > 0 && m_new != m;
-      if (__any_sync(0xffffffffu, grow)) {
-        // O may be touched only once PV(j-1) is done.  PV(j-1) completes
-        // phase (j-1)/2 of o_done[(j-1)%2]; that barrier is at most one phase
-        // behind it (S(j) is done, so PV(j-3) is) and cannot be ahead of it
-        // (PV(j+1) needs P(j+1)), so the parity wait is unambiguous.
-        ok = ok && mbar_wait(&o_done[2 * i + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
-        tc_fence_after_sync();
-        const float alpha = grow ? ex2f(m - m_new) : 1.0f;
-        float o[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld16(tO(i) + lane_off + 64 * hh + c * 16, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tmem_st16(tO(i) + lane_off + 64 * hh + c * 16, o);
-        }
-        tmem_wait_st();
-        l *= alpha;
-      }
-      m = m_new;
-      // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into TMEM
-      // columns 16*hh .. 16*hh+15 of this S buffer (both halves have read
-      // their S columns before the exchange barrier above)
-      const float2 c2 = make_float2(a.sl2e, a.sl2e), nm2 = make_float2(-m, -m);
-      float2 ls = make_float2(0.f, 0.f);
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 x = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
-        const float2 pe = make_float2(ex2f(x.x), ex2f(x.y));
-        ls = make_float2(ls.x + pe.x, ls.y + pe.y);
-        const __half2 hp = __floats2half2_rn(pe.x, pe.y);
-        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
-      }
-      l += ls.x + ls.y;
-      // P(j) goes over S buffer j % 2, which PV(j-1) does not read; each warp
-      // publishes its rows once its stores are done
-      tmem_st16u(tS(i, j & 1) + lane_off + 16 * hh, pk);
-      tmem_wait_st();
+    // The two halves of a row meet through xbar[i] (8 warps, one arrival
+    // each); xe counts its completed phases.  All waits are warp-uniform and
+    // bounded, so a timeout ends every role's loop instead of stranding a
+    // warp at a barrier.
+    int xe = 0;
+    auto exchange = [&]() -> bool {
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[2 * i + (j & 1)]);
-    }
-    if (!ok) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-    // ---- O / l to global memory once the last PV is done (l: both halves)
-    *my_x = l;
-    named_bar(1 + i, 256);
-    const float ltot = l + *other_x;
-    // PV(ni-1) is the last; S(ni-1) is done, so PV(ni-3) is and the parity
-    // wait is unambiguous
-    if (ni > 0 && ok && mbar_wait(&o_done[2 * i + ((ni - 1) & 1)], ((ni - 1) >> 1) & 1)) {
+      if (lane == 0) mbar_arrive(&xbar[i]);
+      const bool r = mbar_wait_warp(&xbar[i], xe & 1);
+      ++xe;
       tc_fence_after_sync();
-      const float inv = 1.0f / ltot;
+      return r;
+    };
+    int g = 0;  // tiles of this slot so far
+    bool ok = true;
+    float v[32];
+    for (int k = 0; ok; ++k) {
+      const int it = pf_item_index(k, a.n_items);
+      if (it < 0) break;
+      const PfItem x = pf_item(a, it);
+      const int ni = i == 0 ? x.nA : x.nB;
+      if (ni == 0) continue;
+      const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
+      const int qidx = q0 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < ni && ok; ++j, ++g) {
+        ok = mbar_wait_warp(&s_full[2 * i + (g & 1)], (g >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after_sync();
+        tmem_ld32(tS(i, g & 1) + lane_off + 32 * hh, v);
+        tmem_wait_ld();
+        const int key0 = j * 64 + 32 * hh;
+        if (key0 + 31 > q0) {  // some keys of this half lie past some rows
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (key0 + c > qidx) v[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(v[e + 16], v[e + 24]));
+        const float pmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // the row max needs both halves; the exchange also orders both
+        // halves' TMEM reads of S before either overwrites part of it with P.
+        // Buffers alternate with the tile, so a half never overwrites a value
+        // its partner has yet to read.
+        float* xb = xmax + ((g & 1) * 2 + i) * 256;
+        xb[hh * 128 + row] = pmax;
+        ok = exchange();
+        if (!ok) break;
+        const float tmax = fmaxf(pmax, xb[(hh ^ 1) * 128 + row]) * a.sl2e;
+        // rescale O only when the row max grew by more than 2^8 (both halves
+        // decide alike: same inputs)
+        const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
+        const bool grow = j > 0 && m_new != m;
+        if (__any_sync(0xffffffffu, grow)) {
+          // O may be touched only once PV(g-1) is done.  PV(g-1) completes a
+          // phase of o_done[(g-1)%2] that is at most one behind (S(g) is done,
+          // so PV(g-3) is) and never ahead (PV(g+1) needs P(g+1)).
+          ok = mbar_wait_warp(&o_done[2 * i + ((g - 1) & 1)], ((g - 1) >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const float alpha = grow ? ex2f(m - m_new) : 1.0f;
+          float o[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld16(tO(i) + lane_off + 64 * hh + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            tmem_st16(tO(i) + lane_off + 64 * hh + c * 16, o);
+          }
+          tmem_wait_st();
+          l *= alpha;
+        }
+        m = m_new;
+        // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into TMEM
+        // columns 16*hh .. 16*hh+15 of this S buffer
+        const float2 c2 = make_float2(a.sl2e, a.sl2e), nm2 = make_float2(-m, -m);
+        float2 ls = make_float2(0.f, 0.f);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 xv = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
+          const float2 pe = make_float2(ex2f(xv.x), ex2f(xv.y));
+          ls = make_float2(ls.x + pe.x, ls.y + pe.y);
+          const __half2 hp = __floats2half2_rn(pe.x, pe.y);
+          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        l += ls.x + ls.y;
+        // P(g) goes over S buffer g % 2, which PV(g-1) does not read; each
+        // warp publishes its rows once its stores are done
+        tmem_st16u(tS(i, g & 1) + lane_off + 16 * hh, pk);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[2 * i + (g & 1)]);
+      }
+      if (!ok) break;
+      // ---- the item's O: row sum of both halves, then O from TMEM once its
+      // last PV is done; O is released to the next item as soon as it is read
+      float* xs = xsum + i * 256;
+      xs[hh * 128 + row] = l;
+      ok = exchange();
+      if (!ok) break;
+      const float inv = 1.0f / (l + xs[(hh ^ 1) * 128 + row]);
+      const int gl = g - 1;  // PV(gl) is the last; S(gl) is done, so PV(gl-2) is
+      ok = mbar_wait_warp(&o_done[2 * i + (gl & 1)], (gl >> 1) & 1);
+      if (!ok) break;
+      tc_fence_after_sync();
+      float* dst = a.out + (((int64_t)x.b * a.T + qidx) * a.Hq + x.h) * kPrefillHD + 64 * hh;
+      const bool in_range = qidx < a.T;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tO(i) + lane_off + 64 * hh + c * 32, v);
         tmem_wait_ld();
-        if (qidx < a.T) {
-          float* dst = a.out + (((int64_t)b * a.T + qidx) * a.Hq + h) * kPrefillHD + 64 * hh + c * 32;
+        if (c == 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[i]);
+        }
+        if (in_range) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + e) =
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
                 make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
         }
       }
     }
+    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -645,10 +738,14 @@ extern "C" int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, in
   aa.Hkv = kv_heads;
   aa.n_qt = (T + 127) / 128;
   aa.n_pairs = (aa.n_qt + 1) / 2;
+  aa.n_items = aa.n_pairs * B * q_heads;
   aa.sl2e = scale * kLog2eP;
   aa.out = out;
   aa.dev_err = dev_err;
-  cudaError_t e = launch_pdl(prefill_attn_kernel, dim3(aa.n_pairs * B * q_heads),
+  const int sms = device_sm_count();
+  if (sms <= 0) return ASR_ERR_CUDA;
+  const int ctas = aa.n_items < sms ? aa.n_items : sms;  // persistent: one per SM
+  cudaError_t e = launch_pdl(prefill_attn_kernel, dim3(ctas),
                              dim3(kAttnThreads), (size_t)kAttnSmem, (cudaStream_t)stream, tq, tk,
                              tv, aa);
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
