@@ -16,11 +16,9 @@ ROOT = os.path.dirname(HERE)
 HEADERS = [os.path.join(ROOT, "include", "asrkv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# per-file flags: the prefill attention kernel runs 576 threads (18 warps) per
-# CTA.  Registers are allocated per SM sub-partition, and 18 warps put 5 warps
-# on some of the four, so each thread may hold at most 16384 / (5 * 32) = 102
-# registers, i.e. 96 in the allocation granule of 8.
-EXTRA = {"prefill.cu": ["-maxrregcount=96"]}
+# per-file flags (none at present: each kernel's __launch_bounds__ sets its
+# register budget)
+EXTRA = {}
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]
 

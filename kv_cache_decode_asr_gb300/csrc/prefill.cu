@@ -210,14 +210,13 @@ struct PrefillAttnArgs {
   int32_t* dev_err;
 };
 
-constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16
-constexpr int kKTile = 64 * 128 * 2;      // 64 keys x 128 dims
-constexpr int kVTile = 128 * 64 * 2;      // V^T: 128 dims x 64 keys
-constexpr int kKVStages = 4;
+constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16 (two 64-dim halves)
+constexpr int kKTile = 128 * 128 * 2;     // 128 keys x 128 dims (two 64-dim halves)
+constexpr int kVTile = 128 * 128 * 2;     // V^T: 128 dims x 128 keys (two 64-key halves)
+constexpr int kKVStages = 2;
 constexpr int kBarBytes = 1024;           // mbarriers and the TMEM address
-constexpr int kXchBytes = 6 * 1024;       // row maxima [tile parity][slot][half][128], row sums [slot][half][128]
-constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + kBarBytes + kXchBytes + 1024;
-constexpr int kAttnThreads = 576;  // warps 0-7, 8-15: softmax of slots A, B; 16: TMA; 17: MMA
+constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + kBarBytes + 1024;
+constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: TMA; 9: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -228,8 +227,7 @@ __device__ __forceinline__ float ex2f(float x) {
 
 // One work item: two adjacent query tiles of one (sequence, head), tile A =
 // 2p in slot A and tile B = 2p+1 in slot B (a lone last tile when n_qt is
-// odd).  Their causal lengths differ by one 128-key tile, so both softmax
-// groups stay busy side by side on the same K/V stream.
+// odd).  Key tiles are 128 keys, so slot B visits one tile more than slot A.
 struct PfItem {
   int b, h, kvh, qt_a, qt_b, nA, nB, n;
 };
@@ -244,8 +242,8 @@ __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   x.kvh = x.h / (a.Hq / a.Hkv);
   x.qt_a = 2 * pair;
   x.qt_b = 2 * pair + 1;
-  x.nA = 2 * (x.qt_a + 1);  // 64-key tiles up to the tile's last row (causal)
-  x.nB = x.qt_b < a.n_qt ? 2 * (x.qt_b + 1) : 0;
+  x.nA = x.qt_a + 1;  // 128-key tiles up to the tile's last row (causal)
+  x.nB = x.qt_b < a.n_qt ? x.qt_b + 1 : 0;
   x.n = x.nA > x.nB ? x.nA : x.nB;
   return x;
 }
@@ -260,37 +258,38 @@ __device__ __forceinline__ int pf_item_index(int k, int n_items) {
 }
 
 // Persistent: one CTA per SM walks its items (pf_item_index) with three
-// roles.  Warps 0-7 and 8-15 run the softmax of slots A and B, two threads
-// per query row (warp w reads TMEM lanes 32*(w%4)..+31; warps w and w+4 take
-// the two halves of the row's keys and of its O columns and exchange their
-// partial row maxima through shared memory).  Warp 16 owns the TMEM
-// allocation and issues the TMA loads (Q per item, K and V^T per 64-key tile
-// through a ring that runs on across items).  Warp 17 issues the MMAs.  Every
-// barrier's phase is counted across items, so the next item's Q and K/V
-// loads and its first S products overlap the end of the current item, and
-// its first PV waits only until the softmax has read the previous O.
-// Launched with kAttnThreads threads; prefill.cu is compiled with a register
-// cap (build.py) that keeps kAttnThreads x registers within one SM's file.
-__global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                        const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
+// roles.  Warps 0-3 and 4-7 run the softmax of slots A and B, one thread per
+// query row (warp w reads TMEM lanes 32*(w%4)..+31) holding the row's 128
+// scores of a key tile.  Warp 8 owns the TMEM allocation and issues the TMA
+// loads (Q per item; K and V^T per 128-key tile through two-stage rings
+// that run on across items).  Warp 9 issues the MMAs.  Each slot has one S
+// buffer: while one slot's softmax turns its S into P, the tensor core runs
+// the other slot's PV and next S (ping-pong), so with the softmax shorter
+// than a slot's MMA work the tensor core stays busy.  K and V^T have rings
+// of their own: K of a tile is free after its S products, one tile before
+// its V^T, so the next K loads well ahead of its S.  Every barrier's phase
+// is counted across items, so the next item's loads and first S products
+// overlap the end of the current item.
+__global__ void __launch_bounds__(kAttnThreads, 1)
+prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char* sQ = smem;                                  // [A, B] x 32 KB
-  unsigned char* sK = sQ + 2 * kQTile;                       // stages x 16 KB
-  unsigned char* sV = sK + kKVStages * kKTile;               // stages x 16 KB
+  unsigned char* sK = sQ + 2 * kQTile;                       // stages x 32 KB
+  unsigned char* sV = sK + kKVStages * kKTile;               // stages x 32 KB
   uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile);
   uint64_t* q_full = bar;                   // 1: Q of the item landed
   uint64_t* q_empty = q_full + 1;           // 1: the item's S products are done with Q
-  uint64_t* kv_full = q_empty + 1;          // kKVStages
-  uint64_t* kv_empty = kv_full + kKVStages;
-  uint64_t* s_full = kv_empty + kKVStages;  // [A0, A1, B0, B1]: S of slot i, buffer g % 2
-  uint64_t* p_full = s_full + 4;            // [A0, A1, B0, B1]: P of slot i, buffer g % 2
-  uint64_t* o_done = p_full + 4;            // [A0, A1, B0, B1]: PV of slot tile g -> g % 2
-  uint64_t* o_free = o_done + 4;            // [A, B]: the softmax has read O of its item
-  uint64_t* xbar = o_free + 2;              // [A, B]: exchange between the two row halves
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(xbar + 2);
-  float* xmax = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bar) + kBarBytes);
-  float* xsum = xmax + 2 * 2 * 2 * 128;
+  uint64_t* k_full = q_empty + 1;           // kKVStages each
+  uint64_t* k_empty = k_full + kKVStages;
+  uint64_t* v_full = k_empty + kKVStages;
+  uint64_t* v_empty = v_full + kKVStages;
+  uint64_t* s_full = v_empty + kKVStages;   // [A, B]: S of the slot's tile g (phase g)
+  uint64_t* p_full = s_full + 2;            // [A, B]: P of the slot's tile g
+  uint64_t* o_done = p_full + 2;            // [A, B]: the slot's last PV of an item
+  uint64_t* o_free = o_done + 2;            // [A, B]: the softmax has read O of its item
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_free + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -298,21 +297,20 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kKVStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);  // one arrival per softmax warp of the slot
-      mbar_init(&o_done[i], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&o_free[i], 8);
-      mbar_init(&xbar[i], 8);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);  // one arrival per softmax warp of the slot
+      mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], 4);
     }
     fence_barrier_init();
   }
-  if (warp == 16) {
+  if (warp == 8) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -322,13 +320,12 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tslot;
-  // TMEM columns: S of slot i, buffer u at 64*(2i+u) (0..255), O_A 256..383,
-  // O_B 384..511.  S is double-buffered so the tensor core computes S(g+1)
-  // while the softmax works on S(g).
-  auto tS = [&](int i, int u) { return tbase + 64u * (2 * i + u); };
+  // TMEM columns: S/P of slot i at 128*i (P: 128 keys packed two per column
+  // over the first 64), O_A at 256, O_B at 384.
+  auto tS = [&](int i) { return tbase + 128u * i; };
   auto tO = [&](int i) { return tbase + 256u + 128u * i; };
 
-  if (warp == 16) {
+  if (warp == 8) {
     // ======================================================= TMA producer
     // The whole warp runs the schedule; one elected lane issues each copy.
     int gk = 0;  // K/V tiles loaded so far (ring position)
@@ -337,103 +334,109 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
       const PfItem x = pf_item(a, it);
-      // Q is overwritten once the previous item's S products are done
-      if (k > 0 && !(ok = mbar_wait_warp(q_empty, (k - 1) & 1))) break;
-      mbar_arrive_expect_tx_warp(q_full, x.nB > 0 ? 2 * kQTile : kQTile);
-      tma_load_3d_warp(sQ, &tq, x.h * 128, x.qt_a * 128, x.b, q_full);
-      tma_load_3d_warp(sQ + kQTile / 2, &tq, x.h * 128 + 64, x.qt_a * 128, x.b, q_full);
-      if (x.nB > 0) {
-        tma_load_3d_warp(sQ + kQTile, &tq, x.h * 128, x.qt_b * 128, x.b, q_full);
-        tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, x.h * 128 + 64, x.qt_b * 128, x.b, q_full);
-      }
       for (int j = 0; j < x.n; ++j, ++gk) {
         const int s = gk % kKVStages;
-        if (gk >= kKVStages && !(ok = mbar_wait_warp(&kv_empty[s], ((gk / kKVStages) - 1) & 1)))
-          break;
-        mbar_arrive_expect_tx_warp(&kv_full[s], kKTile + kVTile);
-        tma_load_3d_warp(sK + s * kKTile, &tk, x.kvh * 128, j * 64, x.b, &kv_full[s]);
-        tma_load_3d_warp(sK + s * kKTile + kKTile / 2, &tk, x.kvh * 128 + 64, j * 64, x.b,
-                         &kv_full[s]);
-        tma_load_3d_warp(sV + s * kVTile, &tv, j * 64, 0, x.b * a.Hkv + x.kvh, &kv_full[s]);
+        const uint32_t ph = ((gk / kKVStages) - 1) & 1;
+        unsigned char* kd = sK + s * kKTile;
+        unsigned char* vd = sV + s * kVTile;
+        if (gk >= kKVStages && !(ok = mbar_wait_warp(&k_empty[s], ph))) break;
+        mbar_arrive_expect_tx_warp(&k_full[s], kKTile);
+        tma_load_3d_warp(kd, &tk, x.kvh * 128, j * 128, x.b, &k_full[s]);
+        tma_load_3d_warp(kd + kKTile / 2, &tk, x.kvh * 128 + 64, j * 128, x.b, &k_full[s]);
+        if (gk >= kKVStages && !(ok = mbar_wait_warp(&v_empty[s], ph))) break;
+        mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
+        tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+        tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+        if (j == 0) {
+          // Q after the item's first K/V tile (which need not wait for it):
+          // Q is overwritten once the previous item's S products are done
+          if (k > 0 && !(ok = mbar_wait_warp(q_empty, (k - 1) & 1))) break;
+          mbar_arrive_expect_tx_warp(q_full, x.nB > 0 ? 2 * kQTile : kQTile);
+          tma_load_3d_warp(sQ, &tq, x.h * 128, x.qt_a * 128, x.b, q_full);
+          tma_load_3d_warp(sQ + kQTile / 2, &tq, x.h * 128 + 64, x.qt_a * 128, x.b, q_full);
+          if (x.nB > 0) {
+            tma_load_3d_warp(sQ + kQTile, &tq, x.h * 128, x.qt_b * 128, x.b, q_full);
+            tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, x.h * 128 + 64, x.qt_b * 128, x.b,
+                             q_full);
+          }
+        }
       }
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-  } else if (warp == 17) {
+  } else if (warp == 9) {
     // ======================================================= MMA issuer
     // The whole warp runs the schedule (operand descriptors stay
     // warp-uniform); one elected lane issues each tcgen05 operation.
-    constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 64);    // S = Q K^T: 128 x 64
+    constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 128);   // S = Q K^T: 128 x 128
     constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
     const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-    int gk = 0;             // K/V tiles consumed so far
-    int gx[2] = {0, 0};     // tiles of slot A / B so far (S, P and PV barrier phases)
-    int ox[2] = {0, 0};     // items whose O slot A / B has accumulated so far
+    int gk = 0;          // K/V tiles consumed so far
+    int gx[2] = {0, 0};  // tiles of slot A / B so far (S and P phases)
+    int ox[2] = {0, 0};  // items whose O slot A / B has accumulated so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
       const PfItem x = pf_item(a, it);
       const int nX[2] = {x.nA, x.nB};
-      ok = mbar_wait_warp(q_full, k & 1) &&
-           mbar_wait_warp(&kv_full[gk % kKVStages], (gk / kKVStages) & 1);
+      ok = mbar_wait_warp(q_full, k & 1);
       if (!ok) break;
-      tc_fence_after_sync();
       int s_left = x.nA + x.nB;  // S products of this item still to issue
-      // S(g) of slot i goes to buffer g % 2; that buffer's previous P (tile
-      // g-2) was consumed by a PV issued before this S
+      // S of slot i for key tile j; the slot's S buffer holds P of its
+      // previous tile, read by a PV issued before this S
       auto issue_s = [&](int i, int j) {
         const int st = (gk + j) % kKVStages;
-        const int g = gx[i] + j;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
-          mma_f16_warp(tS(i, g & 1), sw128_kmajor_desc(aQ + i * kQTile + off),
+          mma_f16_warp(tS(i), sw128_kmajor_desc(aQ + i * kQTile + off),
                        sw128_kmajor_desc(aK + st * kKTile + koff), kIdS, kk > 0);
         }
-        mma_commit_warp(&s_full[2 * i + (g & 1)]);
+        mma_commit_warp(&s_full[i]);
         if (--s_left == 0) mma_commit_warp(q_empty);  // Q free once these finish
       };
-      // P(g) sits in TMEM over its S buffer: 64 keys packed two per column
+      // O += P V for key tile j: P (TMEM, 8 columns per 16 keys) times V^T
+      // (shared memory, 64-key halves)
       auto issue_pv = [&](int i, int j) {
         const int st = (gk + j) % kKVStages;
-        const int g = gx[i] + j;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16_ts_warp(tO(i), tS(i, g & 1) + kk * 8,
-                          sw128_kmajor_desc(aV + st * kVTile + kk * 32), kIdO,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_warp(&o_done[2 * i + (g & 1)]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
+                          sw128_kmajor_desc(aV + st * kVTile + (kk >> 2) * (kVTile / 2) +
+                                            (kk & 3) * 32),
+                          kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        if (j == nX[i] - 1) mma_commit_warp(&o_done[i]);  // the item's O is complete
       };
-      // S runs two tiles ahead of PV within each slot
-      issue_s(0, 0);
-      if (x.nB > 0) issue_s(1, 0);
-      if (x.n > 1) {
-        ok = mbar_wait_warp(&kv_full[(gk + 1) % kKVStages], ((gk + 1) / kKVStages) & 1);
-        tc_fence_after_sync();
-        if (ok && 1 < x.nA) issue_s(0, 1);
-        if (ok && 1 < x.nB) issue_s(1, 1);
-      }
+      // K of tile j is free once both slots' S products for it are issued
+      // (commit: once they finish); V^T of tile j once both slots' PVs are
+      auto k_ready = [&](int j) {
+        return mbar_wait_warp(&k_full[(gk + j) % kKVStages], ((gk + j) / kKVStages) & 1);
+      };
+      ok = k_ready(0);
+      tc_fence_after_sync();
+      if (ok) issue_s(0, 0);
+      if (ok && x.nB > 0) issue_s(1, 0);
+      if (ok) mma_commit_warp(&k_empty[gk % kKVStages]);
       for (int j = 0; j < x.n && ok; ++j) {
-        if (j + 2 < x.n) {
-          ok = mbar_wait_warp(&kv_full[(gk + j + 2) % kKVStages], ((gk + j + 2) / kKVStages) & 1);
-          tc_fence_after_sync();
-        }
+        const int st = (gk + j) % kKVStages;
+        ok = mbar_wait_warp(&v_full[st], ((gk + j) / kKVStages) & 1);
+        if (ok && j + 1 < x.n) ok = k_ready(j + 1);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (ok && j < nX[i]) {
             const int g = gx[i] + j;
-            ok = mbar_wait_warp(&p_full[2 * i + (g & 1)], (g >> 1) & 1);
+            ok = mbar_wait_warp(&p_full[i], g & 1);
             // the first PV of an item overwrites O: the softmax must have
             // read the previous item's O first
             if (ok && j == 0 && ox[i] > 0) ok = mbar_wait_warp(&o_free[i], (ox[i] - 1) & 1);
             tc_fence_after_sync();
             if (ok) issue_pv(i, j);
-            if (i == 0 && ok && j + 2 < x.nA) issue_s(0, j + 2);
+            if (ok && j + 1 < nX[i]) issue_s(i, j + 1);
           }
         }
-        mma_commit_warp(&kv_empty[(gk + j) % kKVStages]);  // stage free once these finish
-        if (ok && j + 2 < x.nB) issue_s(1, j + 2);
+        mma_commit_warp(&v_empty[st]);                               // V^T of tile j
+        if (j + 1 < x.n) mma_commit_warp(&k_empty[(gk + j + 1) % kKVStages]);  // K of tile j+1
       }
       gx[0] += x.nA;
       gx[1] += x.nB;
@@ -444,27 +447,13 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else {
     // ======================================================= softmax
-    const int i = warp >> 3;                  // 0: slot A, 1: slot B
-    const int hh = (warp >> 2) & 1;           // which half of the keys / O columns
+    const int i = warp >> 2;                  // 0: slot A, 1: slot B
     const int row = (warp & 3) * 32 + lane;   // 0..127: TMEM lane = query row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    // The two halves of a row meet through xbar[i] (8 warps, one arrival
-    // each); xe counts its completed phases.  All waits are warp-uniform and
-    // bounded, so a timeout ends every role's loop instead of stranding a
-    // warp at a barrier.
-    int xe = 0;
-    auto exchange = [&]() -> bool {
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[i]);
-      const bool r = mbar_wait_warp(&xbar[i], xe & 1);
-      ++xe;
-      tc_fence_after_sync();
-      return r;
-    };
-    int g = 0;  // tiles of this slot so far
+    int g = 0;   // tiles of this slot so far (phase of s_full / p_full)
+    int ox = 0;  // items of this slot so far (phase of o_done)
     bool ok = true;
-    float v[32];
+    float v[128];
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
@@ -475,114 +464,97 @@ __global__ void prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, cons
       const int qidx = q0 + row;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < ni && ok; ++j, ++g) {
-        ok = mbar_wait_warp(&s_full[2 * i + (g & 1)], (g >> 1) & 1);
+        // S(g) done also means the slot's PV(g-1) is done: it was issued
+        // before S(g), and tcgen05 operations of one thread complete in order
+        ok = mbar_wait_warp(&s_full[i], g & 1);
         if (!ok) break;
         tc_fence_after_sync();
-        tmem_ld32(tS(i, g & 1) + lane_off + 32 * hh, v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS(i) + lane_off + 32 * c, v + 32 * c);
         tmem_wait_ld();
-        const int key0 = j * 64 + 32 * hh;
-        if (key0 + 31 > q0) {  // some keys of this half lie past some rows
+        if (j == ni - 1) {  // the diagonal tile: keys past the row are masked
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (key0 + c > qidx) v[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c > row) v[c] = -INFINITY;
         }
-        float mx[8];
+        float mx[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(v[e], v[e + 8]), fmaxf(v[e + 16], v[e + 24]));
-        const float pmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        // the row max needs both halves; the exchange also orders both
-        // halves' TMEM reads of S before either overwrites part of it with P.
-        // Buffers alternate with the tile, so a half never overwrites a value
-        // its partner has yet to read.
-        float* xb = xmax + ((g & 1) * 2 + i) * 256;
-        xb[hh * 128 + row] = pmax;
-        ok = exchange();
-        if (!ok) break;
-        const float tmax = fmaxf(pmax, xb[(hh ^ 1) * 128 + row]) * a.sl2e;
-        // rescale O only when the row max grew by more than 2^8 (both halves
-        // decide alike: same inputs)
+        for (int e = 0; e < 16; ++e)
+          mx[e] = fmaxf(fmaxf(fmaxf(v[e], v[e + 16]), fmaxf(v[e + 32], v[e + 48])),
+                        fmaxf(fmaxf(v[e + 64], v[e + 80]), fmaxf(v[e + 96], v[e + 112])));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+        const float tmax = mx[0] * a.sl2e;
+        // rescale O only when the row max grew by more than 2^8
         const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
         const bool grow = j > 0 && m_new != m;
         if (__any_sync(0xffffffffu, grow)) {
-          // O may be touched only once PV(g-1) is done.  PV(g-1) completes a
-          // phase of o_done[(g-1)%2] that is at most one behind (S(g) is done,
-          // so PV(g-3) is) and never ahead (PV(g+1) needs P(g+1)).
-          ok = mbar_wait_warp(&o_done[2 * i + ((g - 1) & 1)], ((g - 1) >> 1) & 1);
-          if (!ok) break;
-          tc_fence_after_sync();
           const float alpha = grow ? ex2f(m - m_new) : 1.0f;
           float o[16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld16(tO(i) + lane_off + 64 * hh + c * 16, o);
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            tmem_ld16(tO(i) + lane_off + c * 16, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] *= alpha;
-            tmem_st16(tO(i) + lane_off + 64 * hh + c * 16, o);
+            tmem_st16(tO(i) + lane_off + c * 16, o);
           }
           tmem_wait_st();
           l *= alpha;
         }
         m = m_new;
-        // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into TMEM
-        // columns 16*hh .. 16*hh+15 of this S buffer
+        // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into the
+        // first 64 columns of the S buffer (all of S is in registers)
         const float2 c2 = make_float2(a.sl2e, a.sl2e), nm2 = make_float2(-m, -m);
         float2 ls = make_float2(0.f, 0.f);
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 xv = ffma2(make_float2(v[e], v[e + 1]), c2, nm2);
-          const float2 pe = make_float2(ex2f(xv.x), ex2f(xv.y));
-          ls = make_float2(ls.x + pe.x, ls.y + pe.y);
-          const __half2 hp = __floats2half2_rn(pe.x, pe.y);
-          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 xv = ffma2(make_float2(v[32 * c + e], v[32 * c + e + 1]), c2, nm2);
+            const float2 pe = make_float2(ex2f(xv.x), ex2f(xv.y));
+            ls = make_float2(ls.x + pe.x, ls.y + pe.y);
+            const __half2 hp = __floats2half2_rn(pe.x, pe.y);
+            pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+          }
+          tmem_st16u(tS(i) + lane_off + 16 * c, pk);
         }
         l += ls.x + ls.y;
-        // P(g) goes over S buffer g % 2, which PV(g-1) does not read; each
-        // warp publishes its rows once its stores are done
-        tmem_st16u(tS(i, g & 1) + lane_off + 16 * hh, pk);
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[2 * i + (g & 1)]);
+        if (lane == 0) mbar_arrive(&p_full[i]);
       }
       if (!ok) break;
-      // ---- the item's O: row sum of both halves, then O from TMEM once its
-      // last PV is done; O is released to the next item as soon as it is read
-      float* xs = xsum + i * 256;
-      xs[hh * 128 + row] = l;
-      ok = exchange();
-      if (!ok) break;
-      const float inv = 1.0f / (l + xs[(hh ^ 1) * 128 + row]);
-      const int gl = g - 1;  // PV(gl) is the last; S(gl) is done, so PV(gl-2) is
-      ok = mbar_wait_warp(&o_done[2 * i + (gl & 1)], (gl >> 1) & 1);
+      // ---- the item's O once its last PV is done; O is released to the
+      // next item as soon as it is in registers
+      ok = mbar_wait_warp(&o_done[i], ox & 1);
+      ++ox;
       if (!ok) break;
       tc_fence_after_sync();
-      float* dst = a.out + (((int64_t)x.b * a.T + qidx) * a.Hq + x.h) * kPrefillHD + 64 * hh;
-      const bool in_range = qidx < a.T;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32(tO(i) + lane_off + 64 * hh + c * 32, v);
-        tmem_wait_ld();
-        if (c == 1) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&o_free[i]);
-        }
-        if (in_range) {
+      for (int c = 0; c < 4; ++c) tmem_ld32(tO(i) + lane_off + 32 * c, v + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[i]);
+      if (qidx < a.T) {
+        const float inv = 1.0f / l;
+        float* dst = a.out + (((int64_t)x.b * a.T + qidx) * a.Hq + x.h) * kPrefillHD;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
-        }
+        for (int e = 0; e < 128; e += 4)
+          *reinterpret_cast<float4*>(dst + e) =
+              make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
       }
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 16) {
+  if (warp == 8) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, 512);
   }
@@ -727,7 +699,7 @@ extern "C" int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, in
                         (uint64_t)q_heads * kPrefillHD * 2, (uint64_t)T * q_heads * kPrefillHD * 2,
                         64, 128) ||
       !make_tmap_f16_3d(&tk, cache, (uint64_t)row, capacity, B, (uint64_t)row * 2,
-                        (uint64_t)seq_stride * 2, 64, 64) ||
+                        (uint64_t)seq_stride * 2, 64, 128) ||
       !make_tmap_f16_3d(&tv, ws_vt(ws, B, T, q_heads), Tpad, kPrefillHD, (uint64_t)B * kv_heads,
                         (uint64_t)Tpad * 2, (uint64_t)Tpad * kPrefillHD * 2, 64, 128))
     return ASR_ERR_CUDA;
