@@ -134,6 +134,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Hint: bring `bytes` of global memory at `src` into L2 (no destination, no
+// completion to wait for).  src 16-byte aligned; bytes a multiple of 16.  A
+// prefetch changes no memory and is never observed by loads, so it is safe
+// even on data another kernel may still be writing.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -40,10 +40,11 @@ namespace asrkv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
-// In-place exclusive scan of data[0..n) over the whole block; data[n] gets
-// the total.  tmp: 32 ints of shared memory.  All threads must call it.
-__device__ void block_scan_excl(int* data, int n, int* tmp) {
-  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// In-place exclusive scan of data[0..n) by threads 0..nt-1 (nt a multiple of
+// 32; they synchronise on named barrier 1); data[n] gets the total.  tmp: 32
+// ints of shared memory.  All nt threads must call it.
+__device__ void block_scan_excl(int* data, int n, int* tmp, int nt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = (nt + 31) >> 5;
   const int chunk = (n + nt - 1) / nt;
   const int s = min(tid * chunk, n), e = min(s + chunk, n);
@@ -56,7 +57,7 @@ __device__ void block_scan_excl(int* data, int n, int* tmp) {
     if (lane >= o) incl += t;
   }
   if (lane == 31) tmp[warp] = incl;
-  __syncthreads();
+  named_bar(1, nt);
   if (warp == 0) {
     const int v = lane < nw ? tmp[lane] : 0;
     int inc = v;
@@ -67,7 +68,7 @@ __device__ void block_scan_excl(int* data, int n, int* tmp) {
     }
     if (lane < nw) tmp[lane] = inc - v;
   }
-  __syncthreads();
+  named_bar(1, nt);
   int run = tmp[warp] + incl - local;
   for (int i = s; i < e; ++i) {
     const int v = data[i];
@@ -76,7 +77,45 @@ __device__ void block_scan_excl(int* data, int n, int* tmp) {
   }
   if (s < e && e == n) data[n] = run;
   if (n == 0 && tid == 0) data[0] = 0;
-  __syncthreads();
+  named_bar(1, nt);
+}
+
+// History rows of one self / GQA source that the call streams, from its
+// length entry (0 for an out-of-range entry).  Self: keys including the new
+// token, less the appended one; GQA: n_past, the rows cached before the new
+// token.
+__device__ __forceinline__ int streamed_rows(const DecodeArgs& a, int v) {
+  if (a.mode == kModeSelf) return (v >= 1 && v <= a.capacity) ? v - a.append : 0;
+  return (v >= 0 && v < a.capacity) ? v : 0;
+}
+
+// Exclusive scan by one warp of the streamed-row counts of every self / GQA
+// source (plus its virtual rows) into off[0..S]; returns the total.
+__device__ int warp_scan_sources(const DecodeArgs& a, int* off, int S, int lane, bool cg) {
+  int run = 0;
+  for (int base = 0; base < S; base += 32) {
+    const int g = base + lane;
+    int keys = 0;
+    if (g < S) {
+      if (a.mode == kModeCross) {
+        keys = a.fixed_len + a.seg_rows;  // as if every group had members
+      } else {
+        const int k = streamed_rows(a, cg ? __ldcg(a.lens + g) : a.lens[g]);
+        keys = k > 0 ? k + a.seg_rows : 0;
+      }
+    }
+    int incl = keys;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (g < S) off[g] = run + incl - keys;
+    run += __shfl_sync(kFull, incl, 31);
+  }
+  if (lane == 0) off[S] = run;
+  __syncwarp();
+  return run;
 }
 
 struct Tile {
@@ -243,19 +282,23 @@ __device__ __forceinline__ void norm_rope(float2* x, const float* __restrict__ w
 }
 
 // cos/sin of p * theta_i for i < HD/2 into rope[] (consumer threads
-// 0 .. HD/2-1).  The angle is formed and reduced modulo 2*pi in double; the
-// reduced angle (|r| <= pi) is then evaluated in float.
+// 0 .. HD/2-1).  The angle is handled in turns: theta_i / (2 pi) is given as
+// an unevaluated float pair (hi + lo, 48 bits).  p * hi is split exactly into
+// its rounded value and its error (fmaf), the nearest integer count of turns
+// is removed from the rounded part exactly, and the small terms are added
+// back, so the fraction f of a turn carries about 2^-24 absolute error for
+// any p < 2^24; sincospif then evaluates sin/cos(pi * 2f) with its own
+// trivial reduction.
 template <int HD>
-__device__ __forceinline__ void rope_table(float* rope, const double* theta, int p, int tid) {
+__device__ __forceinline__ void rope_table(float* rope, const float* turns, int p, int tid) {
   if (tid < HD / 2) {
-    const double ang = (double)p * theta[tid];
-    const double two_pi_hi = 6.283185307179586;        // 2*pi rounded to double
-    const double two_pi_lo = 2.4492935982947064e-16;   // 2*pi - two_pi_hi
-    const double kq = rint(ang * 0.15915494309189535);  // ang / (2*pi)
-    double r = fma(-kq, two_pi_hi, ang);
-    r = fma(-kq, two_pi_lo, r);
+    const float hi = turns[2 * tid], lo = turns[2 * tid + 1];
+    const float pf = (float)p;  // exact for p < 2^24
+    const float prod = pf * hi;
+    const float err = fmaf(pf, hi, -prod);  // p * hi - prod, exactly
+    const float f = (prod - rintf(prod)) + fmaf(pf, lo, err);
     float s, c;
-    sincosf((float)r, &s, &c);
+    sincospif(2.0f * f, &s, &c);
     rope[tid] = c;
     rope[HD / 2 + tid] = s;
   }
@@ -319,6 +362,61 @@ __device__ __forceinline__ void merge_row_slots(float (&M)[NQ], float (&Ls)[NQ],
   }
 }
 
+// The last CTA to finish source g merges the partials of every piece of it
+// (its own among them): each consumer thread takes 4 consecutive output
+// values of one query and combines that slice over pieces first..lastp, 4
+// pieces per L2 round trip, then writes it normalised.
+template <int HD>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int g, int first, int lastp,
+                                             int members, int mbase, int tid, int n_cons) {
+  constexpr int U4 = HD / 4;
+  const int qw = a.Hq * HD;
+  const int nunits = members * a.Hq * U4;
+  for (int u = tid; u < nunits; u += n_cons) {
+    const int d0 = (u % U4) * 4;
+    const int qh = u / U4;  // member * Hq + query head
+    const int mem = qh / a.Hq, hq = qh % a.Hq;
+    float M = -INFINITY, Lsum = 0.f;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    for (int kb = first; kb <= lastp; kb += 4) {
+      float2 ml[4];
+      float4 x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kb + i <= lastp) {
+          const int64_t pidx = ((int64_t)(kb + i + g) * a.max_members + mem) * a.Hq + hq;
+          ml[i] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
+          x[i] = ld_cg_f4(a.part_o + pidx * HD + d0);
+        } else {
+          ml[i] = make_float2(-INFINITY, 0.f);
+          x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float mb = M;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mb = fmaxf(mb, ml[i].x);
+      if (mb == -INFINITY) continue;
+      const float ca = ex2(M - mb);
+      const float2 ca2 = make_float2(ca, ca);
+      Lsum *= ca;
+      acc0 = fmul2(acc0, ca2);
+      acc1 = fmul2(acc1, ca2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float c = ex2(ml[i].x - mb);  // 0 for an absent piece
+        const float2 c2 = make_float2(c, c);
+        Lsum = fmaf(ml[i].y, c, Lsum);
+        acc0 = ffma2(c2, make_float2(x[i].x, x[i].y), acc0);
+        acc1 = ffma2(c2, make_float2(x[i].z, x[i].w), acc1);
+      }
+      M = mb;
+    }
+    const float inv = 1.0f / Lsum;
+    *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + hq * HD + d0) =
+        make_float4(acc0.x * inv, acc0.y * inv, acc1.x * inv, acc1.y * inv);
+  }
+}
+
 template <int HD, int NQ, int DPL, int RS, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_constant__ DecodeArgs a) {
   using LL = LaneLayout<HD, DPL>;
@@ -330,6 +428,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   int* ctl = reinterpret_cast<int*>(smem + lay.ctl);  // [0] abort [1] ticket [2] unsorted
   int* off = reinterpret_cast<int*>(smem + lay.off);
   int* mst = reinterpret_cast<int*>(smem + lay.mstart);
+  int* poff_region = reinterpret_cast<int*>(smem + lay.poff);  // the producer's offsets
   float* rope = reinterpret_cast<float*>(smem + lay.rope);
   float* wts = reinterpret_cast<float*>(smem + lay.wts);  // GQA: RMSNorm weights of q, k
   float* merge = reinterpret_cast<float*>(smem + lay.merge);
@@ -351,44 +450,120 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   }
   // Let the next kernel on the stream launch now: its CTAs take SMs as ours
   // leave and wait (griddepcontrol.wait) for this grid to finish before they
-  // touch memory, so only its launch latency overlaps with our tail.
+  // read anything an earlier kernel may write.
   grid_launch_dependents();
-  grid_dependency_wait();
 
-  // ---- keys per source (off) and sequences per source (mst), then scans
-  for (int g = tid; g <= S; g += blockDim.x) {
-    off[g] = 0;
-    mst[g] = 0;
+  // ---- L2 prefetch of the head of this CTA's share, before the wait.  The
+  // K/V history of a step was written by earlier steps, so while the
+  // previous kernel drains, the producer warp asks L2 for the first pf_bytes
+  // of its share.  The lengths are read here only to place these hints (from
+  // L2, bypassing L1); whatever they hold, every address stays inside the
+  // K/V buffer, and a prefetch writes nothing and is never seen by a load, so
+  // the hint cannot change a result.  Its offsets go to the stage ring, which
+  // nothing touches before this warp's first copy.
+  if (warp == cons_warps && a.pf_bytes > 0 && (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
+    int* poff = reinterpret_cast<int*>(stage);
+    const int run = warp_scan_sources(a, poff, S, lane, true);
+    int64_t pshare = ((int64_t)run + gridDim.x - 1) / gridDim.x;
+    if (pshare < a.min_share) pshare = a.min_share;
+    const int64_t pk0 = (int64_t)blockIdx.x * pshare, pk1 = min(pk0 + pshare, (int64_t)run);
+    if (lane == 0 && pk0 < pk1) {
+      TileIter it(poff, S, pk0, pk1, a.tile_rows, a.seg_rows);
+      Tile tl;
+      int left = a.pf_bytes;
+      while (left > 0 && it.next(tl)) {
+        const uint32_t bytes = (uint32_t)tl.nr * (uint32_t)a.row_elems * 2u;
+        bulk_prefetch_l2(a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
+                         bytes);
+        left -= (int)bytes;
+      }
+    }
+    __syncwarp();
   }
-  if (a.mode == kModeGqa)
-    for (int i = tid; i < 2 * HD; i += blockDim.x) wts[i] = i < HD ? a.wq[i] : a.wk[i - HD];
-  __syncthreads();
-  if (a.mode == kModeCross) {
-    for (int b = tid; b < a.B; b += blockDim.x) {
+  grid_dependency_wait();
+  __syncthreads();  // barrier initialisation and ctl are visible to every warp
+
+  if (warp == cons_warps) {
+    // ======================= producer warp: one lane issues bulk copies.
+    // Self / GQA: it scans the lengths itself (the same integers the
+    // consumers compute) and starts at once; cross: it takes the consumers'
+    // offsets, which need the group histogram.
+    int* toff = poff_region;
+    if (a.mode == kModeCross) {
+      named_bar(2, n_cons + 32);  // the consumers' scans are done
+      toff = off;
+      if (ctl[2] != 0) {  // unsorted groups: nothing is streamed
+        grid_launch_dependents();
+        return;
+      }
+    } else {
+      warp_scan_sources(a, toff, S, lane, false);
+    }
+    const int64_t total = toff[S];
+    int64_t share = (total + gridDim.x - 1) / gridDim.x;
+    if (share < a.min_share) share = a.min_share;
+    const int64_t k0 = (int64_t)blockIdx.x * share;
+    const int64_t k1 = min(k0 + share, total);
+    if (lane == 0 && k0 < k1) {
+      const uint64_t pol = policy_evict_first();
+      TileIter it(toff, S, k0, k1, a.tile_rows, a.seg_rows);
+      Tile tl;
+      for (int t = 0; it.next(tl); ++t) {
+        const int s = t % a.stages;
+        if (t >= a.stages && !mbar_wait(&empty[s], ((t / a.stages) - 1) & 1)) {
+          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+          ctl[0] = 1;
+          break;
+        }
+        const uint32_t bytes = (uint32_t)tl.nr * (uint32_t)a.row_elems * 2u;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(stage + (size_t)s * a.stage_elems,
+                 a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems, bytes,
+                 &full[s], pol);
+      }
+    }
+    grid_launch_dependents();
+    return;
+  }
+  if (warp > cons_warps) return;
+
+  // ---- consumers: keys per source (off) and sequences per source (mst).
+  if (a.mode != kModeCross) {
+    // Self / GQA: one warp scans the lengths (the other warps load the
+    // RMSNorm weights meanwhile); one sequence per source, so mst[g] = g.
+    if (warp == 0) {
+      warp_scan_sources(a, off, S, lane, false);
+      for (int g = lane; g <= S; g += 32) mst[g] = g;
+    }
+    if (a.mode == kModeGqa) {
+      const int t0 = n_cons > 32 ? 32 : 0;
+      if (tid >= t0)
+        for (int i = tid - t0; i < 2 * HD; i += n_cons - t0) wts[i] = i < HD ? a.wq[i] : a.wk[i - HD];
+    }
+    named_bar(1, n_cons);
+  } else {
+    for (int g = tid; g <= S; g += n_cons) {
+      off[g] = 0;
+      mst[g] = 0;
+    }
+    named_bar(1, n_cons);
+    for (int b = tid; b < a.B; b += n_cons) {
       const int gr = a.group[b];
       if (gr >= 0 && gr < S) atomicAdd(&mst[gr], 1);
       if (b > 0 && a.group[b - 1] > gr) ctl[2] = 1;
     }
-    __syncthreads();
-    for (int g = tid; g < S; g += blockDim.x) off[g] = mst[g] > 0 ? a.fixed_len + a.seg_rows : 0;
-  } else {
-    for (int g = tid; g < S; g += blockDim.x) {
-      const int v = a.lens[g];
-      int keys;
-      if (a.mode == kModeSelf) keys = (v >= 1 && v <= a.capacity) ? v - a.append : 0;
-      else keys = (v >= 0 && v < a.capacity) ? v : 0;  // rows cached before the new one
-      off[g] = keys > 0 ? keys + a.seg_rows : 0;
-      mst[g] = 1;
-    }
+    named_bar(1, n_cons);
+    for (int g = tid; g < S; g += n_cons) off[g] = mst[g] > 0 ? a.fixed_len + a.seg_rows : 0;
+    named_bar(1, n_cons);
+    block_scan_excl(off, S, reinterpret_cast<int*>(rope), n_cons);
+    block_scan_excl(mst, S, reinterpret_cast<int*>(rope), n_cons);
+    asm volatile("bar.arrive 2, %0;" ::"r"(n_cons + 32) : "memory");
   }
-  __syncthreads();
-  block_scan_excl(off, S, reinterpret_cast<int*>(rope));
-  block_scan_excl(mst, S, reinterpret_cast<int*>(rope));
   const bool unsorted = a.mode == kModeCross && ctl[2] != 0;
 
   // ---- CTA 0 zeroes the outputs of sequences that are skipped
   if (blockIdx.x == 0) {
-    for (int b = warp; b < a.B; b += blockDim.x >> 5) {
+    for (int b = warp; b < a.B; b += cons_warps) {
       int bad = 0;
       if (unsorted) {
         bad = ASR_DEVERR_INDEX;
@@ -414,38 +589,13 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     return;
   }
 
-  // ---- this CTA's share of the flattened key axis
+  // ---- this CTA's share of the flattened key axis (the producer's too)
   const int64_t total = off[S];
   const int P = gridDim.x;
   int64_t share = (total + P - 1) / P;
   if (share < a.min_share) share = a.min_share;
   const int64_t k0 = (int64_t)blockIdx.x * share;
   const int64_t k1 = min(k0 + share, total);
-
-  if (warp == cons_warps) {
-    // ======================= producer warp: one lane issues bulk copies
-    if (lane == 0 && k0 < k1) {
-      const uint64_t pol = policy_evict_first();
-      TileIter it(off, S, k0, k1, a.tile_rows, a.seg_rows);
-      Tile tl;
-      for (int t = 0; it.next(tl); ++t) {
-        const int s = t % a.stages;
-        if (t >= a.stages && !mbar_wait(&empty[s], ((t / a.stages) - 1) & 1)) {
-          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-          ctl[0] = 1;
-          break;
-        }
-        const uint32_t bytes = (uint32_t)tl.nr * (uint32_t)a.row_elems * 2u;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(stage + (size_t)s * a.stage_elems,
-                 a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems, bytes,
-                 &full[s], pol);
-      }
-    }
-    grid_launch_dependents();
-    return;
-  }
-  if (warp > cons_warps) return;
 
   // ======================= consumers
   const int grp = tid / G, li = tid % G;
@@ -456,19 +606,71 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   const int hoff = h * HD;  // element offset of this group's head in a K (or V) half
 
   float2 qv[NQ][NP], o[NQ][NP];
-  float m[NQ], l[NQ], snew[NQ];
-  float2 vn[NP];
+  float m[NQ], l[NQ];
   int nq = 0, mbase = 0;
+
+  // Does this CTA hold the first real row of source g?  That CTA folds the
+  // new token in (append), so no CTA does it at the end of the launch.  A
+  // source with no cached rows is folded by the CTA that handles it alone.
+  auto owns_first_row = [&](int g) {
+    const int64_t go = (int64_t)off[g] + a.seg_rows, gl = (int64_t)off[g + 1] - go;
+    return gl <= 0 || go / share == (int64_t)blockIdx.x;
+  };
+
+  // Append: the new token's key/value (GQA: normed and roped) from kx, vx
+  // (fp32, loaded by the caller), written to the cache by row slot 0 as f16,
+  // then folded, with the value the cache holds, into the running state of
+  // row slot 0 as the first key it sees.  Warp-uniform (it may shuffle).
+  auto append_fold = [&](int g, float2* kx, float2* vx) {
+    const int p = a.mode == kModeGqa ? a.lens[g] : a.lens[g] - 1;
+    if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, wts + HD, a.eps, rope, li, sw);
+    uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
 #pragma unroll
-  for (int qi = 0; qi < NQ; ++qi) snew[qi] = 0.f;
+    for (int j = 0; j < NCH; ++j) {
+      float kf[8], vf[8];
 #pragma unroll
-  for (int t = 0; t < NP; ++t) vn[t] = make_float2(0.f, 0.f);
+      for (int e = 0; e < 4; ++e) {
+        kf[2 * e] = kx[4 * j + e].x;
+        kf[2 * e + 1] = kx[4 * j + e].y;
+        vf[2 * e] = vx[4 * j + e].x;
+        vf[2 * e + 1] = vx[4 * j + e].y;
+      }
+      const uint4 kh = f8_to_h8(kf), vh = f8_to_h8(vf);
+      h8_to_f2x4(kh, kx + 4 * j);  // the key and value as the cache holds them
+      h8_to_f2x4(vh, vx + 4 * j);
+      if (r == 0) {
+        *reinterpret_cast<uint4*>(row + hoff + LL::chunk_off(li, j, sw)) = kh;
+        *reinterpret_cast<uint4*>(row + a.Hkv * HD + hoff + LL::chunk_off(li, j, sw)) = vh;
+      }
+    }
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+      if (qi < nq) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < NP; ++t) acc = ffma2(qv[qi][t], kx[t], acc);
+        const float sc = group_sum<G>(acc.x + acc.y);
+        if (r == 0) {  // one row slot holds it; the slots are merged later
+          m[qi] = sc;  // exp2(score - m) = 1
+          l[qi] = 1.f;
+#pragma unroll
+          for (int t = 0; t < NP; ++t) o[qi][t] = vx[t];
+        }
+      }
+    }
+  };
 
   auto seg_begin = [&](int g) {
     mbase = mst[g];
     nq = min(mst[g + 1] - mst[g], a.max_members) * rep;
-    // every query load is issued before the RoPE table is built, so their
-    // latencies overlap it and one another
+    const bool fold = a.append && owns_first_row(g);
+    // every global load (new token, queries) is issued before the RoPE
+    // table is built, so their latencies overlap it and one another
+    float2 kx[NP], vx[NP];
+    if (fold) {
+      load_head_f32<HD, DPL>(a.k_new + (int64_t)g * a.kv_stride + h * HD, li, sw, kx);
+      load_head_f32<HD, DPL>(a.v_new + (int64_t)g * a.kv_stride + h * HD, li, sw, vx);
+    }
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
       m[qi] = -INFINITY;
@@ -486,7 +688,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
     if (a.mode == kModeGqa) {
       named_bar(1, n_cons);
-      rope_table<HD>(rope, a.theta, a.lens[g], tid);
+      rope_table<HD>(rope, a.rope_turns, a.lens[g], tid);
       named_bar(1, n_cons);
     }
     const float2 s2 = make_float2(a.qscale, a.qscale);
@@ -498,19 +700,12 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
       }
     }
+    if (fold) append_fold(g, kx, vx);
   };
 
-  // Fold the new token (append) into (M, Ls, O) and write the normalised
-  // output of query qi.  No shuffles: callable per group.
+  // Write the normalised output of query qi.  No shuffles: callable per group.
   auto finalize = [&](int qi, float M, float Ls, float2* O) {
-    if (a.append) {
-      const float mn = fmaxf(M, snew[qi]);
-      const float ca = ex2(M - mn), cb = ex2(snew[qi] - mn);
-      Ls = Ls * ca + cb;
-#pragma unroll
-      for (int t = 0; t < NP; ++t)
-        O[t] = ffma2(make_float2(cb, cb), vn[t], fmul2(O[t], make_float2(ca, ca)));
-    }
+    (void)M;
     const int b = mbase + qi / rep;
     const int hq = h * rep + qi % rep;
     const float inv = 1.0f / Ls;
@@ -524,48 +719,6 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
   };
 
-  // Append: the new token's key/value (GQA: normed and roped), computed by
-  // every group (warp-uniform code: it may shuffle), written to the cache by
-  // row slot 0 and scored against this group's queries.  Only the CTA that
-  // writes source g's output runs it.
-  auto append_new = [&](int g) {
-    if (a.append) {
-      const int p = a.mode == kModeGqa ? a.lens[g] : a.lens[g] - 1;
-      float2 kx[NP];
-      load_head_f32<HD, DPL>(a.k_new + (int64_t)g * a.kv_stride + h * HD, li, sw, kx);
-      load_head_f32<HD, DPL>(a.v_new + (int64_t)g * a.kv_stride + h * HD, li, sw, vn);
-      if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, wts + HD, a.eps, rope, li, sw);
-      uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        float kf[8], vf[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kf[2 * e] = kx[4 * j + e].x;
-          kf[2 * e + 1] = kx[4 * j + e].y;
-          vf[2 * e] = vn[4 * j + e].x;
-          vf[2 * e + 1] = vn[4 * j + e].y;
-        }
-        const uint4 kh = f8_to_h8(kf), vh = f8_to_h8(vf);
-        h8_to_f2x4(kh, kx + 4 * j);  // the key as the cache holds it
-        h8_to_f2x4(vh, vn + 4 * j);
-        if (r == 0) {
-          *reinterpret_cast<uint4*>(row + hoff + LL::chunk_off(li, j, sw)) = kh;
-          *reinterpret_cast<uint4*>(row + a.Hkv * HD + hoff + LL::chunk_off(li, j, sw)) = vh;
-        }
-      }
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int t = 0; t < NP; ++t) acc = ffma2(qv[qi][t], kx[t], acc);
-          snew[qi] = group_sum<G>(acc.x + acc.y);
-        }
-      }
-    }
-  };
-
   auto seg_end = [&](int g) {
     merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
     // pieces of this source over the grid
@@ -575,7 +728,6 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     const int lastp = gl > 0 ? (int)((go + gl - 1) / share) : 0;
     const int parts = gl > 0 ? lastp - first + 1 : 0;
     if (parts <= 1) {
-      append_new(g);
       if (r == 0) {
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi)
@@ -612,72 +764,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
     named_bar(1, n_cons);
     if (ctl[1]) {
-      append_new(g);
-      // row slot r merges pieces first + r, first + r + R, ...; then the
-      // slots are merged like a tile's rows.  The running state registers are
-      // reused: this CTA's own piece is already among the partials.
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        m[qi] = -INFINITY;
-        l[qi] = 0.f;
-#pragma unroll
-        for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
-      }
-      // each round loads two pieces before merging them (one L2 round trip)
-      for (int kp = first + r; kp <= lastp; kp += 2 * R) {
-        const bool two = kp + R <= lastp;
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
-            const int64_t qoff = (int64_t)(qi / rep) * a.Hq + h * rep + qi % rep;
-            const int64_t p0 = ((int64_t)(kp + g) * a.max_members) * a.Hq + qoff;
-            const int64_t p1 = two ? ((int64_t)(kp + R + g) * a.max_members) * a.Hq + qoff : p0;
-            const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + p0 * 2));
-            const float2 ml1 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + p1 * 2));
-            float4 u[2][NCH][2];
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              const float* s0 = a.part_o + p0 * HD + LL::chunk_off(li, j, sw);
-              const float* s1 = a.part_o + p1 * HD + LL::chunk_off(li, j, sw);
-              u[0][j][0] = ld_cg_f4(s0);
-              u[0][j][1] = ld_cg_f4(s0 + 4);
-              u[1][j][0] = ld_cg_f4(s1);
-              u[1][j][1] = ld_cg_f4(s1 + 4);
-            }
-            const float m1 = two ? ml1.x : -INFINITY;
-            const float mn = fmaxf(m[qi], fmaxf(ml0.x, m1));
-            if (mn != -INFINITY) {
-              const float ca = ex2(m[qi] - mn), c0 = ex2(ml0.x - mn), c1 = ex2(m1 - mn);
-              l[qi] = l[qi] * ca + ml0.y * c0 + (two ? ml1.y * c1 : 0.f);
-              const float2 ca2 = make_float2(ca, ca), c02 = make_float2(c0, c0),
-                           c12 = make_float2(c1, c1);
-#pragma unroll
-              for (int j = 0; j < NCH; ++j) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  float2 x0 = fmul2(o[qi][4 * j + 2 * e], ca2);
-                  float2 x1 = fmul2(o[qi][4 * j + 2 * e + 1], ca2);
-                  x0 = ffma2(c02, make_float2(u[0][j][e].x, u[0][j][e].y), x0);
-                  x1 = ffma2(c02, make_float2(u[0][j][e].z, u[0][j][e].w), x1);
-                  if (two) {
-                    x0 = ffma2(c12, make_float2(u[1][j][e].x, u[1][j][e].y), x0);
-                    x1 = ffma2(c12, make_float2(u[1][j][e].z, u[1][j][e].w), x1);
-                  }
-                  o[qi][4 * j + 2 * e] = x0;
-                  o[qi][4 * j + 2 * e + 1] = x1;
-                }
-              }
-              m[qi] = mn;
-            }
-          }
-        }
-      }
-      merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
-      if (r == 0) {
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi)
-          if (qi < nq) finalize(qi, m[qi], l[qi], o[qi]);
-      }
+      // the last CTA to finish source g merges every piece's partial
+      merge_pieces<HD>(a, g, first, lastp, min(mst[g + 1] - mst[g], a.max_members), mbase, tid,
+                       n_cons);
     }
   };
 
@@ -846,15 +935,16 @@ static void* kernel_for(int HD, int vi) {
   return nullptr;
 }
 
-// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256"
+// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256,pf_kb=-1"
 // overrides them (ctas / R = 0: chosen automatically; rs: rows per slot;
 // min_kb: fewest K/V bytes one CTA takes; seg_kb: K/V bytes' worth of
 // virtual rows charged to each source, so CTAs that start or finish more
-// sources take fewer rows).
+// sources take fewer rows; pf_kb: K/V bytes a CTA prefetches into L2 before
+// its grid dependency wait, -1 = the stage ring's size, 0 = none).
 // Defaults (measured on GB300): one CTA per SM with about ten consumer
 // warps and two or more stages of large tiles.
 struct DecodeTune {
-  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256;
+  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256, pf_kb = -1;
 };
 
 static DecodeTune decode_tune() {
@@ -872,6 +962,7 @@ static DecodeTune decode_tune() {
         else if (!strcmp(key, "rs")) d.rs = val;
         else if (!strcmp(key, "min_kb")) d.min_kb = val;
         else if (!strcmp(key, "seg_kb")) d.seg_kb = val;
+        else if (!strcmp(key, "pf_kb")) d.pf_kb = val;
 
         e += n;
         if (*e == ',') ++e;
@@ -883,7 +974,7 @@ static DecodeTune decode_tune() {
 }
 
 struct DecodePlan {
-  int R, tile_rows, stages, stage_elems, threads, smem, min_share, seg_rows;
+  int R, tile_rows, stages, stage_elems, threads, smem, min_share, seg_rows, pf_bytes;
 };
 
 // Row slots R: the consumer count R * Hkv * G must be a multiple of 32 and
@@ -922,6 +1013,7 @@ static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_
   const int min_bytes = std::max(tune.min_kb, 1) * 1024;
   p.min_share = std::max(p.tile_rows, (min_bytes + row_bytes - 1) / row_bytes);
   p.seg_rows = std::max(tune.seg_kb, 0) * 1024 / row_bytes;
+  p.pf_bytes = tune.pf_kb < 0 ? stages * p.tile_rows * row_bytes : std::min(tune.pf_kb, 1 << 20) * 1024;
   return true;
 }
 
@@ -993,6 +1085,7 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
   a.min_share = p.min_share;
   a.seg_rows = p.seg_rows;
   a.stages = p.stages;
+  a.pf_bytes = p.pf_bytes;
   a.stage_elems = p.stage_elems;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms * occ);
@@ -1182,6 +1275,12 @@ extern "C" int asr_gqa_step(const float* q, const float* k_new, const float* v_n
   a.wq = q_norm_w;
   a.wk = k_norm_w;
   a.eps = eps;
-  for (int i = 0; i < head_dim / 2; ++i) a.theta[i] = pow((double)rope_base, -2.0 * i / head_dim);
+  for (int i = 0; i < head_dim / 2; ++i) {
+    // theta_i / (2 pi) as a float pair hi + lo
+    const double t = pow((double)rope_base, -2.0 * i / head_dim) / (2.0 * 3.14159265358979323846);
+    const float hi = (float)t;
+    a.rope_turns[2 * i] = hi;
+    a.rope_turns[2 * i + 1] = (float)(t - (double)hi);
+  }
   return launch_decode(a, head_dim, a.rep, ws, ws_bytes, (cudaStream_t)stream);
 }

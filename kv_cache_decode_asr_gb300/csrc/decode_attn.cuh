@@ -44,6 +44,7 @@ struct DecodeArgs {
   int stages;       // pipeline depth
   int stage_elems;  // f16 elements per stage buffer (128-byte multiple)
   int mode;         // DecodeMode
+  int pf_bytes;     // K/V bytes of its share a CTA asks L2 to prefetch before the grid dependency wait
   // new-token append (GQA step, fused self step): the call writes row p and
   // folds that key in; p = n_past (GQA) or lens - 1 (self)
   int append;
@@ -55,12 +56,12 @@ struct DecodeArgs {
   const float* wk;
   float eps;
   uint16_t* cache_w;  // the cache, writable (row p is appended)
-  double theta[64];   // rope_base^(-2i/HD), i < HD/2, computed on the host in double
+  float rope_turns[128];  // theta_i / (2 pi) as float pairs (hi, lo), theta_i = rope_base^(-2i/HD), i < HD/2
 };
 
 // Shared-memory layout of one CTA (bytes from the dynamic smem base).
 struct DecodeSmem {
-  int bars, ctl, off, mstart, rope, wts, merge, stage, total;
+  int bars, ctl, off, mstart, poff, rope, wts, merge, stage, total;
 };
 
 __host__ __device__ inline int dsm_align(int x, int a) { return (x + a - 1) / a * a; }
@@ -72,7 +73,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.ctl = dsm_align(s.bars + 2 * stages * 8, 16);
   s.off = dsm_align(s.ctl + 16 * 4, 16);
   s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
-  s.rope = dsm_align(s.mstart + (n_src + 1) * 4, 16);
+  s.poff = dsm_align(s.mstart + (n_src + 1) * 4, 16);
+  s.rope = dsm_align(s.poff + (n_src + 1) * 4, 16);
   s.wts = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
   s.merge = dsm_align(s.wts + 2 * HD * 4, 16);
   s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 4) * 4, 128);
