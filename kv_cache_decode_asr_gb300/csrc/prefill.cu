@@ -214,8 +214,11 @@ constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16 (two 64
 constexpr int kKTile = 128 * 128 * 2;     // 128 keys x 128 dims (two 64-dim halves)
 constexpr int kVTile = 128 * 128 * 2;     // V^T: 128 dims x 128 keys (two 64-key halves)
 constexpr int kKVStages = 2;
+constexpr int kQBufs = 2;                 // Q tiles: one per slot (use n = 2*item + slot -> n % kQBufs)
+constexpr int kStgBytes = 8 * 32 * 32 * 4;  // output staging: 32 rows x 32 fp32 per softmax warp
 constexpr int kBarBytes = 1024;           // mbarriers and the TMEM address
-constexpr int kAttnSmem = 2 * kQTile + kKVStages * (kKTile + kVTile) + kBarBytes + 1024;
+constexpr int kAttnSmem =
+    kQBufs * kQTile + kKVStages * (kKTile + kVTile) + kStgBytes + kBarBytes + 1024;
 constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: TMA; 9: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
@@ -275,13 +278,14 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;                                  // [A, B] x 32 KB
-  unsigned char* sK = sQ + 2 * kQTile;                       // stages x 32 KB
+  unsigned char* sQ = smem;                                  // kQBufs x 32 KB
+  unsigned char* sK = sQ + kQBufs * kQTile;                  // stages x 32 KB
   unsigned char* sV = sK + kKVStages * kKTile;               // stages x 32 KB
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile);
-  uint64_t* q_full = bar;                   // 1: Q of the item landed
-  uint64_t* q_empty = q_full + 1;           // 1: the item's S products are done with Q
-  uint64_t* k_full = q_empty + 1;           // kKVStages each
+  float* sStg = reinterpret_cast<float*>(sV + kKVStages * kVTile);  // 8 x 4 KB
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile + kStgBytes);
+  uint64_t* q_full = bar;                   // kQBufs: the Q tile of a use landed
+  uint64_t* q_empty = q_full + kQBufs;      // kQBufs: that use's S products are done with it
+  uint64_t* k_full = q_empty + kQBufs;      // kKVStages each
   uint64_t* k_empty = k_full + kKVStages;
   uint64_t* v_full = k_empty + kKVStages;
   uint64_t* v_empty = v_full + kKVStages;
@@ -294,8 +298,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int u = 0; u < kQBufs; ++u) {
+      mbar_init(&q_full[u], 1);
+      mbar_init(&q_empty[u], 1);
+    }
     for (int s = 0; s < kKVStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -328,13 +334,32 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
   if (warp == 8) {
     // ======================================================= TMA producer
     // The whole warp runs the schedule; one elected lane issues each copy.
+    // Q tiles rotate through kQBufs buffers: use n = 2*item + slot takes
+    // buffer n % kQBufs, so the next item's slot-A tile lands in the buffer
+    // the previous item's slot B has finished with, while this item runs.
     int gk = 0;  // K/V tiles loaded so far (ring position)
     bool ok = true;
+    // Q tile of slot i of item k (x): wait until the buffer's previous use
+    // is done, then load (a slot with no tile completes its phase with no
+    // bytes)
+    auto load_q = [&](int k, int i, const PfItem& x) {
+      const int n = 2 * k + i, u = n % kQBufs, c = n / kQBufs;
+      if (c > 0 && !(ok = mbar_wait_warp(&q_empty[u], (c - 1) & 1))) return;
+      const bool has = i == 0 || x.nB > 0;
+      mbar_arrive_expect_tx_warp(&q_full[u], has ? kQTile : 0);
+      if (has) {
+        const int qt = i == 0 ? x.qt_a : x.qt_b;
+        unsigned char* qd = sQ + u * kQTile;
+        tma_load_3d_warp(qd, &tq, x.h * 128, qt * 128, x.b, &q_full[u]);
+        tma_load_3d_warp(qd + kQTile / 2, &tq, x.h * 128 + 64, qt * 128, x.b, &q_full[u]);
+      }
+    };
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
       const PfItem x = pf_item(a, it);
-      for (int j = 0; j < x.n; ++j, ++gk) {
+      load_q(k, 0, x);  // its buffer was freed during the previous item
+      for (int j = 0; j < x.n && ok; ++j, ++gk) {
         const int s = gk % kKVStages;
         const uint32_t ph = ((gk / kKVStages) - 1) & 1;
         unsigned char* kd = sK + s * kKTile;
@@ -347,19 +372,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
         tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
-        if (j == 0) {
-          // Q after the item's first K/V tile (which need not wait for it):
-          // Q is overwritten once the previous item's S products are done
-          if (k > 0 && !(ok = mbar_wait_warp(q_empty, (k - 1) & 1))) break;
-          mbar_arrive_expect_tx_warp(q_full, x.nB > 0 ? 2 * kQTile : kQTile);
-          tma_load_3d_warp(sQ, &tq, x.h * 128, x.qt_a * 128, x.b, q_full);
-          tma_load_3d_warp(sQ + kQTile / 2, &tq, x.h * 128 + 64, x.qt_a * 128, x.b, q_full);
-          if (x.nB > 0) {
-            tma_load_3d_warp(sQ + kQTile, &tq, x.h * 128, x.qt_b * 128, x.b, q_full);
-            tma_load_3d_warp(sQ + kQTile + kQTile / 2, &tq, x.h * 128 + 64, x.qt_b * 128, x.b,
-                             q_full);
-          }
-        }
+        if (j == 0) load_q(k, 1, x);  // the buffer of this item's slot A tile's predecessor
       }
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
@@ -374,27 +387,33 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     int gx[2] = {0, 0};  // tiles of slot A / B so far (S and P phases)
     int ox[2] = {0, 0};  // items whose O slot A / B has accumulated so far
     bool ok = true;
+    bool a_early = false;  // slot A's first S of this item was issued during the previous one
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
       const PfItem x = pf_item(a, it);
       const int nX[2] = {x.nA, x.nB};
-      ok = mbar_wait_warp(q_full, k & 1);
-      if (!ok) break;
-      int s_left = x.nA + x.nB;  // S products of this item still to issue
-      // S of slot i for key tile j; the slot's S buffer holds P of its
-      // previous tile, read by a PV issued before this S
-      auto issue_s = [&](int i, int j) {
-        const int st = (gk + j) % kKVStages;
+      // Q buffer of slot i (use 2k + i) and the wait for its tile
+      const int qb[2] = {(2 * k) % kQBufs, (2 * k + 1) % kQBufs};
+      auto q_ready = [&](int i) {
+        const int n = 2 * k + i;
+        return mbar_wait_warp(&q_full[n % kQBufs], (n / kQBufs) & 1);
+      };
+      // S of slot i from Q buffer qbuf and K stage st; the slot's S buffer
+      // holds P of its previous tile, read by a PV issued before this S
+      auto issue_s_at = [&](int i, int qbuf, int st, bool last) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
-          mma_f16_warp(tS(i), sw128_kmajor_desc(aQ + i * kQTile + off),
+          mma_f16_warp(tS(i), sw128_kmajor_desc(aQ + qbuf * kQTile + off),
                        sw128_kmajor_desc(aK + st * kKTile + koff), kIdS, kk > 0);
         }
         mma_commit_warp(&s_full[i]);
-        if (--s_left == 0) mma_commit_warp(q_empty);  // Q free once these finish
+        if (last) mma_commit_warp(&q_empty[qbuf]);  // its Q free once these finish
+      };
+      auto issue_s = [&](int i, int j) {
+        issue_s_at(i, qb[i], (gk + j) % kKVStages, j == nX[i] - 1);
       };
       // O += P V for key tile j: P (TMEM, 8 columns per 16 keys) times V^T
       // (shared memory, 64-key halves)
@@ -413,10 +432,14 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       auto k_ready = [&](int j) {
         return mbar_wait_warp(&k_full[(gk + j) % kKVStages], ((gk + j) / kKVStages) & 1);
       };
-      ok = k_ready(0);
+      ok = k_ready(0) && (a_early || q_ready(0));
       tc_fence_after_sync();
-      if (ok) issue_s(0, 0);
+      if (ok && !a_early) issue_s(0, 0);
+      a_early = false;
+      if (ok) ok = q_ready(1);
+      tc_fence_after_sync();
       if (ok && x.nB > 0) issue_s(1, 0);
+      if (ok && x.nB == 0) mma_commit_warp(&q_empty[qb[1]]);  // slot B's unused buffer
       if (ok) mma_commit_warp(&k_empty[gk % kKVStages]);
       for (int j = 0; j < x.n && ok; ++j) {
         const int st = (gk + j) % kKVStages;
@@ -437,6 +460,21 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         }
         mma_commit_warp(&v_empty[st]);                               // V^T of tile j
         if (j + 1 < x.n) mma_commit_warp(&k_empty[(gk + j + 1) % kKVStages]);  // K of tile j+1
+        // Slot A is done one tile before slot B: start its part of the next
+        // item now (its Q is already in; its first K tile lands in the stage
+        // this item's tile j has left), while slot B's softmax finishes.
+        if (ok && j == x.nA - 1 && x.nB > x.nA) {
+          const int it2 = pf_item_index(k + 1, a.n_items);
+          if (it2 >= 0) {
+            const PfItem x2 = pf_item(a, it2);
+            const int g0 = gk + x.n, n2 = 2 * (k + 1);
+            ok = mbar_wait_warp(&k_full[g0 % kKVStages], (g0 / kKVStages) & 1) &&
+                 mbar_wait_warp(&q_full[n2 % kQBufs], (n2 / kQBufs) & 1);
+            tc_fence_after_sync();
+            if (ok) issue_s_at(0, n2 % kQBufs, g0 % kKVStages, x2.nA == 1);
+            a_early = ok;
+          }
+        }
       }
       gx[0] += x.nA;
       gx[1] += x.nB;
@@ -461,7 +499,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       const int ni = i == 0 ? x.nA : x.nB;
       if (ni == 0) continue;
       const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
-      const int qidx = q0 + row;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < ni && ok; ++j, ++g) {
         // S(g) done also means the slot's PV(g-1) is done: it was issued
@@ -541,13 +578,36 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[i]);
-      if (qidx < a.T) {
+      // The normalised rows go out through this warp's 4 KB of shared
+      // memory, 32 columns at a time: each thread writes its row's 32
+      // values, then each store instruction carries four whole 128-byte row
+      // pieces instead of 32 rows' 16 bytes.  16-byte chunk c of row r sits
+      // at chunk c ^ (r % 8), so both sides are free of bank conflicts.
+      {
         const float inv = 1.0f / l;
-        float* dst = a.out + (((int64_t)x.b * a.T + qidx) * a.Hq + x.h) * kPrefillHD;
+        float* stg = sStg + warp * (32 * 32);
+        const int r0 = q0 + (warp & 3) * 32;  // query row of lane 0
 #pragma unroll
-        for (int e = 0; e < 128; e += 4)
-          *reinterpret_cast<float4*>(dst + e) =
-              make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+        for (int pc = 0; pc < 4; ++pc) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int e = pc * 32 + c * 4;
+            *reinterpret_cast<float4*>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3), cc = lane & 7;
+            const float4 val =
+                *reinterpret_cast<const float4*>(stg + rr * 32 + ((cc ^ (rr & 7)) * 4));
+            if (r0 + rr < a.T)
+              *reinterpret_cast<float4*>(
+                  a.out + (((int64_t)x.b * a.T + r0 + rr) * a.Hq + x.h) * kPrefillHD + pc * 32 +
+                  cc * 4) = val;
+          }
+          __syncwarp();
+        }
       }
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
