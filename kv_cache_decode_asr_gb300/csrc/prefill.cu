@@ -222,6 +222,13 @@ constexpr int kAttnSmem =
 constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: TMA; 9: MMA
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
+// max of three fp32 values in one instruction (sm_100+)
+__device__ __forceinline__ float fmax3(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
+}
+
 __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -290,8 +297,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
   uint64_t* v_full = k_empty + kKVStages;
   uint64_t* v_empty = v_full + kKVStages;
   uint64_t* s_full = v_empty + kKVStages;   // [A, B]: S of the slot's tile g (phase g)
-  uint64_t* p_full = s_full + 2;            // [A, B]: P of the slot's tile g
-  uint64_t* o_done = p_full + 2;            // [A, B]: the slot's last PV of an item
+  uint64_t* p_full = s_full + 2;            // [A0, A1, B0, B1]: half h (keys 64h..) of P of tile g
+  uint64_t* o_done = p_full + 4;            // [A, B]: the slot's last PV of an item
   uint64_t* o_free = o_done + 2;            // [A, B]: the softmax has read O of its item
   uint32_t* tslot = reinterpret_cast<uint32_t*>(o_free + 2);
 
@@ -310,7 +317,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);  // one arrival per softmax warp of the slot
+      mbar_init(&p_full[2 * i], 4);  // one arrival per softmax warp of the slot
+      mbar_init(&p_full[2 * i + 1], 4);
       mbar_init(&o_done[i], 1);
       mbar_init(&o_free[i], 4);
     }
@@ -415,17 +423,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       auto issue_s = [&](int i, int j) {
         issue_s_at(i, qb[i], (gk + j) % kKVStages, j == nX[i] - 1);
       };
-      // O += P V for key tile j: P (TMEM, 8 columns per 16 keys) times V^T
-      // (shared memory, 64-key halves)
-      auto issue_pv = [&](int i, int j) {
+      // O += P V for keys 64h .. 64h+63 of key tile j: P (TMEM, 8 columns
+      // per 16 keys) times the 64-key half h of V^T (shared memory)
+      auto issue_pv_half = [&](int i, int j, int h) {
         const int st = (gk + j) % kKVStages;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * h + k4;
           mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
-                          sw128_kmajor_desc(aV + st * kVTile + (kk >> 2) * (kVTile / 2) +
-                                            (kk & 3) * 32),
+                          sw128_kmajor_desc(aV + st * kVTile + h * (kVTile / 2) + k4 * 32),
                           kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (j == nX[i] - 1) mma_commit_warp(&o_done[i]);  // the item's O is complete
+        }
+        if (h == 1 && j == nX[i] - 1) mma_commit_warp(&o_done[i]);  // the item's O is complete
       };
       // K of tile j is free once both slots' S products for it are issued
       // (commit: once they finish); V^T of tile j once both slots' PVs are
@@ -449,12 +458,17 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         for (int i = 0; i < 2; ++i) {
           if (ok && j < nX[i]) {
             const int g = gx[i] + j;
-            ok = mbar_wait_warp(&p_full[i], g & 1);
+            // the first half of P goes to the tensor core while the softmax
+            // still computes the second
+            ok = mbar_wait_warp(&p_full[2 * i], g & 1);
             // the first PV of an item overwrites O: the softmax must have
             // read the previous item's O first
             if (ok && j == 0 && ox[i] > 0) ok = mbar_wait_warp(&o_free[i], (ox[i] - 1) & 1);
             tc_fence_after_sync();
-            if (ok) issue_pv(i, j);
+            if (ok) issue_pv_half(i, j, 0);
+            if (ok) ok = mbar_wait_warp(&p_full[2 * i + 1], g & 1);
+            tc_fence_after_sync();
+            if (ok) issue_pv_half(i, j, 1);
             if (ok && j + 1 < nX[i]) issue_s(i, j + 1);
           }
         }
@@ -517,13 +531,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         float mx[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          mx[e] = fmaxf(fmaxf(fmaxf(v[e], v[e + 16]), fmaxf(v[e + 32], v[e + 48])),
-                        fmaxf(fmaxf(v[e + 64], v[e + 80]), fmaxf(v[e + 96], v[e + 112])));
+          mx[e] = fmax3(fmax3(v[e], v[e + 16], v[e + 32]), fmax3(v[e + 48], v[e + 64], v[e + 80]),
+                        fmaxf(v[e + 96], v[e + 112]));
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-        const float tmax = mx[0] * a.sl2e;
+        for (int e = 0; e < 5; ++e) mx[e] = fmax3(mx[3 * e], mx[3 * e + 1], mx[3 * e + 2]);
+        const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmaxf(mx[3], mx[4]), mx[15]) * a.sl2e;
         // rescale O only when the row max grew by more than 2^8
         const float m_new = (j == 0 || tmax > m + kRescaleLog2) ? tmax : m;
         const bool grow = j > 0 && m_new != m;
@@ -544,26 +556,31 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         m = m_new;
         // P = 2^(S*c - m) (masked entries -inf, so 0) as f16 pairs into the
         // first 64 columns of the S buffer (all of S is in registers)
+        // P half h (keys 64h ..) is published as soon as it is stored, so
+        // the tensor core starts on it while the other half is computed
         const float2 c2 = make_float2(a.sl2e, a.sl2e), nm2 = make_float2(-m, -m);
-        float2 ls = make_float2(0.f, 0.f);
+        float2 ls[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          ls[c] = make_float2(0.f, 0.f);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 xv = ffma2(make_float2(v[32 * c + e], v[32 * c + e + 1]), c2, nm2);
             const float2 pe = make_float2(ex2f(xv.x), ex2f(xv.y));
-            ls = make_float2(ls.x + pe.x, ls.y + pe.y);
+            ls[c] = fadd2(ls[c], pe);
             const __half2 hp = __floats2half2_rn(pe.x, pe.y);
             pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hp);
           }
           tmem_st16u(tS(i) + lane_off + 16 * c, pk);
+          if (c & 1) {
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[2 * i + (c >> 1)]);
+          }
         }
-        l += ls.x + ls.y;
-        tmem_wait_st();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[i]);
+        l += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
       }
       if (!ok) break;
       // ---- the item's O once its last PV is done; O is released to the
