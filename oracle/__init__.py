@@ -65,6 +65,8 @@ def _lib():
                                         _int, _int, _int, _u16p, _i64, _int, _u16p]),
             "orc_prefill_attn_rows": (None, [_u16p, _i32p, _int, _u16p, _int, _int, _int, _int,
                                              _dbl, _f64p]),
+            "orc_mha_attn": (_int, [_u16p, _u16p, _u16p, _i32p, _int, _int, _int, _int, _dbl, _int,
+                                    _u16p, _i64, _int, _f64p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -313,6 +315,34 @@ def prefill_attn_rows(qhat_rows, t_of_row, seq_cache, q_heads, kv_heads, head_di
     return out
 
 
+def mha_attn(q, k, v, heads, head_dim, scale, causal, lens=None, cache=None):
+    """Multi-head attention of each sequence's positions among themselves
+    (causal: the prompt prefill; unmasked: the encoder's self-attention).
+    q, k, v uint16 [B, T, heads*hd]; lens int32 [B] or None (all T); cache
+    uint16 [B, capacity, 2*heads*hd] or None (rows [0, lens[b]) get k || v in
+    place).  Returns (out float64 [B, T, heads*hd] with rows past lens[b]
+    left as NaN, number of sequences skipped for a bad length)."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    B, T = q.shape[0], q.shape[1]
+    out = np.full((B, T, heads * head_dim), np.nan, np.float64)
+    lp = None
+    if lens is not None:
+        lens = _c(np.ascontiguousarray(lens, np.int32), np.int32)
+        lp = _p(lens, ctypes.c_int32)
+    cp, cstride, cap = None, 0, 0
+    if cache is not None:
+        cache = _c(cache, np.uint16)
+        cp, cstride, cap = _p(cache, ctypes.c_uint16), cache[0].size, cache.shape[1]
+    n = _lib().orc_mha_attn(_p(q, ctypes.c_uint16), _p(k, ctypes.c_uint16), _p(v, ctypes.c_uint16),
+                            lp, B, T, heads, head_dim, float(scale), 1 if causal else 0, cp,
+                            cstride, cap, _p(out, ctypes.c_double))
+    if n < 0:
+        raise ValueError("T exceeds the cache capacity")
+    return out, n
+
+
 def build():
     """Compile liboracle.so (the checker) if it is missing or stale."""
     return _build.build()
@@ -321,7 +351,7 @@ def build():
 __all__ = [
     "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
     "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
-    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "build",
+    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "build",
 ]
 
 if os.environ.get("ORACLE_THREADS"):

@@ -594,3 +594,90 @@ void orc_prefill_attn_rows(const uint16_t* qhat_rows, const int32_t* t_of_row, i
   free(q);
   free(z);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Next rows: MHA prompt prefill with per-sequence lengths, and the         */
+/* encoder's unmasked self-attention                                        */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* lens;
+  int B, T, heads, head_dim, causal;
+  double scale;
+  double* out;
+} orc_mha_ctx;
+
+static void orc_mha_item(void* vctx, int64_t item) {
+  orc_mha_ctx* c = (orc_mha_ctx*)vctx;
+  int hd = c->head_dim;
+  int b = (int)(item / c->heads);
+  int h = (int)(item % c->heads);
+  int L = c->lens ? c->lens[b] : c->T;
+  int64_t row = (int64_t)c->heads * hd; /* q, k, v rows: all heads of one position */
+  const uint16_t* kb = c->k + (int64_t)b * c->T * row + (int64_t)h * hd;
+  const uint16_t* vb = c->v + (int64_t)b * c->T * row + (int64_t)h * hd;
+  double* q = (double*)malloc(sizeof(double) * hd);
+  double* z = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
+  for (int t = 0; t < L; ++t) {
+    const uint16_t* qt = c->q + ((int64_t)b * c->T + t) * row + (int64_t)h * hd;
+    for (int d = 0; d < hd; ++d) q[d] = orc_f16_to_f64(qt[d]);
+    double* o = c->out + ((int64_t)b * c->T + t) * row + (int64_t)h * hd;
+    /* causal: query t sees keys 0..t; unmasked: every real key 0..L-1 */
+    orc_attend_one(q, kb, vb, row, c->causal ? t + 1 : L, hd, c->scale, z, o);
+  }
+  free(q);
+  free(z);
+}
+
+/* Multi-head attention of the positions of a batch of sequences among
+ * themselves, with the f16 q, k, v as the matrix operands:
+ *  - causal = 1: the decoder's prompt prefill ("Nest whisper-tiny,
+ *    src/lib.linnet", DecoderLayer.prefill: the S prompt tokens' keys and
+ *    values go to cache rows [0, S) and they attend causally among
+ *    themselves);
+ *  - causal = 0: the encoder's self-attention (EncoderLayer.forward: every
+ *    audio frame attends to every other, padding included, no mask).
+ * q, k, v: f16 [B][T][heads*hd].  lens[b] (NULL: T for every sequence) is
+ * the number of real positions of sequence b ("transcribe.cpp,
+ * decoder.h", PrefillBuildBatched: prompts of up to T_prompt_max tokens,
+ * each with its own last real position): query t < lens[b] attends keys
+ * j < lens[b] (j <= t when causal); out rows t >= lens[b] are not written.
+ * cache (may be NULL): rows [0, lens[b]) of sequence b receive k || v, the
+ * row layout of the decoder's self cache.  Returns the number of sequences
+ * skipped for a length outside [0, T], or -1 if T > capacity. */
+int orc_mha_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
+                 int B, int T, int heads, int head_dim, double scale, int causal, uint16_t* cache,
+                 int64_t seq_stride, int capacity, double* out) {
+  if (cache && T > capacity) return -1;
+  int bad = 0;
+  int32_t* L = (int32_t*)malloc(sizeof(int32_t) * (B > 0 ? B : 1));
+  for (int b = 0; b < B; ++b) {
+    int lb = lens ? lens[b] : T;
+    if (lb < 0 || lb > T) {
+      ++bad;
+      lb = 0;
+    }
+    L[b] = lb;
+  }
+  int64_t row = (int64_t)heads * head_dim;
+  if (cache) {
+    for (int b = 0; b < B; ++b) {
+      for (int t = 0; t < L[b]; ++t) {
+        uint16_t* dst = cache + (int64_t)b * seq_stride + (int64_t)t * 2 * row;
+        const uint16_t* ks = k + ((int64_t)b * T + t) * row;
+        const uint16_t* vs = v + ((int64_t)b * T + t) * row;
+        for (int64_t i = 0; i < row; ++i) {
+          dst[i] = ks[i];
+          dst[row + i] = vs[i];
+        }
+      }
+    }
+  }
+  orc_mha_ctx c = {q, k, v, L, B, T, heads, head_dim, causal, scale, out};
+  orc_parallel_for((int64_t)B * heads, orc_mha_item, &c);
+  free(L);
+  return bad;
+}

@@ -442,3 +442,94 @@ def test_step_key_equals_prefill_key(oracle_mod):
     assert np.array_equal(step, pre)
     # outputs differ only by the f16 rounding of the prefill's query
     assert np.allclose(outs[0], outp[0, T - 1], atol=2e-2)
+
+
+# ------------------------------------------- MHA prompt prefill, encoder ----
+
+def _np_attention(q, k, v, heads, hd, scale, causal, L):
+    """Textbook softmax(scale q k^T) v in float64 with numpy, over the first L
+    positions of one sequence (q, k, v: f16 bits [T, heads*hd])."""
+    qd, kd, vd = dec(q), dec(k), dec(v)
+    out = np.full(qd.shape, np.nan)
+    for h in range(heads):
+        sl = slice(h * hd, (h + 1) * hd)
+        s = scale * qd[:L, sl] @ kd[:L, sl].T
+        if causal:
+            s = np.where(np.tril(np.ones((L, L), bool)), s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:L, sl] = (p / p.sum(axis=1, keepdims=True)) @ vd[:L, sl]
+    return out
+
+
+def test_mha_attn_matches_numpy_brute_force(oracle_mod):
+    """Tiny causal and unmasked cases with per-sequence lengths against a
+    numpy restatement (independent f16 decode, matrix form)."""
+    B, T, H, hd = 3, 6, 2, 4
+    q = syn.host_normal_f16bits((B, T, H * hd), 40)
+    k = syn.host_normal_f16bits((B, T, H * hd), 41)
+    v = syn.host_normal_f16bits((B, T, H * hd), 42)
+    lens = np.array([6, 3, 1], np.int32)
+    for causal in (True, False):
+        out, bad = oracle_mod.mha_attn(q, k, v, H, hd, 0.7, causal, lens=lens)
+        assert bad == 0
+        for b in range(B):
+            ref = _np_attention(q[b], k[b], v[b], H, hd, 0.7, causal, lens[b])
+            assert np.allclose(out[b, :lens[b]], ref[:lens[b]], rtol=1e-12, atol=1e-12)
+            assert np.all(np.isnan(out[b, lens[b]:]))        # rows past the length untouched
+    # one real position: its output is its own V row, exactly
+    out, _ = oracle_mod.mha_attn(q, k, v, H, hd, 0.7, False, lens=np.array([1, 1, 1], np.int32))
+    assert np.array_equal(out[:, 0], dec(v[:, 0]))
+
+
+def test_mha_prefill_rows_equal_steps_and_cache(oracle_mod):
+    """Causal row t equals the one-token self-attention step over the cache
+    rows [0, t] the prefill wrote; the cache rows are k || v bitwise and
+    nothing is written past a sequence's length."""
+    B, T, H, hd, cap = 2, 7, 3, 64, 9
+    q = syn.host_normal_f16bits((B, T, H * hd), 43)
+    k = syn.host_normal_f16bits((B, T, H * hd), 44)
+    v = syn.host_normal_f16bits((B, T, H * hd), 45)
+    lens = np.array([7, 4], np.int32)
+    cache = np.zeros((B, cap, 2 * H * hd), np.uint16)
+    out, bad = oracle_mod.mha_attn(q, k, v, H, hd, hd ** -0.5, True, lens=lens, cache=cache)
+    assert bad == 0
+    for b in range(B):
+        L = lens[b]
+        assert np.array_equal(cache[b, :L, :H * hd], k[b, :L])
+        assert np.array_equal(cache[b, :L, H * hd:], v[b, :L])
+        assert np.all(cache[b, L:] == 0)
+    for t in range(T):
+        live = np.nonzero(lens > t)[0]
+        qt = dec(q[live, t]).astype(np.float32)
+        ref, _ = oracle_mod.self_attn_step(qt, np.ascontiguousarray(cache[live]),
+                                           np.full(live.size, t + 1, np.int32), H, hd, hd ** -0.5)
+        assert np.allclose(out[live, t], ref, atol=1e-12)
+
+
+def test_encoder_attn_rows_equal_cross_step(oracle_mod):
+    """Unmasked: every row equals the one-query cross-attention over all the
+    sequence's frames, and a shorter length equals the truncated sequence."""
+    B, T, H, hd = 2, 10, 2, 64
+    q = syn.host_normal_f16bits((B, T, H * hd), 46)
+    k = syn.host_normal_f16bits((B, T, H * hd), 47)
+    v = syn.host_normal_f16bits((B, T, H * hd), 48)
+    out, _ = oracle_mod.mha_attn(q, k, v, H, hd, hd ** -0.5, False)
+    cross = np.ascontiguousarray(np.concatenate([k, v], axis=2))  # [B][T][K | V]
+    for t in (0, 4, 9):
+        ref, _ = oracle_mod.cross_attn_step(dec(q[:, t]).astype(np.float32), cross,
+                                            np.arange(B, dtype=np.int32), H, hd, hd ** -0.5)
+        assert np.allclose(out[:, t], ref, atol=1e-12)
+    L = 6
+    out_l, _ = oracle_mod.mha_attn(q, k, v, H, hd, hd ** -0.5, False,
+                                   lens=np.array([L, L], np.int32))
+    out_t, _ = oracle_mod.mha_attn(np.ascontiguousarray(q[:, :L]), np.ascontiguousarray(k[:, :L]),
+                                   np.ascontiguousarray(v[:, :L]), H, hd, hd ** -0.5, False)
+    assert np.array_equal(out_l[:, :L], out_t)
+    # the encoder attends to every frame: changing the last key moves row 0
+    k2 = k.copy()
+    k2[:, T - 1] = syn.host_normal_f16bits(k2[:, T - 1].shape, 49)
+    out2, _ = oracle_mod.mha_attn(q, k2, v, H, hd, hd ** -0.5, False)
+    assert not np.allclose(out2[:, 0], out[:, 0])
+    # a length outside [0, T] is counted and skipped
+    _, bad = oracle_mod.mha_attn(q, k, v, H, hd, hd ** -0.5, False, lens=np.array([T + 1, 3], np.int32))
+    assert bad == 1
