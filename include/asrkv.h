@@ -75,6 +75,8 @@ enum asr_op {
   ASR_OP_CROSS_ATTN = 2,
   ASR_OP_GQA_STEP = 3,
   ASR_OP_PREFILL_ATTN = 4,
+  ASR_OP_MHA_PREFILL = 5,
+  ASR_OP_ENCODER_ATTN = 6,
 };
 
 /* Limits checked on the host. */
@@ -236,6 +238,44 @@ int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, int head_dim, float scale,
                           const uint16_t* cache, int64_t seq_stride, int capacity, float* out,
                           void* ws, size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+
+/* Next row -- batched multi-head prompt prefill with per-sequence lengths.
+ * Defines: "Nest whisper-tiny, src/lib.linnet", DecoderLayer.prefill (the S
+ * prompt tokens' keys and values go to the self cache at rows [0, S); they
+ * attend causally among themselves); "transcribe.cpp, src/arch/qwen3_asr/
+ * decoder.h", PrefillBuildBatched (prompts of up to T_prompt_max tokens,
+ * each with its own last real position).
+ *   For each sequence b with L = lens[b] (lens NULL: L = T) and t < L:
+ *   cache row t = k_t || v_t (bitwise, all heads);
+ *   out_t,h = sum_{j<=t} softmax_j(scale * q_t,h . k_j,h) v_j,h
+ *   Rows t >= L of out and of the cache are not written.
+ * q, k, v: f16 [B][T][heads*head_dim] (heads = KV heads: multi-head); lens:
+ * int32 [B] device or NULL; a length outside [0, T] skips the sequence
+ * (ASR_DEVERR_LEN).  cache: f16 [B][seq_stride], rows of 2*heads*head_dim;
+ * T <= capacity.  out: fp32 [B][T][heads*head_dim].  head_dim 64 or 128;
+ * heads <= ASR_MAX_KV_HEADS.  The softmax weights enter the P.V product as
+ * f16 (tensor cores, tcgen05).
+ * ws: asr_workspace_size(ASR_OP_MHA_PREFILL, B, heads, 1, heads, head_dim, T)
+ * bytes (V transposed); need not be zeroed. */
+int asr_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
+                    int B, int T, int heads, int head_dim, float scale, uint16_t* cache,
+                    int64_t seq_stride, int capacity, float* out, void* ws, size_t ws_bytes,
+                    int32_t* dev_err, asr_stream_t stream);
+
+/* Next row -- the encoder's self-attention over its frames, unmasked.
+ * Defines: "Nest whisper-tiny, src/lib.linnet", EncoderLayer.forward (every
+ * audio position attends to every other, the padding of the fixed 30 s
+ * included; no mask); "mlx-bun whisper.ts", the encoder blocks' #attention
+ * (no mask).
+ *   For each sequence b with L = lens[b] (lens NULL: L = T) and t < L:
+ *   out_t,h = sum_{j<L} softmax_j(scale * q_t,h . k_j,h) v_j,h
+ *   Rows t >= L of out are not written.
+ * Same arrays, limits and errors as asr_mha_prefill, without the cache.
+ * ws: asr_workspace_size(ASR_OP_ENCODER_ATTN, B, heads, 1, heads, head_dim, T)
+ * bytes; need not be zeroed. */
+int asr_encoder_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
+                     int B, int T, int heads, int head_dim, float scale, float* out, void* ws,
+                     size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device

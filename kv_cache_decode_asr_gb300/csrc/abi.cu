@@ -42,6 +42,12 @@ extern "C" size_t asr_workspace_size(int op, int B, int n_sources, int max_beams
       return 0;
     return prefill_ws_bytes(B, T, q_heads, n_sources);
   }
+  if (op == ASR_OP_MHA_PREFILL || op == ASR_OP_ENCODER_ATTN) {
+    if (B < 1 || B > ASR_MAX_BATCH || T < 1 || q_heads < 1 || q_heads > ASR_MAX_KV_HEADS ||
+        (head_dim != 64 && head_dim != 128))
+      return 0;
+    return mha_ws_bytes(B, T, q_heads, head_dim);
+  }
   if (B < 0 || n_sources < 1 || n_sources > ASR_MAX_BATCH || max_beams < 1 ||
       max_beams > ASR_MAX_BEAMS || q_heads < 1 || (head_dim != 64 && head_dim != 128))
     return 0;

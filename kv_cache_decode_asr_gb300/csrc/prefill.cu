@@ -53,7 +53,7 @@ struct PrepArgs {
   int64_t seq_stride;
   uint16_t* qhat;  // [B][T][Hq*128]
   uint16_t* vt;    // [B*Hkv][128][Tpad]
-  double theta[kPrefillHD / 2];
+  float rope_turns[kPrefillHD];  // theta_i / (2 pi) as float pairs (hi, lo), i < 64
 };
 
 // grid (Tpad / kPrepT, B), 256 threads.  Shared: cos/sin of the chunk's
@@ -86,15 +86,21 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
       vval[u] = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t0 + tt) * kw + c * 8);
   }
 
-  // rotation table: angle in double, reduced modulo 2*pi, then float sin/cos
+  // rotation table: the angle t * theta_i in turns, theta_i / (2 pi) held as
+  // an unevaluated float pair (hi + lo).  t * hi is split exactly into its
+  // rounded value and error (fmaf); the whole turns are removed from the
+  // rounded part exactly and the small terms added back, so the fraction f
+  // carries about 2^-24 absolute error for any t < 2^24, and sincospif
+  // evaluates sin/cos(pi * 2f) with its own trivial reduction.
   for (int idx = tid; idx < kPrepT * HALF; idx += blockDim.x) {
     const int tt = idx / HALF, i = idx % HALF;
-    const double ang = (double)(t0 + tt) * a.theta[i];
-    const double kq = rint(ang * 0.15915494309189535);
-    double r = fma(-kq, 6.283185307179586, ang);
-    r = fma(-kq, 2.4492935982947064e-16, r);
+    const float pf = (float)(t0 + tt);
+    const float hi = a.rope_turns[2 * i], lo = a.rope_turns[2 * i + 1];
+    const float prod = pf * hi;
+    const float err = fmaf(pf, hi, -prod);
+    const float f = (prod - rintf(prod)) + fmaf(pf, lo, err);
     float s, c;
-    sincosf((float)r, &s, &c);
+    sincospif(2.0f * f, &s, &c);
     cs[idx] = c;
     sn[idx] = s;
   }
@@ -201,25 +207,92 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
   }
 }
 
+// --------------------------------------------------------- MHA prep --
+
+struct MhaPrepArgs {
+  const uint16_t* k;  // [B][T][H*HD]
+  const uint16_t* v;
+  const int32_t* lens;  // or null
+  int B, T, Tpad, H, HD;
+  uint16_t* cache;  // or null: rows of [K(H*HD) | V(H*HD)], sequence stride seq_stride
+  int64_t seq_stride;
+  uint16_t* vt;  // [B*H][HD][Tpad]
+};
+
+constexpr int kMhaPrepT = 32;  // positions per CTA
+
+// grid (Tpad / 32, B), 256 threads.  For each head: the chunk's V (and K)
+// vectors are loaded, copied to the cache rows of the real positions, and V
+// is staged in shared memory, then written transposed (32 positions = 64
+// bytes per dim row), zero at and past the sequence's length.
+__global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ MhaPrepArgs a) {
+  __shared__ __align__(16) uint16_t tile[kMhaPrepT][128 + 8];
+  const int tid = threadIdx.x;
+  const int b = blockIdx.y;
+  const int t0 = blockIdx.x * kMhaPrepT;
+  grid_launch_dependents();
+  grid_dependency_wait();
+  int L = a.T;
+  if (a.lens) {
+    L = a.lens[b];
+    if (L < 0 || L > a.T) L = 0;
+  }
+  const int HD = a.HD, vpr = HD / 8;  // 16-byte vectors per head row
+  const int64_t rw = (int64_t)a.H * HD;
+  for (int h = 0; h < a.H; ++h) {
+    for (int idx = tid; idx < kMhaPrepT * vpr; idx += blockDim.x) {
+      const int tt = idx / vpr, c = idx % vpr, t = t0 + tt;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (t < L) {
+        const int64_t off = ((int64_t)b * a.T + t) * rw + h * HD + c * 8;
+        val = *reinterpret_cast<const uint4*>(a.v + off);
+        if (a.cache) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(a.k + off);
+          uint16_t* row = a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * rw;
+          *reinterpret_cast<uint4*>(row + h * HD + c * 8) = kv;
+          *reinterpret_cast<uint4*>(row + rw + h * HD + c * 8) = val;
+        }
+      }
+      *reinterpret_cast<uint4*>(&tile[tt][c * 8]) = val;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < HD * (kMhaPrepT / 8); idx += blockDim.x) {
+      const int d = idx / (kMhaPrepT / 8), q8 = idx % (kMhaPrepT / 8);
+      alignas(16) uint16_t col[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) col[e] = tile[q8 * 8 + e][d];
+      *reinterpret_cast<uint4*>(a.vt + (((int64_t)b * a.H + h) * HD + d) * a.Tpad + t0 + q8 * 8) =
+          *reinterpret_cast<const uint4*>(col);
+    }
+    __syncthreads();
+  }
+}
+
 // ------------------------------------------------------------- attention --
 
 struct PrefillAttnArgs {
   int B, T, Hq, Hkv, n_qt, n_pairs, n_items;
   float sl2e;   // scale * log2(e)
-  float* out;   // [B][T][Hq*128] fp32
+  float* out;   // [B][T][Hq*HD] fp32
+  const int32_t* lens;  // real positions per sequence (device, [B]), or null: T for all
   int32_t* dev_err;
 };
 
-constexpr int kQTile = 128 * 128 * 2;     // 128 queries x 128 dims, f16 (two 64-dim halves)
-constexpr int kKTile = 128 * 128 * 2;     // 128 keys x 128 dims (two 64-dim halves)
-constexpr int kVTile = 128 * 128 * 2;     // V^T: 128 dims x 128 keys (two 64-key halves)
-constexpr int kKVStages = 2;
 constexpr int kQBufs = 2;                 // Q tiles: one per slot (use n = 2*item + slot -> n % kQBufs)
 constexpr int kStgBytes = 8 * 32 * 32 * 4;  // output staging: 32 rows x 32 fp32 per softmax warp
 constexpr int kBarBytes = 1024;           // mbarriers and the TMEM address
-constexpr int kAttnSmem =
-    kQBufs * kQTile + kKVStages * (kKTile + kVTile) + kStgBytes + kBarBytes + 1024;
 constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: TMA; 9: MMA
+
+// Tile sizes for head dimension HD (64 or 128).  Q and K tiles are 128 rows
+// of HD dims, stored as HD/64 blocks of 128 rows x 128 bytes (the 128-byte
+// swizzle atom); V^T tiles are HD rows (dims) of 128 keys, as two 64-key
+// blocks.  The K/V ring is deeper when the tiles are smaller.
+template <int HD>
+struct AttnCfg {
+  static constexpr int QT = 128 * HD * 2, KT = 128 * HD * 2, VT = HD * 128 * 2;
+  static constexpr int STAGES = HD == 128 ? 2 : 4;
+  static constexpr int SMEM = kQBufs * QT + STAGES * (KT + VT) + kStgBytes + kBarBytes + 1024;
+};
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
 // max of three fp32 values in one instruction (sm_100+)
@@ -236,12 +309,16 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 
 // One work item: two adjacent query tiles of one (sequence, head), tile A =
-// 2p in slot A and tile B = 2p+1 in slot B (a lone last tile when n_qt is
-// odd).  Key tiles are 128 keys, so slot B visits one tile more than slot A.
+// 2p in slot A and tile B = 2p+1 in slot B.  Key tiles are 128 keys.
+// Causal: a query tile visits the key tiles up to its own, so slot B visits
+// one tile more than slot A; unmasked: both visit all key tiles of the
+// sequence.  A tile at or past the sequence's real length L (lens[b]) is
+// absent (0 tiles); an item with neither tile is empty.
 struct PfItem {
-  int b, h, kvh, qt_a, qt_b, nA, nB, n;
+  int b, h, kvh, qt_a, qt_b, nA, nB, n, L;
 };
 
+template <bool CAUSAL>
 __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   const int BH = a.B * a.Hq;
   const int pair = a.n_pairs - 1 - it / BH;  // items run longest pairs first
@@ -252,8 +329,20 @@ __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   x.kvh = x.h / (a.Hq / a.Hkv);
   x.qt_a = 2 * pair;
   x.qt_b = 2 * pair + 1;
-  x.nA = x.qt_a + 1;  // 128-key tiles up to the tile's last row (causal)
-  x.nB = x.qt_b < a.n_qt ? x.qt_b + 1 : 0;
+  int L = a.T;
+  if (a.lens) {
+    L = __ldg(a.lens + x.b);
+    if (L < 0 || L > a.T) L = 0;  // reported by the producer warp
+  }
+  x.L = L;
+  const int nt = (L + 127) / 128;  // query (and key) tiles of the sequence
+  if (CAUSAL) {
+    x.nA = x.qt_a < nt ? x.qt_a + 1 : 0;
+    x.nB = x.qt_b < nt ? x.qt_b + 1 : 0;
+  } else {
+    x.nA = x.qt_a < nt ? nt : 0;
+    x.nB = x.qt_b < nt ? nt : 0;
+  }
   x.n = x.nA > x.nB ? x.nA : x.nB;
   return x;
 }
@@ -280,14 +369,18 @@ __device__ __forceinline__ int pf_item_index(int k, int n_items) {
 // its V^T, so the next K loads well ahead of its S.  Every barrier's phase
 // is counted across items, so the next item's loads and first S products
 // overlap the end of the current item.
+template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
+  using C = AttnCfg<HD>;
+  constexpr int kQTile = C::QT, kKTile = C::KT, kVTile = C::VT, kKVStages = C::STAGES;
+  constexpr int kHalfBlock = 128 * 128;  // bytes of one 64-dim block of a Q or K tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;                                  // kQBufs x 32 KB
-  unsigned char* sK = sQ + kQBufs * kQTile;                  // stages x 32 KB
-  unsigned char* sV = sK + kKVStages * kKTile;               // stages x 32 KB
+  unsigned char* sQ = smem;                                  // kQBufs Q tiles
+  unsigned char* sK = sQ + kQBufs * kQTile;                  // stages x K tile
+  unsigned char* sV = sK + kKVStages * kKTile;               // stages x V^T tile
   float* sStg = reinterpret_cast<float*>(sV + kKVStages * kVTile);  // 8 x 4 KB
   uint64_t* bar = reinterpret_cast<uint64_t*>(sV + kKVStages * kVTile + kStgBytes);
   uint64_t* q_full = bar;                   // kQBufs: the Q tile of a use landed
@@ -353,19 +446,24 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     auto load_q = [&](int k, int i, const PfItem& x) {
       const int n = 2 * k + i, u = n % kQBufs, c = n / kQBufs;
       if (c > 0 && !(ok = mbar_wait_warp(&q_empty[u], (c - 1) & 1))) return;
-      const bool has = i == 0 || x.nB > 0;
+      const bool has = (i == 0 ? x.nA : x.nB) > 0;
       mbar_arrive_expect_tx_warp(&q_full[u], has ? kQTile : 0);
       if (has) {
         const int qt = i == 0 ? x.qt_a : x.qt_b;
         unsigned char* qd = sQ + u * kQTile;
-        tma_load_3d_warp(qd, &tq, x.h * 128, qt * 128, x.b, &q_full[u]);
-        tma_load_3d_warp(qd + kQTile / 2, &tq, x.h * 128 + 64, qt * 128, x.b, &q_full[u]);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d_warp(qd + c * kHalfBlock, &tq, x.h * HD + 64 * c, qt * 128, x.b, &q_full[u]);
       }
     };
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item(a, it);
+      const PfItem x = pf_item<CAUSAL>(a, it);
+      if (a.lens && x.h == 0 && x.qt_a == 0 && lane == 0) {
+        const int v = __ldg(a.lens + x.b);
+        if (v < 0 || v > a.T) set_dev_err(a.dev_err, ASR_DEVERR_LEN);
+      }
       load_q(k, 0, x);  // its buffer was freed during the previous item
       for (int j = 0; j < x.n && ok; ++j, ++gk) {
         const int s = gk % kKVStages;
@@ -374,14 +472,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         unsigned char* vd = sV + s * kVTile;
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&k_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&k_full[s], kKTile);
-        tma_load_3d_warp(kd, &tk, x.kvh * 128, j * 128, x.b, &k_full[s]);
-        tma_load_3d_warp(kd + kKTile / 2, &tk, x.kvh * 128 + 64, j * 128, x.b, &k_full[s]);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d_warp(kd + c * kHalfBlock, &tk, x.kvh * HD + 64 * c, j * 128, x.b, &k_full[s]);
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&v_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
         tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         if (j == 0) load_q(k, 1, x);  // the buffer of this item's slot A tile's predecessor
       }
+      if (ok && x.n == 0) load_q(k, 1, x);  // an empty item still completes its slot B use
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else if (warp == 9) {
@@ -389,7 +489,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     // The whole warp runs the schedule (operand descriptors stay
     // warp-uniform); one elected lane issues each tcgen05 operation.
     constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 128);   // S = Q K^T: 128 x 128
-    constexpr uint32_t kIdO = mma_idesc_f16_f32(128, 128);   // O += P V: 128 x 128
+    constexpr uint32_t kIdO = mma_idesc_f16_f32(128, HD);    // O += P V: 128 x HD
     const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
     int gk = 0;          // K/V tiles consumed so far
     int gx[2] = {0, 0};  // tiles of slot A / B so far (S and P phases)
@@ -399,7 +499,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item(a, it);
+      const PfItem x = pf_item<CAUSAL>(a, it);
       const int nX[2] = {x.nA, x.nB};
       // Q buffer of slot i (use 2k + i) and the wait for its tile
       const int qb[2] = {(2 * k) % kQBufs, (2 * k + 1) % kQBufs};
@@ -411,9 +511,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       // holds P of its previous tile, read by a PV issued before this S
       auto issue_s_at = [&](int i, int qbuf, int st, bool last) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kQTile / 2) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (kKTile / 2) + (kk & 3) * 32;
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBlock + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * kHalfBlock + (kk & 3) * 32;
           mma_f16_warp(tS(i), sw128_kmajor_desc(aQ + qbuf * kQTile + off),
                        sw128_kmajor_desc(aK + st * kKTile + koff), kIdS, kk > 0);
         }
@@ -441,6 +541,14 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       auto k_ready = [&](int j) {
         return mbar_wait_warp(&k_full[(gk + j) % kKVStages], ((gk + j) / kKVStages) & 1);
       };
+      if (x.n == 0) {  // an empty item: release both Q uses and move on
+        ok = q_ready(0) && q_ready(1);
+        if (ok) {
+          mma_commit_warp(&q_empty[qb[0]]);
+          mma_commit_warp(&q_empty[qb[1]]);
+        }
+        continue;
+      }
       ok = k_ready(0) && (a_early || q_ready(0));
       tc_fence_after_sync();
       if (ok && !a_early) issue_s(0, 0);
@@ -479,8 +587,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         // this item's tile j has left), while slot B's softmax finishes.
         if (ok && j == x.nA - 1 && x.nB > x.nA) {
           const int it2 = pf_item_index(k + 1, a.n_items);
-          if (it2 >= 0) {
-            const PfItem x2 = pf_item(a, it2);
+          const PfItem x2 = pf_item<CAUSAL>(a, it2 >= 0 ? it2 : 0);
+          if (it2 >= 0 && x2.nA > 0) {
             const int g0 = gk + x.n, n2 = 2 * (k + 1);
             ok = mbar_wait_warp(&k_full[g0 % kKVStages], (g0 / kKVStages) & 1) &&
                  mbar_wait_warp(&q_full[n2 % kQBufs], (n2 / kQBufs) & 1);
@@ -509,7 +617,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item(a, it);
+      const PfItem x = pf_item<CAUSAL>(a, it);
       const int ni = i == 0 ? x.nA : x.nB;
       if (ni == 0) continue;
       const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
@@ -523,10 +631,14 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS(i) + lane_off + 32 * c, v + 32 * c);
         tmem_wait_ld();
-        if (j == ni - 1) {  // the diagonal tile: keys past the row are masked
+        if (j == ni - 1) {
+          // causal: the diagonal tile, keys past the row are masked (keys
+          // past the length are past every real row); unmasked: the last
+          // tile, keys at or past the length are masked
+          const int lim = CAUSAL ? row : x.L - 1 - 128 * j;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c > row) v[c] = -INFINITY;
+            if (c > lim) v[c] = -INFINITY;
         }
         float mx[16];
 #pragma unroll
@@ -543,7 +655,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
           const float alpha = grow ? ex2f(m - m_new) : 1.0f;
           float o[16];
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < HD / 16; ++c) {
             tmem_ld16(tO(i) + lane_off + c * 16, o);
             tmem_wait_ld();
 #pragma unroll
@@ -590,7 +702,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
       if (!ok) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tO(i) + lane_off + 32 * c, v + 32 * c);
+      for (int c = 0; c < HD / 32; ++c) tmem_ld32(tO(i) + lane_off + 32 * c, v + 32 * c);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
@@ -605,7 +717,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         float* stg = sStg + warp * (32 * 32);
         const int r0 = q0 + (warp & 3) * 32;  // query row of lane 0
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
+        for (int pc = 0; pc < HD / 32; ++pc) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int e = pc * 32 + c * 4;
@@ -618,10 +730,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             const int rr = it * 4 + (lane >> 3), cc = lane & 7;
             const float4 val =
                 *reinterpret_cast<const float4*>(stg + rr * 32 + ((cc ^ (rr & 7)) * 4));
-            if (r0 + rr < a.T)
+            if (r0 + rr < x.L)
               *reinterpret_cast<float4*>(
-                  a.out + (((int64_t)x.b * a.T + r0 + rr) * a.Hq + x.h) * kPrefillHD + pc * 32 +
-                  cc * 4) = val;
+                  a.out + (((int64_t)x.b * a.T + r0 + rr) * a.Hq + x.h) * HD + pc * 32 + cc * 4) =
+                  val;
           }
           __syncwarp();
         }
@@ -680,7 +792,12 @@ size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv) {
   return qhat + vt;
 }
 
+size_t mha_ws_bytes(int B, int T, int H, int HD) {
+  return (size_t)B * H * HD * round_up(T, 128) * 2;  // V^T
+}
+
 static std::once_flag g_prefill_attr;
+static std::once_flag g_attn_attr[4];
 
 }  // namespace asrkv
 
@@ -706,13 +823,34 @@ static int prefill_check(int B, int T, int q_heads, int kv_heads, int head_dim, 
 static cudaError_t prefill_attrs() {
   static cudaError_t attr = cudaSuccess;
   std::call_once(g_prefill_attr, [] {
-    attr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kAttnSmem);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  100 * 1024);
+    attr = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                100 * 1024);
   });
   return attr;
+}
+
+// Launch the tensor-core attention for head dimension HD, causal or not.
+// Q tiles are read through tq (dims: Hq*HD, T, B), K tiles through tk (a row
+// buffer whose head h key vector sits at column h*HD), V^T through tv (dims:
+// Tpad, HD, B*Hkv).  Persistent: one CTA per SM, at most one per item.
+template <int HD, bool CAUSAL>
+static int launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          PrefillAttnArgs& aa, cudaStream_t stream) {
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(g_attn_attr[(HD == 64 ? 0 : 2) + (CAUSAL ? 0 : 1)], [] {
+    attr = cudaFuncSetAttribute(attn_tc_kernel<HD, CAUSAL>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<HD>::SMEM);
+  });
+  if (attr != cudaSuccess) return ASR_ERR_CUDA;
+  aa.n_qt = (aa.T + 127) / 128;
+  aa.n_pairs = (aa.n_qt + 1) / 2;
+  aa.n_items = aa.n_pairs * aa.B * aa.Hq;
+  const int sms = device_sm_count();
+  if (sms <= 0) return ASR_ERR_CUDA;
+  const int ctas = aa.n_items < sms ? aa.n_items : sms;
+  cudaError_t e = launch_pdl(attn_tc_kernel<HD, CAUSAL>, dim3(ctas), dim3(kAttnThreads),
+                             (size_t)AttnCfg<HD>::SMEM, stream, tq, tk, tv, aa);
+  return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
 }
 
 static uint16_t* ws_vt(void* ws, int B, int T, int q_heads) {
@@ -749,8 +887,12 @@ extern "C" int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint
   pa.seq_stride = seq_stride;
   pa.qhat = static_cast<uint16_t*>(ws);
   pa.vt = ws_vt(ws, B, T, q_heads);
-  for (int i = 0; i < kPrefillHD / 2; ++i)
-    pa.theta[i] = pow((double)rope_base, -2.0 * i / kPrefillHD);
+  for (int i = 0; i < kPrefillHD / 2; ++i) {
+    const double t = pow((double)rope_base, -2.0 * i / kPrefillHD) / (2.0 * 3.14159265358979323846);
+    const float hi = (float)t;
+    pa.rope_turns[2 * i] = hi;
+    pa.rope_turns[2 * i + 1] = (float)(t - (double)hi);
+  }
   const size_t prep_smem =
       2 * kPrepT * (kPrefillHD / 2) * sizeof(float) + (size_t)kPrepT * kv_heads * kPrefillHD * 2;
   cudaError_t e = launch_pdl(prefill_prep_kernel, dim3(Tpad / kPrepT, B), dim3(256), prep_smem,
@@ -785,19 +927,98 @@ extern "C" int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, in
   aa.T = T;
   aa.Hq = q_heads;
   aa.Hkv = kv_heads;
-  aa.n_qt = (T + 127) / 128;
-  aa.n_pairs = (aa.n_qt + 1) / 2;
-  aa.n_items = aa.n_pairs * B * q_heads;
   aa.sl2e = scale * kLog2eP;
   aa.out = out;
+  aa.lens = nullptr;
   aa.dev_err = dev_err;
-  const int sms = device_sm_count();
-  if (sms <= 0) return ASR_ERR_CUDA;
-  const int ctas = aa.n_items < sms ? aa.n_items : sms;  // persistent: one per SM
-  cudaError_t e = launch_pdl(prefill_attn_kernel, dim3(ctas),
-                             dim3(kAttnThreads), (size_t)kAttnSmem, (cudaStream_t)stream, tq, tk,
-                             tv, aa);
-  return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
+  return launch_attn_tc<kPrefillHD, true>(tq, tk, tv, aa, (cudaStream_t)stream);
+}
+
+// Checks shared by the MHA entry points (host only, before any launch).
+static int mha_check(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int T,
+                     int heads, int head_dim, const float* out, void* ws, size_t ws_bytes) {
+  if (B < 0 || B > ASR_MAX_BATCH || T < 1 || heads < 1) return ASR_ERR_INVALID_ARG;
+  if ((head_dim != 64 && head_dim != 128) || heads > ASR_MAX_KV_HEADS) return ASR_ERR_UNSUPPORTED;
+  if (B == 0) return ASR_OK;
+  if (!q || !k || !v || !out) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ASR_ERR_MISALIGNED;
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < mha_ws_bytes(B, T, heads, head_dim))
+    return ASR_ERR_WORKSPACE;
+  return ASR_OK;
+}
+
+// The MHA prep (V^T, and cache rows when cache is given) then the
+// tensor-core attention with Q and K read where they lie: K from the cache
+// rows (prefill) or from k itself (encoder).
+static int mha_run(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
+                   int B, int T, int heads, int head_dim, float scale, bool causal, uint16_t* cache,
+                   int64_t seq_stride, float* out, void* ws, int32_t* dev_err,
+                   cudaStream_t stream) {
+  const int Tpad = round_up(T, 128);
+  MhaPrepArgs pa = {};
+  pa.k = k;
+  pa.v = v;
+  pa.lens = lens;
+  pa.B = B;
+  pa.T = T;
+  pa.Tpad = Tpad;
+  pa.H = heads;
+  pa.HD = head_dim;
+  pa.cache = cache;
+  pa.seq_stride = seq_stride;
+  pa.vt = static_cast<uint16_t*>(ws);
+  if (launch_pdl(mha_prep_kernel, dim3(Tpad / kMhaPrepT, B), dim3(256), 0, stream, pa) !=
+      cudaSuccess)
+    return ASR_ERR_CUDA;
+  const uint64_t rw = (uint64_t)heads * head_dim;
+  CUtensorMap tq, tk, tv;
+  bool ok = make_tmap_f16_3d(&tq, q, rw, T, B, rw * 2, (uint64_t)T * rw * 2, 64, 128) &&
+            make_tmap_f16_3d(&tv, ws, Tpad, head_dim, (uint64_t)B * heads, (uint64_t)Tpad * 2,
+                             (uint64_t)Tpad * head_dim * 2, 64, head_dim);
+  if (cache)  // rows of [K | V] of 2*rw elements; K of head h at column h*hd
+    ok = ok && make_tmap_f16_3d(&tk, cache, 2 * rw, T, B, 2 * rw * 2, (uint64_t)seq_stride * 2,
+                                64, 128);
+  else
+    ok = ok && make_tmap_f16_3d(&tk, k, rw, T, B, rw * 2, (uint64_t)T * rw * 2, 64, 128);
+  if (!ok) return ASR_ERR_CUDA;
+  PrefillAttnArgs aa = {};
+  aa.B = B;
+  aa.T = T;
+  aa.Hq = heads;
+  aa.Hkv = heads;
+  aa.sl2e = scale * kLog2eP;
+  aa.out = out;
+  aa.lens = lens;
+  aa.dev_err = dev_err;
+  if (head_dim == 64)
+    return causal ? launch_attn_tc<64, true>(tq, tk, tv, aa, stream)
+                  : launch_attn_tc<64, false>(tq, tk, tv, aa, stream);
+  return causal ? launch_attn_tc<128, true>(tq, tk, tv, aa, stream)
+                : launch_attn_tc<128, false>(tq, tk, tv, aa, stream);
+}
+
+extern "C" int asr_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const int32_t* lens, int B, int T, int heads, int head_dim,
+                               float scale, uint16_t* cache, int64_t seq_stride, int capacity,
+                               float* out, void* ws, size_t ws_bytes, int32_t* dev_err,
+                               asr_stream_t stream) {
+  int st = mha_check(q, k, v, B, T, heads, head_dim, out, ws, ws_bytes);
+  if (st != ASR_OK || B == 0) return st;
+  if (capacity < 1 || T > capacity || !cache) return ASR_ERR_INVALID_ARG;
+  if (seq_stride < (int64_t)capacity * 2 * heads * head_dim) return ASR_ERR_INVALID_ARG;
+  if (!aligned16(cache) || seq_stride % 8 != 0) return ASR_ERR_MISALIGNED;
+  return mha_run(q, k, v, lens, B, T, heads, head_dim, scale, true, cache, seq_stride, out, ws,
+                 dev_err, (cudaStream_t)stream);
+}
+
+extern "C" int asr_encoder_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const int32_t* lens, int B, int T, int heads, int head_dim,
+                                float scale, float* out, void* ws, size_t ws_bytes,
+                                int32_t* dev_err, asr_stream_t stream) {
+  int st = mha_check(q, k, v, B, T, heads, head_dim, out, ws, ws_bytes);
+  if (st != ASR_OK || B == 0) return st;
+  return mha_run(q, k, v, lens, B, T, heads, head_dim, scale, false, nullptr, 0, out, ws,
+                 dev_err, (cudaStream_t)stream);
 }
 
 extern "C" int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,

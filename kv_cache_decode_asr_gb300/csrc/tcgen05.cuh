@@ -267,5 +267,7 @@ bool make_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
 // Workspace bytes of the prefill: q^ [B][T][Hq*128] f16 (1024-byte aligned
 // end), then V^T [B*Hkv][128][T rounded up to 128] f16.
 size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv);
+// Workspace bytes of the MHA prefill and encoder attention (V transposed).
+size_t mha_ws_bytes(int B, int T, int H, int HD);
 
 }  // namespace asrkv

@@ -19,6 +19,7 @@ STATUS = {0: "ASR_OK", 1: "ASR_ERR_INVALID_ARG", 2: "ASR_ERR_UNSUPPORTED",
           7: "ASR_ERR_SCRATCH_LIMIT"}
 DEVERR_LEN, DEVERR_INDEX, DEVERR_BEAMS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 OP_SELF_ATTN, OP_CROSS_ATTN, OP_GQA_STEP, OP_PREFILL_ATTN = 1, 2, 3, 4
+OP_MHA_PREFILL, OP_ENCODER_ATTN = 5, 6
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -46,6 +47,9 @@ SIGNATURES = {
                                 _i64, _int, _p, _sz, _p]),
     "asr_prefill_attention": (_int, [_int, _int, _int, _int, _int, _f, _p, _i64, _int, _p, _p,
                                      _sz, _p, _p]),
+    "asr_mha_prefill": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _i64, _int, _p, _p,
+                               _sz, _p, _p]),
+    "asr_encoder_attn": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _p, _sz, _p, _p]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -277,6 +281,41 @@ def asr_prefill_attention(B, T, q_heads, kv_heads, head_dim, scale, cache, capac
                                       cache.stride(0), capacity, _ptr(out), wp, wn, _ptr(dev_err),
                                       _stream(stream))
     _check("asr_prefill_attention", st)
+
+
+def asr_mha_prefill(q, k, v, heads, head_dim, scale, cache, capacity, out, ws, lens=None,
+                    dev_err=None, stream=None):
+    """q, k, v: f16 [B, T, heads*head_dim]; cache: f16 [B, capacity, 2*heads*head_dim];
+    out: fp32 [B, T, heads*head_dim]; lens: int32 [B] or None."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cache, "cache")):
+        _need(t, torch.float16, n)
+    _need(out, torch.float32, "out")
+    if lens is not None:
+        _need(lens, torch.int32, "lens")
+    B, T = q.shape[0], q.shape[1]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_mha_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, T, heads, head_dim,
+                                float(scale), _ptr(cache), cache.stride(0), capacity, _ptr(out),
+                                wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_mha_prefill", st)
+
+
+def asr_encoder_attn(q, k, v, heads, head_dim, scale, out, ws, lens=None, dev_err=None,
+                     stream=None):
+    """q, k, v: f16 [B, T, heads*head_dim]; out: fp32 [B, T, heads*head_dim];
+    lens: int32 [B] or None."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.float16, n)
+    _need(out, torch.float32, "out")
+    if lens is not None:
+        _need(lens, torch.int32, "lens")
+    B, T = q.shape[0], q.shape[1]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_encoder_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, T, heads, head_dim,
+                                 float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_encoder_attn", st)
 
 
 def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,

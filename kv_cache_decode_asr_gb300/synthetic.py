@@ -20,6 +20,11 @@ Workloads (shapes of the pages' models; no weights or audio are needed):
   RMSNorm weights N(1, 0.1).
 * ``qwen3_asr_prefill_b8`` -- the same decoder prefilling 8 prompts of 1536
   tokens (16 prefix + 1500 audio frames + 20 suffix).
+* ``whisper_large_prefill_b32`` -- Large-Whisper decoder prompt prefill
+  (20 heads x 64): 32 prompts of up to 448 tokens, lengths uniform in
+  [1, 448], K/V written to a 448-slot self cache.
+* ``whisper_large_encoder_b8`` -- Large-Whisper encoder self-attention (20
+  heads x 64) over the 1500 frames of 8 utterances, unmasked.
 
 Values: activations and caches N(0, 1); caches are stored as f16 (the fp32
 draw rounded to nearest even).  Host draws use numpy's PCG64; device draws use
@@ -42,6 +47,9 @@ WORKLOADS = {
     "qwen3_asr_prefill_b8": dict(kind="prefill", B=8, T=1536, prefix=16, audio=1500, suffix=20,
                                  q_heads=16, kv_heads=8, head_dim=128, capacity=1536, eps=1e-6,
                                  rope_base=1e6, w_mean=1.0, w_std=0.1),
+    "whisper_large_prefill_b32": dict(kind="mha_prefill", B=32, T=448, heads=20, head_dim=64,
+                                      capacity=448, len_lo=1, len_hi=448),
+    "whisper_large_encoder_b8": dict(kind="encoder", B=8, T=1500, heads=20, head_dim=64),
 }
 
 
