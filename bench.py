@@ -622,6 +622,129 @@ class PrefillStep:
         return self.B * self.Hq
 
 
+class MhaAttnStep:
+    """Large-Whisper multi-head attention of a batch of sequences among
+    themselves, one layer: the decoder's prompt prefill (causal, K/V rows
+    into the self cache, per-sequence lengths) or the encoder's unmasked
+    self-attention over 1500 frames.  One step is one call: a small prep
+    (V transposed, cache rows) and the tcgen05 attention."""
+
+    kernel_sources = PREFILL_SOURCES
+
+    def __init__(self, name, cfg, device, rank=0):
+        import torch
+        from kv_cache_decode_asr_gb300 import ops
+        self.name, self.cfg, self.ops = name, cfg, ops
+        wi = rank_seed_base(name, rank)
+        self.causal = cfg["kind"] == "mha_prefill"
+        B, T, H, hd = cfg["B"], cfg["T"], cfg["heads"], cfg["head_dim"]
+        self.B, self.T, self.H, self.hd, self.L = B, T, H, hd, 1
+        self.scale = hd ** -0.5
+        f16 = torch.float16
+        self.q = syn.dev_normal((B, T, H * hd), syn.seed_for(wi, 1), device, dtype=f16)
+        self.k = syn.dev_normal((B, T, H * hd), syn.seed_for(wi, 2), device, dtype=f16)
+        self.v = syn.dev_normal((B, T, H * hd), syn.seed_for(wi, 3), device, dtype=f16)
+        if self.causal:
+            self.lens_host = syn.lens_uniform(B, cfg["len_lo"], cfg["len_hi"], syn.seed_for(wi, 4))
+            self.lens = torch.from_numpy(self.lens_host).to(device)
+            self.cap = cfg["capacity"]
+            self.cache = torch.zeros(B, self.cap, 2 * H * hd, dtype=f16, device=device)
+            op = ops.OP_MHA_PREFILL
+        else:
+            self.lens_host = np.full(B, T, np.int32)
+            self.lens = None
+            op = ops.OP_ENCODER_ATTN
+        self.out = torch.zeros(B, T, H * hd, device=device)
+        self.ws = ops.workspace(op, B, H, 1, H, hd, T, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        kname = f"attn_tc_kernel<{hd},{'true' if self.causal else 'false'}>"
+        api = "asr_mha_prefill" if self.causal else "asr_encoder_attn"
+        self.dominant = api
+        self.dominant_kernel = f"{kname} with its prep kernel ({api}, the whole call)"
+        self.metric = ("prompt-prefill tokens/s" if self.causal else "encoder frames/s") + \
+            " (tensor-core TFLOP/s and fraction of the f16 peak alongside)"
+
+    def launches(self):
+        return 2
+
+    def step(self, stream=None):
+        if self.causal:
+            self.ops.asr_mha_prefill(self.q, self.k, self.v, self.H, self.hd, self.scale,
+                                     self.cache, self.cap, self.out, self.ws, lens=self.lens,
+                                     dev_err=self.err, stream=stream)
+        else:
+            self.ops.asr_encoder_attn(self.q, self.k, self.v, self.H, self.hd, self.scale,
+                                      self.out, self.ws, dev_err=self.err, stream=stream)
+
+    def traffic_key(self):
+        return self.dominant
+
+    def dominant_call(self, l, stream=None):
+        self.step(stream)
+
+    def flops(self):
+        """QK^T and PV over the keys each real query attends (causal: j <= t)."""
+        L = self.lens_host.astype(np.int64)
+        pairs = (L * (L + 1) // 2).sum() if self.causal else (L * L).sum()
+        return int(4 * self.H * self.hd * pairs)
+
+    def kv_bytes_per_step(self):
+        """q, k, v in (f16, real rows), output out (fp32), cache rows (prefill)."""
+        n = int(self.lens_host.sum()) * self.H * self.hd
+        return n * 2 * 3 + n * 4 + (n * 2 * 2 if self.causal else 0)
+
+    def tokens_per_step(self):
+        return int(self.lens_host.sum())
+
+    def roofline(self, launch_ms, peaks):
+        peak, src = peaks["tensor"]
+        f = self.flops()
+        achieved = f / (launch_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "flops_per_launch": f,
+                "peak_source": f"{src} (dense f16 taken equal to bf16, the nominal ratio 1:1)"}
+
+    def host_io(self):
+        return [self.q, self.k, self.v], [self.out]
+
+    def n_samples(self):
+        return self.B
+
+    def _h16(self, t):
+        import torch
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def oracle_sample(self, i, oracle):
+        """Sequence i, every head and real position."""
+        q, k, v = self._h16(self.q[i:i + 1]), self._h16(self.k[i:i + 1]), self._h16(self.v[i:i + 1])
+        L = int(self.lens_host[i])
+        t0 = time.perf_counter()
+        ref, _ = oracle.mha_attn(q, k, v, self.H, self.hd, self.scale, self.causal,
+                                 lens=np.array([L], np.int32))
+        dt = time.perf_counter() - t0
+        got = self.out[i, :L].cpu().numpy()
+        return dt, L / self.tokens_per_step(), {"out": ref[0, :L]}, {"out": got}, f"sequence {i}"
+
+    def oracle_unit(self, i, oracle, cache):
+        """Reference-arm unit: one head of one sequence."""
+        b = (i // self.H) % self.B
+        h = i % self.H
+        if b not in cache:
+            cache.clear()
+            cache[b] = tuple(self._h16(t[b:b + 1]) for t in (self.q, self.k, self.v))
+        q, k, v = cache[b]
+        sl = slice(h * self.hd, (h + 1) * self.hd)
+        qh, kh, vh = (np.ascontiguousarray(x[:, :, sl]) for x in (q, k, v))
+        L = int(self.lens_host[b])
+        t0 = time.perf_counter()
+        oracle.mha_attn(qh, kh, vh, 1, self.hd, self.scale, self.causal,
+                        lens=np.array([L], np.int32))
+        return time.perf_counter() - t0
+
+    def units_per_step(self):
+        return self.B * self.H
+
+
 def make_workload(name, device, rank=0, layers=0):
     cfg = dict(syn.WORKLOADS[name])
     if layers:
@@ -632,6 +755,8 @@ def make_workload(name, device, rank=0, layers=0):
         return GqaStep(name, cfg, device, rank)
     if cfg["kind"] == "prefill":
         return PrefillStep(name, cfg, device, rank)
+    if cfg["kind"] in ("mha_prefill", "encoder"):
+        return MhaAttnStep(name, cfg, device, rank)
     raise SystemExit(f"workload {name}: not a decode-step bench line")
 
 

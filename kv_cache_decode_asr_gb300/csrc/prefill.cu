@@ -219,16 +219,17 @@ struct MhaPrepArgs {
   uint16_t* vt;  // [B*H][HD][Tpad]
 };
 
-constexpr int kMhaPrepT = 32;  // positions per CTA
+constexpr int kMhaPrepT = 64;  // positions per CTA
 
-// grid (Tpad / 32, B), 256 threads.  For each head: the chunk's V (and K)
-// vectors are loaded, copied to the cache rows of the real positions, and V
-// is staged in shared memory, then written transposed (32 positions = 64
-// bytes per dim row), zero at and past the sequence's length.
+// grid (Tpad / 64, H, B), 256 threads: one head of 64 positions of one
+// sequence per CTA.  Its V (and K) vectors are loaded, copied to the cache
+// rows of the real positions, and V is staged in shared memory, then written
+// transposed (64 positions = 128 bytes per dim row), zero at and past the
+// sequence's length.
 __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ MhaPrepArgs a) {
   __shared__ __align__(16) uint16_t tile[kMhaPrepT][128 + 8];
   const int tid = threadIdx.x;
-  const int b = blockIdx.y;
+  const int h = blockIdx.y, b = blockIdx.z;
   const int t0 = blockIdx.x * kMhaPrepT;
   grid_launch_dependents();
   grid_dependency_wait();
@@ -239,32 +240,29 @@ __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ M
   }
   const int HD = a.HD, vpr = HD / 8;  // 16-byte vectors per head row
   const int64_t rw = (int64_t)a.H * HD;
-  for (int h = 0; h < a.H; ++h) {
-    for (int idx = tid; idx < kMhaPrepT * vpr; idx += blockDim.x) {
-      const int tt = idx / vpr, c = idx % vpr, t = t0 + tt;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (t < L) {
-        const int64_t off = ((int64_t)b * a.T + t) * rw + h * HD + c * 8;
-        val = *reinterpret_cast<const uint4*>(a.v + off);
-        if (a.cache) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(a.k + off);
-          uint16_t* row = a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * rw;
-          *reinterpret_cast<uint4*>(row + h * HD + c * 8) = kv;
-          *reinterpret_cast<uint4*>(row + rw + h * HD + c * 8) = val;
-        }
+  for (int idx = tid; idx < kMhaPrepT * vpr; idx += blockDim.x) {
+    const int tt = idx / vpr, c = idx % vpr, t = t0 + tt;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (t < L) {
+      const int64_t off = ((int64_t)b * a.T + t) * rw + h * HD + c * 8;
+      val = *reinterpret_cast<const uint4*>(a.v + off);
+      if (a.cache) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(a.k + off);
+        uint16_t* row = a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * rw;
+        *reinterpret_cast<uint4*>(row + h * HD + c * 8) = kv;
+        *reinterpret_cast<uint4*>(row + rw + h * HD + c * 8) = val;
       }
-      *reinterpret_cast<uint4*>(&tile[tt][c * 8]) = val;
     }
-    __syncthreads();
-    for (int idx = tid; idx < HD * (kMhaPrepT / 8); idx += blockDim.x) {
-      const int d = idx / (kMhaPrepT / 8), q8 = idx % (kMhaPrepT / 8);
-      alignas(16) uint16_t col[8];
+    *reinterpret_cast<uint4*>(&tile[tt][c * 8]) = val;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < HD * (kMhaPrepT / 8); idx += blockDim.x) {
+    const int d = idx / (kMhaPrepT / 8), q8 = idx % (kMhaPrepT / 8);
+    alignas(16) uint16_t col[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) col[e] = tile[q8 * 8 + e][d];
-      *reinterpret_cast<uint4*>(a.vt + (((int64_t)b * a.H + h) * HD + d) * a.Tpad + t0 + q8 * 8) =
-          *reinterpret_cast<const uint4*>(col);
-    }
-    __syncthreads();
+    for (int e = 0; e < 8; ++e) col[e] = tile[q8 * 8 + e][d];
+    *reinterpret_cast<uint4*>(a.vt + (((int64_t)b * a.H + h) * HD + d) * a.Tpad + t0 + q8 * 8) =
+        *reinterpret_cast<const uint4*>(col);
   }
 }
 
@@ -967,7 +965,7 @@ static int mha_run(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
   pa.cache = cache;
   pa.seq_stride = seq_stride;
   pa.vt = static_cast<uint16_t*>(ws);
-  if (launch_pdl(mha_prep_kernel, dim3(Tpad / kMhaPrepT, B), dim3(256), 0, stream, pa) !=
+  if (launch_pdl(mha_prep_kernel, dim3(Tpad / kMhaPrepT, heads, B), dim3(256), 0, stream, pa) !=
       cudaSuccess)
     return ASR_ERR_CUDA;
   const uint64_t rw = (uint64_t)heads * head_dim;
