@@ -316,7 +316,7 @@ struct PfItem {
   int b, h, kvh, qt_a, qt_b, nA, nB, n, L;
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   const int BH = a.B * a.Hq;
   const int pair = a.n_pairs - 1 - it / BH;  // items run longest pairs first
@@ -328,7 +328,7 @@ __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   x.qt_a = 2 * pair;
   x.qt_b = 2 * pair + 1;
   int L = a.T;
-  if (a.lens) {
+  if (VARLEN) {
     L = __ldg(a.lens + x.b);
     if (L < 0 || L > a.T) L = 0;  // reported by the producer warp
   }
@@ -367,7 +367,7 @@ __device__ __forceinline__ int pf_item_index(int k, int n_items) {
 // its V^T, so the next K loads well ahead of its S.  Every barrier's phase
 // is counted across items, so the next item's loads and first S products
 // overlap the end of the current item.
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
@@ -457,8 +457,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL>(a, it);
-      if (a.lens && x.h == 0 && x.qt_a == 0 && lane == 0) {
+      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
+      if (VARLEN && x.h == 0 && x.qt_a == 0 && lane == 0) {
         const int v = __ldg(a.lens + x.b);
         if (v < 0 || v > a.T) set_dev_err(a.dev_err, ASR_DEVERR_LEN);
       }
@@ -479,7 +479,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         if (j == 0) load_q(k, 1, x);  // the buffer of this item's slot A tile's predecessor
       }
-      if (ok && x.n == 0) load_q(k, 1, x);  // an empty item still completes its slot B use
+      if (VARLEN && ok && x.n == 0) load_q(k, 1, x);  // an empty item still completes its slot B use
     }
     if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   } else if (warp == 9) {
@@ -497,7 +497,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
       const int nX[2] = {x.nA, x.nB};
       // Q buffer of slot i (use 2k + i) and the wait for its tile
       const int qb[2] = {(2 * k) % kQBufs, (2 * k + 1) % kQBufs};
@@ -539,7 +539,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       auto k_ready = [&](int j) {
         return mbar_wait_warp(&k_full[(gk + j) % kKVStages], ((gk + j) / kKVStages) & 1);
       };
-      if (x.n == 0) {  // an empty item: release both Q uses and move on
+      if (VARLEN && x.n == 0) {  // an empty item: release both Q uses and move on
         ok = q_ready(0) && q_ready(1);
         if (ok) {
           mma_commit_warp(&q_empty[qb[0]]);
@@ -585,8 +585,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // this item's tile j has left), while slot B's softmax finishes.
         if (ok && j == x.nA - 1 && x.nB > x.nA) {
           const int it2 = pf_item_index(k + 1, a.n_items);
-          const PfItem x2 = pf_item<CAUSAL>(a, it2 >= 0 ? it2 : 0);
-          if (it2 >= 0 && x2.nA > 0) {
+          if (it2 >= 0 && (!VARLEN || pf_item<CAUSAL, VARLEN>(a, it2).nA > 0)) {
+            const PfItem x2 = pf_item<CAUSAL, VARLEN>(a, it2);
             const int g0 = gk + x.n, n2 = 2 * (k + 1);
             ok = mbar_wait_warp(&k_full[g0 % kKVStages], (g0 / kKVStages) & 1) &&
                  mbar_wait_warp(&q_full[n2 % kQBufs], (n2 / kQBufs) & 1);
@@ -615,7 +615,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
       const int ni = i == 0 ? x.nA : x.nB;
       if (ni == 0) continue;
       const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
@@ -795,7 +795,7 @@ size_t mha_ws_bytes(int B, int T, int H, int HD) {
 }
 
 static std::once_flag g_prefill_attr;
-static std::once_flag g_attn_attr[4];
+static std::once_flag g_attn_attr[8];
 
 }  // namespace asrkv
 
@@ -831,12 +831,12 @@ static cudaError_t prefill_attrs() {
 // Q tiles are read through tq (dims: Hq*HD, T, B), K tiles through tk (a row
 // buffer whose head h key vector sits at column h*HD), V^T through tv (dims:
 // Tpad, HD, B*Hkv).  Persistent: one CTA per SM, at most one per item.
-template <int HD, bool CAUSAL>
-static int launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          PrefillAttnArgs& aa, cudaStream_t stream) {
+template <int HD, bool CAUSAL, bool VARLEN>
+static int launch_attn_tc_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            PrefillAttnArgs& aa, cudaStream_t stream) {
   static cudaError_t attr = cudaSuccess;
-  std::call_once(g_attn_attr[(HD == 64 ? 0 : 2) + (CAUSAL ? 0 : 1)], [] {
-    attr = cudaFuncSetAttribute(attn_tc_kernel<HD, CAUSAL>,
+  std::call_once(g_attn_attr[(HD == 64 ? 0 : 4) + (CAUSAL ? 0 : 2) + (VARLEN ? 1 : 0)], [] {
+    attr = cudaFuncSetAttribute(attn_tc_kernel<HD, CAUSAL, VARLEN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<HD>::SMEM);
   });
   if (attr != cudaSuccess) return ASR_ERR_CUDA;
@@ -846,9 +846,18 @@ static int launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
   const int ctas = aa.n_items < sms ? aa.n_items : sms;
-  cudaError_t e = launch_pdl(attn_tc_kernel<HD, CAUSAL>, dim3(ctas), dim3(kAttnThreads),
+  cudaError_t e = launch_pdl(attn_tc_kernel<HD, CAUSAL, VARLEN>, dim3(ctas), dim3(kAttnThreads),
                              (size_t)AttnCfg<HD>::SMEM, stream, tq, tk, tv, aa);
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
+}
+
+// With per-sequence lengths the kernel reads them per item and may meet
+// empty items; without, that work is compiled out.
+template <int HD, bool CAUSAL>
+static int launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          PrefillAttnArgs& aa, cudaStream_t stream) {
+  return aa.lens ? launch_attn_tc_v<HD, CAUSAL, true>(tq, tk, tv, aa, stream)
+                 : launch_attn_tc_v<HD, CAUSAL, false>(tq, tk, tv, aa, stream);
 }
 
 static uint16_t* ws_vt(void* ws, int B, int T, int q_heads) {
