@@ -67,6 +67,7 @@ def _lib():
                                              _dbl, _f64p]),
             "orc_mha_attn": (_int, [_u16p, _u16p, _u16p, _i32p, _int, _int, _int, _int, _dbl, _int,
                                     _u16p, _i64, _int, _f64p]),
+            "orc_cross_kv_fill": (None, [_u16p, _u16p, _f32p, _int, _int, _int, _u16p, _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -343,6 +344,20 @@ def mha_attn(q, k, v, heads, head_dim, scale, causal, lens=None, cache=None):
     return out, n
 
 
+def cross_kv_fill(enc, w, bias_v, cross):
+    """Cross K/V of one layer from the encoder output: enc uint16 [G, frames, d],
+    w uint16 [2d, d], bias_v float32 [d]; cross uint16 [G, frames_cap, 2d] is
+    written in place (rows [0, frames))."""
+    enc = _c(enc, np.uint16)
+    w = _c(w, np.uint16)
+    bias_v = _c(np.ascontiguousarray(bias_v, np.float32), np.float32)
+    cross = _c(cross, np.uint16)
+    G, frames, d = enc.shape
+    _lib().orc_cross_kv_fill(_p(enc, ctypes.c_uint16), _p(w, ctypes.c_uint16),
+                             _p(bias_v, ctypes.c_float), G, frames, d,
+                             _p(cross, ctypes.c_uint16), cross[0].size)
+
+
 def build():
     """Compile liboracle.so (the checker) if it is missing or stale."""
     return _build.build()
@@ -351,7 +366,7 @@ def build():
 __all__ = [
     "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
     "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
-    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "build",
+    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "cross_kv_fill", "build",
 ]
 
 if os.environ.get("ORACLE_THREADS"):

@@ -681,3 +681,51 @@ int orc_mha_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, const 
   free(L);
   return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Next row: the cross K/V fill                                             */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const uint16_t* enc;
+  const uint16_t* w;
+  const float* bias_v;
+  int frames, d;
+  uint16_t* cross;
+  int64_t group_stride;
+} orc_fill_ctx;
+
+static void orc_fill_item(void* vctx, int64_t item) {
+  orc_fill_ctx* c = (orc_fill_ctx*)vctx;
+  int d = c->d;
+  int64_t g = item / c->frames;
+  int t = (int)(item % c->frames);
+  const uint16_t* e = c->enc + (g * c->frames + t) * (int64_t)d;
+  uint16_t* row = c->cross + g * c->group_stride + (int64_t)t * 2 * d;
+  double* x = (double*)malloc(sizeof(double) * d);
+  for (int k = 0; k < d; ++k) x[k] = orc_f16_to_f64(e[k]);
+  for (int n = 0; n < 2 * d; ++n) {
+    const uint16_t* wn = c->w + (int64_t)n * d;
+    double acc = 0.0;
+    for (int k = 0; k < d; ++k) acc += x[k] * orc_f16_to_f64(wn[k]);
+    if (n >= d) acc += (double)c->bias_v[n - d]; /* k has no bias */
+    row[n] = orc_f64_to_f16(acc);
+  }
+  free(x);
+}
+
+/* The cross-attention K and V of one layer from the encoder output
+ * ("wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_cross: a GEMM of
+ * the encoder rows with the layer's [k | v] weight and a bias epilogue,
+ * then a pack to f16 cache rows; Decoder::load: the bias of k is zero, v
+ * has its own; "Nest whisper-tiny, src/lib.linnet", DecoderLayer.listen).
+ *   cross row t of group g = f16(enc[g][t] . W^T + [0 | bias_v]),
+ *   i.e. element n is sum_k enc[g][t][k] * W[n][k] (+ bias_v[n - d] for
+ *   n >= d): the first d elements are K of all heads, the last d are V.
+ * enc: f16 [G][frames][d]; W: f16 [2d][d] (row n makes output column n);
+ * bias_v: fp32 [d]; cross: f16 [G][group_stride], rows of 2d. */
+void orc_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_v, int G,
+                       int frames, int d, uint16_t* cross, int64_t group_stride) {
+  orc_fill_ctx c = {enc, w, bias_v, frames, d, cross, group_stride};
+  orc_parallel_for((int64_t)G * frames, orc_fill_item, &c);
+}

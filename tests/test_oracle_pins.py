@@ -533,3 +533,38 @@ def test_encoder_attn_rows_equal_cross_step(oracle_mod):
     # a length outside [0, T] is counted and skipped
     _, bad = oracle_mod.mha_attn(q, k, v, H, hd, hd ** -0.5, False, lens=np.array([T + 1, 3], np.int32))
     assert bad == 1
+
+
+# ----------------------------------------------------------- cross K/V fill ----
+
+def test_cross_kv_fill_matches_numpy_and_closed_forms(oracle_mod):
+    """The fill against numpy's float64 matmul of the decoded f16 operands
+    (then numpy's own f16 rounding); identity weights return the encoder
+    rows (K) and the rows plus the bias (V); a zero input gives K = 0 and
+    V = f16(bias); rows past the frames are untouched."""
+    G, frames, d, cap = 2, 5, 16, 7
+    enc = syn.host_normal_f16bits((G, frames, d), 50)
+    w = f16(syn.host_normal_f32((2 * d, d), 51) * d ** -0.5)
+    bias = syn.host_normal_f32(d, 52)
+    cross0 = syn.host_normal_f16bits((G, cap, 2 * d), 53)
+    cross = cross0.copy()
+    oracle_mod.cross_kv_fill(enc, w, bias, cross)
+    ref = dec(enc) @ dec(w).T
+    ref[..., d:] += bias.astype(np.float64)
+    # numpy rounds the float64 result straight to binary16 (nearest even)
+    assert np.array_equal(cross[:, :frames], ref.astype(np.float16).view(np.uint16))
+    assert np.array_equal(cross[:, frames:], cross0[:, frames:])
+    # identity weights: K = enc exactly, V = f16(enc + bias)
+    eye = np.zeros((2 * d, d), np.float32)
+    eye[np.arange(d), np.arange(d)] = 1
+    eye[d + np.arange(d), np.arange(d)] = 1
+    c2 = np.zeros_like(cross0)
+    oracle_mod.cross_kv_fill(enc, f16(eye), bias, c2)
+    assert np.array_equal(c2[:, :frames, :d], enc)
+    want_v = (dec(enc) + bias.astype(np.float64)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(c2[:, :frames, d:], want_v)
+    # zero input
+    c3 = np.zeros_like(cross0)
+    oracle_mod.cross_kv_fill(np.zeros_like(enc), w, bias, c3)
+    assert np.all(c3[:, :frames, :d] == 0)
+    assert np.array_equal(c3[:, :frames, d:], np.broadcast_to(f16(bias), (G, frames, d)))
