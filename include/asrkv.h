@@ -277,6 +277,25 @@ int asr_encoder_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, co
                      int B, int T, int heads, int head_dim, float scale, float* out, void* ws,
                      size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
+/* Next row -- the cross-attention K/V of one decoder layer from the encoder
+ * output.  Defines: "wavo 0.1.0, src/whisper/decoder.rs",
+ * Decoder::record_cross (a GEMM of the encoder rows with the layer's [k | v]
+ * weight and a bias epilogue, then a pack to f16 cache rows) and
+ * Decoder::load (k has no bias; v has its own); "Nest whisper-tiny,
+ * src/lib.linnet", DecoderLayer.listen.
+ *   For each group g and frame t < frames, cross row t of group g:
+ *   element n = f16( sum_k enc[g][t][k] * w[n][k] + (n >= d ? bias_v[n-d] : 0) )
+ *   i.e. K of all heads in elements [0, d), V in [d, 2d) -- the row the
+ *   cross-attention step reads.  Rows at and past `frames` are not written.
+ * enc: f16 [G][frames][d]; w: f16 [2d][d] (row n produces element n); bias_v:
+ * fp32 [d]; cross: f16 [G][group_stride], group_stride >= frames * 2d.
+ * d % 128 == 0 (Whisper: 384, 512, 768, 1024, 1280).  The products run on
+ * the tensor cores (tcgen05, f16 operands, fp32 accumulation); the bias is
+ * added in fp32 and the result rounded to nearest even.  No workspace. */
+int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_v, int G,
+                      int frames, int d, uint16_t* cross, int64_t group_stride, int32_t* dev_err,
+                      asr_stream_t stream);
+
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device
  * memory for a workspace -- a plugin whose host owns every allocation and

@@ -50,6 +50,7 @@ SIGNATURES = {
     "asr_mha_prefill": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _i64, _int, _p, _p,
                                _sz, _p, _p]),
     "asr_encoder_attn": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _p, _sz, _p, _p]),
+    "asr_cross_kv_fill": (_int, [_p, _p, _p, _int, _int, _int, _p, _i64, _p, _p]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -316,6 +317,19 @@ def asr_encoder_attn(q, k, v, heads, head_dim, scale, out, ws, lens=None, dev_er
     st = load().asr_encoder_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, T, heads, head_dim,
                                  float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
     _check("asr_encoder_attn", st)
+
+
+def asr_cross_kv_fill(enc, w, bias_v, cross, frames=None, dev_err=None, stream=None):
+    """enc: f16 [G, frames, d]; w: f16 [2d, d]; bias_v: fp32 [d];
+    cross: f16 [G, capacity, 2d] (rows [0, frames) written)."""
+    import torch
+    for t, n in ((enc, "enc"), (w, "w"), (cross, "cross")):
+        _need(t, torch.float16, n)
+    _need(bias_v, torch.float32, "bias_v")
+    G, F, d = enc.shape
+    st = load().asr_cross_kv_fill(_ptr(enc), _ptr(w), _ptr(bias_v), G, frames or F, d,
+                                  _ptr(cross), cross.stride(0), _ptr(dev_err), _stream(stream))
+    _check("asr_cross_kv_fill", st)
 
 
 def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,

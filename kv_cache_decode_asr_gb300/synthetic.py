@@ -25,6 +25,9 @@ Workloads (shapes of the pages' models; no weights or audio are needed):
   [1, 448], K/V written to a 448-slot self cache.
 * ``whisper_large_encoder_b8`` -- Large-Whisper encoder self-attention (20
   heads x 64) over the 1500 frames of 8 utterances, unmasked.
+* ``whisper_large_cross_fill_b32`` -- the cross K/V of one Large-Whisper
+  decoder layer (d = 1280) from the encoder output of 32 utterances of 1500
+  frames; weights N(0, 1/d), bias N(0, 1).
 
 Values: activations and caches N(0, 1); caches are stored as f16 (the fp32
 draw rounded to nearest even).  Host draws use numpy's PCG64; device draws use
@@ -50,6 +53,7 @@ WORKLOADS = {
     "whisper_large_prefill_b32": dict(kind="mha_prefill", B=32, T=448, heads=20, head_dim=64,
                                       capacity=448, len_lo=1, len_hi=448),
     "whisper_large_encoder_b8": dict(kind="encoder", B=8, T=1500, heads=20, head_dim=64),
+    "whisper_large_cross_fill_b32": dict(kind="cross_fill", G=32, frames=1500, d=1280),
 }
 
 
