@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   using LL = LaneLayout<HD, DPL>;
   constexpr int G = LL::G, NP = LL::NP, NCH = LL::NCH;
   extern __shared__ __align__(128) unsigned char smem[];
-  const DecodeSmem lay = decode_smem_layout(a.stages, a.n_src, a.R, a.Hkv, NQ, HD, a.stage_elems);
+  const int Hv = a.MS * a.Hkv;  // virtual heads: (query split, KV head)
+  const DecodeSmem lay = decode_smem_layout(a.stages, a.n_src, a.R, Hv, NQ, HD, a.stage_elems);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + a.stages;
   int* ctl = reinterpret_cast<int*>(smem + lay.ctl);  // [0] abort [1] ticket [2] unsorted
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   uint16_t* stage = reinterpret_cast<uint16_t*>(smem + lay.stage);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_cons = a.R * a.Hkv * G;  // a multiple of 32
+  const int n_cons = a.R * Hv * G;  // a multiple of 32
   const int cons_warps = n_cons >> 5;
   const int S = a.n_src;
   const int qw = a.Hq * HD;
@@ -598,8 +599,11 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   const int64_t k1 = min(k0 + share, total);
 
   // ======================= consumers
+  // group grp: virtual head hv = (query split ms, KV head h), row slot r
   const int grp = tid / G, li = tid % G;
-  const int h = grp % a.Hkv, r = grp / a.Hkv;
+  const int hv = grp % Hv, r = grp / Hv;
+  const int h = hv % a.Hkv, ms = hv / a.Hkv;
+  const int qb = ms * NQ;  // this group's first query of a source
   const int rep = a.rep;
   const int R = a.R;
   const int sw = LL::kSwap ? (grp & 1) : 0;
@@ -638,19 +642,22 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       const uint4 kh = f8_to_h8(kf), vh = f8_to_h8(vf);
       h8_to_f2x4(kh, kx + 4 * j);  // the key and value as the cache holds them
       h8_to_f2x4(vh, vx + 4 * j);
-      if (r == 0) {
+      if (r == 0 && ms == 0) {
         *reinterpret_cast<uint4*>(row + hoff + LL::chunk_off(li, j, sw)) = kh;
         *reinterpret_cast<uint4*>(row + a.Hkv * HD + hoff + LL::chunk_off(li, j, sw)) = vh;
       }
     }
+    // every query slot runs the group sum (its shuffles need the whole warp,
+    // and groups of one warp may hold different query counts); slots past
+    // nq hold zero queries and are not kept
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
-      if (qi < nq) {
+      {
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t = 0; t < NP; ++t) acc = ffma2(qv[qi][t], kx[t], acc);
         const float sc = group_sum<G>(acc.x + acc.y);
-        if (r == 0) {  // one row slot holds it; the slots are merged later
+        if (r == 0 && qi < nq) {  // one row slot holds it; the slots are merged later
           m[qi] = sc;  // exp2(score - m) = 1
           l[qi] = 1.f;
 #pragma unroll
@@ -662,7 +669,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 
   auto seg_begin = [&](int g) {
     mbase = mst[g];
-    nq = min(mst[g + 1] - mst[g], a.max_members) * rep;
+    nq = min(max(min(mst[g + 1] - mst[g], a.max_members) * rep - qb, 0), NQ);
     const bool fold = a.append && owns_first_row(g);
     // every global load (new token, queries) is issued before the RoPE
     // table is built, so their latencies overlap it and one another
@@ -678,8 +685,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 #pragma unroll
       for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
       if (qi < nq) {
-        const int b = mbase + qi / rep;
-        const int hq = h * rep + qi % rep;
+        const int b = mbase + (qb + qi) / rep;
+        const int hq = h * rep + (qb + qi) % rep;
         load_head_f32<HD, DPL>(a.q + (int64_t)b * a.q_stride + hq * HD, li, sw, qv[qi]);
       } else {
 #pragma unroll
@@ -692,13 +699,12 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       named_bar(1, n_cons);
     }
     const float2 s2 = make_float2(a.qscale, a.qscale);
+    // warp-uniform: norm_rope shuffles (slots past nq hold zeros)
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
-      if (qi < nq) {
-        if (a.mode == kModeGqa) norm_rope<HD, DPL>(qv[qi], wts, a.eps, rope, li, sw);
+      if (a.mode == kModeGqa) norm_rope<HD, DPL>(qv[qi], wts, a.eps, rope, li, sw);
 #pragma unroll
-        for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
-      }
+      for (int t = 0; t < NP; ++t) qv[qi][t] = fmul2(qv[qi][t], s2);
     }
     if (fold) append_fold(g, kx, vx);
   };
@@ -706,8 +712,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   // Write the normalised output of query qi.  No shuffles: callable per group.
   auto finalize = [&](int qi, float M, float Ls, float2* O) {
     (void)M;
-    const int b = mbase + qi / rep;
-    const int hq = h * rep + qi % rep;
+    const int b = mbase + (qb + qi) / rep;
+    const int hq = h * rep + (qb + qi) % rep;
     const float inv = 1.0f / Ls;
     float* dst = a.out + (int64_t)b * qw + hq * HD;
 #pragma unroll
@@ -720,7 +726,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   };
 
   auto seg_end = [&](int g) {
-    merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, h, a.Hkv, li, sw, nq, n_cons);
+    merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, hv, Hv, li, sw, nq, n_cons);
     // pieces of this source over the grid
     // (real rows of g: [off[g] + seg_rows, off[g + 1]))
     const int64_t go = (int64_t)off[g] + a.seg_rows, gl = (int64_t)off[g + 1] - go;
@@ -740,7 +746,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
         if (qi < nq) {
-          const int64_t pidx = (slot * a.max_members + qi / rep) * a.Hq + h * rep + qi % rep;
+          const int64_t pidx =
+              (slot * a.max_members + (qb + qi) / rep) * a.Hq + h * rep + (qb + qi) % rep;
           float* po = a.part_o + pidx * HD;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
@@ -794,27 +801,26 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
           const uint4 u = *reinterpret_cast<const uint4*>(tb + row * a.row_elems + LL::chunk_off(li, j, sw));
           h8_to_f2x4(u, kf + 4 * j);
         }
+        // every query slot is scored and reduced: the reduction's
+        // shuffles need the whole warp, and the groups of one warp may hold
+        // different query counts (slots past nq hold zero queries)
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
-            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < NP; t += 2) {
-              a0 = ffma2(qv[qi][t], kf[t], a0);
-              a1 = ffma2(qv[qi][t + 1], kf[t + 1], a1);
-            }
-            sc[qi][i] = (a0.x + a0.y) + (a1.x + a1.y);
+          for (int t = 0; t < NP; t += 2) {
+            a0 = ffma2(qv[qi][t], kf[t], a0);
+            a1 = ffma2(qv[qi][t + 1], kf[t + 1], a1);
           }
+          sc[qi][i] = (a0.x + a0.y) + (a1.x + a1.y);
         }
       }
 #pragma unroll
       for (int o2 = 1; o2 < G; o2 <<= 1) {
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
-          if (qi < nq) {
 #pragma unroll
-            for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
-          }
+          for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
         }
       }
       // online softmax over the RS rows, one rescale per tile
@@ -935,8 +941,10 @@ static void* kernel_for(int HD, int vi) {
   return nullptr;
 }
 
-// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256,pf_kb=-1"
+// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256,pf_kb=-1,qs=0"
 // overrides them (ctas / R = 0: chosen automatically; rs: rows per slot;
+// qs: queries per thread group when a KV row serves more than two queries,
+// 0 = 2;
 // min_kb: fewest K/V bytes one CTA takes; seg_kb: K/V bytes' worth of
 // virtual rows charged to each source, so CTAs that start or finish more
 // sources take fewer rows; pf_kb: K/V bytes a CTA prefetches into L2 before
@@ -944,7 +952,8 @@ static void* kernel_for(int HD, int vi) {
 // Defaults (measured on GB300): one CTA per SM with about ten consumer
 // warps and two or more stages of large tiles.
 struct DecodeTune {
-  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256, pf_kb = -1;
+  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256, pf_kb = -1,
+      qs = 0;
 };
 
 static DecodeTune decode_tune() {
@@ -963,6 +972,7 @@ static DecodeTune decode_tune() {
         else if (!strcmp(key, "min_kb")) d.min_kb = val;
         else if (!strcmp(key, "seg_kb")) d.seg_kb = val;
         else if (!strcmp(key, "pf_kb")) d.pf_kb = val;
+        else if (!strcmp(key, "qs")) d.qs = val;
 
         e += n;
         if (*e == ',') ++e;
@@ -982,11 +992,11 @@ struct DecodePlan {
 // largest R whose tile fits tile_kb (else the smallest valid R).  Stages: as many as fit smem_kb, 2..8.
 // One CTA takes at least min_kb (64 KB) of rows, so a source splits into a
 // bounded number of partial results.
-static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_src,
+static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_src, int MS,
                         DecodePlan& p) {
   const DecodeTune tune = decode_tune();
   const int G = HD / v.DPL;
-  const int per_slot = Hkv * G;
+  const int per_slot = MS * Hkv * G;
   const int budget = std::min(v.MAXT - 32, 320);
   const int row_bytes = row_elems * 2;
   int best = 0, smallest = 0;
@@ -1005,10 +1015,10 @@ static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_
   const int cap = std::max(tune.smem_kb, 16) * 1024;
   int stages = 8;
   while (stages > 2 &&
-         decode_smem_layout(stages, n_src, p.R, Hkv, v.NQ, HD, p.stage_elems).total > cap)
+         decode_smem_layout(stages, n_src, p.R, MS * Hkv, v.NQ, HD, p.stage_elems).total > cap)
     --stages;
   p.stages = stages;
-  p.smem = decode_smem_layout(stages, n_src, p.R, Hkv, v.NQ, HD, p.stage_elems).total;
+  p.smem = decode_smem_layout(stages, n_src, p.R, MS * Hkv, v.NQ, HD, p.stage_elems).total;
   if (p.smem > 227 * 1024) return false;
   const int min_bytes = std::max(tune.min_kb, 1) * 1024;
   p.min_share = std::max(p.tile_rows, (min_bytes + row_bytes - 1) / row_bytes);
@@ -1053,11 +1063,29 @@ static int occupancy_cached(void* fn, int threads, int smem) {
 
 static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
-  const int vi = variant_index(nq_needed, decode_tune().rs);
+  // More than two queries per KV row (the beams of a group) are split over
+  // groups of threads, `split` queries each, instead of one group holding
+  // them all: fewer registers per thread, more warps per SM.
+  const int qs = decode_tune().qs;
+  const int split = qs > 0 ? qs : (nq_needed > 2 ? 2 : 0);
+  int nq_var = nq_needed, MS = 1;
+  if (split > 0 && split < nq_needed) {
+    nq_var = split;
+    MS = (nq_needed + split - 1) / split;
+  }
+  int vi = variant_index(nq_var, decode_tune().rs);
   if (vi < 0) return ASR_ERR_UNSUPPORTED;
-  const Variant& v = kVariants[vi];
   DecodePlan p;
-  if (!plan_decode(HD, v, a.Hkv, a.row_elems, a.n_src, p)) return ASR_ERR_UNSUPPORTED;
+  if (!plan_decode(HD, kVariants[vi], a.Hkv, a.row_elems, a.n_src, MS, p)) {
+    // the split's thread layout does not fit (many heads): one group per head
+    MS = 1;
+    vi = variant_index(nq_needed, decode_tune().rs);
+    if (vi < 0 || !plan_decode(HD, kVariants[vi], a.Hkv, a.row_elems, a.n_src, 1, p))
+      return ASR_ERR_UNSUPPORTED;
+  }
+  const Variant& v = kVariants[vi];
+  (void)v;
+  a.MS = MS;
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
   const size_t need = decode_ws_bytes(a.n_src, a.max_members, a.Hq, HD, sms);

@@ -38,6 +38,7 @@ struct DecodeArgs {
   int32_t* dev_err;
   // tiling
   int R;            // row slots (groups of the same head working on different rows)
+  int MS;           // query splits: groups of one head and row slot, each on NQ of its queries
   int tile_rows;    // rows per pipeline stage (R * rows per slot)
   int min_share;    // fewest rows one CTA takes (bounds the partials per source)
   int seg_rows;     // virtual rows charged per source on the flattened key axis
