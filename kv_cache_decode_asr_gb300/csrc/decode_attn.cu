@@ -823,13 +823,15 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
           for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
         }
       }
-      // online softmax over the RS rows, one rescale per tile
+      // online softmax over the RS rows, one rescale per tile.  Every query
+      // slot runs it (no branch on nq in the loop); a slot past nq holds a
+      // zero query, stays finite and is never written out.
       float pr[NQ][RS];
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
 #pragma unroll
         for (int i = 0; i < RS; ++i) pr[qi][i] = 0.f;
-        if (qi < nq) {
+        {
           float mt = -INFINITY;
 #pragma unroll
           for (int i = 0; i < RS; ++i)
@@ -865,11 +867,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
           }
 #pragma unroll
           for (int qi = 0; qi < NQ; ++qi) {
-            if (qi < nq) {
-              const float2 p2 = make_float2(pr[qi][i], pr[qi][i]);
+            const float2 p2 = make_float2(pr[qi][i], pr[qi][i]);
 #pragma unroll
-              for (int t = 0; t < NP; ++t) o[qi][t] = ffma2(p2, vf[t], o[qi][t]);
-            }
+            for (int t = 0; t < NP; ++t) o[qi][t] = ffma2(p2, vf[t], o[qi][t]);
           }
         }
       }
