@@ -253,14 +253,16 @@ __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ M
         *reinterpret_cast<uint4*>(row + rw + h * HD + c * 8) = val;
       }
     }
-    *reinterpret_cast<uint4*>(&tile[tt][c * 8]) = val;
+    // 16-byte chunk c of position tt goes to chunk c ^ (tt / 8): the
+    // column reads below then hit 32 different banks
+    *reinterpret_cast<uint4*>(&tile[tt][(c ^ ((tt >> 3) & 7)) * 8]) = val;
   }
   __syncthreads();
   for (int idx = tid; idx < HD * (kMhaPrepT / 8); idx += blockDim.x) {
     const int d = idx / (kMhaPrepT / 8), q8 = idx % (kMhaPrepT / 8);
     alignas(16) uint16_t col[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) col[e] = tile[q8 * 8 + e][d];
+    for (int e = 0; e < 8; ++e) col[e] = tile[q8 * 8 + e][(((d >> 3) ^ q8) << 3) + (d & 7)];
     *reinterpret_cast<uint4*>(a.vt + (((int64_t)b * a.H + h) * HD + d) * a.Tpad + t0 + q8 * 8) =
         *reinterpret_cast<const uint4*>(col);
   }
