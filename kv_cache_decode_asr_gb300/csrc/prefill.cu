@@ -130,44 +130,45 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
   }
   __syncthreads();
 
-  // normed + roped heads: a half-warp per (position, head) vector; lane hl
-  // of the half-warp holds dims 8*hl .. 8*hl+7, so lanes hl and hl ^ 8 hold
-  // NeoX RoPE partners (i, i + 64).  Each half-warp loads kPrepU vectors
-  // before reducing any of them, so several 16-byte loads per lane are in
-  // flight.
+  // normed + roped heads: half-warp hw owns position t0 + hw (256 threads =
+  // 16 half-warps = kPrepT positions) and walks all its q and k heads, so
+  // its cos/sin stay in registers and no index is divided.  Lane hl of the
+  // half-warp holds dims 8*hl .. 8*hl+7, so lanes hl and hl ^ 8 hold NeoX
+  // RoPE partners (i, i + 64).  kPrepU head vectors are loaded before any is
+  // reduced, so several 16-byte loads per lane are in flight.
   constexpr int kPrepU = 4;
   const int hw = tid >> 4, hl = tid & 15;
   const bool upper = hl >= 8;
   const int ib = (hl & 7) * 8;  // frequency index of this lane's first dim
-  float wqr[8], wkr[8];
+  float wqr[8], wkr[8], cr[8], sr[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     wqr[e] = a.wq[8 * hl + e];
     wkr[e] = a.wk[8 * hl + e];
+    cr[e] = cs[hw * HALF + ib + e];
+    sr[e] = sn[hw * HALF + ib + e];
   }
+  const int t = t0 + hw;
+  const bool live = t < a.T;
   const int nheads = a.Hq + a.Hkv;
-  const int items = kPrepT * nheads;
-  const int n_hw = blockDim.x >> 4;
-  for (int base = hw; base < items; base += n_hw * kPrepU) {
+  const uint16_t* qrow = a.q + ((int64_t)b * a.T + t) * a.Hq * HD;
+  const uint16_t* krow = a.k + ((int64_t)b * a.T + t) * kw;
+  uint16_t* qdst = a.qhat + ((int64_t)b * a.T + t) * a.Hq * HD;
+  uint16_t* kdst = a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * kw;
+  for (int base = 0; base < nheads; base += kPrepU) {
     uint4 x[kPrepU];
-    const uint16_t* srcs[kPrepU];
 #pragma unroll
     for (int u = 0; u < kPrepU; ++u) {
-      const int item = base + n_hw * u;
-      const int tt = item / nheads, hh = item % nheads, t = t0 + tt;
+      const int hh = base + u;
       x[u] = make_uint4(0u, 0u, 0u, 0u);
-      srcs[u] = nullptr;
-      if (item < items && t < a.T) {
-        srcs[u] = hh < a.Hq ? a.q + ((int64_t)b * a.T + t) * a.Hq * HD + hh * HD
-                            : a.k + ((int64_t)b * a.T + t) * kw + (hh - a.Hq) * HD;
-        x[u] = *reinterpret_cast<const uint4*>(srcs[u] + 8 * hl);
-      }
+      if (live && hh < nheads)
+        x[u] = *reinterpret_cast<const uint4*>(
+            (hh < a.Hq ? qrow + hh * HD : krow + (hh - a.Hq) * HD) + 8 * hl);
     }
 #pragma unroll
     for (int u = 0; u < kPrepU; ++u) {
-      // every lane runs the shuffles (both half-warps of a warp stay converged)
-      const int item = base + n_hw * u;
-      const int tt = min(item / nheads, kPrepT - 1), hh = item % nheads, t = t0 + tt;
+      // every lane runs the shuffles (both half-warps of a warp walk the same heads)
+      const int hh = base + u;
       const bool is_q = hh < a.Hq;
       float f[8];
       h8_to_f8(x[u], f);
@@ -183,13 +184,10 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float pe = __shfl_xor_sync(0xffffffffu, xn[e], 8);
-        const float c = cs[tt * HALF + ib + e], sv = sn[tt * HALF + ib + e];
-        y[e] = upper ? xn[e] * c + pe * sv : xn[e] * c - pe * sv;
+        y[e] = upper ? xn[e] * cr[e] + pe * sr[e] : xn[e] * cr[e] - pe * sr[e];
       }
-      if (srcs[u] != nullptr) {
-        uint16_t* dst = is_q ? a.qhat + (((int64_t)b * a.T + t) * a.Hq + hh) * HD
-                             : a.cache + (int64_t)b * a.seq_stride + (int64_t)t * 2 * kw +
-                                   (hh - a.Hq) * HD;
+      if (live && hh < nheads) {
+        uint16_t* dst = is_q ? qdst + hh * HD : kdst + (hh - a.Hq) * HD;
         *reinterpret_cast<uint4*>(dst + 8 * hl) = f8_to_h8(y);
       }
     }
