@@ -68,6 +68,10 @@ def _lib():
             "orc_mha_attn": (_int, [_u16p, _u16p, _u16p, _i32p, _int, _int, _int, _int, _dbl, _int,
                                     _u16p, _i64, _int, _f64p]),
             "orc_cross_kv_fill": (None, [_u16p, _u16p, _f32p, _int, _int, _int, _u16p, _i64]),
+            "orc_layer_norm": (None, [_f32p, _i64, _f32p, _f32p, _dbl, _f64p]),
+            "orc_gelu_erf": (_dbl, [_dbl]),
+            "orc_linear": (None, [_f32p, _i64, _int, _int, _f32p, _f32p, _dbl, _u16p, _int, _f32p,
+                                  _int, _f64p, _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -358,6 +362,101 @@ def cross_kv_fill(enc, w, bias_v, cross):
                              _p(cross, ctypes.c_uint16), cross[0].size)
 
 
+# ------------------------------------------- the dense steps of a layer --
+
+LINEAR_MODES = {"store": 0, "residual": 1, "gelu": 2}
+
+
+def layer_norm(x, g, b, eps=1e-5):
+    """LayerNorm of each row of x (float32 [M, K]) with weight g and bias b
+    (float32 [K]); float64 [M, K]."""
+    x = _c(np.ascontiguousarray(x, np.float32), np.float32)
+    g = _c(np.ascontiguousarray(g, np.float32), np.float32)
+    b = _c(np.ascontiguousarray(b, np.float32), np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    out = np.empty(x2.shape, np.float64)
+    for m in range(x2.shape[0]):
+        _lib().orc_layer_norm(_p(x2[m], ctypes.c_float), x2.shape[1], _p(g, ctypes.c_float),
+                              _p(b, ctypes.c_float), float(eps), _p(out[m], ctypes.c_double))
+    return out.reshape(x.shape)
+
+
+def gelu_erf(v):
+    """GELU, error-function form, elementwise on float64 values."""
+    v = np.asarray(v, np.float64)
+    f = _lib().orc_gelu_erf
+    return np.vectorize(lambda t: f(float(t)), otypes=[np.float64])(v)
+
+
+def linear(x, w, bias=None, mode="store", ln=None, eps=1e-5, y=None):
+    """One dense step: a = LayerNorm(x) (ln = (g, b)) or x; v = a W^T + bias;
+    mode "store" -> v, "residual" -> y + v, "gelu" -> gelu(v).
+
+    x: float32 [M, K]; w: uint16 (f16 bits) [N, K]; bias: float32 [N] or None;
+    y: the values the residual is added onto ([M, N]).  Returns float64 [M, N]."""
+    x = _c(np.ascontiguousarray(x, np.float32), np.float32)
+    w = _c(w, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w must be [N, K]")
+    m = LINEAR_MODES[mode]
+    out = np.zeros((M, N), np.float64)
+    if m == 1:
+        if y is None:
+            raise ValueError("residual mode needs y")
+        out[:] = np.asarray(y, np.float64)
+    bp = None
+    if bias is not None:
+        bias = _c(np.ascontiguousarray(bias, np.float32), np.float32)
+        bp = _p(bias, ctypes.c_float)
+    gp = bq = None
+    if ln is not None:
+        g = _c(np.ascontiguousarray(ln[0], np.float32), np.float32)
+        b = _c(np.ascontiguousarray(ln[1], np.float32), np.float32)
+        gp, bq = _p(g, ctypes.c_float), _p(b, ctypes.c_float)
+    _lib().orc_linear(_p(x, ctypes.c_float), K, M, K, gp, bq, float(eps), _p(w, ctypes.c_uint16),
+                      N, bp, m, _p(out, ctypes.c_double), N)
+    return out
+
+
+def whisper_decoder_layer_step(x, p, cache, lens, cross, group, heads, head_dim, eps=1e-5):
+    """One Whisper decoder layer for one new token per sequence, in the order
+    of "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step:
+
+      qkv = LN_self(x) W_qkv^T + b_qkv;  k, v -> cache row lens-1;
+      x  += attend(q, own cache, lens) W_o^T + b_o;
+      qx  = LN_cross(x) W_cq^T + b_cq;   x += attend(qx, cross) W_co^T + b_co;
+      x  += gelu(LN_ffn(x) W_1^T + b_1) W_2^T + b_2.
+
+    Each step computes in double; its result is stored as float32, as the
+    pages' buffers (x, qkv, att, h) are f32, and the cache row as f16.
+    x: float32 [B, d]; p: the layer's parameters (keys ln1_g, ln1_b, w_qkv,
+    b_qkv, w_o, b_o, ln2_g, ln2_b, w_cq, b_cq, w_co, b_co, ln3_g, ln3_b,
+    w_fc1, b_fc1, w_fc2, b_fc2; weights uint16 f16 bits [out, in], the rest
+    float32); cache: uint16 [B, capacity, 2d] (row lens-1 written in place);
+    lens: int32 [B] keys incl. the new token; cross: uint16 [G, frames, 2d];
+    group: int32 [B].  Returns (x_out float32 [B, d], intermediates)."""
+    d = heads * head_dim
+    scale = head_dim ** -0.5
+    f32 = np.float32
+    x = np.ascontiguousarray(x, f32)
+    lens = np.ascontiguousarray(lens, np.int32)
+    qkv = linear(x, p["w_qkv"], p["b_qkv"], ln=(p["ln1_g"], p["ln1_b"]), eps=eps).astype(f32)
+    kv_append(qkv[:, d:2 * d], qkv[:, 2 * d:], cache, lens - 1, heads, head_dim)
+    att, _ = self_attn_step(qkv, cache, lens, heads, head_dim, scale, q_stride=3 * d)
+    att = att.astype(f32)
+    x1 = linear(att, p["w_o"], p["b_o"], mode="residual", y=x).astype(f32)
+    qx = linear(x1, p["w_cq"], p["b_cq"], ln=(p["ln2_g"], p["ln2_b"]), eps=eps).astype(f32)
+    attc, _ = cross_attn_step(qx, cross, group, heads, head_dim, scale)
+    attc = attc.astype(f32)
+    x2 = linear(attc, p["w_co"], p["b_co"], mode="residual", y=x1).astype(f32)
+    h = linear(x2, p["w_fc1"], p["b_fc1"], mode="gelu", ln=(p["ln3_g"], p["ln3_b"]),
+               eps=eps).astype(f32)
+    x3 = linear(h, p["w_fc2"], p["b_fc2"], mode="residual", y=x2).astype(f32)
+    return x3, {"qkv": qkv, "att": att, "x1": x1, "qx": qx, "attc": attc, "x2": x2, "h": h}
+
+
 def build():
     """Compile liboracle.so (the checker) if it is missing or stale."""
     return _build.build()
@@ -366,7 +465,8 @@ def build():
 __all__ = [
     "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
     "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
-    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "cross_kv_fill", "build",
+    "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "cross_kv_fill",
+    "layer_norm", "gelu_erf", "linear", "whisper_decoder_layer_step", "build",
 ]
 
 if os.environ.get("ORACLE_THREADS"):

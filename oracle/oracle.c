@@ -729,3 +729,90 @@ void orc_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias
   orc_fill_ctx c = {enc, w, bias_v, frames, d, cross, group_stride};
   orc_parallel_for((int64_t)G * frames, orc_fill_item, &c);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Next row: the dense steps of a decoder layer around the attention         */
+/* ------------------------------------------------------------------------ */
+
+/* LayerNorm of one row of K values ("Nest whisper-tiny, src/lib.linnet",
+ * LayerNorm: torch.nn.LayerNorm's definition with its default eps 1e-5):
+ *   mean = sum_k x_k / K,  var = sum_k (x_k - mean)^2 / K  (biased),
+ *   y_k = (x_k - mean) / sqrt(var + eps) * g_k + b_k. */
+void orc_layer_norm(const float* x, int64_t K, const float* g, const float* b, double eps,
+                    double* y) {
+  double mean = 0.0;
+  for (int64_t k = 0; k < K; ++k) mean += (double)x[k];
+  mean /= (double)K;
+  double var = 0.0;
+  for (int64_t k = 0; k < K; ++k) {
+    double dx = (double)x[k] - mean;
+    var += dx * dx;
+  }
+  var /= (double)K;
+  double inv = 1.0 / sqrt(var + eps);
+  for (int64_t k = 0; k < K; ++k) y[k] = ((double)x[k] - mean) * inv * (double)g[k] + (double)b[k];
+}
+
+/* GELU in its error-function form (Whisper's config asks for `gelu`, the
+ * exact one; "Nest whisper-tiny, src/lib.linnet" uses gelu_erf):
+ *   gelu(v) = v * Phi(v) = v / 2 * (1 + erf(v / sqrt(2))). */
+double orc_gelu_erf(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+
+typedef struct {
+  const float* x;
+  int64_t x_stride;
+  int K, N;
+  const float* ln_g;
+  const float* ln_b;
+  double eps;
+  const double* w; /* decoded weights [N][K] */
+  const float* bias;
+  int mode;
+  double* y;
+  int64_t y_stride;
+} orc_linear_ctx;
+
+static void orc_linear_item(void* vctx, int64_t m) {
+  orc_linear_ctx* c = (orc_linear_ctx*)vctx;
+  const float* xm = c->x + m * c->x_stride;
+  double* a = (double*)malloc(sizeof(double) * c->K);
+  if (c->ln_g) {
+    orc_layer_norm(xm, c->K, c->ln_g, c->ln_b, c->eps, a);
+  } else {
+    for (int k = 0; k < c->K; ++k) a[k] = (double)xm[k];
+  }
+  double* ym = c->y + m * c->y_stride;
+  for (int n = 0; n < c->N; ++n) {
+    const double* wn = c->w + (int64_t)n * c->K;
+    double v = 0.0;
+    for (int k = 0; k < c->K; ++k) v += a[k] * wn[k];
+    if (c->bias) v += (double)c->bias[n];
+    if (c->mode == 1) {
+      ym[n] += v; /* Residual(1.0): added onto what y holds */
+    } else if (c->mode == 2) {
+      ym[n] = orc_gelu_erf(v);
+    } else {
+      ym[n] = v;
+    }
+  }
+  free(a);
+}
+
+/* One dense step of a decoder layer ("wavo 0.1.0, src/whisper/decoder.rs",
+ * Decoder::record_step: `layer_norm` into y, then `gemv` of y with a weight
+ * and one of the epilogues Bias, Residual(1.0) or Gelu):
+ *   a_m = LayerNorm(x_m; ln_g, ln_b, eps) if ln_g is given, else x_m;
+ *   v_mn = sum_k a_mk * W[n][k] + bias_n  (bias may be NULL: 0);
+ *   mode 0: y_mn = v_mn;  mode 1: y_mn = y_mn + v_mn;  mode 2: y_mn = gelu(v_mn).
+ * x: fp32 [M][x_stride] (K used); W: f16 [N][K] (row n makes output n);
+ * y: double [M][y_stride].  The activations are used as their fp32 values
+ * (the pages' buffers are f32); every sum is in double. */
+void orc_linear(const float* x, int64_t x_stride, int M, int K, const float* ln_g,
+                const float* ln_b, double eps, const uint16_t* w, int N, const float* bias, int mode,
+                double* y, int64_t y_stride) {
+  double* wd = (double*)malloc(sizeof(double) * (size_t)N * (size_t)K);
+  for (int64_t i = 0; i < (int64_t)N * K; ++i) wd[i] = orc_f16_to_f64(w[i]);
+  orc_linear_ctx c = {x, x_stride, K, N, ln_g, ln_b, eps, wd, bias, mode, y, y_stride};
+  orc_parallel_for(M, orc_linear_item, &c);
+  free(wd);
+}

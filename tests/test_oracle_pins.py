@@ -568,3 +568,145 @@ def test_cross_kv_fill_matches_numpy_and_closed_forms(oracle_mod):
     oracle_mod.cross_kv_fill(np.zeros_like(enc), w, bias, c3)
     assert np.all(c3[:, :frames, :d] == 0)
     assert np.array_equal(c3[:, :frames, d:], np.broadcast_to(f16(bias), (G, frames, d)))
+
+
+# ------------------------------------------- dense steps of a decoder layer --
+
+def test_layer_norm_worked_examples(oracle_mod):
+    """torch.nn.LayerNorm's definition: biased variance, eps inside the root.
+    [1, 2, 3, 4] has mean 2.5 and variance 1.25 (the unbiased 5/3 would fail);
+    an alternating row +-a normalises to +-a/sqrt(a^2 + eps); a constant row
+    gives the bias exactly; the weight scales and the bias shifts."""
+    one = np.ones(4, np.float32)
+    zero = np.zeros(4, np.float32)
+    y = oracle_mod.layer_norm(np.array([[1, 2, 3, 4]], np.float32), one, zero, eps=0.0)
+    want = np.array([-1.5, -0.5, 0.5, 1.5]) / math.sqrt(1.25)
+    np.testing.assert_allclose(y[0], want, rtol=0, atol=1e-15)
+    a, eps = 2.0, 1e-5
+    row = np.array([[a, -a, a, -a, a, -a]], np.float32)
+    y = oracle_mod.layer_norm(row, np.ones(6, np.float32), np.zeros(6, np.float32), eps=eps)
+    s = a / math.sqrt(a * a + eps)
+    np.testing.assert_allclose(y[0], [s, -s, s, -s, s, -s], rtol=0, atol=1e-15)
+    b = np.array([0.25, -1.0, 3.0, 0.5], np.float32)
+    y = oracle_mod.layer_norm(np.full((1, 4), 7.5, np.float32), one, b, eps=eps)
+    assert np.array_equal(y[0], b.astype(np.float64))
+    g = np.array([2.0, -1.0, 0.5, 3.0], np.float32)
+    x = np.array([[0.3, -1.2, 2.5, 0.1]], np.float32)
+    y0 = oracle_mod.layer_norm(x, one, zero, eps=eps)
+    y1 = oracle_mod.layer_norm(x, g, b, eps=eps)
+    np.testing.assert_allclose(y1, y0 * g + b, rtol=0, atol=1e-14)
+    # random rows: zero mean, mean square var / (var + eps)
+    xr = syn.host_normal_f32((5, 64), 60, mean=0.7, std=2.0)
+    yr = oracle_mod.layer_norm(xr, np.ones(64, np.float32), np.zeros(64, np.float32), eps=eps)
+    var = xr.astype(np.float64).var(axis=1)
+    np.testing.assert_allclose(yr.mean(axis=1), 0, atol=1e-13)
+    np.testing.assert_allclose((yr ** 2).mean(axis=1), var / (var + eps), rtol=1e-12)
+
+
+def test_gelu_erf_table_values(oracle_mod):
+    """gelu(v) = v * Phi(v), Phi the standard normal CDF: Phi(1) =
+    0.8413447460685429, Phi(2) = 0.9772498680518208 (normal tables); gelu(v)
+    - gelu(-v) = v; the tanh approximation (0.8411919906 at 1) is not it."""
+    g = oracle_mod.gelu_erf(np.array([0.0, 1.0, -1.0, 2.0, -2.0]))
+    np.testing.assert_allclose(g, [0.0, 0.8413447460685429, -0.15865525393145707,
+                                   1.9544997361036416, -0.04550026389635842], rtol=0,
+                               atol=1e-15)
+    v = syn.host_normal_f32(50, 61, std=3.0).astype(np.float64)
+    np.testing.assert_allclose(oracle_mod.gelu_erf(v) - oracle_mod.gelu_erf(-v), v, atol=1e-14)
+    assert abs(oracle_mod.gelu_erf(1.0) - 0.8411919906082768) > 1e-4
+
+
+def test_linear_matches_numpy_and_closed_forms(oracle_mod):
+    """The dense step against numpy's float64 matmul of the decoded f16
+    weights, in each mode; identity weights return x (+ bias); zero weights
+    leave the residual untouched; LayerNorm of an alternating row is its
+    closed form before the product."""
+    M, K, N = 3, 64, 40
+    x = syn.host_normal_f32((M, K), 62)
+    w = f16(syn.host_normal_f32((N, K), 63) * K ** -0.5)
+    bias = syn.host_normal_f32(N, 64)
+    y0 = syn.host_normal_f32((M, N), 65)
+    ref = x.astype(np.float64) @ dec(w).T + bias
+    np.testing.assert_allclose(oracle_mod.linear(x, w, bias), ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle_mod.linear(x, w, bias, mode="residual", y=y0),
+                               y0 + ref, rtol=0, atol=1e-12)
+    gref = 0.5 * ref * (1 + np.vectorize(math.erf)(ref / math.sqrt(2)))
+    np.testing.assert_allclose(oracle_mod.linear(x, w, bias, mode="gelu"), gref, rtol=0,
+                               atol=1e-12)
+    np.testing.assert_allclose(oracle_mod.linear(x, w, None), ref - bias, rtol=0, atol=1e-12)
+    eye = f16(np.eye(K, dtype=np.float32))
+    bk = syn.host_normal_f32(K, 66)
+    np.testing.assert_allclose(oracle_mod.linear(x, eye, bk), x.astype(np.float64) + bk,
+                               rtol=0, atol=0)
+    zw = np.zeros((N, K), np.uint16)
+    assert np.array_equal(oracle_mod.linear(x, zw, None, mode="residual", y=y0),
+                          y0.astype(np.float64))
+    # LayerNorm first: rows +-a normalise to +-a/sqrt(a^2+eps), then g, b
+    a, eps = 1.5, 1e-5
+    alt = np.tile(np.array([a, -a], np.float32), (M, K // 2))
+    g = syn.host_normal_f32(K, 67, mean=1.0, std=0.1)
+    b = syn.host_normal_f32(K, 68, std=0.1)
+    s = a / math.sqrt(a * a + eps)
+    an = np.tile(np.array([s, -s]), (M, K // 2)) * g + b
+    np.testing.assert_allclose(oracle_mod.linear(alt, w, bias, ln=(g, b), eps=eps),
+                               an @ dec(w).T + bias, rtol=0, atol=1e-12)
+
+
+def _layer_params(d, inner, seed, zero_out=False):
+    p = {}
+    for i, (name, n_out, n_in) in enumerate((("qkv", 3 * d, d), ("o", d, d), ("cq", d, d),
+                                              ("co", d, d), ("fc1", inner, d),
+                                              ("fc2", d, inner))):
+        w = syn.host_normal_f32((n_out, n_in), seed + 2 * i) * n_in ** -0.5
+        if zero_out and name in ("o", "co", "fc2"):
+            w[:] = 0
+        p["w_" + name] = f16(w)
+        p["b_" + name] = syn.host_normal_f32(n_out, seed + 2 * i + 1, std=0.1)
+    p["b_qkv"][d:2 * d] = 0  # the key projection has no bias
+    for j in (1, 2, 3):
+        p[f"ln{j}_g"] = syn.host_normal_f32(d, seed + 20 + j, mean=1.0, std=0.1)
+        p[f"ln{j}_b"] = syn.host_normal_f32(d, seed + 30 + j, std=0.1)
+    return p
+
+
+def test_decoder_layer_step_residuals_and_cache(oracle_mod):
+    """With the three output projections zero, the layer adds exactly its
+    three output biases to x (each sum rounded to f32, as the buffers are
+    f32); the new token's k, v land in cache row lens-1 as f16 of the
+    LayerNorm-ed projection and no other row changes.  With identity output
+    projections the two attentions' outputs are added onto the stream."""
+    B, H, hd, cap, F = 3, 2, 8, 6, 5
+    d, inner = H * hd, 4 * H * hd
+    x = syn.host_normal_f32((B, d), 70)
+    lens = np.array([1, 4, 6], np.int32)
+    cache0 = syn.host_normal_f16bits((B, cap, 2 * d), 71)
+    cross = syn.host_normal_f16bits((2, F, 2 * d), 72)
+    group = np.array([0, 0, 1], np.int32)
+    p = _layer_params(d, inner, 80, zero_out=True)
+    cache = cache0.copy()
+    xo, mid = oracle_mod.whisper_decoder_layer_step(x, p, cache, lens, cross, group, H, hd)
+    x1 = (x.astype(np.float64) + p["b_o"]).astype(np.float32)
+    x2 = (x1.astype(np.float64) + p["b_co"]).astype(np.float32)
+    x3 = (x2.astype(np.float64) + p["b_fc2"]).astype(np.float32)
+    assert np.array_equal(xo, x3)
+    ln1 = oracle_mod.layer_norm(x, p["ln1_g"], p["ln1_b"])
+    kv = ln1 @ dec(p["w_qkv"][d:]).T + p["b_qkv"][d:]
+    for bi in range(B):
+        assert np.array_equal(cache[bi, lens[bi] - 1], f16(kv[bi].astype(np.float32)))
+        keep = np.arange(cap) != lens[bi] - 1
+        assert np.array_equal(cache[bi, keep], cache0[bi, keep])
+    # identity output projections: x1 = x + self-attention, x2 = x1 + cross
+    p = _layer_params(d, inner, 90, zero_out=True)
+    p["w_o"] = f16(np.eye(d, dtype=np.float32))
+    p["w_co"] = f16(np.eye(d, dtype=np.float32))
+    for k in ("b_o", "b_co", "b_fc2"):
+        p[k][:] = 0
+    cache = cache0.copy()
+    xo, mid = oracle_mod.whisper_decoder_layer_step(x, p, cache, lens, cross, group, H, hd)
+    scale = hd ** -0.5
+    att, _ = oracle_mod.self_attn_step(mid["qkv"], cache, lens, H, hd, scale, q_stride=3 * d)
+    assert np.array_equal(mid["x1"], (x.astype(np.float64) + att.astype(np.float32)).astype(
+        np.float32))
+    attc, _ = oracle_mod.cross_attn_step(mid["qx"], cross, group, H, hd, scale)
+    assert np.array_equal(xo, (mid["x1"].astype(np.float64) + attc.astype(np.float32)).astype(
+        np.float32))
