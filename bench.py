@@ -846,6 +846,181 @@ class CrossFillStep:
         return self.G
 
 
+class DecoderStep(WhisperStep):
+    """The whole Large-Whisper decoder step around the attention, eight
+    launches per layer (kv_cache_decode_asr_gb300.decoder): LayerNorm + qkv,
+    append + self-attention, out-projection, LayerNorm + cross query,
+    cross-attention, cross out-projection, LayerNorm + fc1 + GELU, fc2.  The
+    step starts from its input x (the embedded token, a device copy) and
+    ends with the residual stream after the last layer."""
+
+    kernel_sources = DECODE_SOURCES
+    dominant = "cross"
+    dominant_kernel = "decode_attn_kernel<64,1> (asr_cross_attn_step)"
+    profile_kernel = "cross"
+    # 256 launches a step: the end-to-end figure replays the captured step
+    # graph (as a caller would) instead of re-issuing every call from Python
+    e2e_via_graph = True
+
+    def __init__(self, name, cfg, device, rank=0):
+        import torch
+        from kv_cache_decode_asr_gb300 import decoder
+        super().__init__(name, dict(cfg, lens="uniform", rearrange=False), device, rank)
+        self.cfg = cfg
+        self.decoder = decoder
+        wi = rank_seed_base(name, rank)
+        self.inner = cfg["inner"]
+        self.p = syn.dev_layer_params(self.L, self.d, self.inner, syn.seed_for(wi, 20), device)
+        self.pl = [{k: v[l] for k, v in self.p.items()} for l in range(self.L)]
+        self.x_in = syn.dev_normal((self.B, self.d), syn.seed_for(wi, 21), device)
+        self.x = self.x_in.clone()
+        self.bufs = decoder.DecoderBuffers(self.B, self.d, self.inner, self.H, self.hd, self.G,
+                                           self.beam, device)
+        self.snaps = None
+        self.metric = ("decoder-step tokens/s: the whole Large-Whisper decoder step "
+                       "(dense layers + attention; step K/V+weight HBM GB/s alongside)")
+
+    def launches(self):
+        return self.decoder.LAUNCHES_PER_LAYER * self.L
+
+    def layer(self, l, stream=None):
+        self.decoder.whisper_decoder_layer(self.x, self.pl[l], self.cache[:, l], self.lens,
+                                           self.cross[l], self.group, self.F, self.bufs,
+                                           dev_err=self.err, stream=stream)
+
+    def step(self, stream=None):
+        self.x.copy_(self.x_in)
+        for l in range(self.L):
+            self.layer(l, stream)
+
+    def weight_bytes_per_layer(self):
+        d, inner = self.d, self.inner
+        w = (3 * d * d + 3 * d * d + 2 * d * inner) * 2
+        b = (3 * d + 3 * d + inner + d + 6 * d) * 4
+        return w + b
+
+    def dense_bytes_per_layer(self):
+        """The six dense launches of a layer: weights and vectors, activations
+        in and out (the residual stream read and written by three of them)."""
+        B, d, inner = self.B, self.d, self.inner
+        act = 4 * B * (d + 3 * d + d + 2 * d + d + d + 2 * d + d + inner + inner + 2 * d)
+        return self.weight_bytes_per_layer() + act
+
+    def kv_bytes_per_step(self):
+        """K/V read and written by the attention plus the dense layers' bytes."""
+        return super().kv_bytes_per_step() + self.L * self.dense_bytes_per_layer()
+
+    def extra_rooflines(self, stream, peaks):
+        """The dense launches alone (six per layer, every layer, one graph):
+        algorithmic bytes per layer / time per layer, against HBM."""
+        import torch
+        ops = self.ops
+        g = torch.cuda.CUDAGraph()
+        bufs, x = self.bufs, self.x
+        wl = bufs.ws_lin
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(self.L):
+                p = self.pl[l]
+                ops.asr_linear(x, p["w_qkv"], bufs.qkv, bias=p["b_qkv"],
+                               ln=(p["ln1_g"], p["ln1_b"]), ws=wl, dev_err=self.err)
+                ops.asr_linear(bufs.att, p["w_o"], x, bias=p["b_o"], mode="residual", ws=wl,
+                               dev_err=self.err)
+                ops.asr_linear(x, p["w_cq"], bufs.qx, bias=p["b_cq"],
+                               ln=(p["ln2_g"], p["ln2_b"]), ws=wl, dev_err=self.err)
+                ops.asr_linear(bufs.attc, p["w_co"], x, bias=p["b_co"], mode="residual", ws=wl,
+                               dev_err=self.err)
+                ops.asr_linear(x, p["w_fc1"], bufs.h, bias=p["b_fc1"],
+                               ln=(p["ln3_g"], p["ln3_b"]), mode="gelu", ws=wl, dev_err=self.err)
+                ops.asr_linear(bufs.h, p["w_fc2"], x, bias=p["b_fc2"], mode="residual", ws=wl,
+                               dev_err=self.err)
+        reps = 20
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        layer_ms = e0.elapsed_time(e1) / (reps * self.L)
+        peak, src = peaks["hbm"]
+        b = self.dense_bytes_per_layer()
+        achieved = b / (layer_ms / 1e3) / 1e9
+        return {"roofline_dense": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "bytes_per_layer": b, "launches_per_layer": 6,
+            "us_per_layer": layer_ms * 1e3, "us_per_launch": layer_ms * 1e3 / 6,
+            "kernel": "linear_kernel (asr_linear: LayerNorm + tcgen05 product + epilogue)",
+            "traffic": None, "peak_source": f"{src} hbm_gbs"}}
+
+    def host_io(self):
+        return [self.x_in], [self.x]
+
+    # ---- CPU oracle: whole layers, from the GPU's own input to each layer
+    def _host_layer(self, l):
+        import torch
+        out = {}
+        for k, v in self.pl[l].items():
+            if v.dtype == torch.float16:
+                out[k] = v.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            else:
+                out[k] = v.contiguous().cpu().numpy()
+        return out
+
+    def _snapshots(self):
+        import torch
+        if self.snaps is None:
+            torch.cuda.synchronize()
+            self.x.copy_(self.x_in)
+            snaps = [self.x.clone()]
+            for l in range(self.L):
+                self.layer(l)
+                snaps.append(self.x.clone())
+            torch.cuda.synchronize()
+            self.snaps = [t.cpu().numpy() for t in snaps]
+        return self.snaps
+
+    def oracle_sample(self, i, oracle):
+        """Layer i of every sequence, from the GPU's input to that layer."""
+        import torch
+        snaps = self._snapshots()
+        p = self._host_layer(i)
+        cache = self.cache[:, i].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        cross = self.cross[i].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        ref, _ = oracle.whisper_decoder_layer_step(snaps[i], p, cache, self.lens_eff, cross,
+                                                   self.group_host, self.H, self.hd)
+        dt = time.perf_counter() - t0
+        return dt, 1.0 / self.L, {"x": ref}, {"x": snaps[i + 1]}, f"layer {i}"
+
+    def oracle_unit(self, i, oracle, cache):
+        """Reference-arm unit: one sequence through one layer."""
+        import torch
+        l = i % self.L
+        b = (i // self.L) % self.B
+        if cache.get("layer") != l:
+            cache.clear()
+            cache["layer"] = l
+            cache["p"] = self._host_layer(l)
+        key = ("seq", b)
+        if key not in cache:
+            g = int(self.group_host[b])
+            cache[key] = (
+                self.cache[b:b + 1, l].contiguous().view(torch.int16).cpu().numpy()
+                .view(np.uint16),
+                self.cross[l, g:g + 1].contiguous().view(torch.int16).cpu().numpy()
+                .view(np.uint16),
+                self.x_in[b:b + 1].cpu().numpy())
+        sc, cr, x = cache[key]
+        sc = sc.copy()
+        t0 = time.perf_counter()
+        oracle.whisper_decoder_layer_step(x, cache["p"], sc, self.lens_eff[b:b + 1], cr,
+                                          np.zeros(1, np.int32), self.H, self.hd)
+        return time.perf_counter() - t0
+
+
 def make_workload(name, device, rank=0, layers=0):
     cfg = dict(syn.WORKLOADS[name])
     if layers:
@@ -860,6 +1035,8 @@ def make_workload(name, device, rank=0, layers=0):
         return MhaAttnStep(name, cfg, device, rank)
     if cfg["kind"] == "cross_fill":
         return CrossFillStep(name, cfg, device, rank)
+    if cfg["kind"] == "decoder_step":
+        return DecoderStep(name, cfg, device, rank)
     raise SystemExit(f"workload {name}: not a decode-step bench line")
 
 
@@ -997,6 +1174,7 @@ def run_ours(args):
     roof.update({"traffic": recorded_traffic(wl.kernel_sources, args.workload,
                                              wl.traffic_key()),
                  "kernel": wl.dominant_kernel, "launch_us": launch_ms * 1e3})
+    extra = wl.extra_rooflines(stream, peaks) if hasattr(wl, "extra_rooflines") else {}
 
     # ---- end to end through host buffers: per step, H2D of the step's
     # activations from pinned memory, the step, D2H of its outputs
@@ -1015,7 +1193,10 @@ def run_ours(args):
         for _ in range(e2e_steps):
             for h, t in zip(h_ins, ins):
                 t.copy_(h, non_blocking=True)
-            wl.step()
+            if getattr(wl, "e2e_via_graph", False):
+                graph.replay()  # the static step graph a caller captures once and replays
+            else:
+                wl.step()
             for h, t in zip(h_outs, outs):
                 h.copy_(t, non_blocking=True)
     stream.synchronize()
@@ -1075,6 +1256,7 @@ def run_ours(args):
             "kv_frac_of_hbm": kv_gbs / world / peaks["hbm"][0],
             "kv_bytes_per_step": kv_bytes,
             "roofline": roof,
+            **extra,
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},

@@ -79,6 +79,13 @@ enum asr_op {
   ASR_OP_ENCODER_ATTN = 6,
 };
 
+/* Epilogues of asr_linear. */
+enum asr_linear_mode {
+  ASR_LINEAR_STORE = 0,    /* y = v            (wavo's Epilogue::Bias) */
+  ASR_LINEAR_RESIDUAL = 1, /* y = y + v        (Epilogue::Residual(1.0)) */
+  ASR_LINEAR_GELU = 2,     /* y = v * Phi(v)   (Epilogue::Gelu, the erf form) */
+};
+
 /* Limits checked on the host. */
 #define ASR_MAX_BATCH 2048 /* sequences (and groups) per call */
 #define ASR_MAX_BEAMS 8    /* sequences sharing one cross source; also max Hq/Hkv */
@@ -295,6 +302,38 @@ int asr_encoder_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, co
 int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_v, int G,
                       int frames, int d, uint16_t* cross, int64_t group_stride, int32_t* dev_err,
                       asr_stream_t stream);
+
+/* Next row -- one dense step of a decoder layer around the attention.
+ * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
+ * (layer_norm of x, then gemv with the layer's qkv / self_out / cross_q /
+ * cross_out / fc1 / fc2 weight and the epilogue Bias, Residual(1.0) or
+ * Gelu); "Nest whisper-tiny, src/lib.linnet", LayerNorm (torch.nn.LayerNorm,
+ * eps 1e-5) and Mlp (fc2(gelu_erf(fc1(x)))).
+ *   a_m  = (x_m - mean_m) / sqrt(var_m + eps) * ln_g + ln_b   if ln_g != NULL
+ *          (mean and biased variance over the K values of row m), else x_m
+ *   v_mn = sum_k a_mk * w[n][k] + bias[n]                     (bias NULL: 0)
+ *   y_mn = v_mn (ASR_LINEAR_STORE) | y_mn + v_mn (ASR_LINEAR_RESIDUAL)
+ *        | v_mn * Phi(v_mn) = v/2 (1 + erf(v/sqrt 2)) (ASR_LINEAR_GELU)
+ * x: fp32 [M][x_stride] (the first K used; 16-byte aligned, x_stride % 4 ==
+ * 0); ln_g, ln_b: fp32 [K] (both or neither; 16-byte aligned); w: f16 [N][K]
+ * (row n makes output n: torch's Linear layout; 16-byte aligned); bias: fp32
+ * [N] or NULL; y: fp32 [M][y_stride] (the first N written), and y must not
+ * overlap x (ASR_ERR_ALIAS).  K % 64 == 0 (else ASR_ERR_UNSUPPORTED).
+ * Numerics: the activations enter the tensor cores as two f16 parts (a = hi
+ * + lo, both multiplied by the f16 weight), so they keep about 22 bits; the
+ * sums are fp32.  The LayerNorm is folded into the product (the operand is
+ * (x - x_0) * ln_g with x_0 the row's first element; the row statistics and
+ * the ln_g / ln_b terms are applied after the sum), which is the same
+ * function up to fp32 rounding.  ws: asr_linear_workspace_size(M, N, K) bytes, zero-filled
+ * before first use and 256-byte aligned (NULL allowed when that size is 0);
+ * every call leaves it zero again unless a wait times out
+ * (ASR_DEVERR_TIMEOUT), after which it must be zeroed before reuse.  The
+ * weight is read before the previous kernel on the stream has finished when
+ * that kernel is one of this library's (none of them writes a weight). */
+size_t asr_linear_workspace_size(int M, int N, int K);
+int asr_linear(const float* x, int64_t x_stride, const float* ln_g, const float* ln_b, float eps,
+               const uint16_t* w, const float* bias, int M, int N, int K, int mode, float* y,
+               int64_t y_stride, void* ws, size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device

@@ -51,6 +51,9 @@ SIGNATURES = {
                                _sz, _p, _p]),
     "asr_encoder_attn": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _p, _sz, _p, _p]),
     "asr_cross_kv_fill": (_int, [_p, _p, _p, _int, _int, _int, _p, _i64, _p, _p]),
+    "asr_linear": (_int, [_p, _i64, _p, _p, _f, _p, _p, _int, _int, _int, _int, _p, _i64, _p, _sz,
+                          _p, _p]),
+    "asr_linear_workspace_size": (_sz, [_int, _int, _int]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
@@ -330,6 +333,55 @@ def asr_cross_kv_fill(enc, w, bias_v, cross, frames=None, dev_err=None, stream=N
     st = load().asr_cross_kv_fill(_ptr(enc), _ptr(w), _ptr(bias_v), G, frames or F, d,
                                   _ptr(cross), cross.stride(0), _ptr(dev_err), _stream(stream))
     _check("asr_cross_kv_fill", st)
+
+
+LINEAR_MODES = {"store": 0, "residual": 1, "gelu": 2}
+
+
+def linear_workspace(M, N, K, device=None):
+    """A zero-filled workspace for asr_linear on M x K activations and an
+    N x K weight (None when the call needs none)."""
+    import torch
+    n = load().asr_linear_workspace_size(int(M), int(N), int(K))
+    if n == 0:
+        return None
+    return torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+
+
+def asr_linear(x, w, y, bias=None, ln=None, eps=1e-5, mode="store", ws=None, dev_err=None,
+               stream=None):
+    """y (fp32 [M, N], row-strided) = epilogue(LayerNorm(x) @ w^T + bias).
+
+    x: fp32 [M, K] (row-strided, unit inner stride); w: f16 [N, K]; bias:
+    fp32 [N] or None; ln: (g, b) fp32 [K] each, or None; mode "store",
+    "residual" (y += ...) or "gelu"."""
+    import torch
+    _need(x, torch.float32, "x")
+    _need(w, torch.float16, "w")
+    _need(y, torch.float32, "y")
+    if x.dim() != 2 or y.dim() != 2 or x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x and y must be 2-D with unit inner stride")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or y.shape[0] != M or y.shape[1] != N:
+        raise ValueError("shapes do not match: x [M, K], w [N, K], y [M, N]")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    g = b = None
+    if ln is not None:
+        g, b = ln
+        _need(g, torch.float32, "ln_g")
+        _need(b, torch.float32, "ln_b")
+    if ws is None:
+        wp, wn = None, 0
+    else:
+        wp, wn = _ws_ptr(ws)
+    st = load().asr_linear(_ptr(x), x.stride(0), _ptr(g), _ptr(b), float(eps), _ptr(w),
+                           _ptr(bias), M, N, K, LINEAR_MODES[mode], _ptr(y), y.stride(0), wp, wn,
+                           _ptr(dev_err), _stream(stream))
+    _check("asr_linear", st)
 
 
 def asr_kv_rearrange(src, dst, idx, lens_src, lens_dst, n_layers, row_elems, capacity,

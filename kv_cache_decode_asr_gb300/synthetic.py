@@ -28,6 +28,16 @@ Workloads (shapes of the pages' models; no weights or audio are needed):
 * ``whisper_large_cross_fill_b32`` -- the cross K/V of one Large-Whisper
   decoder layer (d = 1280) from the encoder output of 32 utterances of 1500
   frames; weights N(0, 1/d), bias N(0, 1).
+* ``whisper_large_decoder_step_b32`` -- the whole Large-Whisper decoder step
+  around the attention (32 layers, d = 1280, 20 heads x 64, MLP 5120), 32
+  sequences, self lengths uniform in [1, 448], 1500 cross frames: per layer
+  LayerNorm + qkv, append + self-attention, out-projection, LayerNorm +
+  cross query, cross-attention, cross out-projection, LayerNorm + fc1 + GELU,
+  fc2.  Random weights (``layer_params``).
+
+Layer weights (``layer_params``): every projection N(0, 1/fan_in) stored as
+f16, biases N(0, 0.1) with the key bias zero, LayerNorm weights N(1, 0.1) and
+biases N(0, 0.1); the residual stream x starts N(0, 1).
 
 Values: activations and caches N(0, 1); caches are stored as f16 (the fp32
 draw rounded to nearest even).  Host draws use numpy's PCG64; device draws use
@@ -54,7 +64,34 @@ WORKLOADS = {
                                       capacity=448, len_lo=1, len_hi=448),
     "whisper_large_encoder_b8": dict(kind="encoder", B=8, T=1500, heads=20, head_dim=64),
     "whisper_large_cross_fill_b32": dict(kind="cross_fill", G=32, frames=1500, d=1280),
+    "whisper_large_decoder_step_b32": dict(kind="decoder_step", B=32, d=1280, heads=20,
+                                           head_dim=64, inner=5120, layers=32, capacity=448,
+                                           frames=1500, beam=1, len_lo=1, len_hi=448),
 }
+
+# projections of one decoder layer: name, output size, input size (d units)
+LAYER_PROJ = (("qkv", 3, 1), ("o", 1, 1), ("cq", 1, 1), ("co", 1, 1), ("fc1", "inner", 1),
+              ("fc2", 1, "inner"))
+
+
+def _proj_shapes(d, inner):
+    size = lambda u: inner if u == "inner" else u * d
+    return [(name, size(o), size(i)) for name, o, i in LAYER_PROJ]
+
+
+def layer_params(d, inner, seed):
+    """Host parameters of one decoder layer (numpy): w_* f16 bits [out, in],
+    b_* float32 [out] (the key third of b_qkv zero), ln{1,2,3}_{g,b} float32 [d]."""
+    p = {}
+    for i, (name, n_out, n_in) in enumerate(_proj_shapes(d, inner)):
+        w = host_normal_f32((n_out, n_in), seed + 2 * i, std=n_in ** -0.5)
+        p["w_" + name] = w.astype(np.float16).view(np.uint16)
+        p["b_" + name] = host_normal_f32(n_out, seed + 2 * i + 1, std=0.1)
+    p["b_qkv"][d:2 * d] = 0
+    for j in (1, 2, 3):
+        p[f"ln{j}_g"] = host_normal_f32(d, seed + 20 + j, mean=1.0, std=0.1)
+        p[f"ln{j}_b"] = host_normal_f32(d, seed + 30 + j, std=0.1)
+    return p
 
 
 def seed_for(workload_index, tensor_id):
@@ -114,6 +151,25 @@ def dev_normal(shape, seed, device, dtype=None, mean=0.0, std=1.0):
     if dtype is not None and dtype != torch.float32:
         x = x.to(dtype)
     return x
+
+
+def dev_layer_params(n_layers, d, inner, seed, device):
+    """The parameters of n_layers decoder layers drawn on the device, stacked
+    on a leading layer axis (weights f16, the rest fp32); same recipe as
+    layer_params."""
+    import torch
+    p = {}
+    for i, (name, n_out, n_in) in enumerate(_proj_shapes(d, inner)):
+        w = torch.empty(n_layers, n_out, n_in, dtype=torch.float16, device=device)
+        dev_fill_normal_(w, seed + 2 * i)
+        w.mul_(n_in ** -0.5)
+        p["w_" + name] = w
+        p["b_" + name] = dev_normal((n_layers, n_out), seed + 2 * i + 1, device, std=0.1)
+    p["b_qkv"][:, d:2 * d] = 0
+    for j in (1, 2, 3):
+        p[f"ln{j}_g"] = dev_normal((n_layers, d), seed + 20 + j, device, mean=1.0, std=0.1)
+        p[f"ln{j}_b"] = dev_normal((n_layers, d), seed + 30 + j, device, std=0.1)
+    return p
 
 
 def dev_fill_normal_(t, seed, chunk_elems=1 << 28):

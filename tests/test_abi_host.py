@@ -161,3 +161,25 @@ def test_prefill_rejects(lib):
     assert f(*args(ss=1536 * row - 8)) == INVALID
     assert f(*args(ss=1536 * row + 4)) == MISAL
     assert f(*args(B=0)) == OK
+
+
+def test_linear_rejects(lib):
+    f = lib.asr_linear
+    x, w, y = P(0x100000), P(0x200000), P(0x900000)
+
+    def args(**kw):
+        return [kw.get("x", x), kw.get("xs", 1280), kw.get("g", None), kw.get("b", None),
+                ctypes.c_float(1e-5), w, None, kw.get("M", 32), kw.get("N", 3840),
+                kw.get("K", 1280), kw.get("mode", 0), kw.get("y", y), kw.get("ys", 3840), None,
+                ctypes.c_size_t(0), None, None]
+
+    assert f(*args(K=1000)) == UNSUP           # K not a multiple of 64
+    assert f(*args(mode=3)) == INVALID
+    assert f(*args(N=0)) == INVALID
+    assert f(*args(xs=1000)) == INVALID        # row stride below K
+    assert f(*args(ys=100)) == INVALID
+    assert f(*args(g=P(0x300000))) == INVALID  # LayerNorm weight without its bias
+    assert f(*args(x=P(0x100004))) == MISAL
+    assert f(*args(xs=1282)) == MISAL
+    assert f(*args(y=P(0x100000 + 64))) == ALIAS  # y overlaps x
+    assert f(*args(M=0)) == OK
