@@ -321,7 +321,9 @@ int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_
  * overlap x (ASR_ERR_ALIAS).  K % 64 == 0 (else ASR_ERR_UNSUPPORTED).
  * Numerics: the activations enter the tensor cores as two f16 parts (a = hi
  * + lo, both multiplied by the f16 weight), so they keep about 22 bits; the
- * sums are fp32.  The LayerNorm is folded into the product (the operand is
+ * sums are fp32 (with the K axis split across CTAs, a residual without
+ * LayerNorm adds the parts onto y in an unspecified order, so repeated calls
+ * may differ in the last bits).  The LayerNorm is folded into the product (the operand is
  * (x - x_0) * ln_g with x_0 the row's first element; the row statistics and
  * the ln_g / ln_b terms are applied after the sum), which is the same
  * function up to fp32 rounding.  ws: asr_linear_workspace_size(M, N, K) bytes, zero-filled

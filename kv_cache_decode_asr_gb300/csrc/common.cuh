@@ -134,6 +134,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// As bulk_g2s, without a cache policy.
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Hint: bring `bytes` of global memory at `src` into L2 (no destination, no
 // completion to wait for).  src 16-byte aligned; bytes a multiple of 16.  A
 // prefetch changes no memory and is never observed by loads, so it is safe

@@ -23,10 +23,12 @@
 // core is idle most of the time here anyway).
 //
 // Work split: 128 weight rows x a range of K per CTA.  With few weight rows
-// (N = 1280 is ten tiles) the K axis is split until the grid covers the GPU;
-// the CTAs of one tile add their partial sums into a zero fp32 tile in the
-// workspace (red.add), and the last to arrive (a counter per tile) applies
-// the epilogue, writes y and puts the tile and the counter back to zero.
+// (N = 1280 is ten tiles) the K axis is split until the grid covers the GPU.
+// A residual without LayerNorm is linear in the partial sums, so each CTA
+// adds its part straight onto y (red.add).  Otherwise the CTAs of one tile
+// add their partial sums into a zero fp32 tile in the workspace, and the last
+// to arrive (a counter per tile) applies the epilogue, writes y and puts the
+// tile and the counter back to zero.
 //
 // LayerNorm without a pass over whole rows: a CTA only sees its K range, so
 // the normalisation is folded into the product.  With x_0 the row's first
@@ -38,11 +40,12 @@
 //   sum_k a_mk W_nk = rstd * (sum_k (x_k - x_0) g_k W_nk - (mean - x_0) cn) + dn.
 // Shifting by x_0 keeps both differences of the size of the row's spread.
 //
-// Roles: warp 4 streams W (128 rows x 64 k per stage, 128-byte swizzle) and
-// holds the TMEM allocation; warp 5 issues tcgen05.mma; warps 0-3 write the
-// hi/lo operand to shared memory in the same swizzled layout (with the
-// LayerNorm sums), then drain the accumulator (thread = weight row, one TMEM
-// lane each) and run the epilogue.  W is never written by a kernel of this
+// Roles: warp 8 streams W (128 rows x 64 k per stage, 128-byte swizzle) and
+// holds the TMEM allocation; warp 9 issues tcgen05.mma; warps 0-7 bring the
+// fp32 activations in with bulk copies and write the hi/lo operand to shared
+// memory in the same swizzled layout (with the LayerNorm sums); warps 0-3
+// then drain the accumulator (thread = weight row, one TMEM lane each) and
+// run the epilogue.  W is never written by a kernel of this
 // library, so the weight loads start before the wait on the previous grid
 // (programmatic dependent launch): they overlap its tail.
 #include <mutex>
@@ -54,10 +57,20 @@ namespace asrkv {
 
 constexpr int kLinStages = 4;
 constexpr int kLinWTile = 128 * 64 * 2;  // 16 KB: 128 weight rows x 64 k
-constexpr int kLinThreads = 192;         // warps 0-3 operand + epilogue, 4 TMA, 5 MMA
+constexpr int kLinStageThreads = 256;    // warps 0-7 build the operand; warps 0-3 then drain TMEM
+constexpr int kLinTmaWarp = 8, kLinMmaWarp = 9;
+constexpr int kLinThreads = 320;
 constexpr int kLinMaxMT = 256;           // the MMA's N
-constexpr int kLinXCap = 96 * 1024;      // both activation planes of one CTA
 constexpr int kLinSmemFixed = 1024 + kLinStages * kLinWTile + 256 + 4 * kLinMaxMT * 4;
+constexpr int kLinSmemMax = 232448;      // the largest dynamic shared memory of one CTA
+
+// Bytes of the fp32 staging of one CTA: MR rows of its K range (nkb_max
+// k-blocks of 64), and with LayerNorm the same range of g and b and 16
+// bytes of each row's head.
+__host__ __device__ constexpr int lin_f32_bytes(int MR, int nkb_max, bool ln) {
+  return ((MR * (nkb_max * 64 + 4) + (ln ? 2 * (nkb_max * 64 + 4) + MR * 4 : 0)) * 4 + 15) / 16 *
+         16;
+}
 
 struct LinArgs {
   const float* x;
@@ -69,7 +82,7 @@ struct LinArgs {
   float* y;
   int64_t y_stride;
   float* acc;         // [tiles][MT][128] fp32, zero between calls
-  float* stats;       // [tiles][MT][2] fp32 (LayerNorm sums), zero between calls
+  float* stats;       // [tiles][2][MT] fp32 (LayerNorm sums), zero between calls
   uint32_t* tickets;  // [tiles], zero between calls
   int M, N, K, mode;
   int MT, MR, n_tiles, S, KB, nkb_max;  // MR: sequences per tile (MT - 2 or fewer with LayerNorm)
@@ -83,6 +96,27 @@ __device__ __forceinline__ float lin_epilogue(int mode, float v, float yold) {
   return v;
 }
 
+// Bulk (TMA) reduction: global[dst .. dst+bytes) += shared[src ..] as fp32,
+// element by element, performed at L2.  16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const float* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   dst),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+
+// Commit this thread's bulk operations and wait until they have completed
+// (their writes performed).
+__device__ __forceinline__ void bulk_commit_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Order this thread's async-proxy accesses of global memory against its
+// generic-proxy ones (both directions).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Row statistics of the LayerNorm from the K-sums of the values shifted by
 // the row's first element x_0: s1 = sum (x - x_0), s2 = sum (x - x_0)^2.
 // dm = mean - x_0 and rstd = 1 / sqrt(var + eps), var = s2/K - (s1/K)^2.
@@ -94,23 +128,26 @@ __device__ __forceinline__ void lin_row_stats(float s1, float s2, float inv_k, f
   s_rs[t] = rsqrtf(var + eps);
 }
 
+// Old values of a residual's rows m_first .. m_first+cnt-1 at column n, all
+// loads issued together (zeros when there is no residual).
+__device__ __forceinline__ void lin_load_old(const LinArgs& a, int m_first, int cnt, int n,
+                                             bool resid, float* yo) {
+  // rows past the last one re-read it (a valid address): no branch per load
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    yo[e] = resid ? a.y[(int64_t)(m_first + min(e, cnt - 1)) * a.y_stride + n] : 0.f;
+}
+
 // Outputs (m_first + e, n) for e < cnt from the K-sums v[e]:
 //   LayerNorm: a_mk = ((x_mk - x_0) - dm) * rstd * g_k + b_k, so
 //   sum_k a_mk W_nk = rstd * (v - dm * cn) + dn with cn = sum_k g_k W_nk and
 //   dn = sum_k b_k W_nk; otherwise the sum is v itself.  Then bias, epilogue.
-// The old values of a residual are loaded before any store.
-__device__ __forceinline__ void lin_emit16(const LinArgs& a, int m_first, int cnt, int n,
-                                           const float* v, float bn, bool ln, const float* dm,
-                                           const float* rs, float cn, float dn) {
+__device__ __forceinline__ void lin_emit(const LinArgs& a, int m_first, int cnt, int n,
+                                         const float* v, const float* yo, float bn, bool ln,
+                                         const float* dm, const float* rs, float cn, float dn) {
   if (n >= a.N) return;
-  float yo[16];
-  if (a.mode == ASR_LINEAR_RESIDUAL) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      yo[e] = e < cnt ? a.y[(int64_t)(m_first + e) * a.y_stride + n] : 0.f;
-  }
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
+  for (int e = 0; e < 32; ++e) {
     if (e < cnt) {
       const float t = ln ? rs[e] * (v[e] - dm[e] * cn) + dn : v[e];
       a.y[(int64_t)(m_first + e) * a.y_stride + n] = lin_epilogue(a.mode, t + bn, yo[e]);
@@ -123,18 +160,22 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int MT = a.MT;
+  const bool ln = a.ln_g != nullptr;
   const int plane = MT * 128 * a.nkb_max;                  // bytes of one activation plane
   unsigned char* sW = smem;                                // stages x 16 KB
   unsigned char* sXh = sW + kLinStages * kLinWTile;        // hi plane: [nkb][MT rows][128 B]
   unsigned char* sXl = sXh + plane;                        // lo plane
-  uint64_t* full = reinterpret_cast<uint64_t*>(sXl + plane);
+  unsigned char* sFb = sXl + plane;                        // fp32 staging
+  const int f32b = lin_f32_bytes(a.MR, a.nkb_max, ln);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sFb + f32b);
   uint64_t* empty = full + kLinStages;
-  uint64_t* x_full = empty + kLinStages;   // the activation operand is in shared memory
-  uint64_t* acc_full = x_full + 1;         // the accumulator is complete
+  uint64_t* xin_full = empty + kLinStages;  // the fp32 activations have landed
+  uint64_t* x_full = xin_full + 1;          // the f16 operand is in shared memory
+  uint64_t* acc_full = x_full + 1;          // the accumulator is complete
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
   int* last_flag = reinterpret_cast<int*>(tslot + 1);
   int* abort_flag = last_flag + 1;  // a wait of warps 0-3 gave up
-  float* s_s1 = reinterpret_cast<float*>(smem + kLinStages * kLinWTile + 2 * plane + 256);
+  float* s_s1 = reinterpret_cast<float*>(sFb + f32b + 256);
   float* s_s2 = s_s1 + kLinMaxMT;  // LayerNorm sums of this CTA's K range
   float* s_dm = s_s2 + kLinMaxMT;  // mean - x_0 of each row
   float* s_rs = s_dm + kLinMaxMT;  // 1 / sqrt(var + eps)
@@ -153,12 +194,14 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(x_full, 128);
+    mbar_init(xin_full, 1);
+    mbar_init(x_full, kLinStageThreads);
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (tid < MT) s_s1[tid] = s_s2[tid] = 0.f;
+  if (warp == kLinTmaWarp) {
     tmem_alloc(tslot, a.tmem_cols);
     tmem_relinquish();
   }
@@ -169,7 +212,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
   grid_launch_dependents();
   bool ok = true;
 
-  if (warp == 4) {
+  if (warp == kLinTmaWarp) {
     // ================================================ W producer (no wait)
     int j = 0;
     for (; j < nkb; ++j) {
@@ -181,7 +224,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
     // every issued copy has landed before the CTA may leave
     for (int i = max(0, j - kLinStages); i < j; ++i)
       if (!mbar_wait_warp(&full[i % kLinStages], (i / kLinStages) & 1)) ok = false;
-  } else if (warp == 5) {
+  } else if (warp == kLinMmaWarp) {
     // ================================================ MMA issuer
     const uint32_t idesc = mma_idesc_f16_f32(128, MT);
     const uint32_t aW = smem_addr(sW), aH = smem_addr(sXh), aL = smem_addr(sXl);
@@ -203,183 +246,286 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
     }
     if (ok) mma_commit_warp(acc_full);
   } else {
-    // ================================================ operand + epilogue
+    // ================================================ operand (warps 0-7)
     grid_dependency_wait();  // x (and y, the workspace) belong to earlier grids
-    const bool ln = a.ln_g != nullptr;
-    if (ln) {
-      for (int i = tid; i < MT; i += 128) s_s1[i] = s_s2[i] = 0.f;
-      named_bar(1, 128);
-    }
-    // The operand: MT rows x nkb k-blocks x eight 16-byte chunks; chunk c of
-    // row r sits at c ^ (r % 8) (the 128-byte swizzle the MMA reads).  Rows
-    // < Mv: the activations (LayerNorm: (x - x_0) * g, see the epilogue);
-    // with LayerNorm, row Mv holds g and row Mv+1 holds b, so that the
-    // accumulator also collects sum_k g_k W_nk and sum_k b_k W_nk; the rest
-    // is zero.  Loads of four items are issued before any is used.
-    const int items = MT * nkb * 8;  // a multiple of 128: warp-uniform batches
-    for (int i0 = tid; i0 < items; i0 += 4 * 128) {
-      float4 xv[4][2], gv[4][2];
-      float shv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = i0 + q * 128;
-        const int c = i & 7, j = (i >> 3) % nkb, r = (i >> 3) / nkb;
-        const int k = (kb0 + j) * 64 + c * 8;
-        xv[q][0] = xv[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        gv[q][0] = gv[q][1] = xv[q][0];
-        shv[q] = 0.f;
-        if (i < items) {
-          const float* src = nullptr;
-          if (r < Mv) {
-            src = a.x + (int64_t)(m0 + r) * a.x_stride + k;
-            if (ln) {
-              shv[q] = __ldg(a.x + (int64_t)(m0 + r) * a.x_stride);
-              gv[q][0] = __ldg(reinterpret_cast<const float4*>(a.ln_g + k));
-              gv[q][1] = __ldg(reinterpret_cast<const float4*>(a.ln_g + k + 4));
-            }
-          } else if (ln && r == Mv) {
-            src = a.ln_g + k;
-          } else if (ln && r == Mv + 1) {
-            src = a.ln_b + k;
-          }
-          if (src) {
-            xv[q][0] = __ldg(reinterpret_cast<const float4*>(src));
-            xv[q][1] = __ldg(reinterpret_cast<const float4*>(src + 4));
-          }
-        }
+    // 1. Bulk copies bring this CTA's K range of each activation row (and,
+    // with LayerNorm, of g and b, and each row's first 16 bytes) into shared
+    // memory as fp32: one round trip.
+    const int RS = a.nkb_max * 64 + 4;  // floats per staged row (+4: rows start 16 banks apart)
+    float* xs = reinterpret_cast<float*>(sFb);
+    float* gs = xs + a.MR * RS;
+    float* bs = gs + RS;
+    float* hs = bs + RS;  // [MR][4]: x_0 of each row in hs[4 r]
+    const uint32_t q_bytes = (uint32_t)nkb * 256;
+    if (warp == 0) {
+      if (lane == 0)
+        mbar_arrive_expect_tx(xin_full, Mv * q_bytes + (ln ? 2 * q_bytes + Mv * 16 : 0));
+      __syncwarp();
+      for (int r = lane; r < Mv; r += 32) {
+        const float* row = a.x + (int64_t)(m0 + r) * a.x_stride;
+        bulk_g2s_plain(xs + r * RS, row + kb0 * 64, q_bytes, xin_full);
+        if (ln) bulk_g2s_plain(hs + r * 4, row, 16, xin_full);
       }
+      if (ln && lane == 0) {
+        bulk_g2s_plain(gs, a.ln_g + kb0 * 64, q_bytes, xin_full);
+        bulk_g2s_plain(bs, a.ln_b + kb0 * 64, q_bytes, xin_full);
+      }
+    }
+    if (!mbar_wait(xin_full, 0)) ok = false;
+    // 2. The operand: MT rows x nkb k-blocks x eight 16-byte chunks; chunk c
+    // of row r sits at c ^ (r % 8) (the 128-byte swizzle the MMA reads).
+    // Rows < Mv: the activations (LayerNorm: (x - x_0) * g, see the
+    // epilogue); with LayerNorm, row Mv holds g and row Mv+1 holds b, so that
+    // the accumulator also collects sum_k g_k W_nk and sum_k b_k W_nk; the
+    // rest is zero.  Thread (rr, c) = (tid / 8, tid % 8) converts chunk c of
+    // every k-block of rows rr, rr + 32, ... (a warp's four rows are all
+    // below MT or all above: MT is a multiple of 16), keeping the row's
+    // LayerNorm sums in registers until its last k-block.
+    {
+      const int rr = tid >> 3, c = tid & 7;
+      for (int r = rr; r < MT; r += 32) {
+        const float* srow = nullptr;
+        if (r < Mv) srow = xs + r * RS;
+        else if (ln && r == Mv) srow = gs;
+        else if (ln && r == Mv + 1) srow = bs;
+        const bool act = ln && r < Mv;  // a LayerNorm-ed activation row
+        const float sh = act ? hs[r * 4] : 0.f;
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < nkb; ++j) {
+          const int ko = j * 64 + c * 8;
+          float f[8];
+          if (srow) {
+            const float4 u0 = *reinterpret_cast<const float4*>(srow + ko);
+            const float4 u1 = *reinterpret_cast<const float4*>(srow + ko + 4);
+            f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
+            f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
+          } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = i0 + q * 128;
-        if (i >= items) break;  // uniform across the warp
-        const int c = i & 7, j = (i >> 3) % nkb, r = (i >> 3) / nkb;
-        float f[8] = {xv[q][0].x, xv[q][0].y, xv[q][0].z, xv[q][0].w,
-                      xv[q][1].x, xv[q][1].y, xv[q][1].z, xv[q][1].w};
-        if (ln) {
-          // shifted values of this K range: their sum and sum of squares
-          // (the row statistics), and (x - x_0) * g as the operand
-          const float g[8] = {gv[q][0].x, gv[q][0].y, gv[q][0].z, gv[q][0].w,
-                              gv[q][1].x, gv[q][1].y, gv[q][1].z, gv[q][1].w};
-          float s1 = 0.f, s2 = 0.f;
-          if (r < Mv) {
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+          }
+          if (act) {
+            // shifted values: their sum and sum of squares (the row
+            // statistics), and (x - x_0) * g as the operand
+            const float4 g0 = *reinterpret_cast<const float4*>(gs + ko);
+            const float4 g1 = *reinterpret_cast<const float4*>(gs + ko + 4);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float t = f[e] - shv[q];
-              s1 += t;
-              s2 += t * t;
-              f[e] = t * g[e];
+              const float d = f[e] - sh;
+              s1 += d;
+              s2 += d * d;
+              f[e] = d * g[e];
             }
           }
-          // the eight lanes of one row piece share r
+          uint4 hv, lv;
+          __half2* h = reinterpret_cast<__half2*>(&hv);
+          __half2* l = reinterpret_cast<__half2*>(&lv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 hi = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+            const float2 hf = __half22float2(hi);
+            h[e] = hi;
+            l[e] = __floats2half2_rn(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
+          }
+          const int off = j * MT * 128 + r * 128 + ((c ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(sXh + off) = hv;
+          *reinterpret_cast<uint4*>(sXl + off) = lv;
+        }
+        if (ln) {
+          // the eight lanes of one row share r
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) {
             s1 += __shfl_xor_sync(0xffffffffu, s1, o);
             s2 += __shfl_xor_sync(0xffffffffu, s2, o);
           }
-          if (c == 0 && r < Mv) {
-            atomicAdd(&s_s1[r], s1);
-            atomicAdd(&s_s2[r], s2);
+          if (c == 0 && act) {
+            s_s1[r] = s1;
+            s_s2[r] = s2;
           }
         }
-        uint4 hv, lv;
-        __half2* h = reinterpret_cast<__half2*>(&hv);
-        __half2* l = reinterpret_cast<__half2*>(&lv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2 hi = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
-          const float2 hf = __half22float2(hi);
-          h[e] = hi;
-          l[e] = __floats2half2_rn(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
-        }
-        const int off = j * MT * 128 + r * 128 + ((c ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sXh + off) = hv;
-        *reinterpret_cast<uint4*>(sXl + off) = lv;
       }
     }
     fence_async_shared();
     mbar_arrive(x_full);
+    named_bar(1, kLinStageThreads);  // the LayerNorm sums are complete
 
-    // ---- the accumulator: thread = weight row n, TMEM columns = rows m
-    // warps 0-3 agree on the outcome before any of them meets barrier 1 again
-    if (!mbar_wait_warp(acc_full, 0) && lane == 0) atomicExch(abort_flag, 1);
-    named_bar(1, 128);  // also: the statistics of this K range are complete
-    ok = *reinterpret_cast<volatile int*>(abort_flag) == 0;
-    tc_fence_after_sync();
-    const int f = warp * 32 + lane, n = n0 + f;
-    const uint32_t taddr = tbase + ((uint32_t)(warp * 32) << 16);
-    const float bn = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
-    const int rows = Mv + (ln ? 2 : 0);  // accumulator columns with content
-    const float inv_k = 1.0f / (float)a.K;
-    if (ok) {
-      if (a.S == 1) {
-        float cn = 0.f, dn = 0.f;
-        if (ln) {
-          cn = tmem_ld1(taddr + Mv);
-          dn = tmem_ld1(taddr + Mv + 1);
-          tmem_wait_ld();
-          for (int t = tid; t < Mv; t += 128) lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs);
-          named_bar(1, 128);
-        }
-        for (int c0 = 0; c0 < Mv; c0 += 16) {
-          float v[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_wait_ld();
-          lin_emit16(a, m0 + c0, min(16, Mv - c0), n, v, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
-        }
-      } else {
-        float* accp = a.acc + (int64_t)tile * MT * 128 + f;
-        float* stp = a.stats + (int64_t)tile * MT * 2;
-        for (int c0 = 0; c0 < rows; c0 += 16) {
-          float v[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (c0 + e < rows) atomicAdd(accp + (c0 + e) * 128, v[e]);
-        }
-        if (ln)
-          for (int t = tid; t < Mv; t += 128) {
-            atomicAdd(stp + 2 * t, s_s1[t]);
-            atomicAdd(stp + 2 * t + 1, s_s2[t]);
-          }
-        __threadfence();
-        named_bar(1, 128);
-        if (tid == 0) *last_flag = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.S - 1));
-        named_bar(1, 128);
-        if (*last_flag) {
-          __threadfence();
+    if (warp < 4) {
+      // ============================================== epilogue (warps 0-3)
+      // thread = weight row n (one TMEM lane), TMEM columns = rows m.  The
+      // four warps agree on the outcome before any of them meets barrier 2.
+      if (!mbar_wait_warp(acc_full, 0) && lane == 0) atomicExch(abort_flag, 1);
+      named_bar(2, 128);
+      ok = ok && *reinterpret_cast<volatile int*>(abort_flag) == 0;
+      tc_fence_after_sync();
+      const int f = warp * 32 + lane, n = n0 + f;
+      const uint32_t taddr = tbase + ((uint32_t)(warp * 32) << 16);
+      const float bn = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
+      const int rows = Mv + (ln ? 2 : 0);  // accumulator columns with content
+      const float inv_k = 1.0f / (float)a.K;
+      const bool resid = a.mode == ASR_LINEAR_RESIDUAL && n < a.N;
+      if (*reinterpret_cast<volatile int*>(abort_flag) == 0) {
+        if (a.S == 1) {
           float cn = 0.f, dn = 0.f;
           if (ln) {
-            cn = __ldcg(accp + Mv * 128);
-            dn = __ldcg(accp + (Mv + 1) * 128);
-            for (int t = tid; t < Mv; t += 128) {
-              const float s1 = __ldcg(stp + 2 * t), s2 = __ldcg(stp + 2 * t + 1);
-              lin_row_stats(s1, s2, inv_k, a.eps, t, s_dm, s_rs);
-            }
-            named_bar(1, 128);
-            __stcg(accp + Mv * 128, 0.f);
-            __stcg(accp + (Mv + 1) * 128, 0.f);
-            for (int t = tid; t < 2 * Mv; t += 128) __stcg(stp + t, 0.f);
+            cn = tmem_ld1(taddr + Mv);
+            dn = tmem_ld1(taddr + Mv + 1);
+            tmem_wait_ld();
+            for (int t = tid; t < Mv; t += 128)
+              lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs);
+            named_bar(2, 128);
           }
+          for (int c0 = 0; c0 < Mv; c0 += 32) {
+            const int cnt = min(32, Mv - c0);
+            float v[32], yo[32];
+            tmem_ld16(taddr + c0, v);
+            if (c0 + 16 < MT) tmem_ld16(taddr + c0 + 16, v + 16);  // MT is a multiple of 16
+            lin_load_old(a, m0 + c0, cnt, n, resid, yo);
+            tmem_wait_ld();
+            lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+          }
+        } else if (a.mode == ASR_LINEAR_RESIDUAL && !ln) {
+          // a residual without LayerNorm is linear in each partial sum: every
+          // K split adds its part (split 0 with the bias) straight onto y
+          const float b0 = s == 0 ? bn : 0.f;
           for (int c0 = 0; c0 < Mv; c0 += 16) {
             float v[16];
-            const int cnt = min(16, Mv - c0);
+            tmem_ld16(taddr + c0, v);
+            tmem_wait_ld();
+            if (n < a.N) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = e < cnt ? __ldcg(accp + (c0 + e) * 128) : 0.f;
+              for (int e = 0; e < 16; ++e)
+                if (c0 + e < Mv) atomicAdd(a.y + (int64_t)(m0 + c0 + e) * a.y_stride + n, v[e] + b0);
+            }
+          }
+        } else if (rows <= 128) {
+          // Split K, one pass of bulk operations: the partial tile goes
+          // through shared memory (the W ring, free now) and is added into
+          // the workspace tile with one bulk reduction; the last CTA of the
+          // tile loads the whole sum back with one bulk copy.
+          float* P = reinterpret_cast<float*>(sW);  // [rows][128] fp32
+          float* acct = a.acc + (int64_t)tile * MT * 128;
+          float* stt = a.stats + (int64_t)tile * MT * 2;
+          for (int c0 = 0; c0 < rows; c0 += 16) {
+            float v[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (e < cnt) __stcg(accp + (c0 + e) * 128, 0.f);
-            lin_emit16(a, m0 + c0, cnt, n, v, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+              if (c0 + e < rows) P[(c0 + e) * 128 + f] = v[e];
           }
-          if (tid == 0) a.tickets[tile] = 0u;
+          fence_async_shared();
+          named_bar(2, 128);
+          if (tid == 0) {
+            bulk_reduce_add_f32(acct, P, (uint32_t)rows * 512);
+            if (ln) {
+              bulk_reduce_add_f32(stt, s_s1, (uint32_t)MT * 4);
+              bulk_reduce_add_f32(stt + MT, s_s2, (uint32_t)MT * 4);
+            }
+            bulk_commit_wait_all();     // the sums are in global memory
+            fence_proxy_async_global();  // ... and ordered before the ticket
+            __threadfence();
+            *last_flag = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.S - 1));
+            if (*last_flag) {
+              __threadfence();
+              fence_proxy_async_global();
+              mbar_arrive_expect_tx(xin_full, (uint32_t)rows * 512 + (ln ? (uint32_t)MT * 8 : 0u));
+              bulk_g2s_plain(P, acct, (uint32_t)rows * 512, xin_full);
+              if (ln) {
+                bulk_g2s_plain(s_s1, stt, (uint32_t)MT * 4, xin_full);
+                bulk_g2s_plain(s_s2, stt + MT, (uint32_t)MT * 4, xin_full);
+              }
+            }
+          }
+          named_bar(2, 128);
+          if (*last_flag) {
+            // xin_full's second phase: the whole tile and its row sums
+            if (!mbar_wait(xin_full, 1)) atomicExch(abort_flag, 1);
+            float cn = 0.f, dn = 0.f;
+            if (ln) {
+              cn = P[Mv * 128 + f];
+              dn = P[(Mv + 1) * 128 + f];
+              for (int t = tid; t < Mv; t += 128)
+                lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs);
+            }
+            named_bar(2, 128);
+            // put the workspace back to zero
+            for (int m = 0; m < rows; ++m) __stcg(acct + m * 128 + f, 0.f);
+            if (ln)
+              for (int t = tid; t < 2 * MT; t += 128) __stcg(stt + t, 0.f);
+            if (tid == 0) a.tickets[tile] = 0u;
+            for (int c0 = 0; c0 < Mv; c0 += 32) {
+              const int cnt = min(32, Mv - c0);
+              float v[32], yo[32];
+              lin_load_old(a, m0 + c0, cnt, n, resid, yo);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = P[min(c0 + e, rows - 1) * 128 + f];
+              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+            }
+            if (*reinterpret_cast<volatile int*>(abort_flag) != 0) ok = false;
+          }
+        } else {
+          float* accp = a.acc + (int64_t)tile * MT * 128 + f;
+          float* stp = a.stats + (int64_t)tile * MT * 2;
+          for (int c0 = 0; c0 < rows; c0 += 16) {
+            float v[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (c0 + e < rows) atomicAdd(accp + (c0 + e) * 128, v[e]);
+          }
+          if (ln)
+            for (int t = tid; t < Mv; t += 128) {
+              atomicAdd(stp + t, s_s1[t]);
+              atomicAdd(stp + MT + t, s_s2[t]);
+            }
+          __threadfence();
+          named_bar(2, 128);
+          if (tid == 0) *last_flag = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.S - 1));
+          named_bar(2, 128);
+          if (*last_flag) {
+            __threadfence();
+            float cn = 0.f, dn = 0.f;
+            for (int c0 = 0; c0 < Mv; c0 += 32) {
+              const int cnt = min(32, Mv - c0);
+              float v[32], yo[32];
+              // every load of the chunk is issued before any is used; rows
+              // past the tile re-read its last row (always a valid address)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __ldcg(accp + min(c0 + e, MT - 1) * 128);
+              lin_load_old(a, m0 + c0, cnt, n, resid, yo);
+              if (c0 == 0 && ln) {
+                cn = __ldcg(accp + Mv * 128);
+                dn = __ldcg(accp + (Mv + 1) * 128);
+                for (int t = tid; t < Mv; t += 128)
+                  lin_row_stats(__ldcg(stp + t), __ldcg(stp + MT + t), inv_k, a.eps, t, s_dm,
+                                s_rs);
+                named_bar(2, 128);  // uniform: every thread of the last CTA is here
+                __stcg(accp + Mv * 128, 0.f);
+                __stcg(accp + (Mv + 1) * 128, 0.f);
+                for (int t = tid; t < Mv; t += 128) {
+                  __stcg(stp + t, 0.f);
+                  __stcg(stp + MT + t, 0.f);
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e < cnt) __stcg(accp + (c0 + e) * 128, 0.f);
+              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+            }
+            if (tid == 0) a.tickets[tile] = 0u;
+          }
         }
+      } else {
+        ok = false;
       }
     }
   }
   if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kLinTmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, a.tmem_cols);
   }
@@ -394,8 +540,8 @@ struct LinPlan {
 
 // Tiles of 128 weight rows x MT operand rows (the sequences of the tile, plus
 // the g and b rows with LayerNorm); the K axis split S ways so that the grid
-// covers the GPU once without a second wave; the activation planes capped at
-// kLinXCap.
+// covers the GPU once without a second wave, more if one CTA's share of the
+// activations would not fit in shared memory.
 static bool lin_plan(int M, int N, int K, bool ln, int sms, LinPlan* p) {
   if (M < 1 || N < 1 || K < 64 || K % 64 != 0 || sms < 1) return false;
   const int extra = ln ? 2 : 0;
@@ -409,10 +555,13 @@ static bool lin_plan(int M, int N, int K, bool ln, int sms, LinPlan* p) {
   const int tiles = p->m_tiles * p->n_tiles;
   int S = sms / tiles;  // one wave: one CTA per SM at most
   if (S > p->KB) S = p->KB;
-  const int cap = kLinXCap / (2 * p->MT * 128);  // k-blocks of activations per CTA (>= 1)
-  const int s_min = (p->KB + cap - 1) / cap;
-  if (S < s_min) S = s_min;
   if (S < 1) S = 1;
+  auto smem_of = [&](int s) {
+    const int nkb = (p->KB + s - 1) / s;
+    return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, ln);
+  };
+  while (smem_of(S) > kLinSmemMax && S < p->KB) ++S;  // fewer k-blocks per CTA
+  if (smem_of(S) > kLinSmemMax) return false;
   p->S = S;
   p->nkb_max = (p->KB + S - 1) / S;
   uint32_t cols = 32;
@@ -421,7 +570,7 @@ static bool lin_plan(int M, int N, int K, bool ln, int sms, LinPlan* p) {
   p->acc_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 128 * 4, 256) : 0;
   p->stats_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 2 * 4, 256) : 0;
   p->ws_bytes = S > 1 ? p->acc_bytes + p->stats_bytes + align_up((size_t)tiles * 4, 256) : 0;
-  p->smem = kLinSmemFixed + 2 * p->MT * 128 * p->nkb_max;
+  p->smem = smem_of(S);
   return true;
 }
 
@@ -467,7 +616,7 @@ extern "C" int asr_linear(const float* x, int64_t x_stride, const float* ln_g, c
   static cudaError_t attr = cudaSuccess;
   std::call_once(g_lin_attr, [] {
     attr = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kLinSmemFixed + kLinXCap);
+                                kLinSmemMax);
   });
   if (attr != cudaSuccess) return ASR_ERR_CUDA;
   CUtensorMap tw;
