@@ -510,7 +510,7 @@ class PrefillStep:
     causal tensor-core attention (a8) of B prompts of T tokens, one layer."""
 
     dominant = "prefill_attention"
-    dominant_kernel = "prefill_attn_kernel (tcgen05, asr_prefill_attention)"
+    dominant_kernel = "attn_tc_kernel<128,true> (tcgen05, asr_prefill_attention)"
     kernel_sources = PREFILL_SOURCES
     metric = "prefill tokens/s (tensor-core TFLOP/s and fraction of the f16 peak alongside)"
 
