@@ -70,8 +70,9 @@ def _lib():
             "orc_cross_kv_fill": (None, [_u16p, _u16p, _f32p, _int, _int, _int, _u16p, _i64]),
             "orc_layer_norm": (None, [_f32p, _i64, _f32p, _f32p, _dbl, _f64p]),
             "orc_gelu_erf": (_dbl, [_dbl]),
-            "orc_linear": (None, [_f32p, _i64, _int, _int, _f32p, _f32p, _dbl, _u16p, _int, _f32p,
-                                  _int, _f64p, _i64]),
+            "orc_silu": (_dbl, [_dbl]),
+            "orc_linear": (None, [_f32p, _i64, _int, _int, _int, _f32p, _f32p, _dbl, _int, _u16p,
+                                  _int, _f32p, _int, _f64p, _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -388,18 +389,29 @@ def gelu_erf(v):
     return np.vectorize(lambda t: f(float(t)), otypes=[np.float64])(v)
 
 
-def linear(x, w, bias=None, mode="store", ln=None, eps=1e-5, y=None):
-    """One dense step: a = LayerNorm(x) (ln = (g, b)) or x; v = a W^T + bias;
+def silu(v):
+    """SiLU v * sigmoid(v), elementwise on float64 values."""
+    v = np.asarray(v, np.float64)
+    f = _lib().orc_silu
+    return np.vectorize(lambda t: f(float(t)), otypes=[np.float64])(v)
+
+
+def linear(x, w, bias=None, mode="store", ln=None, eps=1e-5, y=None, rms=None, swiglu=False):
+    """One dense step: a = LayerNorm(x) (ln = (g, b)), RMSNorm(x) (rms = g),
+    silu(x[:, :K]) * x[:, K:] (swiglu) or x; v = a W^T + bias;
     mode "store" -> v, "residual" -> y + v, "gelu" -> gelu(v).
 
-    x: float32 [M, K]; w: uint16 (f16 bits) [N, K]; bias: float32 [N] or None;
-    y: the values the residual is added onto ([M, N]).  Returns float64 [M, N]."""
+    x: float32 [M, K] ([M, 2K] with swiglu); w: uint16 (f16 bits) [N, K];
+    bias: float32 [N] or None; y: the values the residual is added onto
+    ([M, N]).  Returns float64 [M, N]."""
     x = _c(np.ascontiguousarray(x, np.float32), np.float32)
     w = _c(w, np.uint16)
-    M, K = x.shape
-    N = w.shape[0]
-    if w.shape[1] != K:
-        raise ValueError("w must be [N, K]")
+    M = x.shape[0]
+    N, K = w.shape
+    if x.shape[1] != (2 * K if swiglu else K):
+        raise ValueError("x must be [M, K] ([M, 2K] with swiglu) for w [N, K]")
+    if sum(t is not None for t in (ln, rms)) + bool(swiglu) > 1:
+        raise ValueError("one of ln, rms, swiglu at most")
     m = LINEAR_MODES[mode]
     out = np.zeros((M, N), np.float64)
     if m == 1:
@@ -411,12 +423,19 @@ def linear(x, w, bias=None, mode="store", ln=None, eps=1e-5, y=None):
         bias = _c(np.ascontiguousarray(bias, np.float32), np.float32)
         bp = _p(bias, ctypes.c_float)
     gp = bq = None
+    norm = 0
     if ln is not None:
+        norm = 1
         g = _c(np.ascontiguousarray(ln[0], np.float32), np.float32)
         b = _c(np.ascontiguousarray(ln[1], np.float32), np.float32)
         gp, bq = _p(g, ctypes.c_float), _p(b, ctypes.c_float)
-    _lib().orc_linear(_p(x, ctypes.c_float), K, M, K, gp, bq, float(eps), _p(w, ctypes.c_uint16),
-                      N, bp, m, _p(out, ctypes.c_double), N)
+    elif rms is not None:
+        norm = 2
+        g = _c(np.ascontiguousarray(rms, np.float32), np.float32)
+        gp = _p(g, ctypes.c_float)
+    _lib().orc_linear(_p(x, ctypes.c_float), x.shape[1], M, K, norm, gp, bq, float(eps),
+                      1 if swiglu else 0, _p(w, ctypes.c_uint16), N, bp, m,
+                      _p(out, ctypes.c_double), N)
     return out
 
 
@@ -457,6 +476,39 @@ def whisper_decoder_layer_step(x, p, cache, lens, cross, group, heads, head_dim,
     return x3, {"qkv": qkv, "att": att, "x1": x1, "qx": qx, "attc": attc, "x2": x2, "h": h}
 
 
+def qwen3_decoder_layer_step(x, p, cache, n_past, q_heads, kv_heads, head_dim, eps=1e-6,
+                             rope_base=1e6):
+    """One Qwen3-ASR decoder layer for one new token per sequence
+    ("transcribe.cpp, src/arch/qwen3_asr/decoder.h", header comment and
+    StepBuildBatched): pre-norm RMSNorm (eps 1e-6), the q/k/v projections,
+    the GQA step (per-head Q/K RMSNorm, NeoX RoPE at base 1e6, K/V written at
+    row n_past, attention over rows [0, n_past]), the output projection onto
+    the residual, then RMSNorm and the SwiGLU MLP down(silu(gate(x)) * up(x))
+    onto the residual.  No projection has a bias.
+
+    Each step computes in double and stores its result as float32 (the
+    buffers between steps are f32), the cache row as f16.  x: float32 [B, d];
+    p: w_qkv [(Hq + 2 Hkv) hd, d] (q rows, then k, then v), w_o [d, Hq hd],
+    w_gu [2 I, d] (gate rows, then up rows), w_down [d, I] (f16 bits),
+    rms1, rms2 float32 [d], q_norm, k_norm float32 [hd]; cache: uint16
+    [B, capacity, 2 Hkv hd] (row n_past written in place); n_past: int32 [B].
+    Returns (x_out float32 [B, d], intermediates)."""
+    f32 = np.float32
+    x = np.ascontiguousarray(x, f32)
+    nq, nk = q_heads * head_dim, kv_heads * head_dim
+    qkv = linear(x, p["w_qkv"], None, rms=p["rms1"], eps=eps).astype(f32)
+    q = np.ascontiguousarray(qkv[:, :nq])
+    k = np.ascontiguousarray(qkv[:, nq:nq + nk])
+    v = np.ascontiguousarray(qkv[:, nq + nk:])
+    att, _ = gqa_step(q, k, v, p["q_norm"], p["k_norm"], eps, rope_base, n_past, cache, q_heads,
+                      kv_heads, head_dim, head_dim ** -0.5)
+    att = att.astype(f32)
+    x1 = linear(att, p["w_o"], None, mode="residual", y=x).astype(f32)
+    gu = linear(x1, p["w_gu"], None, rms=p["rms2"], eps=eps).astype(f32)
+    x2 = linear(gu, p["w_down"], None, mode="residual", y=x1, swiglu=True).astype(f32)
+    return x2, {"qkv": qkv, "att": att, "x1": x1, "gu": gu}
+
+
 def build():
     """Compile liboracle.so (the checker) if it is missing or stale."""
     return _build.build()
@@ -466,7 +518,8 @@ __all__ = [
     "set_threads", "get_threads", "f16_to_f64", "f32_to_f16", "f64_to_f16", "attend_one",
     "rmsnorm", "rope_neox", "kv_append", "self_attn_step", "cross_attn_step", "gqa_step",
     "kv_rearrange", "prefill_prep", "prefill_attn", "prefill_attn_rows", "mha_attn", "cross_kv_fill",
-    "layer_norm", "gelu_erf", "linear", "whisper_decoder_layer_step", "build",
+    "layer_norm", "gelu_erf", "silu", "linear", "whisper_decoder_layer_step",
+    "qwen3_decoder_layer_step", "build",
 ]
 
 if os.environ.get("ORACLE_THREADS"):

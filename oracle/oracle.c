@@ -758,13 +758,20 @@ void orc_layer_norm(const float* x, int64_t K, const float* g, const float* b, d
  *   gelu(v) = v * Phi(v) = v / 2 * (1 + erf(v / sqrt(2))). */
 double orc_gelu_erf(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
 
+/* SiLU, the gate of the SwiGLU MLP ("transcribe.cpp,
+ * src/arch/qwen3_asr/decoder.h", header comment: down_proj(silu(gate_proj(x))
+ * * up_proj(x))): silu(v) = v * sigmoid(v) = v / (1 + e^-v). */
+double orc_silu(double v) { return v / (1.0 + exp(-v)); }
+
 typedef struct {
   const float* x;
   int64_t x_stride;
   int K, N;
+  int norm; /* 0 none, 1 LayerNorm, 2 RMSNorm */
   const float* ln_g;
   const float* ln_b;
   double eps;
+  int act; /* 0 none, 1 SwiGLU input */
   const double* w; /* decoded weights [N][K] */
   const float* bias;
   int mode;
@@ -776,8 +783,20 @@ static void orc_linear_item(void* vctx, int64_t m) {
   orc_linear_ctx* c = (orc_linear_ctx*)vctx;
   const float* xm = c->x + m * c->x_stride;
   double* a = (double*)malloc(sizeof(double) * c->K);
-  if (c->ln_g) {
+  if (c->norm == 1) {
     orc_layer_norm(xm, c->K, c->ln_g, c->ln_b, c->eps, a);
+  } else if (c->norm == 2) {
+    double* xd = (double*)malloc(sizeof(double) * c->K);
+    double* wd = (double*)malloc(sizeof(double) * c->K);
+    for (int k = 0; k < c->K; ++k) {
+      xd[k] = (double)xm[k];
+      wd[k] = (double)c->ln_g[k];
+    }
+    orc_rmsnorm(xd, wd, c->eps, c->K, a);
+    free(xd);
+    free(wd);
+  } else if (c->act == 1) {
+    for (int k = 0; k < c->K; ++k) a[k] = orc_silu((double)xm[k]) * (double)xm[c->K + k];
   } else {
     for (int k = 0; k < c->K; ++k) a[k] = (double)xm[k];
   }
@@ -800,19 +819,22 @@ static void orc_linear_item(void* vctx, int64_t m) {
 
 /* One dense step of a decoder layer ("wavo 0.1.0, src/whisper/decoder.rs",
  * Decoder::record_step: `layer_norm` into y, then `gemv` of y with a weight
- * and one of the epilogues Bias, Residual(1.0) or Gelu):
- *   a_m = LayerNorm(x_m; ln_g, ln_b, eps) if ln_g is given, else x_m;
+ * and one of the epilogues Bias, Residual(1.0) or Gelu; "transcribe.cpp,
+ * src/arch/qwen3_asr/decoder.h", header comment: pre-norm RMSNorm and the
+ * SwiGLU MLP):
+ *   a_m = LayerNorm(x_m; ln_g, ln_b, eps) (norm 1), RMSNorm(x_m; ln_g, eps)
+ *         (norm 2), silu(x_m[0..K)) * x_m[K..2K) (act 1, no norm), else x_m;
  *   v_mn = sum_k a_mk * W[n][k] + bias_n  (bias may be NULL: 0);
  *   mode 0: y_mn = v_mn;  mode 1: y_mn = y_mn + v_mn;  mode 2: y_mn = gelu(v_mn).
  * x: fp32 [M][x_stride] (K used); W: f16 [N][K] (row n makes output n);
  * y: double [M][y_stride].  The activations are used as their fp32 values
  * (the pages' buffers are f32); every sum is in double. */
-void orc_linear(const float* x, int64_t x_stride, int M, int K, const float* ln_g,
-                const float* ln_b, double eps, const uint16_t* w, int N, const float* bias, int mode,
-                double* y, int64_t y_stride) {
+void orc_linear(const float* x, int64_t x_stride, int M, int K, int norm, const float* ln_g,
+                const float* ln_b, double eps, int act, const uint16_t* w, int N, const float* bias,
+                int mode, double* y, int64_t y_stride) {
   double* wd = (double*)malloc(sizeof(double) * (size_t)N * (size_t)K);
   for (int64_t i = 0; i < (int64_t)N * K; ++i) wd[i] = orc_f16_to_f64(w[i]);
-  orc_linear_ctx c = {x, x_stride, K, N, ln_g, ln_b, eps, wd, bias, mode, y, y_stride};
+  orc_linear_ctx c = {x, x_stride, K, N, norm, ln_g, ln_b, eps, act, wd, bias, mode, y, y_stride};
   orc_parallel_for(M, orc_linear_item, &c);
   free(wd);
 }

@@ -710,3 +710,88 @@ def test_decoder_layer_step_residuals_and_cache(oracle_mod):
     attc, _ = oracle_mod.cross_attn_step(mid["qx"], cross, group, H, hd, scale)
     assert np.array_equal(xo, (mid["x1"].astype(np.float64) + attc.astype(np.float32)).astype(
         np.float32))
+
+
+def test_silu_values(oracle_mod):
+    """silu(v) = v * sigmoid(v): silu(0) = 0, silu(1) = 1/(1 + 1/e) =
+    0.7310585786300049, silu(v) - silu(-v) = v, and silu(30) = 30 - 2.807e-12
+    (30 e^-30 below 30)."""
+    np.testing.assert_allclose(oracle_mod.silu([0.0, 1.0, -1.0, 30.0]),
+                               [0.0, 0.7310585786300049, -0.2689414213699951, 29.999999999997193],
+                               rtol=0, atol=1e-14)
+    v = syn.host_normal_f32(40, 90, std=4.0).astype(np.float64)
+    np.testing.assert_allclose(oracle_mod.silu(v) - oracle_mod.silu(-v), v, atol=1e-13)
+
+
+def test_linear_rms_and_swiglu(oracle_mod):
+    """RMSNorm before the product equals the (pinned) per-vector RMSNorm of
+    each row, then numpy's matmul; a row of equal values c normalises to
+    c/sqrt(c^2 + eps) * w; the SwiGLU input is silu(gate) * up of the two
+    halves of each row (numpy brute force with the closed-form sigmoid)."""
+    M, K, N = 3, 64, 24
+    x = syn.host_normal_f32((M, K), 91, mean=0.2, std=1.3)
+    w = f16(syn.host_normal_f32((N, K), 92) * K ** -0.5)
+    g = syn.host_normal_f32(K, 93, mean=1.0, std=0.1)
+    eps = 1e-6
+    a = np.stack([oracle_mod.rmsnorm(x[m].astype(np.float64), g.astype(np.float64), eps)
+                  for m in range(M)])
+    np.testing.assert_allclose(oracle_mod.linear(x, w, None, rms=g, eps=eps), a @ dec(w).T,
+                               rtol=0, atol=1e-12)
+    c = np.float32(1.75)
+    flat = np.full((1, K), c, np.float32)
+    want = (float(c) / math.sqrt(float(c) ** 2 + eps) * g.astype(np.float64)) @ dec(w).T
+    np.testing.assert_allclose(oracle_mod.linear(flat, w, None, rms=g, eps=eps)[0], want,
+                               rtol=0, atol=1e-12)
+    xg = syn.host_normal_f32((M, 2 * K), 94, std=2.0)
+    gate, up = xg[:, :K].astype(np.float64), xg[:, K:].astype(np.float64)
+    act = gate / (1.0 + np.exp(-gate)) * up
+    y0 = syn.host_normal_f32((M, N), 95)
+    np.testing.assert_allclose(oracle_mod.linear(xg, w, None, mode="residual", y=y0, swiglu=True),
+                               y0 + act @ dec(w).T, rtol=0, atol=1e-12)
+
+
+def test_qwen3_decoder_layer_step_residuals_and_cache(oracle_mod):
+    """With the output and down projections zero the layer leaves x
+    unchanged; the new k, v land in cache row n_past as the GQA step writes
+    them; otherwise the attention output goes through w_o onto the stream and
+    the MLP adds silu(gate) * up through w_down (numpy brute force)."""
+    B, Hq, Hkv, hd, cap, d, inner = 2, 4, 2, 64, 8, 128, 192
+    x = syn.host_normal_f32((B, d), 96)
+    n_past = np.array([0, 5], np.int32)
+    cache0 = syn.host_normal_f16bits((B, cap, 2 * Hkv * hd), 97)
+    nq, nk = Hq * hd, Hkv * hd
+
+    def params(seed, zero_out):
+        p = {"w_qkv": f16(syn.host_normal_f32((nq + 2 * nk, d), seed) * d ** -0.5),
+             "w_o": f16(np.zeros((d, nq), np.float32) if zero_out else
+                        syn.host_normal_f32((d, nq), seed + 1) * nq ** -0.5),
+             "w_gu": f16(syn.host_normal_f32((2 * inner, d), seed + 2) * d ** -0.5),
+             "w_down": f16(np.zeros((d, inner), np.float32) if zero_out else
+                           syn.host_normal_f32((d, inner), seed + 3) * inner ** -0.5),
+             "rms1": syn.host_normal_f32(d, seed + 4, mean=1.0, std=0.1),
+             "rms2": syn.host_normal_f32(d, seed + 5, mean=1.0, std=0.1),
+             "q_norm": syn.host_normal_f32(hd, seed + 6, mean=1.0, std=0.1),
+             "k_norm": syn.host_normal_f32(hd, seed + 7, mean=1.0, std=0.1)}
+        return p
+
+    p = params(100, True)
+    cache = cache0.copy()
+    xo, mid = oracle_mod.qwen3_decoder_layer_step(x, p, cache, n_past, Hq, Hkv, hd)
+    assert np.array_equal(xo, x)
+    ref = cache0.copy()
+    qkv = mid["qkv"]
+    oracle_mod.gqa_step(np.ascontiguousarray(qkv[:, :nq]), np.ascontiguousarray(qkv[:, nq:nq + nk]),
+                        np.ascontiguousarray(qkv[:, nq + nk:]), p["q_norm"], p["k_norm"], 1e-6,
+                        1e6, n_past, ref, Hq, Hkv, hd, hd ** -0.5)
+    assert np.array_equal(cache, ref)
+    # non-zero output and down projections: each adds its product onto the stream
+    p = params(200, False)
+    cache = cache0.copy()
+    xo, mid = oracle_mod.qwen3_decoder_layer_step(x, p, cache, n_past, Hq, Hkv, hd)
+    x1 = (x.astype(np.float64) + mid["att"].astype(np.float64) @ dec(p["w_o"]).T).astype(
+        np.float32)
+    np.testing.assert_allclose(mid["x1"], x1, rtol=0, atol=1e-6)
+    gate, up = mid["gu"][:, :inner].astype(np.float64), mid["gu"][:, inner:].astype(np.float64)
+    x2 = (x1.astype(np.float64) + (gate / (1 + np.exp(-gate)) * up) @ dec(p["w_down"]).T).astype(
+        np.float32)
+    np.testing.assert_allclose(xo, x2, rtol=0, atol=1e-6)
