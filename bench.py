@@ -1021,6 +1021,158 @@ class DecoderStep(WhisperStep):
         return time.perf_counter() - t0
 
 
+class QwenDecoderStep(GqaStep):
+    """The whole Qwen3-ASR decoder step around the GQA step, five launches
+    per layer (kv_cache_decode_asr_gb300.decoder.qwen3_decoder_layer):
+    RMSNorm + q/k/v, the fused GQA step, the output projection, RMSNorm +
+    gate/up, SwiGLU + down.  The step starts from its input x (the embedded
+    token, a device copy) and ends with the residual stream after the last
+    layer."""
+
+    dominant = "gqa"
+    dominant_kernel = "decode_attn_kernel<128,2> (asr_gqa_step)"
+    e2e_via_graph = True
+
+    def __init__(self, name, cfg, device, rank=0):
+        from kv_cache_decode_asr_gb300 import decoder
+        super().__init__(name, cfg, device, rank)
+        self.decoder = decoder
+        wi = rank_seed_base(name, rank)
+        self.d, self.inner = cfg["d"], cfg["inner"]
+        self.p = syn.dev_qwen_layer_params(self.L, self.d, self.inner, self.Hq, self.Hkv, self.hd,
+                                           syn.seed_for(wi, 20), device)
+        self.pl = [{k: v[l] for k, v in self.p.items()} for l in range(self.L)]
+        self.x_in = syn.dev_normal((self.B, self.d), syn.seed_for(wi, 21), device)
+        self.x = self.x_in.clone()
+        self.bufs = decoder.QwenDecoderBuffers(self.B, self.d, self.inner, self.Hq, self.Hkv,
+                                               self.hd, device)
+        self.snaps = None
+        self.metric = ("decoder-step tokens/s: the whole Qwen3-ASR decoder step "
+                       "(dense layers + GQA step; step K/V+weight HBM GB/s alongside)")
+
+    def launches(self):
+        return self.decoder.QWEN_LAUNCHES_PER_LAYER * self.L
+
+    def layer(self, l, stream=None):
+        self.decoder.qwen3_decoder_layer(self.x, self.pl[l], self.cache[l], self.n_past, self.bufs,
+                                         eps=self.eps, rope_base=self.base, dev_err=self.err,
+                                         stream=stream)
+
+    def step(self, stream=None):
+        self.x.copy_(self.x_in)
+        for l in range(self.L):
+            self.layer(l, stream)
+
+    def dense_bytes_per_layer(self):
+        """The four dense launches of a layer: weights, norm vectors, and the
+        activations read and written."""
+        B, d, I, nq, nk = self.B, self.d, self.inner, self.Hq * self.hd, self.Hkv * self.hd
+        w = 2 * ((nq + 2 * nk) * d + d * nq + 2 * I * d + d * I) + 4 * 2 * d
+        act = 4 * B * ((d + nq + 2 * nk) + (nq + 2 * d) + (d + 2 * I) + (2 * I + 2 * d))
+        return w + act
+
+    def kv_bytes_per_step(self):
+        return super().kv_bytes_per_step() + self.L * self.dense_bytes_per_layer()
+
+    def extra_rooflines(self, stream, peaks):
+        import torch
+        ops, bufs, x = self.ops, self.bufs, self.x
+        wl = bufs.ws_lin
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(self.L):
+                p = self.pl[l]
+                ops.asr_linear(x, p["w_qkv"], bufs.qkv, rms=p["rms1"], eps=self.eps, ws=wl,
+                               dev_err=self.err)
+                ops.asr_linear(bufs.att, p["w_o"], x, mode="residual", ws=wl, dev_err=self.err)
+                ops.asr_linear(x, p["w_gu"], bufs.gu, rms=p["rms2"], eps=self.eps, ws=wl,
+                               dev_err=self.err)
+                ops.asr_linear(bufs.gu, p["w_down"], x, swiglu=True, mode="residual", ws=wl,
+                               dev_err=self.err)
+        reps = 20
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        layer_ms = e0.elapsed_time(e1) / (reps * self.L)
+        peak, src = peaks["hbm"]
+        b = self.dense_bytes_per_layer()
+        achieved = b / (layer_ms / 1e3) / 1e9
+        return {"roofline_dense": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "bytes_per_layer": b, "launches_per_layer": 4,
+            "us_per_layer": layer_ms * 1e3, "us_per_launch": layer_ms * 1e3 / 4,
+            "kernel": "linear_kernel (asr_linear: RMSNorm / SwiGLU + tcgen05 product)",
+            "traffic": None, "peak_source": f"{src} hbm_gbs"}}
+
+    def host_io(self):
+        return [self.x_in], [self.x]
+
+    def _host_layer(self, l):
+        import torch
+        out = {}
+        for k, v in self.pl[l].items():
+            if v.dtype == torch.float16:
+                out[k] = v.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            else:
+                out[k] = v.contiguous().cpu().numpy()
+        return out
+
+    def _snapshots(self):
+        import torch
+        if self.snaps is None:
+            torch.cuda.synchronize()
+            self.x.copy_(self.x_in)
+            snaps = [self.x.clone()]
+            for l in range(self.L):
+                self.layer(l)
+                snaps.append(self.x.clone())
+            torch.cuda.synchronize()
+            self.snaps = [t.cpu().numpy() for t in snaps]
+        return self.snaps
+
+    def oracle_sample(self, i, oracle):
+        """Layer i of every sequence, from the GPU's input to that layer."""
+        import torch
+        snaps = self._snapshots()
+        p = self._host_layer(i)
+        cache = self.cache[i].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        ref, _ = oracle.qwen3_decoder_layer_step(snaps[i], p, cache, self.n_past_host, self.Hq,
+                                                 self.Hkv, self.hd, eps=self.eps,
+                                                 rope_base=self.base)
+        dt = time.perf_counter() - t0
+        return dt, 1.0 / self.L, {"x": ref}, {"x": snaps[i + 1]}, f"layer {i}"
+
+    def oracle_unit(self, i, oracle, cache):
+        """Reference-arm unit: one sequence through one layer."""
+        import torch
+        l = i % self.L
+        b = (i // self.L) % self.B
+        if cache.get("layer") != l:
+            cache.clear()
+            cache["layer"] = l
+            cache["p"] = self._host_layer(l)
+        key = ("seq", b)
+        if key not in cache:
+            cache[key] = (
+                self.cache[l, b:b + 1].contiguous().view(torch.int16).cpu().numpy()
+                .view(np.uint16),
+                self.x_in[b:b + 1].cpu().numpy())
+        c, x = cache[key]
+        c = c.copy()
+        t0 = time.perf_counter()
+        oracle.qwen3_decoder_layer_step(x, cache["p"], c, self.n_past_host[b:b + 1], self.Hq,
+                                        self.Hkv, self.hd, eps=self.eps, rope_base=self.base)
+        return time.perf_counter() - t0
+
+
 def make_workload(name, device, rank=0, layers=0):
     cfg = dict(syn.WORKLOADS[name])
     if layers:
@@ -1037,6 +1189,8 @@ def make_workload(name, device, rank=0, layers=0):
         return CrossFillStep(name, cfg, device, rank)
     if cfg["kind"] == "decoder_step":
         return DecoderStep(name, cfg, device, rank)
+    if cfg["kind"] == "qwen_decoder_step":
+        return QwenDecoderStep(name, cfg, device, rank)
     raise SystemExit(f"workload {name}: not a decode-step bench line")
 
 

@@ -86,6 +86,19 @@ enum asr_linear_mode {
   ASR_LINEAR_GELU = 2,     /* y = v * Phi(v)   (Epilogue::Gelu, the erf form) */
 };
 
+/* Pre-norms of asr_linear. */
+enum asr_norm {
+  ASR_NORM_NONE = 0,
+  ASR_NORM_LAYER = 1, /* LayerNorm: (x - mean) / sqrt(var + eps) * w + b */
+  ASR_NORM_RMS = 2,   /* RMSNorm:   x / sqrt(mean(x^2) + eps) * w */
+};
+
+/* Input activations of asr_linear. */
+enum asr_act {
+  ASR_ACT_NONE = 0,
+  ASR_ACT_SWIGLU = 1, /* a_k = silu(x_k) * x_{K+k}: rows hold [gate | up], 2K values */
+};
+
 /* Limits checked on the host. */
 #define ASR_MAX_BATCH 2048 /* sequences (and groups) per call */
 #define ASR_MAX_BEAMS 8    /* sequences sharing one cross source; also max Hq/Hkv */
@@ -174,14 +187,16 @@ int asr_cross_attn_step(const float* q, int64_t q_stride, const uint16_t* cross,
  *   cache row p = f16(k^) || f16(v_new_b)                    (written by this call)
  *   out_bh = attention of q^_h over rows [0, p] of KV head h / (Hq/Hkv)
  *   RoPE_p turns the pair (i, i + hd/2) by p * rope_base^(-2i/hd).
- * q: fp32 [B][q_heads*hd]; k_new, v_new: fp32 [B][kv_heads*hd]; q_norm_w,
+ * q: fp32 [B][q_stride] (q_heads*hd used); k_new, v_new: fp32 [B][kv_stride]
+ * (kv_heads*hd used; one stride for both; strides % 4 == 0); q_norm_w,
  * k_norm_w: fp32 [hd] (shared by all heads); n_past: int32 [B], device, in
  * [0, capacity) (else output zeroed, cache untouched, ASR_DEVERR_LEN);
  * out: fp32 [B][q_heads*hd].  head_dim in {64, 128}; q_heads % kv_heads == 0;
  * q_heads/kv_heads <= ASR_MAX_BEAMS.
  * ws: asr_workspace_size(ASR_OP_GQA_STEP, B, B, 1, q_heads, head_dim, 0) bytes. */
-int asr_gqa_step(const float* q, const float* k_new, const float* v_new, const float* q_norm_w,
-                 const float* k_norm_w, float eps, float rope_base, const int32_t* n_past,
+int asr_gqa_step(const float* q, int64_t q_stride, const float* k_new, const float* v_new,
+                 int64_t kv_stride, const float* q_norm_w, const float* k_norm_w, float eps,
+                 float rope_base, const int32_t* n_past,
                  uint16_t* cache, int64_t seq_stride, int capacity, int B, int q_heads,
                  int kv_heads, int head_dim, float scale, float* out, void* ws, size_t ws_bytes,
                  int32_t* dev_err, asr_stream_t stream);
@@ -308,34 +323,44 @@ int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_
  * (layer_norm of x, then gemv with the layer's qkv / self_out / cross_q /
  * cross_out / fc1 / fc2 weight and the epilogue Bias, Residual(1.0) or
  * Gelu); "Nest whisper-tiny, src/lib.linnet", LayerNorm (torch.nn.LayerNorm,
- * eps 1e-5) and Mlp (fc2(gelu_erf(fc1(x)))).
- *   a_m  = (x_m - mean_m) / sqrt(var_m + eps) * ln_g + ln_b   if ln_g != NULL
- *          (mean and biased variance over the K values of row m), else x_m
+ * eps 1e-5) and Mlp (fc2(gelu_erf(fc1(x)))); "transcribe.cpp,
+ * src/arch/qwen3_asr/decoder.h", header comment (pre-norm RMSNorm
+ * weight * rsqrt(mean(x^2) + eps) * x; SwiGLU MLP down(silu(gate(x)) * up(x))).
+ *   a_m  = x_m                                  norm ASR_NORM_NONE
+ *        = (x_m - mean_m) / sqrt(var_m + eps) * norm_w + norm_b   ASR_NORM_LAYER
+ *          (mean and biased variance over the K values of row m)
+ *        = x_m / sqrt(mean_k x_mk^2 + eps) * norm_w                ASR_NORM_RMS
+ *   with act ASR_ACT_SWIGLU (no norm): a_mk = silu(x_mk) * x_m,K+k, silu(v) =
+ *   v / (1 + e^-v): the row holds the gate half then the up half.
  *   v_mn = sum_k a_mk * w[n][k] + bias[n]                     (bias NULL: 0)
  *   y_mn = v_mn (ASR_LINEAR_STORE) | y_mn + v_mn (ASR_LINEAR_RESIDUAL)
  *        | v_mn * Phi(v_mn) = v/2 (1 + erf(v/sqrt 2)) (ASR_LINEAR_GELU)
- * x: fp32 [M][x_stride] (the first K used; 16-byte aligned, x_stride % 4 ==
- * 0); ln_g, ln_b: fp32 [K] (both or neither; 16-byte aligned); w: f16 [N][K]
- * (row n makes output n: torch's Linear layout; 16-byte aligned); bias: fp32
- * [N] or NULL; y: fp32 [M][y_stride] (the first N written), and y must not
- * overlap x (ASR_ERR_ALIAS).  K % 64 == 0 (else ASR_ERR_UNSUPPORTED).
+ * x: fp32 [M][x_stride] (the first K values used, 2K with SwiGLU; 16-byte
+ * aligned, x_stride % 4 == 0); norm_w, norm_b: fp32 [K] (16-byte aligned;
+ * norm_b only for LayerNorm); w: f16 [N][K] (row n makes output n: torch's
+ * Linear layout; 16-byte aligned); bias: fp32 [N] or NULL; y: fp32
+ * [M][y_stride] (the first N written), and y must not overlap x
+ * (ASR_ERR_ALIAS).  K % 64 == 0 and SwiGLU without a norm (else
+ * ASR_ERR_UNSUPPORTED).
  * Numerics: the activations enter the tensor cores as two f16 parts (a = hi
  * + lo, both multiplied by the f16 weight), so they keep about 22 bits; the
- * sums are fp32 (with the K axis split across CTAs, a residual without
- * LayerNorm adds the parts onto y in an unspecified order, so repeated calls
- * may differ in the last bits).  The LayerNorm is folded into the product (the operand is
- * (x - x_0) * ln_g with x_0 the row's first element; the row statistics and
- * the ln_g / ln_b terms are applied after the sum), which is the same
- * function up to fp32 rounding.  ws: asr_linear_workspace_size(M, N, K) bytes, zero-filled
- * before first use and 256-byte aligned (NULL allowed when that size is 0);
- * every call leaves it zero again unless a wait times out
- * (ASR_DEVERR_TIMEOUT), after which it must be zeroed before reuse.  The
+ * sums are fp32 (with the K axis split across CTAs, a residual without a
+ * norm adds the parts onto y in an unspecified order, so repeated calls may
+ * differ in the last bits).  The norms are folded into the product (the
+ * operand is (x - x_0) * norm_w for LayerNorm, x_0 the row's first element,
+ * and x * norm_w for RMSNorm; the row statistics and the norm_b terms are
+ * applied after the sum), which is the same function up to fp32 rounding.
+ * ws: asr_linear_workspace_size(M, N, K) bytes (the largest any norm or input
+ * needs), zero-filled before first use and 256-byte aligned (NULL allowed
+ * when that size is 0); every call leaves it zero again unless a wait times
+ * out (ASR_DEVERR_TIMEOUT), after which it must be zeroed before reuse.  The
  * weight is read before the previous kernel on the stream has finished when
  * that kernel is one of this library's (none of them writes a weight). */
 size_t asr_linear_workspace_size(int M, int N, int K);
-int asr_linear(const float* x, int64_t x_stride, const float* ln_g, const float* ln_b, float eps,
-               const uint16_t* w, const float* bias, int M, int N, int K, int mode, float* y,
-               int64_t y_stride, void* ws, size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
+int asr_linear(const float* x, int64_t x_stride, int norm, const float* norm_w,
+               const float* norm_b, float eps, int act, const uint16_t* w, const float* bias,
+               int M, int N, int K, int mode, float* y, int64_t y_stride, void* ws,
+               size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
 /* Self-attention without a caller workspace (no counterpart in the pages: it
  * is a convenience of this library).  For callers that cannot allocate device

@@ -1256,9 +1256,10 @@ extern "C" int asr_cross_attn_step(const float* q, int64_t q_stride, const uint1
   return launch_decode(a, head_dim, max_beams, ws, ws_bytes, (cudaStream_t)stream);
 }
 
-extern "C" int asr_gqa_step(const float* q, const float* k_new, const float* v_new,
-                            const float* q_norm_w, const float* k_norm_w, float eps,
-                            float rope_base, const int32_t* n_past, uint16_t* cache,
+extern "C" int asr_gqa_step(const float* q, int64_t q_stride, const float* k_new,
+                            const float* v_new, int64_t kv_stride, const float* q_norm_w,
+                            const float* k_norm_w, float eps, float rope_base,
+                            const int32_t* n_past, uint16_t* cache,
                             int64_t seq_stride, int capacity, int B, int q_heads, int kv_heads,
                             int head_dim, float scale, float* out, void* ws, size_t ws_bytes,
                             int32_t* dev_err, asr_stream_t stream) {
@@ -1272,14 +1273,17 @@ extern "C" int asr_gqa_step(const float* q, const float* k_new, const float* v_n
   if (!q || !k_new || !v_new || !q_norm_w || !k_norm_w || !n_past || !cache || !out)
     return ASR_ERR_INVALID_ARG;
   const int64_t row = 2LL * kv_heads * head_dim;
-  if (seq_stride < (int64_t)capacity * row) return ASR_ERR_INVALID_ARG;
+  if (seq_stride < (int64_t)capacity * row || q_stride < (int64_t)q_heads * head_dim ||
+      kv_stride < (int64_t)kv_heads * head_dim)
+    return ASR_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_norm_w) ||
-      !aligned16(k_norm_w) || !aligned16(cache) || !aligned16(out) || seq_stride % 8 != 0)
+      !aligned16(k_norm_w) || !aligned16(cache) || !aligned16(out) || seq_stride % 8 != 0 ||
+      q_stride % 4 != 0 || kv_stride % 4 != 0)
     return ASR_ERR_MISALIGNED;
   if (!rows_fit_int(B, capacity)) return ASR_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   a.q = q;
-  a.q_stride = (int64_t)q_heads * head_dim;
+  a.q_stride = q_stride;
   a.kv = cache;
   a.cache_w = cache;
   a.src_stride = seq_stride;
@@ -1297,7 +1301,7 @@ extern "C" int asr_gqa_step(const float* q, const float* k_new, const float* v_n
   a.dev_err = dev_err;
   a.mode = kModeGqa;
   a.append = 1;
-  a.kv_stride = (int64_t)kv_heads * head_dim;
+  a.kv_stride = kv_stride;
   a.k_new = k_new;
   a.v_new = v_new;
   a.wq = q_norm_w;

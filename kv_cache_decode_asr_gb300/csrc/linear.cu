@@ -65,18 +65,25 @@ constexpr int kLinSmemFixed = 1024 + kLinStages * kLinWTile + 256 + 4 * kLinMaxM
 constexpr int kLinSmemMax = 232448;      // the largest dynamic shared memory of one CTA
 
 // Bytes of the fp32 staging of one CTA: MR rows of its K range (nkb_max
-// k-blocks of 64), and with LayerNorm the same range of g and b and 16
+// k-blocks of 64; twice that for a SwiGLU input: gate and up), with a norm
+// the same range of its weight, and with LayerNorm also of its bias and 16
 // bytes of each row's head.
-__host__ __device__ constexpr int lin_f32_bytes(int MR, int nkb_max, bool ln) {
-  return ((MR * (nkb_max * 64 + 4) + (ln ? 2 * (nkb_max * 64 + 4) + MR * 4 : 0)) * 4 + 15) / 16 *
-         16;
+__host__ __device__ constexpr int lin_f32_bytes(int MR, int nkb_max, int norm, bool glu) {
+  return ((MR * (nkb_max * 64 + 4) * (glu ? 2 : 1) +
+           (norm != ASR_NORM_NONE ? (nkb_max * 64 + 4) : 0) +
+           (norm == ASR_NORM_LAYER ? (nkb_max * 64 + 4) + MR * 4 : 0)) *
+              4 +
+          15) /
+         16 * 16;
 }
 
 struct LinArgs {
   const float* x;
   int64_t x_stride;
-  const float* ln_g;
-  const float* ln_b;
+  const float* norm_w;  // LayerNorm / RMSNorm weight [K] (NULL: no norm)
+  const float* norm_b;  // LayerNorm bias [K]
+  int norm;             // ASR_NORM_*
+  int act;              // ASR_ACT_*
   float eps;
   const float* bias;
   float* y;
@@ -117,12 +124,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Row statistics of the LayerNorm from the K-sums of the values shifted by
-// the row's first element x_0: s1 = sum (x - x_0), s2 = sum (x - x_0)^2.
-// dm = mean - x_0 and rstd = 1 / sqrt(var + eps), var = s2/K - (s1/K)^2.
+// Row statistics from K-sums.  LayerNorm: of the values shifted by the row's
+// first element x_0, s1 = sum (x - x_0), s2 = sum (x - x_0)^2, so dm = mean -
+// x_0 and rstd = 1 / sqrt(var + eps), var = s2/K - (s1/K)^2.  RMSNorm: s2 =
+// sum x^2, dm = 0 and rstd = 1 / sqrt(s2/K + eps).
 __device__ __forceinline__ void lin_row_stats(float s1, float s2, float inv_k, float eps, int t,
-                                              float* s_dm, float* s_rs) {
-  const float dm = s1 * inv_k;
+                                              float* s_dm, float* s_rs, bool ln) {
+  const float dm = ln ? s1 * inv_k : 0.f;  // RMSNorm: the mean square, nothing subtracted
   const float var = fmaxf(s2 * inv_k - dm * dm, 0.f);
   s_dm[t] = dm;
   s_rs[t] = rsqrtf(var + eps);
@@ -141,15 +149,18 @@ __device__ __forceinline__ void lin_load_old(const LinArgs& a, int m_first, int 
 // Outputs (m_first + e, n) for e < cnt from the K-sums v[e]:
 //   LayerNorm: a_mk = ((x_mk - x_0) - dm) * rstd * g_k + b_k, so
 //   sum_k a_mk W_nk = rstd * (v - dm * cn) + dn with cn = sum_k g_k W_nk and
-//   dn = sum_k b_k W_nk; otherwise the sum is v itself.  Then bias, epilogue.
+//   dn = sum_k b_k W_nk; RMSNorm: a_mk = x_mk * rstd * g_k, so the sum is
+//   rstd * v; otherwise the sum is v itself.  Then bias, epilogue.
 __device__ __forceinline__ void lin_emit(const LinArgs& a, int m_first, int cnt, int n,
-                                         const float* v, const float* yo, float bn, bool ln,
+                                         const float* v, const float* yo, float bn, int norm,
                                          const float* dm, const float* rs, float cn, float dn) {
   if (n >= a.N) return;
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     if (e < cnt) {
-      const float t = ln ? rs[e] * (v[e] - dm[e] * cn) + dn : v[e];
+      const float t = norm == ASR_NORM_LAYER ? rs[e] * (v[e] - dm[e] * cn) + dn
+                      : norm == ASR_NORM_RMS ? rs[e] * v[e]
+                                             : v[e];
       a.y[(int64_t)(m_first + e) * a.y_stride + n] = lin_epilogue(a.mode, t + bn, yo[e]);
     }
   }
@@ -160,13 +171,15 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int MT = a.MT;
-  const bool ln = a.ln_g != nullptr;
+  const bool ln = a.norm == ASR_NORM_LAYER;  // the g and b operand rows, the x_0 shift
+  const bool nrm = a.norm != ASR_NORM_NONE;   // row statistics
+  const bool glu = a.act == ASR_ACT_SWIGLU;   // activations silu(gate) * up
   const int plane = MT * 128 * a.nkb_max;                  // bytes of one activation plane
   unsigned char* sW = smem;                                // stages x 16 KB
   unsigned char* sXh = sW + kLinStages * kLinWTile;        // hi plane: [nkb][MT rows][128 B]
   unsigned char* sXl = sXh + plane;                        // lo plane
   unsigned char* sFb = sXl + plane;                        // fp32 staging
-  const int f32b = lin_f32_bytes(a.MR, a.nkb_max, ln);
+  const int f32b = lin_f32_bytes(a.MR, a.nkb_max, a.norm, glu);
   uint64_t* full = reinterpret_cast<uint64_t*>(sFb + f32b);
   uint64_t* empty = full + kLinStages;
   uint64_t* xin_full = empty + kLinStages;  // the fp32 activations have landed
@@ -253,23 +266,24 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
     // memory as fp32: one round trip.
     const int RS = a.nkb_max * 64 + 4;  // floats per staged row (+4: rows start 16 banks apart)
     float* xs = reinterpret_cast<float*>(sFb);
-    float* gs = xs + a.MR * RS;
+    float* xu = xs + a.MR * RS;         // SwiGLU: the up half of each row
+    float* gs = xu + (glu ? a.MR * RS : 0);
     float* bs = gs + RS;
     float* hs = bs + RS;  // [MR][4]: x_0 of each row in hs[4 r]
     const uint32_t q_bytes = (uint32_t)nkb * 256;
     if (warp == 0) {
       if (lane == 0)
-        mbar_arrive_expect_tx(xin_full, Mv * q_bytes + (ln ? 2 * q_bytes + Mv * 16 : 0));
+        mbar_arrive_expect_tx(xin_full, Mv * q_bytes * (glu ? 2u : 1u) + (nrm ? q_bytes : 0u) +
+                                            (ln ? q_bytes + Mv * 16 : 0u));
       __syncwarp();
       for (int r = lane; r < Mv; r += 32) {
         const float* row = a.x + (int64_t)(m0 + r) * a.x_stride;
         bulk_g2s_plain(xs + r * RS, row + kb0 * 64, q_bytes, xin_full);
+        if (glu) bulk_g2s_plain(xu + r * RS, row + a.K + kb0 * 64, q_bytes, xin_full);
         if (ln) bulk_g2s_plain(hs + r * 4, row, 16, xin_full);
       }
-      if (ln && lane == 0) {
-        bulk_g2s_plain(gs, a.ln_g + kb0 * 64, q_bytes, xin_full);
-        bulk_g2s_plain(bs, a.ln_b + kb0 * 64, q_bytes, xin_full);
-      }
+      if (nrm && lane == 0) bulk_g2s_plain(gs, a.norm_w + kb0 * 64, q_bytes, xin_full);
+      if (ln && lane == 0) bulk_g2s_plain(bs, a.norm_b + kb0 * 64, q_bytes, xin_full);
     }
     if (!mbar_wait(xin_full, 0)) ok = false;
     // 2. The operand: MT rows x nkb k-blocks x eight 16-byte chunks; chunk c
@@ -288,8 +302,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
         if (r < Mv) srow = xs + r * RS;
         else if (ln && r == Mv) srow = gs;
         else if (ln && r == Mv + 1) srow = bs;
-        const bool act = ln && r < Mv;  // a LayerNorm-ed activation row
-        const float sh = act ? hs[r * 4] : 0.f;
+        const bool act = nrm && r < Mv;  // a normalised activation row
+        const float sh = (ln && r < Mv) ? hs[r * 4] : 0.f;
         float s1 = 0.f, s2 = 0.f;
 #pragma unroll 2
         for (int j = 0; j < nkb; ++j) {
@@ -304,9 +318,18 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
           }
+          if (glu && r < Mv) {
+            // SwiGLU: silu(gate) * up, silu(v) = v / (1 + e^-v)
+            const float4 w0 = *reinterpret_cast<const float4*>(xu + r * RS + ko);
+            const float4 w1 = *reinterpret_cast<const float4*>(xu + r * RS + ko + 4);
+            const float up[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = f[e] / (1.0f + expf(-f[e])) * up[e];
+          }
           if (act) {
-            // shifted values: their sum and sum of squares (the row
-            // statistics), and (x - x_0) * g as the operand
+            // shifted values (LayerNorm; RMSNorm: unshifted): their sum and
+            // sum of squares (the row statistics), and (x - x_0) * g as the
+            // operand
             const float4 g0 = *reinterpret_cast<const float4*>(gs + ko);
             const float4 g1 = *reinterpret_cast<const float4*>(gs + ko + 4);
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
@@ -332,7 +355,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
           *reinterpret_cast<uint4*>(sXh + off) = hv;
           *reinterpret_cast<uint4*>(sXl + off) = lv;
         }
-        if (ln) {
+        if (nrm) {
           // the eight lanes of one row share r
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) {
@@ -371,8 +394,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
             cn = tmem_ld1(taddr + Mv);
             dn = tmem_ld1(taddr + Mv + 1);
             tmem_wait_ld();
+          }
+          if (nrm) {
             for (int t = tid; t < Mv; t += 128)
-              lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs);
+              lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs, ln);
             named_bar(2, 128);
           }
           for (int c0 = 0; c0 < Mv; c0 += 32) {
@@ -382,9 +407,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
             if (c0 + 16 < MT) tmem_ld16(taddr + c0 + 16, v + 16);  // MT is a multiple of 16
             lin_load_old(a, m0 + c0, cnt, n, resid, yo);
             tmem_wait_ld();
-            lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+            lin_emit(a, m0 + c0, cnt, n, v, yo, bn, a.norm, s_dm + c0, s_rs + c0, cn, dn);
           }
-        } else if (a.mode == ASR_LINEAR_RESIDUAL && !ln) {
+        } else if (a.mode == ASR_LINEAR_RESIDUAL && !nrm) {
           // a residual without LayerNorm is linear in each partial sum: every
           // K split adds its part (split 0 with the bias) straight onto y
           const float b0 = s == 0 ? bn : 0.f;
@@ -418,7 +443,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
           named_bar(2, 128);
           if (tid == 0) {
             bulk_reduce_add_f32(acct, P, (uint32_t)rows * 512);
-            if (ln) {
+            if (nrm) {
               bulk_reduce_add_f32(stt, s_s1, (uint32_t)MT * 4);
               bulk_reduce_add_f32(stt + MT, s_s2, (uint32_t)MT * 4);
             }
@@ -429,9 +454,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
             if (*last_flag) {
               __threadfence();
               fence_proxy_async_global();
-              mbar_arrive_expect_tx(xin_full, (uint32_t)rows * 512 + (ln ? (uint32_t)MT * 8 : 0u));
+              mbar_arrive_expect_tx(xin_full, (uint32_t)rows * 512 + (nrm ? (uint32_t)MT * 8 : 0u));
               bulk_g2s_plain(P, acct, (uint32_t)rows * 512, xin_full);
-              if (ln) {
+              if (nrm) {
                 bulk_g2s_plain(s_s1, stt, (uint32_t)MT * 4, xin_full);
                 bulk_g2s_plain(s_s2, stt + MT, (uint32_t)MT * 4, xin_full);
               }
@@ -445,13 +470,14 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
             if (ln) {
               cn = P[Mv * 128 + f];
               dn = P[(Mv + 1) * 128 + f];
-              for (int t = tid; t < Mv; t += 128)
-                lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs);
             }
+            if (nrm)
+              for (int t = tid; t < Mv; t += 128)
+                lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs, ln);
             named_bar(2, 128);
             // put the workspace back to zero
             for (int m = 0; m < rows; ++m) __stcg(acct + m * 128 + f, 0.f);
-            if (ln)
+            if (nrm)
               for (int t = tid; t < 2 * MT; t += 128) __stcg(stt + t, 0.f);
             if (tid == 0) a.tickets[tile] = 0u;
             for (int c0 = 0; c0 < Mv; c0 += 32) {
@@ -460,7 +486,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
               lin_load_old(a, m0 + c0, cnt, n, resid, yo);
 #pragma unroll
               for (int e = 0; e < 32; ++e) v[e] = P[min(c0 + e, rows - 1) * 128 + f];
-              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, a.norm, s_dm + c0, s_rs + c0, cn, dn);
             }
             if (*reinterpret_cast<volatile int*>(abort_flag) != 0) ok = false;
           }
@@ -475,7 +501,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
             for (int e = 0; e < 16; ++e)
               if (c0 + e < rows) atomicAdd(accp + (c0 + e) * 128, v[e]);
           }
-          if (ln)
+          if (nrm)
             for (int t = tid; t < Mv; t += 128) {
               atomicAdd(stp + t, s_s1[t]);
               atomicAdd(stp + MT + t, s_s2[t]);
@@ -495,15 +521,19 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
 #pragma unroll
               for (int e = 0; e < 32; ++e) v[e] = __ldcg(accp + min(c0 + e, MT - 1) * 128);
               lin_load_old(a, m0 + c0, cnt, n, resid, yo);
-              if (c0 == 0 && ln) {
-                cn = __ldcg(accp + Mv * 128);
-                dn = __ldcg(accp + (Mv + 1) * 128);
+              if (c0 == 0 && nrm) {
+                if (ln) {
+                  cn = __ldcg(accp + Mv * 128);
+                  dn = __ldcg(accp + (Mv + 1) * 128);
+                }
                 for (int t = tid; t < Mv; t += 128)
                   lin_row_stats(__ldcg(stp + t), __ldcg(stp + MT + t), inv_k, a.eps, t, s_dm,
-                                s_rs);
+                                s_rs, ln);
                 named_bar(2, 128);  // uniform: every thread of the last CTA is here
-                __stcg(accp + Mv * 128, 0.f);
-                __stcg(accp + (Mv + 1) * 128, 0.f);
+                if (ln) {
+                  __stcg(accp + Mv * 128, 0.f);
+                  __stcg(accp + (Mv + 1) * 128, 0.f);
+                }
                 for (int t = tid; t < Mv; t += 128) {
                   __stcg(stp + t, 0.f);
                   __stcg(stp + MT + t, 0.f);
@@ -512,7 +542,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (e < cnt) __stcg(accp + (c0 + e) * 128, 0.f);
-              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, ln, s_dm + c0, s_rs + c0, cn, dn);
+              lin_emit(a, m0 + c0, cnt, n, v, yo, bn, a.norm, s_dm + c0, s_rs + c0, cn, dn);
             }
             if (tid == 0) a.tickets[tile] = 0u;
           }
@@ -542,9 +572,9 @@ struct LinPlan {
 // the g and b rows with LayerNorm); the K axis split S ways so that the grid
 // covers the GPU once without a second wave, more if one CTA's share of the
 // activations would not fit in shared memory.
-static bool lin_plan(int M, int N, int K, bool ln, int sms, LinPlan* p) {
+static bool lin_plan(int M, int N, int K, int norm, bool glu, int sms, LinPlan* p) {
   if (M < 1 || N < 1 || K < 64 || K % 64 != 0 || sms < 1) return false;
-  const int extra = ln ? 2 : 0;
+  const int extra = norm == ASR_NORM_LAYER ? 2 : 0;
   const int per_tile = kLinMaxMT - extra;
   p->m_tiles = (M + per_tile - 1) / per_tile;
   p->MR = (M + p->m_tiles - 1) / p->m_tiles;
@@ -558,7 +588,7 @@ static bool lin_plan(int M, int N, int K, bool ln, int sms, LinPlan* p) {
   if (S < 1) S = 1;
   auto smem_of = [&](int s) {
     const int nkb = (p->KB + s - 1) / s;
-    return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, ln);
+    return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, norm, glu);
   };
   while (smem_of(S) > kLinSmemMax && S < p->KB) ++S;  // fewer k-blocks per CTA
   if (smem_of(S) > kLinSmemMax) return false;
@@ -581,35 +611,49 @@ static std::once_flag g_lin_attr;
 using namespace asrkv;
 
 extern "C" size_t asr_linear_workspace_size(int M, int N, int K) {
-  LinPlan p, q;  // with and without LayerNorm: the larger serves both
+  // the largest over the norms and inputs: one workspace serves every call
   const int sms = device_sm_count();
-  if (!lin_plan(M, N, K, true, sms, &p) || !lin_plan(M, N, K, false, sms, &q)) return 0;
-  return p.ws_bytes > q.ws_bytes ? p.ws_bytes : q.ws_bytes;
+  const int cases[4][2] = {{ASR_NORM_NONE, 0}, {ASR_NORM_LAYER, 0}, {ASR_NORM_RMS, 0},
+                           {ASR_NORM_NONE, 1}};
+  size_t best = 0;
+  for (const auto& c : cases) {
+    LinPlan p;
+    if (!lin_plan(M, N, K, c[0], c[1] != 0, sms, &p)) return 0;
+    if (p.ws_bytes > best) best = p.ws_bytes;
+  }
+  return best;
 }
 
-extern "C" int asr_linear(const float* x, int64_t x_stride, const float* ln_g, const float* ln_b,
-                          float eps, const uint16_t* w, const float* bias, int M, int N, int K,
-                          int mode, float* y, int64_t y_stride, void* ws, size_t ws_bytes,
-                          int32_t* dev_err, asr_stream_t stream) {
-  if (M < 0 || N < 1 || K < 1 || mode < ASR_LINEAR_STORE || mode > ASR_LINEAR_GELU)
+extern "C" int asr_linear(const float* x, int64_t x_stride, int norm, const float* norm_w,
+                          const float* norm_b, float eps, int act, const uint16_t* w,
+                          const float* bias, int M, int N, int K, int mode, float* y,
+                          int64_t y_stride, void* ws, size_t ws_bytes, int32_t* dev_err,
+                          asr_stream_t stream) {
+  if (M < 0 || N < 1 || K < 1 || mode < ASR_LINEAR_STORE || mode > ASR_LINEAR_GELU ||
+      norm < ASR_NORM_NONE || norm > ASR_NORM_RMS || act < ASR_ACT_NONE || act > ASR_ACT_SWIGLU)
     return ASR_ERR_INVALID_ARG;
   if (K % 64 != 0 || N > (1 << 20) || K > (1 << 20)) return ASR_ERR_UNSUPPORTED;
+  if (act == ASR_ACT_SWIGLU && norm != ASR_NORM_NONE) return ASR_ERR_UNSUPPORTED;
   if (M == 0) return ASR_OK;
-  if (!x || !w || !y || ((ln_g == nullptr) != (ln_b == nullptr))) return ASR_ERR_INVALID_ARG;
-  if (x_stride < K || y_stride < N || !(eps >= 0.f)) return ASR_ERR_INVALID_ARG;
+  const int xw = act == ASR_ACT_SWIGLU ? 2 * K : K;  // x values read per row
+  if (!x || !w || !y) return ASR_ERR_INVALID_ARG;
+  if ((norm != ASR_NORM_NONE && !norm_w) || (norm == ASR_NORM_LAYER && !norm_b))
+    return ASR_ERR_INVALID_ARG;
+  if (x_stride < xw || y_stride < N || !(eps >= 0.f)) return ASR_ERR_INVALID_ARG;
   if (!aligned16(x) || x_stride % 4 != 0 || !aligned16(w) ||
-      (ln_g && (!aligned16(ln_g) || !aligned16(ln_b))))
+      (norm != ASR_NORM_NONE && !aligned16(norm_w)) ||
+      (norm == ASR_NORM_LAYER && !aligned16(norm_b)))
     return ASR_ERR_MISALIGNED;
   // y must not overlap x: other CTAs still read x while the epilogue writes y
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(x);
-  const uintptr_t x1 = reinterpret_cast<uintptr_t>(x + (int64_t)(M - 1) * x_stride + K);
+  const uintptr_t x1 = reinterpret_cast<uintptr_t>(x + (int64_t)(M - 1) * x_stride + xw);
   const uintptr_t y0 = reinterpret_cast<uintptr_t>(y);
   const uintptr_t y1 = reinterpret_cast<uintptr_t>(y + (int64_t)(M - 1) * y_stride + N);
   if (x0 < y1 && y0 < x1) return ASR_ERR_ALIAS;
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
   LinPlan p;
-  if (!lin_plan(M, N, K, ln_g != nullptr, sms, &p)) return ASR_ERR_UNSUPPORTED;
+  if (!lin_plan(M, N, K, norm, act == ASR_ACT_SWIGLU, sms, &p)) return ASR_ERR_UNSUPPORTED;
   if (p.ws_bytes > 0 &&
       (!ws || ws_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0))
     return ASR_ERR_WORKSPACE;
@@ -626,8 +670,10 @@ extern "C" int asr_linear(const float* x, int64_t x_stride, const float* ln_g, c
   LinArgs la = {};
   la.x = x;
   la.x_stride = x_stride;
-  la.ln_g = ln_g;
-  la.ln_b = ln_b;
+  la.norm_w = norm != ASR_NORM_NONE ? norm_w : nullptr;
+  la.norm_b = norm == ASR_NORM_LAYER ? norm_b : nullptr;
+  la.norm = norm;
+  la.act = act;
   la.eps = eps;
   la.bias = bias;
   la.y = y;

@@ -1,6 +1,6 @@
-"""The whole Whisper decoder step around the attention, composed from the
-library's entry points (argument marshalling only: every step runs in the
-library's kernels).
+"""The whole decoder step around the attention, composed from the library's
+entry points (argument marshalling only: every step runs in the library's
+kernels): the Whisper decoder layer and the Qwen3-ASR decoder layer.
 
 Order of the steps ("wavo 0.1.0, src/whisper/decoder.rs",
 Decoder::record_step), for one new token per sequence:
@@ -82,3 +82,63 @@ def whisper_decoder_layer(x, p, cache, lens, cross, group, frames, bufs, eps=1e-
 
 
 LAUNCHES_PER_LAYER = 8
+
+
+# ------------------------------------------------------------- Qwen3-ASR --
+#
+# Order ("transcribe.cpp, src/arch/qwen3_asr/decoder.h", header comment and
+# StepBuildBatched), for one new token per sequence at position n_past:
+#
+#     qkv = RMSNorm(x) [W_q | W_k | W_v]^T     asr_linear (RMSNorm fused, no bias)
+#     q/k RMSNorm, RoPE, append, GQA           asr_gqa_step
+#     x  += att W_o^T                          asr_linear (Residual)
+#     gu  = RMSNorm(x) [W_gate | W_up]^T       asr_linear (RMSNorm fused)
+#     x  += (silu(gate) * up) W_down^T         asr_linear (SwiGLU input, Residual)
+#
+# Five launches per layer.
+
+class QwenDecoderBuffers:
+    """Scratch of one Qwen3-ASR decoder step: qkv fp32 [B, (Hq + 2 Hkv) hd],
+    att fp32 [B, Hq hd], gu fp32 [B, 2 inner] and the workspaces."""
+
+    def __init__(self, B, d, inner, q_heads, kv_heads, head_dim, device=None):
+        import torch
+        device = device or "cuda"
+        f32 = torch.float32
+        self.B, self.d, self.inner = B, d, inner
+        self.q_heads, self.kv_heads, self.head_dim = q_heads, kv_heads, head_dim
+        nq, nk = q_heads * head_dim, kv_heads * head_dim
+        self.nq, self.nk = nq, nk
+        self.qkv = torch.zeros(B, nq + 2 * nk, dtype=f32, device=device)
+        self.att = torch.zeros(B, nq, dtype=f32, device=device)
+        self.gu = torch.zeros(B, 2 * inner, dtype=f32, device=device)
+        self.ws_gqa = ops.workspace(ops.OP_GQA_STEP, B, B, 1, q_heads, head_dim, device=device)
+        sizes = [(nq + 2 * nk, d), (d, nq), (2 * inner, d), (d, inner)]
+        need = max(ops.load().asr_linear_workspace_size(B, n, k) for n, k in sizes)
+        self.ws_lin = (torch.zeros(need + 256, dtype=torch.uint8, device=device) if need else None)
+
+
+def qwen3_decoder_layer(x, p, cache, n_past, bufs, eps=1e-6, rope_base=1e6, dev_err=None,
+                        stream=None):
+    """One Qwen3-ASR decoder layer on the new token of every sequence.
+
+    x: fp32 [B, d], updated in place; p: the layer's parameters (w_qkv,
+    w_o, w_gu, w_down f16 [out, in]; rms1, rms2 fp32 [d]; q_norm, k_norm
+    fp32 [head_dim]); cache: f16 [B, capacity, 2 Hkv hd] (row n_past
+    written); n_past: int32 [B]; bufs: QwenDecoderBuffers."""
+    nq, nk, hd = bufs.nq, bufs.nk, bufs.head_dim
+    wl = bufs.ws_lin
+    qkv = bufs.qkv
+    ops.asr_linear(x, p["w_qkv"], qkv, rms=p["rms1"], eps=eps, ws=wl, dev_err=dev_err,
+                   stream=stream)
+    ops.asr_gqa_step(qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], p["q_norm"], p["k_norm"],
+                     eps, rope_base, n_past, cache, cache.shape[1], bufs.q_heads, bufs.kv_heads,
+                     hd, hd ** -0.5, bufs.att, bufs.ws_gqa, dev_err=dev_err, stream=stream)
+    ops.asr_linear(bufs.att, p["w_o"], x, mode="residual", ws=wl, dev_err=dev_err, stream=stream)
+    ops.asr_linear(x, p["w_gu"], bufs.gu, rms=p["rms2"], eps=eps, ws=wl, dev_err=dev_err,
+                   stream=stream)
+    ops.asr_linear(bufs.gu, p["w_down"], x, swiglu=True, mode="residual", ws=wl,
+                   dev_err=dev_err, stream=stream)
+
+
+QWEN_LAUNCHES_PER_LAYER = 5

@@ -35,7 +35,8 @@ SIGNATURES = {
                                          _int, _f, _p, _p, _sz, _p, _p]),
     "asr_cross_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _int, _int, _f,
                                    _p, _p, _sz, _p, _p]),
-    "asr_gqa_step": (_int, [_p, _p, _p, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int, _int, _int,
+    "asr_gqa_step": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int,
+                            _int, _int,
                             _f, _p, _p, _sz, _p, _p]),
     "asr_kv_rearrange": (_int, [_p, _p, _i64, _i64, _int, _int, _int, _p, _p, _p, _int, _p, _p]),
     "asr_self_attn_step_noalloc": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _f, _p,
@@ -51,8 +52,8 @@ SIGNATURES = {
                                _sz, _p, _p]),
     "asr_encoder_attn": (_int, [_p, _p, _p, _p, _int, _int, _int, _int, _f, _p, _p, _sz, _p, _p]),
     "asr_cross_kv_fill": (_int, [_p, _p, _p, _int, _int, _int, _p, _i64, _p, _p]),
-    "asr_linear": (_int, [_p, _i64, _p, _p, _f, _p, _p, _int, _int, _int, _int, _p, _i64, _p, _sz,
-                          _p, _p]),
+    "asr_linear": (_int, [_p, _i64, _int, _p, _p, _f, _int, _p, _p, _int, _int, _int, _int, _p,
+                          _i64, _p, _sz, _p, _p]),
     "asr_linear_workspace_size": (_sz, [_int, _int, _int]),
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
@@ -235,8 +236,14 @@ def asr_gqa_step(q, k_new, v_new, q_norm_w, k_norm_w, eps, rope_base, n_past, ca
     _need(n_past, torch.int32, "n_past")
     _need(cache, torch.float16, "cache")
     B = n_past.shape[0]
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{n} must be 2-D with unit inner stride")
+    if k_new.stride(0) != v_new.stride(0):
+        raise ValueError("k_new and v_new must share one row stride")
     wp, wn = _ws_ptr(ws)
-    st = load().asr_gqa_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(q_norm_w), _ptr(k_norm_w),
+    st = load().asr_gqa_step(_ptr(q), q.stride(0), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+                             _ptr(q_norm_w), _ptr(k_norm_w),
                              float(eps), float(rope_base), _ptr(n_past), _ptr(cache),
                              cache.stride(0), capacity, B, q_heads, kv_heads, head_dim,
                              float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
@@ -348,13 +355,18 @@ def linear_workspace(M, N, K, device=None):
     return torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
 
 
-def asr_linear(x, w, y, bias=None, ln=None, eps=1e-5, mode="store", ws=None, dev_err=None,
-               stream=None):
-    """y (fp32 [M, N], row-strided) = epilogue(LayerNorm(x) @ w^T + bias).
+NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
+ACT_NONE, ACT_SWIGLU = 0, 1
 
-    x: fp32 [M, K] (row-strided, unit inner stride); w: f16 [N, K]; bias:
-    fp32 [N] or None; ln: (g, b) fp32 [K] each, or None; mode "store",
-    "residual" (y += ...) or "gelu"."""
+
+def asr_linear(x, w, y, bias=None, ln=None, rms=None, eps=1e-5, swiglu=False, mode="store",
+               ws=None, dev_err=None, stream=None):
+    """y (fp32 [M, N], row-strided) = epilogue(norm(x) @ w^T + bias).
+
+    x: fp32 [M, K] (row-strided, unit inner stride; [M, 2K] = [gate | up]
+    with swiglu=True); w: f16 [N, K]; bias: fp32 [N] or None; ln: (g, b)
+    fp32 [K] each for a LayerNorm, or rms: g fp32 [K] for an RMSNorm (at
+    most one); mode "store", "residual" (y += ...) or "gelu"."""
     import torch
     _need(x, torch.float32, "x")
     _need(w, torch.float16, "w")
@@ -363,24 +375,30 @@ def asr_linear(x, w, y, bias=None, ln=None, eps=1e-5, mode="store", ws=None, dev
         raise ValueError("x and y must be 2-D with unit inner stride")
     if not w.is_contiguous():
         raise ValueError("w must be contiguous")
-    M, K = x.shape
-    N = w.shape[0]
-    if w.shape[1] != K or y.shape[0] != M or y.shape[1] != N:
-        raise ValueError("shapes do not match: x [M, K], w [N, K], y [M, N]")
+    M = x.shape[0]
+    N, K = w.shape
+    if x.shape[1] != (2 * K if swiglu else K) or y.shape[0] != M or y.shape[1] != N:
+        raise ValueError("shapes do not match: x [M, K] ([M, 2K] with swiglu), w [N, K], y [M, N]")
+    if ln is not None and rms is not None:
+        raise ValueError("one norm at most")
     if bias is not None:
         _need(bias, torch.float32, "bias")
-    g = b = None
+    norm, g, b = NORM_NONE, None, None
     if ln is not None:
-        g, b = ln
+        norm, (g, b) = NORM_LAYER, ln
         _need(g, torch.float32, "ln_g")
         _need(b, torch.float32, "ln_b")
+    elif rms is not None:
+        norm, g = NORM_RMS, rms
+        _need(g, torch.float32, "rms_g")
     if ws is None:
         wp, wn = None, 0
     else:
         wp, wn = _ws_ptr(ws)
-    st = load().asr_linear(_ptr(x), x.stride(0), _ptr(g), _ptr(b), float(eps), _ptr(w),
-                           _ptr(bias), M, N, K, LINEAR_MODES[mode], _ptr(y), y.stride(0), wp, wn,
-                           _ptr(dev_err), _stream(stream))
+    st = load().asr_linear(_ptr(x), x.stride(0), norm, _ptr(g), _ptr(b), float(eps),
+                           ACT_SWIGLU if swiglu else ACT_NONE, _ptr(w), _ptr(bias), M, N, K,
+                           LINEAR_MODES[mode], _ptr(y), y.stride(0), wp, wn, _ptr(dev_err),
+                           _stream(stream))
     _check("asr_linear", st)
 
 

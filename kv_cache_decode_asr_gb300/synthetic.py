@@ -35,6 +35,12 @@ Workloads (shapes of the pages' models; no weights or audio are needed):
   cross query, cross-attention, cross out-projection, LayerNorm + fc1 + GELU,
   fc2.  Random weights (``layer_params``).
 
+* ``qwen3_asr_decoder_step_b16`` -- the whole Qwen3-ASR decoder step around
+  the GQA step (28 layers, 16 Q / 8 KV heads of 128, d = 2048, MLP 6144),
+  16 sequences, n_past uniform in [1024, 4096]: per layer RMSNorm + q/k/v,
+  the fused GQA step, the output projection, RMSNorm + gate/up, SwiGLU +
+  down.  Random weights (``qwen_layer_params``).
+
 Layer weights (``layer_params``): every projection N(0, 1/fan_in) stored as
 f16, biases N(0, 0.1) with the key bias zero, LayerNorm weights N(1, 0.1) and
 biases N(0, 0.1); the residual stream x starts N(0, 1).
@@ -67,6 +73,10 @@ WORKLOADS = {
     "whisper_large_decoder_step_b32": dict(kind="decoder_step", B=32, d=1280, heads=20,
                                            head_dim=64, inner=5120, layers=32, capacity=448,
                                            frames=1500, beam=1, len_lo=1, len_hi=448),
+    "qwen3_asr_decoder_step_b16": dict(kind="qwen_decoder_step", B=16, layers=28, q_heads=16,
+                                       kv_heads=8, head_dim=128, d=2048, inner=6144,
+                                       capacity=4224, n_past_lo=1024, n_past_hi=4096, eps=1e-6,
+                                       rope_base=1e6, w_mean=1.0, w_std=0.1),
 }
 
 # projections of one decoder layer: name, output size, input size (d units)
@@ -151,6 +161,44 @@ def dev_normal(shape, seed, device, dtype=None, mean=0.0, std=1.0):
     if dtype is not None and dtype != torch.float32:
         x = x.to(dtype)
     return x
+
+
+def _qwen_shapes(d, inner, q_heads, kv_heads, head_dim):
+    nq, nk = q_heads * head_dim, kv_heads * head_dim
+    return [("qkv", nq + 2 * nk, d), ("o", d, nq), ("gu", 2 * inner, d), ("down", d, inner)]
+
+
+def qwen_layer_params(d, inner, q_heads, kv_heads, head_dim, seed):
+    """Host parameters of one Qwen3-ASR decoder layer (numpy): w_qkv (q rows,
+    then k, then v), w_o, w_gu (gate rows, then up rows), w_down as f16 bits
+    [out, in], each N(0, 1/fan_in); rms1, rms2 float32 [d] and q_norm, k_norm
+    float32 [head_dim], N(1, 0.1).  No biases."""
+    p = {}
+    for i, (name, n_out, n_in) in enumerate(_qwen_shapes(d, inner, q_heads, kv_heads, head_dim)):
+        w = host_normal_f32((n_out, n_in), seed + i, std=n_in ** -0.5)
+        p["w_" + name] = w.astype(np.float16).view(np.uint16)
+    p["rms1"] = host_normal_f32(d, seed + 10, mean=1.0, std=0.1)
+    p["rms2"] = host_normal_f32(d, seed + 11, mean=1.0, std=0.1)
+    p["q_norm"] = host_normal_f32(head_dim, seed + 12, mean=1.0, std=0.1)
+    p["k_norm"] = host_normal_f32(head_dim, seed + 13, mean=1.0, std=0.1)
+    return p
+
+
+def dev_qwen_layer_params(n_layers, d, inner, q_heads, kv_heads, head_dim, seed, device):
+    """qwen_layer_params of n_layers layers drawn on the device, stacked on a
+    leading layer axis."""
+    import torch
+    p = {}
+    for i, (name, n_out, n_in) in enumerate(_qwen_shapes(d, inner, q_heads, kv_heads, head_dim)):
+        w = torch.empty(n_layers, n_out, n_in, dtype=torch.float16, device=device)
+        dev_fill_normal_(w, seed + i)
+        w.mul_(n_in ** -0.5)
+        p["w_" + name] = w
+    p["rms1"] = dev_normal((n_layers, d), seed + 10, device, mean=1.0, std=0.1)
+    p["rms2"] = dev_normal((n_layers, d), seed + 11, device, mean=1.0, std=0.1)
+    p["q_norm"] = dev_normal((n_layers, head_dim), seed + 12, device, mean=1.0, std=0.1)
+    p["k_norm"] = dev_normal((n_layers, head_dim), seed + 13, device, mean=1.0, std=0.1)
+    return p
 
 
 def dev_layer_params(n_layers, d, inner, seed, device):

@@ -116,7 +116,8 @@ def test_cross_attn_rejects(lib):
 def test_gqa_rejects(lib):
     f = lib.asr_gqa_step
     row = 2 * 8 * 128
-    args = lambda **kw: [A16, A16, A16, A16, A16, ctypes.c_float(kw.get("eps", 1e-6)),
+    args = lambda **kw: [A16, kw.get("qs", 2048), A16, A16, kw.get("kvs", 1024), A16, A16,
+                         ctypes.c_float(kw.get("eps", 1e-6)),
                          ctypes.c_float(kw.get("base", 1e6)), A16c, A16b, kw.get("ss", 4224 * row),
                          4224, 16, kw.get("hq", 16), kw.get("hkv", 8), kw.get("hd", 128),
                          ctypes.c_float(0.088), P(0x40000), P(0x50000), ctypes.c_size_t(1 << 20),
@@ -127,6 +128,8 @@ def test_gqa_rejects(lib):
     assert f(*args(eps=-1.0)) == INVALID
     assert f(*args(ss=4223 * row)) == INVALID
     assert f(*args(hd=96)) == UNSUP
+    assert f(*args(qs=2044)) == INVALID      # q rows narrower than 16 heads x 128
+    assert f(*args(kvs=1026)) == MISAL       # k/v row stride not a multiple of 4
 
 
 def test_rearrange_rejects(lib):
@@ -168,17 +171,22 @@ def test_linear_rejects(lib):
     x, w, y = P(0x100000), P(0x200000), P(0x900000)
 
     def args(**kw):
-        return [kw.get("x", x), kw.get("xs", 1280), kw.get("g", None), kw.get("b", None),
-                ctypes.c_float(1e-5), w, None, kw.get("M", 32), kw.get("N", 3840),
-                kw.get("K", 1280), kw.get("mode", 0), kw.get("y", y), kw.get("ys", 3840), None,
-                ctypes.c_size_t(0), None, None]
+        return [kw.get("x", x), kw.get("xs", 1280), kw.get("norm", 0), kw.get("g", None),
+                kw.get("b", None), ctypes.c_float(1e-5), kw.get("act", 0), w, None,
+                kw.get("M", 32), kw.get("N", 3840), kw.get("K", 1280), kw.get("mode", 0),
+                kw.get("y", y), kw.get("ys", 3840), None, ctypes.c_size_t(0), None, None]
 
     assert f(*args(K=1000)) == UNSUP           # K not a multiple of 64
     assert f(*args(mode=3)) == INVALID
     assert f(*args(N=0)) == INVALID
     assert f(*args(xs=1000)) == INVALID        # row stride below K
     assert f(*args(ys=100)) == INVALID
-    assert f(*args(g=P(0x300000))) == INVALID  # LayerNorm weight without its bias
+    assert f(*args(norm=1, g=P(0x300000))) == INVALID  # LayerNorm weight without its bias
+    assert f(*args(norm=2)) == INVALID         # RMSNorm without its weight
+    assert f(*args(norm=3)) == INVALID
+    assert f(*args(act=2)) == INVALID
+    assert f(*args(act=1, norm=2, g=P(0x300000))) == UNSUP  # SwiGLU input takes no norm
+    assert f(*args(act=1)) == INVALID          # SwiGLU rows hold 2K values: stride 1280 < 2560
     assert f(*args(x=P(0x100004))) == MISAL
     assert f(*args(xs=1282)) == MISAL
     assert f(*args(y=P(0x100000 + 64))) == ALIAS  # y overlaps x

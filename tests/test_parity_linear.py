@@ -242,3 +242,118 @@ def test_whisper_decoder_layer_matches_oracle():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_attn_close(host(x_b), x_ref, "whisper_decoder_layer")
+
+
+# ------------------------------------------------ RMSNorm and SwiGLU inputs --
+
+# M sequences, N weight rows, K inputs, epilogue, input kind
+CASES_QWEN = [
+    (16, 4096, 2048, "store", "rms"),        # Qwen3-ASR q/k/v: RMSNorm, K split, bulk reduction
+    (16, 12288, 2048, "store", "rms"),       # gate/up: 96 weight tiles, one CTA per tile (no split)
+    (16, 2048, 6144, "residual", "swiglu"),  # down: silu(gate) * up onto the stream
+    (37, 300, 192, "gelu", "rms"),           # ragged rows and weight tile
+    (5, 256, 128, "residual", "rms"),        # RMSNorm with a residual: the ticket path
+    (300, 256, 128, "store", "rms"),         # two row tiles of 150 (> 128 rows: the scalar path)
+    (7, 640, 320, "gelu", "swiglu"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,mode,kind", CASES_QWEN)
+def test_linear_rms_swiglu_matches_oracle(M, N, K, mode, kind):
+    seed = 7400 + M + N + K
+    xw = 2 * K if kind == "swiglu" else K
+    x = syn.host_normal_f32((M, xw), seed, mean=0.2, std=1.4)
+    w = (syn.host_normal_f32((N, K), seed + 1) * np.float32(K ** -0.5)).astype(
+        np.float16).view(np.uint16)
+    g = syn.host_normal_f32(K, seed + 3, mean=1.0, std=0.2)
+    y0 = syn.host_normal_f32((M, N), seed + 5)
+    res = mode == "residual"
+    kw = {"rms": g} if kind == "rms" else {"swiglu": True}
+    ref = oracle.linear(x, w, None, mode=mode, eps=1e-6, y=y0 if res else None, **kw)
+    if kind == "rms":
+        a = np.stack([oracle.rmsnorm(x[m].astype(np.float64), g.astype(np.float64), 1e-6)
+                      for m in range(M)])
+    else:
+        a = oracle.silu(x[:, :K]) * x[:, K:].astype(np.float64)
+    tol, s = linear_bound(a, w, None, mode, y0 if res else None)
+    y_d = dev(y0) if res else torch.full((M, N), float("nan"), device="cuda")
+    ws = ops.linear_workspace(M, N, K)
+    err = new_err()
+    dkw = {"rms": dev(g)} if kind == "rms" else {"swiglu": True}
+    ops.asr_linear(dev(x), dev(w), y_d, mode=mode, eps=1e-6, ws=ws, dev_err=err, **dkw)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    worst = assert_linear_close(host(y_d), ref, tol, s, f"M={M} N={N} K={K} {mode} {kind}")
+    print(f"M={M} N={N} K={K} {mode} {kind}: worst err / sum|a||w| = {worst:.2e}")
+    if ws is not None:
+        assert int(ws.count_nonzero().item()) == 0
+
+
+def test_qwen3_decoder_layer_matches_oracle():
+    """A Qwen3-ASR-shaped layer (16 Q / 8 KV heads of 128, d 256, MLP 384),
+    3 sequences at n_past 0, 30 and 63 of a 64-row cache.  Each step against
+    the oracle on the GPU's own input to it (the dense bound, the attention
+    tolerance, the cache row bit for bit), then the whole layer."""
+    from kv_cache_decode_asr_gb300 import decoder
+    B, Hq, Hkv, hd, cap, d, inner = 3, 16, 8, 128, 64, 256, 384
+    nq, nk = Hq * hd, Hkv * hd
+    p = syn.qwen_layer_params(d, inner, Hq, Hkv, hd, 7500)
+    x0 = syn.host_normal_f32((B, d), 7600)
+    n_past = np.array([0, 30, 63], np.int32)
+    cache0 = syn.host_normal_f16bits((B, cap, 2 * nk), 7601)
+    pd = {k: dev(v) for k, v in p.items()}
+    bufs = decoder.QwenDecoderBuffers(B, d, inner, Hq, Hkv, hd)
+    x = dev(x0)
+    cache = dev(cache0)
+    np_d = dev(n_past)
+    err = new_err()
+    wl = bufs.ws_lin
+    ops.asr_linear(x, pd["w_qkv"], bufs.qkv, rms=pd["rms1"], eps=1e-6, ws=wl, dev_err=err)
+    ops.asr_gqa_step(bufs.qkv[:, :nq], bufs.qkv[:, nq:nq + nk], bufs.qkv[:, nq + nk:],
+                     pd["q_norm"], pd["k_norm"], 1e-6, 1e6, np_d, cache, cap, Hq, Hkv, hd,
+                     hd ** -0.5, bufs.att, bufs.ws_gqa, dev_err=err)
+    ops.asr_linear(bufs.att, pd["w_o"], x, mode="residual", ws=wl, dev_err=err)
+    x1 = host(x).copy()
+    ops.asr_linear(x, pd["w_gu"], bufs.gu, rms=pd["rms2"], eps=1e-6, ws=wl, dev_err=err)
+    ops.asr_linear(bufs.gu, pd["w_down"], x, swiglu=True, mode="residual", ws=wl, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    qkv, att, gu, x2 = host(bufs.qkv), host(bufs.att), host(bufs.gu), host(x)
+
+    def dense(xin, wk, mode, rms, y_old, got, what, swiglu=False):
+        ref = oracle.linear(xin, p[wk], None, mode=mode, eps=1e-6, y=y_old,
+                            rms=p[rms] if rms else None, swiglu=swiglu)
+        if rms:
+            a = np.stack([oracle.rmsnorm(xin[m].astype(np.float64), p[rms].astype(np.float64),
+                                         1e-6) for m in range(xin.shape[0])])
+        elif swiglu:
+            K = p[wk].shape[1]
+            a = oracle.silu(xin[:, :K]) * xin[:, K:].astype(np.float64)
+        else:
+            a = xin.astype(np.float64)
+        tol, s = linear_bound(a, p[wk], None, mode, y_old)
+        assert_linear_close(got, ref, tol, s, what)
+
+    dense(x0, "w_qkv", "store", "rms1", None, qkv, "q/k/v")
+    cache_ref = cache0.copy()
+    att_ref, _ = oracle.gqa_step(np.ascontiguousarray(qkv[:, :nq]),
+                                 np.ascontiguousarray(qkv[:, nq:nq + nk]),
+                                 np.ascontiguousarray(qkv[:, nq + nk:]), p["q_norm"], p["k_norm"],
+                                 1e-6, 1e6, n_past, cache_ref, Hq, Hkv, hd, hd ** -0.5)
+    assert_attn_close(att, att_ref, "GQA step")
+    k_rows = host_u16(cache)[np.arange(B), n_past]
+    assert np.array_equal(k_rows[:, nk:], cache_ref[np.arange(B), n_past][:, nk:])  # V bitwise
+    dense(att, "w_o", "residual", None, x0, x1, "output projection")
+    dense(x1, "w_gu", "store", "rms2", None, gu, "gate/up")
+    dense(gu, "w_down", "residual", None, x1, x2, "SwiGLU down", swiglu=True)
+
+    cache_o = cache0.copy()
+    x_ref, _ = oracle.qwen3_decoder_layer_step(x0, p, cache_o, n_past, Hq, Hkv, hd)
+    assert_attn_close(x2, x_ref, "whole layer")
+
+    xb = dev(x0)
+    cb = dev(cache0)
+    decoder.qwen3_decoder_layer(xb, pd, cb, np_d, bufs, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(host(xb), x_ref, "qwen3_decoder_layer")
