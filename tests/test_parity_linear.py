@@ -75,6 +75,7 @@ CASES = [
     (45, 200, 320, "store", True, False),      # ragged rows, partial last weight tile, K % 128 = 64
     (300, 384, 384, "gelu", True, False),      # two row tiles
     (5, 1536, 64, "residual", False, False),   # one K block: no K split
+    (3, 100, 128, "store", True, False),       # fewer weight rows than one 128-row tile
 ]
 
 
@@ -357,3 +358,47 @@ def test_qwen3_decoder_layer_matches_oracle():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_attn_close(host(xb), x_ref, "qwen3_decoder_layer")
+
+
+def test_linear_one_workspace_every_mode():
+    """One workspace serves calls in every norm and input mode, back to back
+    on one stream (each leaves it zero for the next)."""
+    M, N, K = 9, 768, 512
+    ws = ops.linear_workspace(M, N, K)
+    assert ws is not None
+    x = syn.host_normal_f32((M, 2 * K), 7700)
+    w = (syn.host_normal_f32((N, K), 7701) * np.float32(K ** -0.5)).astype(
+        np.float16).view(np.uint16)
+    g = syn.host_normal_f32(K, 7702, mean=1.0, std=0.1)
+    b = syn.host_normal_f32(K, 7703, std=0.1)
+    bias = syn.host_normal_f32(N, 7704, std=0.1)
+    xd, wd, gd, bd, biasd = dev(x), dev(w), dev(g), dev(b), dev(bias)
+    xk = np.ascontiguousarray(x[:, :K])
+    calls = [("ln", dict(ln=(gd, bd)), dict(ln=(g, b)), "store"),
+             ("rms", dict(rms=gd), dict(rms=g), "gelu"),
+             ("swiglu", dict(swiglu=True), dict(swiglu=True), "store"),
+             ("plain", {}, {}, "gelu")]
+    err = new_err()
+    outs = []
+    for name, dkw, okw, mode in calls:
+        src = xd if name == "swiglu" else xd[:, :K]
+        y = torch.full((M, N), float("nan"), device="cuda")
+        ops.asr_linear(src, wd, y, bias=biasd, mode=mode, eps=1e-5, ws=ws, dev_err=err, **dkw)
+        outs.append((name, okw, mode, y))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert int(ws.count_nonzero().item()) == 0
+    for name, okw, mode, y in outs:
+        xin = x if name == "swiglu" else xk
+        ref = oracle.linear(xin, w, bias, mode=mode, eps=1e-5, **okw)
+        if name == "ln":
+            a = oracle.layer_norm(xk, g, b, eps=1e-5)
+        elif name == "rms":
+            a = np.stack([oracle.rmsnorm(xk[m].astype(np.float64), g.astype(np.float64), 1e-5)
+                          for m in range(M)])
+        elif name == "swiglu":
+            a = oracle.silu(x[:, :K]) * x[:, K:].astype(np.float64)
+        else:
+            a = xk.astype(np.float64)
+        tol, s = linear_bound(a, w, bias, mode)
+        assert_linear_close(host(y), ref, tol, s, name)
