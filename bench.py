@@ -25,6 +25,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -116,7 +117,10 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw samples go to a scratch file of this run; the JSON line
+        # carries their summary
+        self.path = os.path.join(os.environ.get("ASR_BENCH_OUT", tempfile.gettempdir()),
+                                 f"asr_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
