@@ -576,32 +576,36 @@ static bool lin_plan(int M, int N, int K, int norm, bool glu, int sms, LinPlan* 
   if (M < 1 || N < 1 || K < 64 || K % 64 != 0 || sms < 1) return false;
   const int extra = norm == ASR_NORM_LAYER ? 2 : 0;
   const int per_tile = kLinMaxMT - extra;
-  p->m_tiles = (M + per_tile - 1) / per_tile;
-  p->MR = (M + p->m_tiles - 1) / p->m_tiles;
-  const int mt = p->MR + extra;
-  p->MT = mt < 16 ? 16 : (mt + 15) / 16 * 16;
   p->n_tiles = (N + 127) / 128;
   p->KB = K / 64;
-  const int tiles = p->m_tiles * p->n_tiles;
-  int S = sms / tiles;  // one wave: one CTA per SM at most
-  if (S > p->KB) S = p->KB;
-  if (S < 1) S = 1;
-  auto smem_of = [&](int s) {
-    const int nkb = (p->KB + s - 1) / s;
-    return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, norm, glu);
-  };
-  while (smem_of(S) > kLinSmemMax && S < p->KB) ++S;  // fewer k-blocks per CTA
-  if (smem_of(S) > kLinSmemMax) return false;
-  p->S = S;
-  p->nkb_max = (p->KB + S - 1) / S;
-  uint32_t cols = 32;
-  while (cols < (uint32_t)p->MT) cols <<= 1;
-  p->tmem_cols = cols;
-  p->acc_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 128 * 4, 256) : 0;
-  p->stats_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 2 * 4, 256) : 0;
-  p->ws_bytes = S > 1 ? p->acc_bytes + p->stats_bytes + align_up((size_t)tiles * 4, 256) : 0;
-  p->smem = smem_of(S);
-  return true;
+  // more, shorter row tiles when even one k-block of a tile's activations
+  // would not fit in shared memory (wide SwiGLU rows)
+  for (p->m_tiles = (M + per_tile - 1) / per_tile; p->m_tiles <= M; ++p->m_tiles) {
+    p->MR = (M + p->m_tiles - 1) / p->m_tiles;
+    const int mt = p->MR + extra;
+    p->MT = mt < 16 ? 16 : (mt + 15) / 16 * 16;
+    const int tiles = p->m_tiles * p->n_tiles;
+    int S = sms / tiles;  // one wave: one CTA per SM at most
+    if (S > p->KB) S = p->KB;
+    if (S < 1) S = 1;
+    auto smem_of = [&](int s) {
+      const int nkb = (p->KB + s - 1) / s;
+      return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, norm, glu);
+    };
+    while (smem_of(S) > kLinSmemMax && S < p->KB) ++S;  // fewer k-blocks per CTA
+    if (smem_of(S) > kLinSmemMax) continue;
+    p->S = S;
+    p->nkb_max = (p->KB + S - 1) / S;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)p->MT) cols <<= 1;
+    p->tmem_cols = cols;
+    p->acc_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 128 * 4, 256) : 0;
+    p->stats_bytes = S > 1 ? align_up((size_t)tiles * p->MT * 2 * 4, 256) : 0;
+    p->ws_bytes = S > 1 ? p->acc_bytes + p->stats_bytes + align_up((size_t)tiles * 4, 256) : 0;
+    p->smem = smem_of(S);
+    return true;
+  }
+  return false;
 }
 
 static std::once_flag g_lin_attr;
@@ -618,8 +622,7 @@ extern "C" size_t asr_linear_workspace_size(int M, int N, int K) {
   size_t best = 0;
   for (const auto& c : cases) {
     LinPlan p;
-    if (!lin_plan(M, N, K, c[0], c[1] != 0, sms, &p)) return 0;
-    if (p.ws_bytes > best) best = p.ws_bytes;
+    if (lin_plan(M, N, K, c[0], c[1] != 0, sms, &p) && p.ws_bytes > best) best = p.ws_bytes;
   }
   return best;
 }

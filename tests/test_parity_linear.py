@@ -256,6 +256,7 @@ CASES_QWEN = [
     (5, 256, 128, "residual", "rms"),        # RMSNorm with a residual: the ticket path
     (300, 256, 128, "store", "rms"),         # two row tiles of 150 (> 128 rows: the scalar path)
     (7, 640, 320, "gelu", "swiglu"),
+    (254, 256, 128, "residual", "swiglu"),   # wide rows: two row tiles so one k-block fits
 ]
 
 
