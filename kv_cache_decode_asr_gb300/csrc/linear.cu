@@ -1,14 +1,16 @@
 // linear.cu -- the dense steps of a decoder layer around the attention (next
-// row): LayerNorm, then the product of the activations with an f16 weight,
-// with a Bias, Residual or Gelu epilogue.
+// row): a pre-norm (LayerNorm or RMSNorm) or a SwiGLU input, then the product
+// of the activations with an f16 weight, with a Bias, Residual or Gelu
+// epilogue.
 //
 // Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
 // (layer_norm of x into y; gemv of y with the qkv, self_out, cross_q,
 // cross_out, fc1 and fc2 weights, epilogue Bias, Residual(1.0) or Gelu);
 // "Nest whisper-tiny, src/lib.linnet", LayerNorm (eps 1e-5) and Mlp (fc2 of
-// gelu_erf of fc1).
+// gelu_erf of fc1); "transcribe.cpp, src/arch/qwen3_asr/decoder.h", header
+// comment (pre-norm RMSNorm, SwiGLU MLP down(silu(gate(x)) * up(x))).
 //
-//   a_m  = LayerNorm(x_m) * g + b      (or x_m when no LayerNorm is asked)
+//   a_m  = LayerNorm(x_m) * g + b  |  RMSNorm(x_m) * g  |  silu(gate_m) * up_m  |  x_m
 //   v_mn = sum_k a_mk W[n][k] + bias_n
 //   y_mn = v_mn | y_mn + v_mn | v_mn * Phi(v_mn)
 //
@@ -24,30 +26,34 @@
 //
 // Work split: 128 weight rows x a range of K per CTA.  With few weight rows
 // (N = 1280 is ten tiles) the K axis is split until the grid covers the GPU.
-// A residual without LayerNorm is linear in the partial sums, so each CTA
-// adds its part straight onto y (red.add).  Otherwise the CTAs of one tile
-// add their partial sums into a zero fp32 tile in the workspace, and the last
-// to arrive (a counter per tile) applies the epilogue, writes y and puts the
-// tile and the counter back to zero.
+// A residual without a norm is linear in the partial sums, so each CTA adds
+// its part straight onto y (red.add).  Otherwise the CTAs of one tile add
+// their partial sums into a zero fp32 tile in the workspace with one bulk
+// reduction each, and the last to arrive (a counter per tile) loads the sum
+// back, applies the epilogue, writes y and puts the tile and the counter
+// back to zero.
 //
-// LayerNorm without a pass over whole rows: a CTA only sees its K range, so
-// the normalisation is folded into the product.  With x_0 the row's first
-// element, the operand is (x_k - x_0) * g_k, and two more operand rows hold g
-// and b, so the same accumulator collects cn = sum_k g_k W_nk and dn =
-// sum_k b_k W_nk; the CTA also sums (x_k - x_0) and its square over its K
-// range.  Once all K is in (after the split reduction), mean - x_0 = s1/K,
-// var = s2/K - (s1/K)^2 and
+// The norms without a pass over whole rows: a CTA only sees its K range, so
+// the normalisation is folded into the product.  LayerNorm: with x_0 the
+// row's first element, the operand is (x_k - x_0) * g_k, and two more
+// operand rows hold g and b, so the same accumulator collects cn = sum_k g_k
+// W_nk and dn = sum_k b_k W_nk; the CTA also sums (x_k - x_0) and its square
+// over its K range.  Once all K is in (after the split reduction), mean - x_0
+// = s1/K, var = s2/K - (s1/K)^2 and
 //   sum_k a_mk W_nk = rstd * (sum_k (x_k - x_0) g_k W_nk - (mean - x_0) cn) + dn.
 // Shifting by x_0 keeps both differences of the size of the row's spread.
+// RMSNorm: the operand is x_k * g_k, the CTA sums x_k^2, and the sum is
+// rstd * sum_k x_k g_k W_nk.  A SwiGLU input forms silu(gate) * up in fp32
+// from the two halves of each row while staging.
 //
 // Roles: warp 8 streams W (128 rows x 64 k per stage, 128-byte swizzle) and
 // holds the TMEM allocation; warp 9 issues tcgen05.mma; warps 0-7 bring the
 // fp32 activations in with bulk copies and write the hi/lo operand to shared
-// memory in the same swizzled layout (with the LayerNorm sums); warps 0-3
-// then drain the accumulator (thread = weight row, one TMEM lane each) and
-// run the epilogue.  W is never written by a kernel of this
-// library, so the weight loads start before the wait on the previous grid
-// (programmatic dependent launch): they overlap its tail.
+// memory in the same swizzled layout (with the norm sums); warps 0-3 then
+// drain the accumulator (thread = weight row, one TMEM lane each) and run
+// the epilogue.  W is never written by a kernel of this library, so the
+// weight loads start before the wait on the previous grid (programmatic
+// dependent launch): they overlap its tail.
 #include <mutex>
 
 #include "common.cuh"
