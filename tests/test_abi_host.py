@@ -191,3 +191,33 @@ def test_linear_rejects(lib):
     assert f(*args(xs=1282)) == MISAL
     assert f(*args(y=P(0x100000 + 64))) == ALIAS  # y overlaps x
     assert f(*args(M=0)) == OK
+
+
+def test_binding_signatures_match_header():
+    """Every entry point the header declares has a ctypes signature in the
+    binding with the same number of arguments (catches drift of the ABI)."""
+    from kv_cache_decode_asr_gb300 import ops
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = re.findall(r"^\s*(?:int|size_t|const char\*)\s+(asr_\w+)\s*\(([^;]*?)\)\s*;", text,
+                        re.M | re.S)
+    assert protos
+    for name, params in protos:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert name in ops.SIGNATURES, f"{name} has no binding"
+        assert len(ops.SIGNATURES[name][1]) == n, f"{name}: header {n} args, binding " \
+            f"{len(ops.SIGNATURES[name][1])}"
+
+
+def test_linear_wrapper_checks_before_the_library():
+    """The Python wrapper of asr_linear rejects CPU tensors and mismatched
+    shapes before it calls the library."""
+    torch = pytest.importorskip("torch")
+    from kv_cache_decode_asr_gb300 import ops
+    x = torch.zeros(4, 128)
+    w = torch.zeros(256, 128, dtype=torch.float16)
+    y = torch.zeros(4, 256)
+    with pytest.raises(ValueError):
+        ops.asr_linear(x, w, y)  # not CUDA tensors
+    with pytest.raises(TypeError):
+        ops.asr_linear(x.double(), w, y)
