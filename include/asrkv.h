@@ -343,7 +343,9 @@ int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_
  * (ASR_ERR_ALIAS).  K % 64 == 0 and SwiGLU without a norm (else
  * ASR_ERR_UNSUPPORTED).
  * Numerics: the activations enter the tensor cores as two f16 parts (a = hi
- * + lo, both multiplied by the f16 weight), so they keep about 22 bits; the
+ * + lo, both multiplied by the f16 weight), so they keep about 22 bits, and
+ * the operand values (x, silu(gate) * up, or (x - x_0) * norm_w and
+ * x * norm_w with the norms) must stay below 65504 in magnitude; the
  * sums are fp32 (with the K axis split across CTAs, a residual without a
  * norm adds the parts onto y in an unspecified order, so repeated calls may
  * differ in the last bits).  The norms are folded into the product (the
