@@ -340,8 +340,8 @@ int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const float* bias_
  * norm_b only for LayerNorm); w: f16 [N][K] (row n makes output n: torch's
  * Linear layout; 16-byte aligned); bias: fp32 [N] or NULL; y: fp32
  * [M][y_stride] (the first N written), and y must not overlap x
- * (ASR_ERR_ALIAS).  K % 64 == 0 and SwiGLU without a norm (else
- * ASR_ERR_UNSUPPORTED).
+ * (ASR_ERR_ALIAS).  K % 64 == 0, K >= 128 with a norm, and SwiGLU without a
+ * norm (else ASR_ERR_UNSUPPORTED).
  * Numerics: the activations enter the tensor cores as two f16 parts (a = hi
  * + lo, both multiplied by the f16 weight), so they keep about 22 bits, and
  * the operand values (x, silu(gate) * up, or (x - x_0) * norm_w and

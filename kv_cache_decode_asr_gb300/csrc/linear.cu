@@ -395,17 +395,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
       const bool resid = a.mode == ASR_LINEAR_RESIDUAL && n < a.N;
       if (*reinterpret_cast<volatile int*>(abort_flag) == 0) {
         if (a.S == 1) {
-          float cn = 0.f, dn = 0.f;
-          if (ln) {
-            cn = tmem_ld1(taddr + Mv);
-            dn = tmem_ld1(taddr + Mv + 1);
-            tmem_wait_ld();
-          }
-          if (nrm) {
-            for (int t = tid; t < Mv; t += 128)
-              lin_row_stats(s_s1[t], s_s2[t], inv_k, a.eps, t, s_dm, s_rs, ln);
-            named_bar(2, 128);
-          }
+          // one CTA holds the whole K of its tile (the plan splits K at
+          // least twice under a norm, so there is no norm here)
+          const float cn = 0.f, dn = 0.f;
           for (int c0 = 0; c0 < Mv; c0 += 32) {
             const int cnt = min(32, Mv - c0);
             float v[32], yo[32];
@@ -584,6 +576,10 @@ static bool lin_plan(int M, int N, int K, int norm, bool glu, int sms, LinPlan* 
   const int per_tile = kLinMaxMT - extra;
   p->n_tiles = (N + 127) / 128;
   p->KB = K / 64;
+  // under a norm the K axis is always split (the norm terms are applied by
+  // the last CTA of a tile, after the split reduction)
+  const int s_min = norm != ASR_NORM_NONE ? 2 : 1;
+  if (p->KB < s_min) return false;
   // more, shorter row tiles when even one k-block of a tile's activations
   // would not fit in shared memory (wide SwiGLU rows)
   for (p->m_tiles = (M + per_tile - 1) / per_tile; p->m_tiles <= M; ++p->m_tiles) {
@@ -593,7 +589,7 @@ static bool lin_plan(int M, int N, int K, int norm, bool glu, int sms, LinPlan* 
     const int tiles = p->m_tiles * p->n_tiles;
     int S = sms / tiles;  // one wave: one CTA per SM at most
     if (S > p->KB) S = p->KB;
-    if (S < 1) S = 1;
+    if (S < s_min) S = s_min;
     auto smem_of = [&](int s) {
       const int nkb = (p->KB + s - 1) / s;
       return kLinSmemFixed + 2 * p->MT * 128 * nkb + lin_f32_bytes(p->MR, nkb, norm, glu);
@@ -643,6 +639,7 @@ extern "C" int asr_linear(const float* x, int64_t x_stride, int norm, const floa
     return ASR_ERR_INVALID_ARG;
   if (K % 64 != 0 || N > (1 << 20) || K > (1 << 20)) return ASR_ERR_UNSUPPORTED;
   if (act == ASR_ACT_SWIGLU && norm != ASR_NORM_NONE) return ASR_ERR_UNSUPPORTED;
+  if (norm != ASR_NORM_NONE && K < 128) return ASR_ERR_UNSUPPORTED;
   if (M == 0) return ASR_OK;
   const int xw = act == ASR_ACT_SWIGLU ? 2 * K : K;  // x values read per row
   if (!x || !w || !y) return ASR_ERR_INVALID_ARG;

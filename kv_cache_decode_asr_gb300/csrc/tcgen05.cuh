@@ -211,13 +211,6 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-// One TMEM column: thread t of warp w reads lane 32*(w%4) + t.
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-  uint32_t r;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
-  return __uint_as_float(r);
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

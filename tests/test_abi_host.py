@@ -187,6 +187,7 @@ def test_linear_rejects(lib):
     assert f(*args(act=2)) == INVALID
     assert f(*args(act=1, norm=2, g=P(0x300000))) == UNSUP  # SwiGLU input takes no norm
     assert f(*args(act=1)) == INVALID          # SwiGLU rows hold 2K values: stride 1280 < 2560
+    assert f(*args(norm=2, g=P(0x300000), K=64, xs=64)) == UNSUP  # a norm needs K >= 128
     assert f(*args(x=P(0x100004))) == MISAL
     assert f(*args(xs=1282)) == MISAL
     assert f(*args(y=P(0x100000 + 64))) == ALIAS  # y overlaps x
