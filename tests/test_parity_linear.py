@@ -76,7 +76,7 @@ CASES = [
     (300, 384, 384, "gelu", True, False),      # two row tiles
     (5, 1536, 64, "residual", False, False),   # one K block: no K split
     (3, 100, 128, "store", True, False),       # fewer weight rows than one 128-row tile
-    (4, 10240, 128, "gelu", True, False),      # 80 weight tiles: no K split, LayerNorm from TMEM
+    (4, 10240, 128, "gelu", True, False),      # 80 weight tiles, K split in two under the norm
 ]
 
 
@@ -258,7 +258,7 @@ CASES_QWEN = [
     (300, 256, 128, "store", "rms"),         # two row tiles of 150 (> 128 rows: the scalar path)
     (7, 640, 320, "gelu", "swiglu"),
     (254, 256, 128, "residual", "swiglu"),   # wide rows: two row tiles so one k-block fits
-    (4, 10240, 128, "store", "rms"),         # 80 weight tiles: no K split, RMSNorm sums in smem
+    (4, 10240, 128, "store", "rms"),         # 80 weight tiles, K split in two under the norm
 ]
 
 
