@@ -907,7 +907,11 @@ class DecoderStep(WhisperStep):
         """The six dense launches of a layer: weights and vectors, activations
         in and out (the residual stream read and written by three of them)."""
         B, d, inner = self.B, self.d, self.inner
-        act = 4 * B * (d + 3 * d + d + 2 * d + d + d + 2 * d + d + inner + inner + 2 * d)
+        # qkv: x in, qkv out; out: att in, x read + written; cross q: x in, qx
+        # out; cross out: attc in, x read + written; fc1: x in, h out; fc2: h
+        # in, x read + written
+        act = 4 * B * ((d + 3 * d) + (d + 2 * d) + (d + d) + (d + 2 * d) + (d + inner) +
+                       (inner + 2 * d))
         return self.weight_bytes_per_layer() + act
 
     def kv_bytes_per_step(self):
