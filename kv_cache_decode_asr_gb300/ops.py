@@ -214,6 +214,9 @@ def asr_noalloc_scratch_bytes():
 
 def asr_cross_attn_step(q, cross, group, G, max_beams, heads, head_dim, frames, scale, out, ws,
                         dev_err=None, stream=None):
+    """q: f32 [B, >=H*hd] (row stride q.stride(0)); cross: f16 [G, >=frames,
+    2*H*hd] (group stride cross.stride(0)); group: int32 [B], non-decreasing,
+    at most max_beams sequences per group; out: f32 [B, H*hd]."""
     import torch
     _need(q, torch.float32, "q")
     _need(cross, torch.float16, "cross")
@@ -229,6 +232,10 @@ def asr_cross_attn_step(q, cross, group, G, max_beams, heads, head_dim, frames, 
 
 def asr_gqa_step(q, k_new, v_new, q_norm_w, k_norm_w, eps, rope_base, n_past, cache, capacity,
                  q_heads, kv_heads, head_dim, scale, out, ws, dev_err=None, stream=None):
+    """q: f32 [B, >=Hq*hd]; k_new, v_new: f32 [B, >=Hkv*hd] sharing one row
+    stride (for instance the thirds of a fused q/k/v projection); q_norm_w,
+    k_norm_w: f32 [hd]; n_past: int32 [B]; cache: f16 [B, capacity,
+    2*Hkv*hd] (row n_past written); out: f32 [B, Hq*hd]."""
     import torch
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (q_norm_w, "q_norm_w"),
                  (k_norm_w, "k_norm_w"), (out, "out")):
