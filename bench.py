@@ -80,29 +80,25 @@ def code_sha(rels):
     return h.hexdigest()[:16]
 
 
-TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+TRAFFIC_RECORDS = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def recorded_traffic(kernel_sources, workload, kernel):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
-    from the committed ncu summary table, if its row for this workload and
-    kernel was taken on the current code of the kernel; else None."""
+    of one kernel on one workload, from the committed ncu records, if the
+    record was taken on the current code of the kernel; else None."""
     try:
-        with open(TRAFFIC_TABLE) as f:
-            lines = f.read().splitlines()
-    except OSError:
+        with open(TRAFFIC_RECORDS) as f:
+            records = json.load(f)["records"]
+    except (OSError, ValueError, KeyError):
         return None
     sha = code_sha(kernel_sources)
-    for line in lines:
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) < 4 or cells[0] != workload or cells[1] != kernel:
-            continue
-        if cells[2] != sha:
-            return None
-        try:
-            return int(cells[3].replace(",", ""))
-        except ValueError:
-            return None
+    for r in records:
+        if r.get("workload") == workload and r.get("kernel") == kernel:
+            if r.get("code_sha") != sha:
+                return None
+            b = r.get("dram_bytes_per_launch")
+            return int(b) if isinstance(b, (int, float)) else None
     return None
 
 
@@ -358,40 +354,6 @@ class WhisperStep:
                 "frac": achieved / peak, "bytes_per_launch": b,
                 "peak_source": f"{src} hbm_gbs"}
 
-    # one small reference-arm unit: one sequence of one layer
-    def oracle_unit(self, i, oracle, cache):
-        l = i % self.L
-        b = (i // self.L) % self.B
-        if (l, b) not in cache:
-            import torch
-            src = self.cache_src[self.idx_host[b] if self.rearrange else b, l]
-            cache[(l, b)] = (
-                src.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)[None],
-                self.cross[l, self.group_host[b]].contiguous().view(torch.int16).cpu().numpy()
-                .view(np.uint16)[None],
-                self.qkv[l, b:b + 1].cpu().numpy(), self.qx[l, b:b + 1].cpu().numpy())
-            if len(cache) > 64:
-                cache.pop(next(iter(cache)))
-        sc, cr, qkv, qx = cache[(l, b)]
-        sc = sc.copy()
-        d = self.d
-        n = int(self.lens_eff[b])
-        t0 = time.perf_counter()
-        if self.rearrange:
-            dst = np.zeros_like(sc)[:, None]
-            oracle.kv_rearrange(sc[:, None], dst, np.zeros(1, np.int32), np.array([n], np.int32),
-                                self.cap)
-            sc = np.ascontiguousarray(dst[:, 0])
-        oracle.kv_append(qkv[:, d:2 * d], qkv[:, 2 * d:], sc, np.array([n - 1], np.int32), self.H,
-                         self.hd)
-        oracle.self_attn_step(qkv, sc, np.array([n], np.int32), self.H, self.hd, self.scale,
-                              q_stride=3 * d)
-        oracle.cross_attn_step(qx, cr, np.zeros(1, np.int32), self.H, self.hd, self.scale)
-        return time.perf_counter() - t0
-
-    def units_per_step(self):
-        return self.B * self.L
-
 
 class GqaStep:
     """Qwen3-ASR decode step: the fused GQA step per layer."""
@@ -486,28 +448,6 @@ class GqaStep:
 
     roofline = WhisperStep.roofline
 
-    def oracle_unit(self, i, oracle, cache):
-        import torch
-        l = i % self.L
-        b = (i // self.L) % self.B
-        if (l, b) not in cache:
-            cache[(l, b)] = (
-                self.cache[l, b:b + 1].contiguous().view(torch.int16).cpu().numpy()
-                .view(np.uint16),
-                [t[l, b:b + 1].cpu().numpy() for t in (self.q, self.kn, self.vn)],
-                [t[l].cpu().numpy() for t in (self.wq, self.wk)])
-            if len(cache) > 16:
-                cache.pop(next(iter(cache)))
-        c, acts, ws = cache[(l, b)]
-        c = c.copy()
-        t0 = time.perf_counter()
-        oracle.gqa_step(*acts, *ws, self.eps, self.base, self.n_past_host[b:b + 1], c, self.Hq,
-                        self.Hkv, self.hd, self.scale)
-        return time.perf_counter() - t0
-
-    def units_per_step(self):
-        return self.B * self.L
-
 
 class PrefillStep:
     """Qwen3-ASR batched prefill: RMSNorm + RoPE + cache write (a7) and the
@@ -598,32 +538,6 @@ class PrefillStep:
         dt = time.perf_counter() - t0
         return dt, 1.0 / self.B, {"out": ref[0]}, {"out": self.out[i].cpu().numpy()}, \
             f"sequence {i}"
-
-    def oracle_unit(self, i, oracle, cache):
-        """Reference-arm unit: one head of one sequence (its causal attention
-        over all positions, plus its share of the preparation)."""
-        import torch
-        b = (i // self.Hq) % self.B
-        h = i % self.Hq
-        if b not in cache:
-            h16 = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-            q, k, v = h16(self.q[b:b + 1]), h16(self.k[b:b + 1]), h16(self.v[b:b + 1])
-            c = np.zeros((1, self.cap, self.row), np.uint16)
-            t0 = time.perf_counter()
-            qhat = oracle.prefill_prep(q, k, v, self.wq.cpu().numpy(), self.wk.cpu().numpy(),
-                                       self.eps, self.base, self.Hq, self.Hkv, self.hd, c)
-            prep_s = time.perf_counter() - t0
-            cache.clear()
-            cache[b] = (qhat, c, prep_s)
-        qhat, c, prep_s = cache[b]
-        ts = np.arange(self.T, dtype=np.int32)
-        t0 = time.perf_counter()
-        oracle.prefill_attn_rows(qhat[0, :, h * self.hd:(h + 1) * self.hd], ts, c[0], self.Hq,
-                                 self.Hkv, self.hd, h, self.scale)
-        return time.perf_counter() - t0 + prep_s / self.Hq
-
-    def units_per_step(self):
-        return self.B * self.Hq
 
 
 class MhaAttnStep:
@@ -729,25 +643,6 @@ class MhaAttnStep:
         got = self.out[i, :L].cpu().numpy()
         return dt, L / self.tokens_per_step(), {"out": ref[0, :L]}, {"out": got}, f"sequence {i}"
 
-    def oracle_unit(self, i, oracle, cache):
-        """Reference-arm unit: one head of one sequence."""
-        b = (i // self.H) % self.B
-        h = i % self.H
-        if b not in cache:
-            cache.clear()
-            cache[b] = tuple(self._h16(t[b:b + 1]) for t in (self.q, self.k, self.v))
-        q, k, v = cache[b]
-        sl = slice(h * self.hd, (h + 1) * self.hd)
-        qh, kh, vh = (np.ascontiguousarray(x[:, :, sl]) for x in (q, k, v))
-        L = int(self.lens_host[b])
-        t0 = time.perf_counter()
-        oracle.mha_attn(qh, kh, vh, 1, self.hd, self.scale, self.causal,
-                        lens=np.array([L], np.int32))
-        return time.perf_counter() - t0
-
-    def units_per_step(self):
-        return self.B * self.H
-
 
 class CrossFillStep:
     """The cross K/V of one Large-Whisper decoder layer from the encoder
@@ -832,22 +727,6 @@ class CrossFillStep:
         # compared as the excess beyond one f16 step of the reference
         excess = np.maximum(np.abs(g - r) - ulp, 0.0)
         return dt, 1.0 / self.G, {"rows": np.zeros_like(excess)}, {"rows": excess}, f"utterance {i}"
-
-    def oracle_unit(self, i, oracle, cache):
-        """Reference-arm unit: 64 frames of one utterance."""
-        g = (i // 24) % self.G
-        t0 = (i % 24) * 64 % self.F
-        if "w" not in cache:
-            cache["w"] = self._h16(self.w)
-            cache["b"] = self.bias.cpu().numpy()
-        enc = self._h16(self.enc[g:g + 1, t0:t0 + 64])
-        ref = np.zeros((1, enc.shape[1], 2 * self.d), np.uint16)
-        t1 = time.perf_counter()
-        oracle.cross_kv_fill(enc, cache["w"], cache["b"], ref)
-        return (time.perf_counter() - t1) * self.F / enc.shape[1]
-
-    def units_per_step(self):
-        return self.G
 
 
 class DecoderStep(WhisperStep):
@@ -1003,31 +882,6 @@ class DecoderStep(WhisperStep):
         dt = time.perf_counter() - t0
         return dt, 1.0 / self.L, {"x": ref}, {"x": snaps[i + 1]}, f"layer {i}"
 
-    def oracle_unit(self, i, oracle, cache):
-        """Reference-arm unit: one sequence through one layer."""
-        import torch
-        l = i % self.L
-        b = (i // self.L) % self.B
-        if cache.get("layer") != l:
-            cache.clear()
-            cache["layer"] = l
-            cache["p"] = self._host_layer(l)
-        key = ("seq", b)
-        if key not in cache:
-            g = int(self.group_host[b])
-            cache[key] = (
-                self.cache[b:b + 1, l].contiguous().view(torch.int16).cpu().numpy()
-                .view(np.uint16),
-                self.cross[l, g:g + 1].contiguous().view(torch.int16).cpu().numpy()
-                .view(np.uint16),
-                self.x_in[b:b + 1].cpu().numpy())
-        sc, cr, x = cache[key]
-        sc = sc.copy()
-        t0 = time.perf_counter()
-        oracle.whisper_decoder_layer_step(x, cache["p"], sc, self.lens_eff[b:b + 1], cr,
-                                          np.zeros(1, np.int32), self.H, self.hd)
-        return time.perf_counter() - t0
-
 
 class QwenDecoderStep(GqaStep):
     """The whole Qwen3-ASR decoder step around the GQA step, five launches
@@ -1158,28 +1012,6 @@ class QwenDecoderStep(GqaStep):
         dt = time.perf_counter() - t0
         return dt, 1.0 / self.L, {"x": ref}, {"x": snaps[i + 1]}, f"layer {i}"
 
-    def oracle_unit(self, i, oracle, cache):
-        """Reference-arm unit: one sequence through one layer."""
-        import torch
-        l = i % self.L
-        b = (i // self.L) % self.B
-        if cache.get("layer") != l:
-            cache.clear()
-            cache["layer"] = l
-            cache["p"] = self._host_layer(l)
-        key = ("seq", b)
-        if key not in cache:
-            cache[key] = (
-                self.cache[l, b:b + 1].contiguous().view(torch.int16).cpu().numpy()
-                .view(np.uint16),
-                self.x_in[b:b + 1].cpu().numpy())
-        c, x = cache[key]
-        c = c.copy()
-        t0 = time.perf_counter()
-        oracle.qwen3_decoder_layer_step(x, cache["p"], c, self.n_past_host[b:b + 1], self.Hq,
-                                        self.Hkv, self.hd, eps=self.eps, rope_base=self.base)
-        return time.perf_counter() - t0
-
 
 def make_workload(name, device, rank=0, layers=0):
     cfg = dict(syn.WORKLOADS[name])
@@ -1258,6 +1090,131 @@ def cpu_count():
 
 # ------------------------------------------------------------- our arm ----
 
+# The five decode/prefill configurations the headline metric is stated for;
+# the default run measures each of them in the same process (``configs``).
+CONFIG_WORKLOADS = ["whisper_tiny_b1", "whisper_tiny_b64_beam5", "whisper_large_b32",
+                    "qwen3_asr_gqa_b16", "qwen3_asr_prefill_b8"]
+
+
+def capture_step(wl, stream):
+    """Run the step twice, then capture it in one CUDA graph."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            wl.step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        wl.step()
+    torch.cuda.synchronize()
+    if int(wl.err.item()) != 0:
+        raise RuntimeError(f"{wl.name}: device error flags {int(wl.err.item()):#x}")
+    return graph
+
+
+def time_graph(graph, stream, steps, warmup, world=1):
+    """Milliseconds of `steps` back-to-back replays (CUDA events on the
+    launching stream, barrier and synchronisation on both sides)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    stream.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
+
+
+def time_dominant(wl, stream):
+    """The dominant kernel: a CUDA graph of back-to-back launches of it, one
+    per layer (each on its own layer's data, together larger than L2), timed
+    with CUDA events on the launching stream; milliseconds per launch."""
+    import torch
+    dom_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dom_graph, stream=stream):
+        for l in range(wl.L):
+            wl.dominant_call(l)
+    reps = max(3, min(200, 2000 // max(wl.L, 1)))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dom_graph.replay()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(reps):
+            dom_graph.replay()
+        d1.record(stream)
+    d1.synchronize()
+    return d0.elapsed_time(d1) / (reps * wl.L)
+
+
+def step_fraction(wl, ms_step, peaks):
+    """The whole step against its roofline: K/V (or I/O) bytes per step for
+    the HBM-bound decode steps, FLOPs per step for the tensor-bound ones."""
+    if hasattr(wl, "flops"):
+        tf = wl.flops() / (ms_step / 1e3) / 1e12
+        return {"bound": "tensor", "step_tflops": tf, "step_frac_of_peak": tf / peaks["tensor"][0]}
+    gbs = wl.kv_bytes_per_step() / (ms_step / 1e3) / 1e9
+    return {"bound": "hbm", "kv_gbs": gbs, "step_frac_of_peak": gbs / peaks["hbm"][0]}
+
+
+def parity_check(wl, oracle, first_only=False, budget=10.0):
+    """Compare the GPU outputs of the timed step with the oracle on a bounded
+    sample of whole units (layers, sequences).  Returns (oracle seconds,
+    fraction of the step covered, max abs error, units done)."""
+    spent, frac, max_err, done = 0.0, 0.0, 0.0, []
+    i = 0
+    while i < wl.n_samples() and (i == 0 or (not first_only and spent < budget)):
+        dt, f, ref, got, what = wl.oracle_sample(i, oracle)
+        for k in ref:
+            max_err = max(max_err, float(np.abs(got[k] - ref[k]).max()))
+        spent += dt
+        frac += f
+        done.append(what)
+        i += 1
+    return spent, frac, max_err, done
+
+
+def measure_config(name, device, steps, warmup, peaks, oracle):
+    """One configuration of the headline metric, in this process: step time,
+    tokens/s, the step's fraction of its roofline, the dominant kernel's
+    fraction, and the oracle's max error on the first unit of the step."""
+    import torch
+    wl = make_workload(name, device)
+    stream = torch.cuda.Stream(device)
+    graph = capture_step(wl, stream)
+    ms_step = time_graph(graph, stream, steps, warmup) / steps
+    launch_ms = time_dominant(wl, stream)
+    roof = wl.roofline(launch_ms, peaks)
+    _, _, err, done = parity_check(wl, oracle, first_only=True)
+    entry = {"ms_per_step": ms_step, "tokens_per_s": wl.tokens_per_step() / (ms_step / 1e3),
+             "steps": steps, **step_fraction(wl, ms_step, peaks),
+             "dominant_kernel": wl.dominant_kernel, "dominant_launch_us": launch_ms * 1e3,
+             "dominant_frac_of_peak": roof["frac"], "dominant_bound": roof["bound"],
+             "parity_max_abs_err": err, "parity_checked": f"{done[0]} vs oracle"}
+    del graph, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def config_dict(args, wl, world, kv_bytes):
+    return {"workload": args.workload, **{k: v for k, v in wl.cfg.items()},
+            "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB touched per step "
+                  f"vs {L2_BYTES / 1e6:.0f} MB L2)",
+            "parallelism": f"replicas x{world} (batch per GPU fixed)"}
+
+
 def run_ours(args):
     import torch
     import oracle
@@ -1276,67 +1233,25 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
 
-    # ---- capture the whole step in one CUDA graph
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            wl.step()
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        wl.step()
-    torch.cuda.synchronize()
-    if int(wl.err.item()) != 0:
-        raise RuntimeError(f"device error flags {int(wl.err.item()):#x}")
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            graph.replay()
-    stream.synchronize()
-
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+    # ---- the whole step in one CUDA graph, K replays timed
+    graph = capture_step(wl, stream)
     with ClockSampler(local) as clocks:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            ev1.record(stream)
-        ev1.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
+        ms_total = time_graph(graph, stream, args.steps, args.warmup, world)
     ms_step, value = job_throughput(ms_total, args.steps, wl.tokens_per_step(), world, device)
     tokens = wl.tokens_per_step() * world
     kv_bytes = wl.kv_bytes_per_step()
     kv_gbs = kv_bytes * world / (ms_step / 1e3) / 1e9
 
-    # ---- dominant kernel: a CUDA graph of back-to-back launches of it, one
-    # per layer (each on its own layer's data, together larger than L2),
-    # timed with CUDA events on the launching stream; average per launch
     peaks = load_all_peaks()
-    dom_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(dom_graph, stream=stream):
-        for l in range(wl.L):
-            wl.dominant_call(l)
-    reps = max(3, min(200, 2000 // max(wl.L, 1)))
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            dom_graph.replay()
-        d0 = torch.cuda.Event(enable_timing=True)
-        d1 = torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        for _ in range(reps):
-            dom_graph.replay()
-        d1.record(stream)
-    d1.synchronize()
-    launch_ms = d0.elapsed_time(d1) / (reps * wl.L)
+    launch_ms = time_dominant(wl, stream)
     roof = wl.roofline(launch_ms, peaks)
     roof.update({"traffic": recorded_traffic(wl.kernel_sources, args.workload,
                                              wl.traffic_key()),
                  "kernel": wl.dominant_kernel, "launch_us": launch_ms * 1e3})
     extra = wl.extra_rooflines(stream, peaks) if hasattr(wl, "extra_rooflines") else {}
+
+    cfg_line = config_dict(args, wl, world, kv_bytes)
+    gpu_launches = wl.launches() * args.steps
 
     # ---- end to end through host buffers: per step, H2D of the step's
     # activations from pinned memory, the step, D2H of its outputs
@@ -1375,17 +1290,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_count()
         oracle.set_threads(threads)
-        budget = args.cpu_seconds
-        spent, frac, max_err, done = 0.0, 0.0, 0.0, []
-        i = 0
-        while i < wl.n_samples() and (i == 0 or spent < budget):
-            dt, f, ref, got, what = wl.oracle_sample(i, oracle)
-            for k in ref:
-                max_err = max(max_err, float(np.abs(got[k] - ref[k]).max()))
-            spent += dt
-            frac += f
-            done.append(what)
-            i += 1
+        spent, frac, max_err, done = parity_check(wl, oracle, budget=args.cpu_seconds)
         step_s = spent / frac
         cpu = {"value": wl.tokens_per_step() / step_s, "unit": "tokens/s", "cores": threads,
                "kind": "oracle",
@@ -1396,9 +1301,38 @@ def run_ours(args):
         if hasattr(wl, "parity_note"):
             parity["note"] = wl.parity_note
 
+    # ---- every configuration of the headline metric, same process and box,
+    # under one clock record (rank 0 at N = 1, default workload only)
+    configs = None
+    metric = wl.metric
+    if (rank == 0 and world == 1 and not args.no_configs and args.workload == DEFAULT_WORKLOAD
+            and not args.layers):
+        main_entry = {"ms_per_step": ms_step, "tokens_per_s": value, "steps": args.steps,
+                      **step_fraction(wl, ms_step, peaks),
+                      "dominant_kernel": wl.dominant_kernel,
+                      "dominant_launch_us": launch_ms * 1e3,
+                      "dominant_frac_of_peak": roof["frac"], "dominant_bound": roof["bound"],
+                      "parity_max_abs_err": parity["max_abs_err"] if parity else None,
+                      "parity_checked": parity["checked"] if parity else None,
+                      "note": "the main line's own measurement"}
+        metric = wl.metric
+        del graph, wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        oracle.set_threads(cpu_count())
+        configs = {}
+        with ClockSampler(local) as cclocks:
+            for name in CONFIG_WORKLOADS:
+                if name == args.workload:
+                    configs[name] = main_entry
+                else:
+                    configs[name] = measure_config(name, device, min(args.steps, 200),
+                                                   args.warmup, peaks, oracle)
+        configs["clocks"] = cclocks.summary()
+
     if rank == 0:
         line = {
-            "metric": wl.metric,
+            "metric": metric,
             "value": value,
             "unit": "tokens/s",
             "n_gpus": world,
@@ -1410,10 +1344,7 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "f16 K/V, fp32 math",
             "data": "synthetic (seeded N(0,1); no weights or audio)",
-            "config": {"workload": args.workload, **{k: v for k, v in wl.cfg.items()},
-                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB touched per step "
-                             f"vs {L2_BYTES / 1e6:.0f} MB L2)",
-                       "parallelism": f"replicas x{world} (batch per GPU fixed)"},
+            "config": cfg_line,
             "kv_gbs": kv_gbs,
             "kv_frac_of_hbm": kv_gbs / world / peaks["hbm"][0],
             "kv_bytes_per_step": kv_bytes,
@@ -1422,10 +1353,12 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": wl.launches() * args.steps,
+            "gpu_launches": gpu_launches,
             "cpu_baseline": cpu,
             "parity": parity,
         }
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -1435,8 +1368,10 @@ def run_ours(args):
 # ------------------------------------------------------- reference arm ----
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step is one bounded unit of
-    the workload (one sequence of one layer), scaled to the whole step."""
+    """The CPU oracle as the reference arm.  Each timed step is one whole
+    unit of the workload as the CPU baseline takes it (one layer of every
+    sequence; one sequence of a prefill), so `steps` x `ms_per_step` is the
+    oracle time actually spent; `value` scales a unit to the whole step."""
     world, rank, local = dist_setup(args)
     if rank != 0:
         return
@@ -1450,24 +1385,32 @@ def run_reference(args):
     if wl is None:
         print(json.dumps({"impl": "reference", "unavailable": "needs the device-drawn inputs"}))
         return
-    cache = {}
+    n = wl.n_samples()
     for i in range(args.warmup):
-        wl.oracle_unit(i, oracle, cache)
-    times = [wl.oracle_unit(args.warmup + i, oracle, cache) for i in range(args.steps)]
+        wl.oracle_sample(i % n, oracle)
+    times, fracs = [], []
+    for i in range(args.steps):
+        dt, f, _, _, _ = wl.oracle_sample((args.warmup + i) % n, oracle)
+        times.append(dt)
+        fracs.append(f)
     unit_s = sum(times) / len(times)
-    step_s = unit_s * wl.units_per_step()
+    step_s = sum(times) / sum(fracs)
     value = wl.tokens_per_step() / step_s
+    kv_bytes = wl.kv_bytes_per_step()
     line = {
         "impl": "reference",
         "metric": wl.metric,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": unit_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded N(0,1); no weights or audio)",
-        "config": {"workload": args.workload, **wl.cfg},
+        "config": config_dict(args, wl, world, kv_bytes),
+        "units_per_workload_step": round(1.0 / (sum(fracs) / len(fracs)), 3),
+        "workload_step_ms": step_s * 1e3,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: one unit ({wl.units_per_step()} per "
-                                   f"workload step), scaled to the whole step"},
+                         "sample": f"each timed step is one whole unit of the workload "
+                                   f"({n} units make one workload step; "
+                                   f"ms_per_step is the oracle time of one unit)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1482,6 +1425,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate-append", action="store_true",
                     help="Whisper: launch the K/V append and the self-attention separately")

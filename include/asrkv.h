@@ -379,7 +379,10 @@ int asr_linear(const float* x, int64_t x_stride, int norm, const float* norm_w,
  * device current; make that first call before any stream capture.  Each call
  * enqueues a small memset (the counters) and the kernel, and allocates
  * nothing.  All calls on a device share the array: calls that can overlap on
- * the GPU (unordered streams) race and give wrong results. */
+ * the GPU (unordered streams) race and give wrong results.  The address is
+ * kept for the life of the process: after cudaDeviceReset on a device that
+ * has had a call, this entry point must not be used on it again (the reset
+ * unloads the array and the kept address would be stale). */
 int asr_self_attn_step_noalloc(const float* q, int64_t q_stride, const uint16_t* cache,
                                int64_t seq_stride, const int32_t* lens, int B, int heads,
                                int head_dim, int capacity, float scale, float* out,
@@ -401,6 +404,18 @@ const char* asr_status_string(int status);
 
 /* ABI version (major*100 + minor). */
 int asr_version(void);
+
+/* Test support for the bounded waits (no counterpart in the pages).  Arms the
+ * next decode-attention launch (asr_self_attn_step, asr_self_attn_append_step,
+ * asr_cross_attn_step, asr_gqa_step or asr_self_attn_step_noalloc) made by
+ * the calling host thread: its producer issues no copies, so every pipeline
+ * wait of that launch runs out after wait_ns nanoseconds (0 < wait_ns <= 2 s).
+ * The kernel then sets ASR_DEVERR_TIMEOUT in dev_err, passes over its
+ * remaining work without waiting and returns; its outputs are undefined, the
+ * workspace counters are left at zero, and the next call works normally.
+ * Nothing faults or hangs.  Returns ASR_OK, or ASR_ERR_INVALID_ARG for a
+ * wait_ns out of range (the launch is then not armed). */
+int asr_debug_stall_next_decode(uint64_t wait_ns);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,37 @@ int device_sm_count() {
   return cached[dev];
 }
 
+cudaError_t ensure_dynamic_smem(const void* fn, int bytes) {
+  struct Entry {
+    const void* fn;
+    int dev, bytes;
+  };
+  static Entry done[256];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  for (int i = 0; i < n; ++i)
+    if (done[i].fn == fn && done[i].dev == dev) {
+      done[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (n < 256) done[n++] = {fn, dev, bytes};
+  return cudaSuccess;
+}
+
 }  // namespace asrkv
 
 using namespace asrkv;

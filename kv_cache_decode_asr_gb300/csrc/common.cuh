@@ -21,6 +21,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // 0 if no device is usable.
 int device_sm_count();
 
+// Let kernel `fn` use `bytes` of dynamic shared memory on the current device.
+// The setting belongs to a (device, kernel) pair, so it is made once per
+// device the kernel is launched on and remembered only when it succeeded (a
+// failure is retried on the next call).  Returns the CUDA status.
+cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
+
 // Launch with the Programmatic-Dependent-Launch attribute so the grid may be
 // scheduled while the previous kernel on the stream drains; every kernel
 // launched this way executes griddepcontrol.wait before touching memory that
@@ -106,13 +112,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false if kWaitLimitNs passed first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// false if limit_ns (default kWaitLimitNs) passed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -195,8 +195,6 @@ cross_fill_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant_
   }
 }
 
-static std::once_flag g_fill_attr;
-
 }  // namespace asrkv
 
 using namespace asrkv;
@@ -212,12 +210,8 @@ extern "C" int asr_cross_kv_fill(const uint16_t* enc, const uint16_t* w, const f
   if (!aligned16(enc) || !aligned16(w) || !aligned16(bias_v) || !aligned16(cross) ||
       group_stride % 8 != 0)
     return ASR_ERR_MISALIGNED;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(g_fill_attr, [] {
-    attr = cudaFuncSetAttribute(cross_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kFillSmem);
-  });
-  if (attr != cudaSuccess) return ASR_ERR_CUDA;
+  if (ensure_dynamic_smem((const void*)cross_fill_kernel, kFillSmem) != cudaSuccess)
+    return ASR_ERR_CUDA;
   // A: enc (dims d, frames, G); B: W (dims d, 2d)
   CUtensorMap ta, tb;
   if (!make_tmap_f16_3d(&ta, enc, d, frames, G, (uint64_t)d * 2, (uint64_t)frames * d * 2, kFillBK,

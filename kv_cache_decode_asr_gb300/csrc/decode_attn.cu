@@ -1,21 +1,26 @@
 // decode_attn.cu -- one-token attention over f16 K/V caches (a2, a3, a4, a5).
 //
-// Method: split-K flash-decoding with a log-sum-exp combine.  Every
-// (source, key) pair of a call is laid on one flattened key axis (source =
-// the sequence for self-attention and the GQA step, the beam group for
-// cross-attention) and a persistent grid of P CTAs takes equal contiguous
-// shares of it, so variable lengths stay balanced to within one tile.  A CTA
-// streams its share as tiles of whole cache rows (K and V of every head are
-// contiguous in a row) with one bulk TMA copy per tile into a multi-stage
-// shared-memory ring (mbarrier full/empty pairs, one producer warp).  The
-// consumer threads form groups of G = HD/DPL lanes (DPL = 16 dims per lane
-// for one or two queries, 8 for four or eight); a group owns one KV head,
-// keeps its queries (all beams of the group x all query heads of the KV
-// head) in registers, and runs an online softmax in the log2 domain over the
-// rows it is given.  At the end of a source's piece the row
-// slots are merged in shared memory; a source split over several CTAs leaves
-// (max, sum, unnormalised output) partials in the workspace and the last CTA
-// to finish it (atomic ticket, no waiting) merges them and writes the output.
+// Method: split-K flash-decoding with a log-sum-exp combine.  The work of a
+// call is cut into units: a unit is one source (the sequence for
+// self-attention and the GQA step, the beam group for cross-attention) and
+// one group of hs of its KV heads (HS = Hkv / hs groups per source; HS = 1
+// when the sources are short next to a CTA's share).  Every (unit, key)
+// pair lies on one flattened key axis and a persistent grid of P CTAs takes
+// equal contiguous shares of it, so variable lengths stay balanced to within
+// one tile.  A CTA streams its share as tiles of cache rows into a
+// multi-stage shared-memory ring (mbarrier full/empty pairs, one producer
+// warp): whole rows with one bulk TMA copy per tile when HS = 1, else the
+// unit's K and V chunks of each row through a 5-D tensor map.  The consumer
+// threads form groups of G = HD/DPL lanes (DPL = 16 dims per lane for one or
+// two queries, 8 for four or eight); a group owns one KV head of the unit,
+// keeps its queries (beams of the group x query heads of the KV head) in
+// registers, and runs an online softmax in the log2 domain over the rows it
+// is given.  At the end of a unit's piece the row slots are merged in shared
+// memory (a tree); a unit split over several CTAs leaves (max, sum,
+// unnormalised output) partials in the workspace and the last CTA to finish
+// it (atomic ticket, no waiting) merges them and writes the output.  Cutting
+// a long source into head groups divides both the number of partials of a
+// unit and the query heads each holds, so that last merge stays short.
 //
 // Semantics follow: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
 // (attend over pos+1 own rows and over all cross frames); "Nest whisper-tiny,
@@ -27,58 +32,22 @@
 #include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
-#include <string.h>
 
 #include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
 #include "decode_attn.cuh"
+#include "tcgen05.cuh"
 
 namespace asrkv {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Merges a CTA defers to the end of its tiles.  Only a unit that crosses an
+// end of the CTA's share has pieces in other CTAs, so a CTA takes at most two
+// tickets per launch.
+constexpr int kMergeList = 2;
 constexpr unsigned kFull = 0xffffffffu;
-
-// In-place exclusive scan of data[0..n) by threads 0..nt-1 (nt a multiple of
-// 32; they synchronise on named barrier 1); data[n] gets the total.  tmp: 32
-// ints of shared memory.  All nt threads must call it.
-__device__ void block_scan_excl(int* data, int n, int* tmp, int nt) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = (nt + 31) >> 5;
-  const int chunk = (n + nt - 1) / nt;
-  const int s = min(tid * chunk, n), e = min(s + chunk, n);
-  int local = 0;
-  for (int i = s; i < e; ++i) local += data[i];
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) tmp[warp] = incl;
-  named_bar(1, nt);
-  if (warp == 0) {
-    const int v = lane < nw ? tmp[lane] : 0;
-    int inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(kFull, inc, o);
-      if (lane >= o) inc += t;
-    }
-    if (lane < nw) tmp[lane] = inc - v;
-  }
-  named_bar(1, nt);
-  int run = tmp[warp] + incl - local;
-  for (int i = s; i < e; ++i) {
-    const int v = data[i];
-    data[i] = run;
-    run += v;
-  }
-  if (s < e && e == n) data[n] = run;
-  if (n == 0 && tid == 0) data[0] = 0;
-  named_bar(1, nt);
-}
 
 // History rows of one self / GQA source that the call streams, from its
 // length entry (0 for an out-of-range entry).  Self: keys including the new
@@ -89,19 +58,39 @@ __device__ __forceinline__ int streamed_rows(const DecodeArgs& a, int v) {
   return (v >= 0 && v < a.capacity) ? v : 0;
 }
 
-// Exclusive scan by one warp of the streamed-row counts of every self / GQA
-// source (plus its virtual rows) into off[0..S]; returns the total.
-__device__ int warp_scan_sources(const DecodeArgs& a, int* off, int S, int lane, bool cg) {
+// Offsets of the sources on the flattened key axis, computed by one warp:
+// off[g] = HS * sum over g' < g of (virtual rows + streamed rows of g'),
+// off[S] = the total (returned).  A source with nothing to stream takes no
+// room.  Cross: a group is streamed when some sequence belongs to it (the
+// flags go through off[] itself, which is then scanned in place); returns -1
+// when the group indices are not sorted.  cg: read the inputs from L2 only
+// (the early, hint-only pass before the grid dependency wait).
+__device__ int warp_offsets(const DecodeArgs& a, int* off, int S, int lane, bool cg,
+                             int* lens_out = nullptr) {
+  if (a.mode == kModeCross) {
+    for (int g = lane; g <= S; g += 32) off[g] = 0;
+    __syncwarp();
+    bool unsorted = false;
+    for (int b = lane; b < a.B; b += 32) {
+      const int gr = cg ? __ldcg(a.group + b) : a.group[b];
+      if (b > 0 && (cg ? __ldcg(a.group + b - 1) : a.group[b - 1]) > gr) unsorted = true;
+      if (gr >= 0 && gr < S) off[gr] = 1;  // every writer stores the same value
+    }
+    if (__any_sync(kFull, unsorted)) return -1;
+    __syncwarp();
+  }
   int run = 0;
   for (int base = 0; base < S; base += 32) {
     const int g = base + lane;
     int keys = 0;
     if (g < S) {
       if (a.mode == kModeCross) {
-        keys = a.fixed_len + a.seg_rows;  // as if every group had members
+        keys = off[g] ? a.HS * (a.fixed_len + a.seg_rows) : 0;
       } else {
-        const int k = streamed_rows(a, cg ? __ldcg(a.lens + g) : a.lens[g]);
-        keys = k > 0 ? k + a.seg_rows : 0;
+        const int v = cg ? __ldcg(a.lens + g) : a.lens[g];
+        if (lens_out) lens_out[g] = v;
+        const int k = streamed_rows(a, v);
+        keys = k > 0 ? a.HS * (k + a.seg_rows) : 0;
       }
     }
     int incl = keys;
@@ -110,6 +99,7 @@ __device__ int warp_scan_sources(const DecodeArgs& a, int* off, int S, int lane,
       const int t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
+    __syncwarp();
     if (g < S) off[g] = run + incl - keys;
     run += __shfl_sync(kFull, incl, 31);
   }
@@ -119,24 +109,61 @@ __device__ int warp_scan_sources(const DecodeArgs& a, int* off, int S, int lane,
 }
 
 struct Tile {
-  int g;       // source
+  int u;       // unit (source g, head group hg): u = g * HS + hg
+  int g, hg;
   int row0;    // first row within the source
   int nr;      // rows in this tile
-  bool first;  // first tile of this CTA's piece of source g
-  bool last;   // last tile of this CTA's piece of source g
+  bool first;  // first tile of this CTA's piece of unit u
+  bool last;   // last tile of this CTA's piece of unit u
 };
 
+// Where unit u lies on the flattened axis: its first real row go and its
+// real rows gl (gl <= 0: the unit streams nothing).  Each unit of a source
+// spans the same length: vrows virtual rows (never loaded; they charge the
+// CTA that enters the unit for its per-unit work) then the source's rows.
+// The axis fits in int (checked on the host), so 32-bit arithmetic serves.
+struct UnitSpan {
+  int go, gl;
+};
+__device__ __forceinline__ UnitSpan unit_span(const int* off, int HS, int vrows, int u) {
+  const int g = HS == 1 ? u : u / HS, hg = u - g * HS;
+  const int base = off[g];
+  const int len = HS == 1 ? off[g + 1] - base : (off[g + 1] - base) / HS;
+  return {base + hg * len + vrows, len - vrows};
+}
+
+// Cross: the first sequence of each group.  The groups are sorted, so the
+// first sequence of group g is the first b with group[b] >= g: sequence b
+// (with group[-1] = -1 and group[B] = S, values clamped into [-1, S]) sets
+// m[g] = b for every g in (group[b-1], group[b]].  Threads t, t + nt, ...
+__device__ __forceinline__ void first_members(const DecodeArgs& a, int* m, int S, int t, int nt) {
+  for (int b = t; b <= a.B; b += nt) {
+    const int cur = b < a.B ? min(max(a.group[b], -1), S) : S;
+    const int prev = b > 0 ? min(max(a.group[b - 1], -1), S) : -1;
+    for (int g = prev + 1; g <= cur; ++g) m[g] = b;
+  }
+}
+
+// Does CTA c hold the first real row of unit u?  That CTA folds the new
+// token in (append).  A unit with no cached rows is folded by the CTA that
+// handles it alone.
+__device__ __forceinline__ bool owns_first_row(const int* off, int HS, int vrows, int share, int u,
+                                               int c) {
+  const UnitSpan sp = unit_span(off, HS, vrows, u);
+  return sp.gl <= 0 || sp.go / share == c;
+}
+
 // Walks the tiles of the key range [k, k1) in order; the producer and the
-// consumers run identical copies.  Each non-empty source g spans
-// [off[g], off[g+1]) on the flattened axis: a head of `vrows` virtual rows
-// (never loaded; they charge the CTA that enters the source for its
-// per-source work) followed by its real rows.
+// consumers run identical copies.  It steps from unit to unit without
+// dividing (one division places the start).
 struct TileIter {
   const int* off;
-  int S, tile_rows, vrows, g, prev_g;
-  int64_t k, k1;
-  __device__ TileIter(const int* off_, int S_, int64_t k0, int64_t k1_, int tr, int vr)
-      : off(off_), S(S_), tile_rows(tr), vrows(vr), g(0), prev_g(-1), k(k0), k1(k1_) {
+  int S, HS, tile_rows, vrows;
+  int g, hg, ustart, len, prev_u;
+  int k, k1;
+  __device__ TileIter(const int* off_, int S_, int HS_, int k0, int k1_, int tr, int vr)
+      : off(off_), S(S_), HS(HS_), tile_rows(tr), vrows(vr), g(0), hg(0), ustart(0), len(0),
+        prev_u(-1), k(k0), k1(k1_) {
     if (k0 < k1_) {
       int lo = 0, hi = S_;  // largest g < S with off[g] <= k0
       while (hi - lo > 1) {
@@ -144,29 +171,68 @@ struct TileIter {
         if (off[mid] <= k0) lo = mid;
         else hi = mid;
       }
+      while (off[lo + 1] <= k0) ++lo;  // skip sources that take no room
       g = lo;
+      len = HS == 1 ? off[g + 1] - off[g] : (off[g + 1] - off[g]) / HS;
+      hg = HS == 1 ? 0 : (k0 - off[g]) / len;
+      ustart = off[g] + hg * len;
     }
   }
   __device__ bool next(Tile& t) {
     if (k >= k1) return false;
-    while (off[g + 1] <= k) ++g;
-    const int64_t real0 = (int64_t)off[g] + vrows;  // < off[g + 1]: a source has a real row
+    while (k >= ustart + len) {  // the next unit: same source, else the next source with room
+      if (++hg == HS) {
+        hg = 0;
+        do {
+          ++g;
+        } while (off[g + 1] == off[g]);
+        len = HS == 1 ? off[g + 1] - off[g] : (off[g + 1] - off[g]) / HS;
+        ustart = off[g];
+      } else {
+        ustart += len;
+      }
+    }
+    const int real0 = ustart + vrows;  // < ustart + len: a unit has a real row
     if (k < real0) {
       k = real0;
       if (k >= k1) return false;
     }
-    const int64_t end = min((int64_t)off[g + 1], k1);
-    const int nr = (int)min((int64_t)tile_rows, end - k);
+    const int end = min(ustart + len, k1);
+    const int nr = min(tile_rows, end - k);
     t.g = g;
-    t.row0 = (int)(k - real0);
+    t.hg = hg;
+    t.u = g * HS + hg;
+    t.row0 = k - real0;
     t.nr = nr;
-    t.first = g != prev_g;
+    t.first = t.u != prev_u;
     t.last = k + nr == end;
-    prev_g = g;
+    prev_u = t.u;
     k += nr;
     return true;
   }
 };
+
+// Tiled 5-D TMA load of one box into shared memory, completing its bytes on
+// bar, with an L2 cache policy.  c0 (innermost) is always 0 here.
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c1, int c2,
+                                            int c3, int c4, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// Hint: bring one box of a 5-D tensor into L2 (writes nothing, completes
+// nothing).
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* map, int c1, int c2, int c3,
+                                                int c4) {
+  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
 
 // ---- packed fp32 pairs and the fast base-2 exponential ---------------------
 
@@ -304,41 +370,45 @@ __device__ __forceinline__ void rope_table(float* rope, const float* turns, int 
   }
 }
 
-// Merge the (max, sum, output) states of row slots 1..R-1 into row slot 0
-// through shared memory.  Called by all consumer threads.
+// Merge the (max, sum, output) states of the R row slots into row slot 0
+// through shared memory, as a tree: at each level the upper half of the
+// remaining slots hands its state to the lower half.  Called by all consumer
+// threads; merge holds R/2 entries of Hv x NQ states.
 template <int HD, int NQ, int DPL>
 __device__ __forceinline__ void merge_row_slots(float (&M)[NQ], float (&Ls)[NQ],
                                                 float2 (&O)[NQ][DPL / 2], float* merge, int r,
-                                                int R, int h, int Hkv, int li, int sw, int nq,
+                                                int R, int hv, int Hv, int li, int sw, int nq,
                                                 int n_cons) {
   using LL = LaneLayout<HD, DPL>;
-  named_bar(1, n_cons);
-  if (r > 0) {
-#pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) {
-      if (qi < nq) {
-        float* mb = merge + (((r - 1) * Hkv + h) * NQ + qi) * (HD + 4);
-#pragma unroll
-        for (int j = 0; j < LL::NCH; ++j) {
-          float4* dst = reinterpret_cast<float4*>(mb + LL::chunk_off(li, j, sw));
-          dst[0] = make_float4(O[qi][4 * j].x, O[qi][4 * j].y, O[qi][4 * j + 1].x, O[qi][4 * j + 1].y);
-          dst[1] = make_float4(O[qi][4 * j + 2].x, O[qi][4 * j + 2].y, O[qi][4 * j + 3].x,
-                               O[qi][4 * j + 3].y);
-        }
-        if (li == 0) {
-          mb[HD] = M[qi];
-          mb[HD + 1] = Ls[qi];
-        }
-      }
-    }
-  }
-  named_bar(1, n_cons);
-  if (r == 0) {
-    for (int r2 = 1; r2 < R; ++r2) {
+  for (int n = R; n > 1;) {
+    const int half = (n + 1) >> 1;
+    named_bar(1, n_cons);  // the previous readers of the buffer are done
+    if (r >= half && r < n) {
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
         if (qi < nq) {
-          const float* mb = merge + (((r2 - 1) * Hkv + h) * NQ + qi) * (HD + 4);
+          float* mb = merge + (((r - half) * Hv + hv) * NQ + qi) * (HD + 4);
+#pragma unroll
+          for (int j = 0; j < LL::NCH; ++j) {
+            float4* dst = reinterpret_cast<float4*>(mb + LL::chunk_off(li, j, sw));
+            dst[0] = make_float4(O[qi][4 * j].x, O[qi][4 * j].y, O[qi][4 * j + 1].x,
+                                 O[qi][4 * j + 1].y);
+            dst[1] = make_float4(O[qi][4 * j + 2].x, O[qi][4 * j + 2].y, O[qi][4 * j + 3].x,
+                                 O[qi][4 * j + 3].y);
+          }
+          if (li == 0) {
+            mb[HD] = M[qi];
+            mb[HD + 1] = Ls[qi];
+          }
+        }
+      }
+    }
+    named_bar(1, n_cons);
+    if (r < n - half) {
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) {
+        if (qi < nq) {
+          const float* mb = merge + ((r * Hv + hv) * NQ + qi) * (HD + 4);
           const float m2 = mb[HD], l2 = mb[HD + 1];
           const float mn = fmaxf(M[qi], m2);
           if (mn != -INFINITY) {
@@ -359,42 +429,47 @@ __device__ __forceinline__ void merge_row_slots(float (&M)[NQ], float (&Ls)[NQ],
         }
       }
     }
+    n = half;
   }
 }
 
-// The last CTA to finish source g merges the partials of every piece of it
-// (its own among them): each consumer thread takes 4 consecutive output
-// values of one query and combines that slice over pieces first..lastp, 4
-// pieces per L2 round trip, then writes it normalised.
+// The last CTA to finish unit u (source g, head group hg) merges the
+// partials of every piece of it (its own among them): each consumer thread
+// takes 4 consecutive output values of one query and combines that slice
+// over pieces first..lastp, 8 pieces per L2 round trip, then writes it
+// normalised.  The piece of CTA c sits in partial slot c + u.
 template <int HD>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int g, int first, int lastp,
-                                             int members, int mbase, int tid, int n_cons) {
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int u, int hg, int first,
+                                             int lastp, int members, int mbase, int tid,
+                                             int n_cons) {
   constexpr int U4 = HD / 4;
+  constexpr int KB = 8;
+  const int hqu = a.hs * a.rep;  // query heads of a unit
   const int qw = a.Hq * HD;
-  const int nunits = members * a.Hq * U4;
-  for (int u = tid; u < nunits; u += n_cons) {
-    const int d0 = (u % U4) * 4;
-    const int qh = u / U4;  // member * Hq + query head
-    const int mem = qh / a.Hq, hq = qh % a.Hq;
+  const int nunits = members * hqu * U4;
+  for (int x = tid; x < nunits; x += n_cons) {
+    const int d0 = (x % U4) * 4;
+    const int mj = x / U4;  // member * hqu + query head within the unit
+    const int mem = mj / hqu, j = mj - mem * hqu;
     float M = -INFINITY, Lsum = 0.f;
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    for (int kb = first; kb <= lastp; kb += 4) {
-      float2 ml[4];
-      float4 x[4];
+    for (int kb = first; kb <= lastp; kb += KB) {
+      float2 ml[KB];
+      float4 xv[KB];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < KB; ++i) {
         if (kb + i <= lastp) {
-          const int64_t pidx = ((int64_t)(kb + i + g) * a.max_members + mem) * a.Hq + hq;
+          const int64_t pidx = ((int64_t)(kb + i + u) * a.max_members + mem) * hqu + j;
           ml[i] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
-          x[i] = ld_cg_f4(a.part_o + pidx * HD + d0);
+          xv[i] = ld_cg_f4(a.part_o + pidx * HD + d0);
         } else {
           ml[i] = make_float2(-INFINITY, 0.f);
-          x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       float mb = M;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mb = fmaxf(mb, ml[i].x);
+      for (int i = 0; i < KB; ++i) mb = fmaxf(mb, ml[i].x);
       if (mb == -INFINITY) continue;
       const float ca = ex2(M - mb);
       const float2 ca2 = make_float2(ca, ca);
@@ -402,17 +477,17 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int g, int fir
       acc0 = fmul2(acc0, ca2);
       acc1 = fmul2(acc1, ca2);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < KB; ++i) {
         const float c = ex2(ml[i].x - mb);  // 0 for an absent piece
         const float2 c2 = make_float2(c, c);
         Lsum = fmaf(ml[i].y, c, Lsum);
-        acc0 = ffma2(c2, make_float2(x[i].x, x[i].y), acc0);
-        acc1 = ffma2(c2, make_float2(x[i].z, x[i].w), acc1);
+        acc0 = ffma2(c2, make_float2(xv[i].x, xv[i].y), acc0);
+        acc1 = ffma2(c2, make_float2(xv[i].z, xv[i].w), acc1);
       }
       M = mb;
     }
     const float inv = 1.0f / Lsum;
-    *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + hq * HD + d0) =
+    *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + j) * HD + d0) =
         make_float4(acc0.x * inv, acc0.y * inv, acc1.x * inv, acc1.y * inv);
   }
 }
@@ -422,24 +497,33 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   using LL = LaneLayout<HD, DPL>;
   constexpr int G = LL::G, NP = LL::NP, NCH = LL::NCH;
   extern __shared__ __align__(128) unsigned char smem[];
-  const int Hv = a.MS * a.Hkv;  // virtual heads: (query split, KV head)
-  const DecodeSmem lay = decode_smem_layout(a.stages, a.n_src, a.R, Hv, NQ, HD, a.stage_elems);
+  const int hs = a.hs, HS = a.HS;
+  const int Hv = a.MS * hs;  // virtual heads of a unit: (query split, KV head of the group)
+  const DecodeSmem lay =
+      decode_smem_layout(a.stages, a.n_src, a.R, Hv, NQ, HD, a.stage_elems);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + a.stages;
-  int* ctl = reinterpret_cast<int*>(smem + lay.ctl);  // [0] abort [1] ticket [2] unsorted
+  // ctl: [0] abort, [1] ticket, [2] unsorted groups, [3] units to merge,
+  // [4 .. 4 + kMergeList) those units
+  int* ctl = reinterpret_cast<int*>(smem + lay.ctl);
   int* off = reinterpret_cast<int*>(smem + lay.off);
   int* mst = reinterpret_cast<int*>(smem + lay.mstart);
   int* poff_region = reinterpret_cast<int*>(smem + lay.poff);  // the producer's offsets
+  int* slen = reinterpret_cast<int*>(smem + lay.slen);         // length entry per source
   float* rope = reinterpret_cast<float*>(smem + lay.rope);
   float* wts = reinterpret_cast<float*>(smem + lay.wts);  // GQA: RMSNorm weights of q, k
   float* merge = reinterpret_cast<float*>(smem + lay.merge);
   uint16_t* stage = reinterpret_cast<uint16_t*>(smem + lay.stage);
+  volatile int* abort_flag = ctl;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_cons = a.R * Hv * G;  // a multiple of 32
   const int cons_warps = n_cons >> 5;
   const int S = a.n_src;
   const int qw = a.Hq * HD;
+  const int chunk = a.chunk_elems;  // f16 per row chunk in a stage
+  const uint32_t chunk_bytes = (uint32_t)chunk * 2u;
+  const int hqu = hs * a.rep;  // query heads of a unit
 
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -457,26 +541,67 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   // ---- L2 prefetch of the head of this CTA's share, before the wait.  The
   // K/V history of a step was written by earlier steps, so while the
   // previous kernel drains, the producer warp asks L2 for the first pf_bytes
-  // of its share.  The lengths are read here only to place these hints (from
-  // L2, bypassing L1); whatever they hold, every address stays inside the
-  // K/V buffer, and a prefetch writes nothing and is never seen by a load, so
-  // the hint cannot change a result.  Its offsets go to the stage ring, which
-  // nothing touches before this warp's first copy.
-  if (warp == cons_warps && a.pf_bytes > 0 && (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
+  // of its share.  The lengths (groups) are read here only to place these
+  // hints (from L2, bypassing L1); whatever they hold, every address stays
+  // inside the K/V buffer, and a prefetch writes nothing and is never seen by
+  // a load, so the hint cannot change a result.  Its offsets go to the stage
+  // ring, which nothing touches before this warp's first copy.
+  if (warp == cons_warps && !a.stall && a.pf_bytes > 0 &&
+      (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
     int* poff = reinterpret_cast<int*>(stage);
-    const int run = warp_scan_sources(a, poff, S, lane, true);
-    int64_t pshare = ((int64_t)run + gridDim.x - 1) / gridDim.x;
-    if (pshare < a.min_share) pshare = a.min_share;
-    const int64_t pk0 = (int64_t)blockIdx.x * pshare, pk1 = min(pk0 + pshare, (int64_t)run);
-    if (lane == 0 && pk0 < pk1) {
-      TileIter it(poff, S, pk0, pk1, a.tile_rows, a.seg_rows);
-      Tile tl;
-      int left = a.pf_bytes;
-      while (left > 0 && it.next(tl)) {
-        const uint32_t bytes = (uint32_t)tl.nr * (uint32_t)a.row_elems * 2u;
-        bulk_prefetch_l2(a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
-                         bytes);
-        left -= (int)bytes;
+    const int run = warp_offsets(a, poff, S, lane, true);
+    if (run > 0) {
+      const int pshare = max((int)((run + gridDim.x - 1) / gridDim.x), a.min_share);
+      const int pk0 = (int)min((int64_t)blockIdx.x * pshare, (int64_t)run);
+      const int pk1 = min(pk0 + pshare, run);
+      // the query rows (and the new token's k, v rows) of the sources the
+      // share starts: the same hint, so that the first loads after the wait
+      // find them in L2 instead of queueing behind everyone's K/V streams
+      if (pk0 < pk1) {
+        int lo = 0, hi = S;  // the sources holding pk0 and pk1 - 1
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (poff[mid] <= pk0) lo = mid;
+          else hi = mid;
+        }
+        const int g0 = lo;
+        hi = S;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (poff[mid] <= pk1 - 1) lo = mid;
+          else hi = mid;
+        }
+        const int g1 = min(lo, g0 + 63);
+        const uint32_t qbytes = (uint32_t)a.Hq * HD * 4;
+        if (a.mode == kModeCross) {
+          for (int b = lane; b < a.B; b += 32) {
+            const int gr = __ldcg(a.group + b);
+            if (gr >= g0 && gr <= g1) bulk_prefetch_l2(a.q + (int64_t)b * a.q_stride, qbytes);
+          }
+        } else {
+          for (int g = g0 + lane; g <= g1; g += 32) {
+            bulk_prefetch_l2(a.q + (int64_t)g * a.q_stride, qbytes);
+            if (a.append) {
+              bulk_prefetch_l2(a.k_new + (int64_t)g * a.kv_stride, (uint32_t)a.Hkv * HD * 4);
+              bulk_prefetch_l2(a.v_new + (int64_t)g * a.kv_stride, (uint32_t)a.Hkv * HD * 4);
+            }
+          }
+        }
+      }
+      if (lane == 0 && pk0 < pk1) {
+        TileIter it(poff, S, HS, pk0, pk1, a.tile_rows, a.seg_rows);
+        Tile tl;
+        int left = a.pf_bytes;
+        while (left > 0 && it.next(tl)) {
+          if (HS == 1) {
+            bulk_prefetch_l2(a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
+                             (uint32_t)tl.nr * chunk_bytes);
+          } else {
+            for (int rr = 0; rr < tl.nr; rr += kBoxRows)
+              tma_prefetch_5d(&a.tmap_rows, tl.hg * hs, 0, tl.row0 + rr, tl.g);
+          }
+          left -= tl.nr * (int)chunk_bytes;
+        }
       }
     }
     __syncwarp();
@@ -485,55 +610,64 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   __syncthreads();  // barrier initialisation and ctl are visible to every warp
 
   if (warp == cons_warps) {
-    // ======================= producer warp: one lane issues bulk copies.
-    // Self / GQA: it scans the lengths itself (the same integers the
-    // consumers compute) and starts at once; cross: it takes the consumers'
-    // offsets, which need the group histogram.
+    // ======================= producer warp: one lane issues the copies.  It
+    // computes the offsets itself (the same integers the consumers compute)
+    // and starts at once.
     int* toff = poff_region;
-    if (a.mode == kModeCross) {
-      named_bar(2, n_cons + 32);  // the consumers' scans are done
-      toff = off;
-      if (ctl[2] != 0) {  // unsorted groups: nothing is streamed
-        grid_launch_dependents();
-        return;
-      }
-    } else {
-      warp_scan_sources(a, toff, S, lane, false);
+    const int total = warp_offsets(a, toff, S, lane, false);
+    if (total <= 0 || a.stall) {  // nothing to stream, unsorted groups, or the stall test
+      grid_launch_dependents();
+      return;
     }
-    const int64_t total = toff[S];
-    int64_t share = (total + gridDim.x - 1) / gridDim.x;
-    if (share < a.min_share) share = a.min_share;
-    const int64_t k0 = (int64_t)blockIdx.x * share;
-    const int64_t k1 = min(k0 + share, total);
+    const int share = max((int)((total + gridDim.x - 1) / gridDim.x), a.min_share);
+    const int k0 = (int)min((int64_t)blockIdx.x * share, (int64_t)total);
+    const int k1 = min(k0 + share, total);
     if (lane == 0 && k0 < k1) {
       const uint64_t pol = policy_evict_first();
-      TileIter it(toff, S, k0, k1, a.tile_rows, a.seg_rows);
+      TileIter it(toff, S, HS, k0, k1, a.tile_rows, a.seg_rows);
       Tile tl;
-      for (int t = 0; it.next(tl); ++t) {
+      int t = 0;
+      for (; it.next(tl); ++t) {
         const int s = t % a.stages;
-        if (t >= a.stages && !mbar_wait(&empty[s], ((t / a.stages) - 1) & 1)) {
+        if (t >= a.stages && !mbar_wait(&empty[s], ((t / a.stages) - 1) & 1, a.wait_ns)) {
           set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-          ctl[0] = 1;
+          *abort_flag = 1;
           break;
         }
-        const uint32_t bytes = (uint32_t)tl.nr * (uint32_t)a.row_elems * 2u;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(stage + (size_t)s * a.stage_elems,
-                 a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems, bytes,
-                 &full[s], pol);
+        if (*abort_flag) break;  // the consumers gave up: issue nothing more
+        uint16_t* dst = stage + (size_t)s * a.stage_elems;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)tl.nr * chunk_bytes);
+        if (HS == 1) {
+          bulk_g2s(dst, a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
+                   (uint32_t)tl.nr * chunk_bytes, &full[s], pol);
+        } else {
+          const int c1 = tl.hg * hs;
+          int rr = 0;
+          for (; rr + kBoxRows <= tl.nr; rr += kBoxRows)
+            tma_load_5d(dst + (size_t)rr * chunk, &a.tmap_rows, c1, 0, tl.row0 + rr, tl.g, &full[s],
+                        pol);
+          for (; rr < tl.nr; ++rr)
+            tma_load_5d(dst + (size_t)rr * chunk, &a.tmap_row, c1, 0, tl.row0 + rr, tl.g, &full[s],
+                        pol);
+        }
       }
+      // The CTA must not end while a copy into its shared memory is in
+      // flight: wait (bounded) until the last copies issued have landed.
+      for (int t2 = max(0, t - a.stages); t2 < t; ++t2)
+        if (!mbar_wait(&full[t2 % a.stages], (t2 / a.stages) & 1, a.wait_ns))
+          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
     }
     grid_launch_dependents();
     return;
   }
   if (warp > cons_warps) return;
 
-  // ---- consumers: keys per source (off) and sequences per source (mst).
+  // ---- consumers: keys per source (off) and first sequence per source (mst)
   if (a.mode != kModeCross) {
-    // Self / GQA: one warp scans the lengths (the other warps load the
+    // Self / GQA: one warp computes the offsets (the other warps load the
     // RMSNorm weights meanwhile); one sequence per source, so mst[g] = g.
     if (warp == 0) {
-      warp_scan_sources(a, off, S, lane, false);
+      warp_offsets(a, off, S, lane, false, slen);
       for (int g = lane; g <= S; g += 32) mst[g] = g;
     }
     if (a.mode == kModeGqa) {
@@ -541,25 +675,16 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       if (tid >= t0)
         for (int i = tid - t0; i < 2 * HD; i += n_cons - t0) wts[i] = i < HD ? a.wq[i] : a.wk[i - HD];
     }
-    named_bar(1, n_cons);
   } else {
-    for (int g = tid; g <= S; g += n_cons) {
-      off[g] = 0;
-      mst[g] = 0;
+    // Cross: warp 0 computes the offsets, the other warps the first
+    // sequence of each group.
+    if (warp == 0) {
+      if (warp_offsets(a, off, S, lane, false) < 0 && lane == 0) ctl[2] = 1;
+    } else {
+      first_members(a, mst, S, tid - 32, n_cons - 32);
     }
-    named_bar(1, n_cons);
-    for (int b = tid; b < a.B; b += n_cons) {
-      const int gr = a.group[b];
-      if (gr >= 0 && gr < S) atomicAdd(&mst[gr], 1);
-      if (b > 0 && a.group[b - 1] > gr) ctl[2] = 1;
-    }
-    named_bar(1, n_cons);
-    for (int g = tid; g < S; g += n_cons) off[g] = mst[g] > 0 ? a.fixed_len + a.seg_rows : 0;
-    named_bar(1, n_cons);
-    block_scan_excl(off, S, reinterpret_cast<int*>(rope), n_cons);
-    block_scan_excl(mst, S, reinterpret_cast<int*>(rope), n_cons);
-    asm volatile("bar.arrive 2, %0;" ::"r"(n_cons + 32) : "memory");
   }
+  named_bar(1, n_cons);
   const bool unsorted = a.mode == kModeCross && ctl[2] != 0;
 
   // ---- CTA 0 zeroes the outputs of sequences that are skipped
@@ -573,7 +698,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         if (gr < 0 || gr >= S) bad = ASR_DEVERR_INDEX;
         else if (b - mst[gr] >= a.max_members) bad = ASR_DEVERR_BEAMS;
       } else {
-        const int v = a.lens[b];
+        const int v = slen[b];
         const bool ok =
             a.mode == kModeSelf ? (v >= 1 && v <= a.capacity) : (v >= 0 && v < a.capacity);
         if (!ok) bad = ASR_DEVERR_LEN;
@@ -591,42 +716,35 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   }
 
   // ---- this CTA's share of the flattened key axis (the producer's too)
-  const int64_t total = off[S];
+  const int total = off[S];
   const int P = gridDim.x;
-  int64_t share = (total + P - 1) / P;
-  if (share < a.min_share) share = a.min_share;
-  const int64_t k0 = (int64_t)blockIdx.x * share;
-  const int64_t k1 = min(k0 + share, total);
+  const int share = max((total + P - 1) / P, a.min_share);
+  const int k0 = (int)min((int64_t)blockIdx.x * share, (int64_t)total);
+  const int k1 = min(k0 + share, total);
 
   // ======================= consumers
-  // group grp: virtual head hv = (query split ms, KV head h), row slot r
+  // group grp: virtual head hv = (query split ms, KV head hl of the unit's
+  // group), row slot r
   const int grp = tid / G, li = tid % G;
   const int hv = grp % Hv, r = grp / Hv;
-  const int h = hv % a.Hkv, ms = hv / a.Hkv;
+  const int hl = hv % hs, ms = hv / hs;
   const int qb = ms * NQ;  // this group's first query of a source
   const int rep = a.rep;
   const int R = a.R;
   const int sw = LL::kSwap ? (grp & 1) : 0;
-  const int hoff = h * HD;  // element offset of this group's head in a K (or V) half
+  const int hoff = hl * HD;  // element offset of this group's head in a chunk's K (or V) half
+  const int voff = hs * HD;  // element offset of the V half of a chunk
 
   float2 qv[NQ][NP], o[NQ][NP];
   float m[NQ], l[NQ];
-  int nq = 0, mbase = 0;
-
-  // Does this CTA hold the first real row of source g?  That CTA folds the
-  // new token in (append), so no CTA does it at the end of the launch.  A
-  // source with no cached rows is folded by the CTA that handles it alone.
-  auto owns_first_row = [&](int g) {
-    const int64_t go = (int64_t)off[g] + a.seg_rows, gl = (int64_t)off[g + 1] - go;
-    return gl <= 0 || go / share == (int64_t)blockIdx.x;
-  };
+  int nq = 0, mbase = 0, h = 0;
 
   // Append: the new token's key/value (GQA: normed and roped) from kx, vx
   // (fp32, loaded by the caller), written to the cache by row slot 0 as f16,
   // then folded, with the value the cache holds, into the running state of
   // row slot 0 as the first key it sees.  Warp-uniform (it may shuffle).
   auto append_fold = [&](int g, float2* kx, float2* vx) {
-    const int p = a.mode == kModeGqa ? a.lens[g] : a.lens[g] - 1;
+    const int p = a.mode == kModeGqa ? slen[g] : slen[g] - 1;
     if (a.mode == kModeGqa) norm_rope<HD, DPL>(kx, wts + HD, a.eps, rope, li, sw);
     uint16_t* row = a.cache_w + (int64_t)g * a.src_stride + (int64_t)p * a.row_elems;
 #pragma unroll
@@ -643,8 +761,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
       h8_to_f2x4(kh, kx + 4 * j);  // the key and value as the cache holds them
       h8_to_f2x4(vh, vx + 4 * j);
       if (r == 0 && ms == 0) {
-        *reinterpret_cast<uint4*>(row + hoff + LL::chunk_off(li, j, sw)) = kh;
-        *reinterpret_cast<uint4*>(row + a.Hkv * HD + hoff + LL::chunk_off(li, j, sw)) = vh;
+        *reinterpret_cast<uint4*>(row + h * HD + LL::chunk_off(li, j, sw)) = kh;
+        *reinterpret_cast<uint4*>(row + a.Hkv * HD + h * HD + LL::chunk_off(li, j, sw)) = vh;
       }
     }
     // every query slot runs the group sum (its shuffles need the whole warp,
@@ -667,16 +785,24 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
   };
 
-  auto seg_begin = [&](int g) {
+  // Start unit u: its queries, and the new token in the CTA that folds it
+  // in.  Warp-uniform.
+  auto seg_begin = [&](int u) {
+    const int g = u / HS, hg = u - g * HS;
+    h = hg * hs + hl;  // this group's KV head
     mbase = mst[g];
     nq = min(max(min(mst[g + 1] - mst[g], a.max_members) * rep - qb, 0), NQ);
-    const bool fold = a.append && owns_first_row(g);
+    const bool fold = a.append && owns_first_row(off, HS, a.seg_rows, share, u, (int)blockIdx.x);
+    // member m, query head x of the unit at qsrc + m * q_stride + x * HD;
     // every global load (new token, queries) is issued before the RoPE
     // table is built, so their latencies overlap it and one another
+    const float* qsrc = a.q + (int64_t)mbase * a.q_stride + (int64_t)hg * hqu * HD;
+    const float* ksrc = a.k_new + (int64_t)g * a.kv_stride + h * HD;
+    const float* vsrc = a.v_new + (int64_t)g * a.kv_stride + h * HD;
     float2 kx[NP], vx[NP];
     if (fold) {
-      load_head_f32<HD, DPL>(a.k_new + (int64_t)g * a.kv_stride + h * HD, li, sw, kx);
-      load_head_f32<HD, DPL>(a.v_new + (int64_t)g * a.kv_stride + h * HD, li, sw, vx);
+      load_head_f32<HD, DPL>(ksrc, li, sw, kx);
+      load_head_f32<HD, DPL>(vsrc, li, sw, vx);
     }
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
@@ -685,9 +811,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 #pragma unroll
       for (int t = 0; t < NP; ++t) o[qi][t] = make_float2(0.f, 0.f);
       if (qi < nq) {
-        const int b = mbase + (qb + qi) / rep;
-        const int hq = h * rep + (qb + qi) % rep;
-        load_head_f32<HD, DPL>(a.q + (int64_t)b * a.q_stride + hq * HD, li, sw, qv[qi]);
+        const int mem = (qb + qi) / rep;
+        const int x = hl * rep + (qb + qi) % rep;  // query head within the unit
+        load_head_f32<HD, DPL>(qsrc + mem * a.q_stride + x * HD, li, sw, qv[qi]);
       } else {
 #pragma unroll
         for (int t = 0; t < NP; ++t) qv[qi][t] = make_float2(0.f, 0.f);
@@ -695,7 +821,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
     if (a.mode == kModeGqa) {
       named_bar(1, n_cons);
-      rope_table<HD>(rope, a.rope_turns, a.lens[g], tid);
+      rope_table<HD>(rope, a.rope_turns, slen[g], tid);
       named_bar(1, n_cons);
     }
     const float2 s2 = make_float2(a.qscale, a.qscale);
@@ -710,8 +836,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   };
 
   // Write the normalised output of query qi.  No shuffles: callable per group.
-  auto finalize = [&](int qi, float M, float Ls, float2* O) {
-    (void)M;
+  auto finalize = [&](int qi, float Ls, float2* O) {
     const int b = mbase + (qb + qi) / rep;
     const int hq = h * rep + (qb + qi) % rep;
     const float inv = 1.0f / Ls;
@@ -725,29 +850,38 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
   };
 
-  auto seg_end = [&](int g) {
+  // The merge of unit u's partials by the last CTA to finish it.
+  auto merge_unit = [&](int u) {
+    const UnitSpan sp = unit_span(off, HS, a.seg_rows, u);
+    const int first = sp.go / share, lastp = (sp.go + sp.gl - 1) / share;
+    const int g = u / HS;
+    merge_pieces<HD>(a, u, u - g * HS, first, lastp, min(mst[g + 1] - mst[g], a.max_members),
+                     mst[g], tid, n_cons);
+  };
+
+  auto seg_end = [&](int u) {
     merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, hv, Hv, li, sw, nq, n_cons);
-    // pieces of this source over the grid
-    // (real rows of g: [off[g] + seg_rows, off[g + 1]))
-    const int64_t go = (int64_t)off[g] + a.seg_rows, gl = (int64_t)off[g + 1] - go;
-    const int first = gl > 0 ? (int)(go / share) : 0;
-    const int lastp = gl > 0 ? (int)((go + gl - 1) / share) : 0;
-    const int parts = gl > 0 ? lastp - first + 1 : 0;
+    // pieces of this unit over the grid
+    const UnitSpan sp = unit_span(off, HS, a.seg_rows, u);
+    const int first = sp.gl > 0 ? sp.go / share : 0;
+    const int lastp = sp.gl > 0 ? (sp.go + sp.gl - 1) / share : 0;
+    const int parts = sp.gl > 0 ? lastp - first + 1 : 0;
     if (parts <= 1) {
       if (r == 0) {
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi)
-          if (qi < nq) finalize(qi, m[qi], l[qi], o[qi]);
+          if (qi < nq) finalize(qi, l[qi], o[qi]);
       }
       return;
     }
+    const int hqu = hs * rep;
     if (r == 0) {
-      const int64_t slot = (int64_t)blockIdx.x + g;
+      const int64_t slot = (int64_t)blockIdx.x + u;
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
         if (qi < nq) {
           const int64_t pidx =
-              (slot * a.max_members + (qb + qi) / rep) * a.Hq + h * rep + (qb + qi) % rep;
+              (slot * a.max_members + (qb + qi) / rep) * hqu + hl * rep + (qb + qi) % rep;
           float* po = a.part_o + pidx * HD;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
@@ -764,132 +898,146 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     // release; the acquire side lets the last CTA read everyone's partials
     named_bar(1, n_cons);
     if (tid == 0) {
-      const int old = atomic_add_acq_rel_gpu(&a.counters[g], 1);
+      const int old = atomic_add_acq_rel_gpu(&a.counters[u], 1);
       const int is_last = old == parts - 1;
-      if (is_last) a.counters[g] = 0;  // no other CTA touches it again in this launch
+      if (is_last) a.counters[u] = 0;  // no other CTA touches it again in this launch
       ctl[1] = is_last;
     }
     named_bar(1, n_cons);
     if (ctl[1]) {
-      // the last CTA to finish source g merges every piece's partial
-      merge_pieces<HD>(a, g, first, lastp, min(mst[g + 1] - mst[g], a.max_members), mbase, tid,
-                       n_cons);
+      // the last CTA to finish unit u merges every piece's partial, after
+      // its tiles (the last arrival is nearly always at the end of a share
+      // anyway, and outside the tile loop the merge has the registers)
+      named_bar(1, n_cons);  // every thread has read ctl[1]
+      if (tid == 0) ctl[4 + ctl[3]++] = u;
     }
   };
 
   if (k0 < k1) {
-    TileIter it(off, S, k0, k1, a.tile_rows, a.seg_rows);
+    TileIter it(off, S, HS, k0, k1, a.tile_rows, a.seg_rows);
     Tile tl;
     for (int t = 0; it.next(tl); ++t) {
-      if (tl.first) seg_begin(tl.g);
+      if (tl.first) seg_begin(tl.u);
       const int s = t % a.stages;
-      if (!mbar_wait(&full[s], (t / a.stages) & 1)) {
+      // A wait that runs out aborts the CTA: every warp then passes over its
+      // remaining tiles without waiting or reading them (so the control flow,
+      // named barriers and tickets stay the same in every warp) and the
+      // producer issues nothing more.  The outputs of such a call are
+      // undefined; ASR_DEVERR_TIMEOUT tells the host.
+      bool ok = __shfl_sync(kFull, *abort_flag, 0) == 0;
+      if (ok) ok = __all_sync(kFull, mbar_wait(&full[s], (t / a.stages) & 1, a.wait_ns));
+      if (!ok && lane == 0 && *abort_flag == 0) {
+        *abort_flag = 1;
         set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-        break;
       }
-      const uint16_t* tb = stage + (size_t)s * a.stage_elems + hoff;
-      // scores of this group's rows (row r + i*R of the tile)
-      float sc[NQ][RS];
-      bool val[RS];
+      if (ok) {
+        const uint16_t* tb = stage + (size_t)s * a.stage_elems + hoff;
+        // scores of this group's rows (row r + i*R of the tile)
+        float sc[NQ][RS];
+        bool val[RS];
 #pragma unroll
-      for (int i = 0; i < RS; ++i) {
-        const int row = r + i * R;  // < tile_rows: always inside the stage buffer
-        val[i] = row < tl.nr;
-        float2 kf[NP];
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const uint4 u = *reinterpret_cast<const uint4*>(tb + row * a.row_elems + LL::chunk_off(li, j, sw));
-          h8_to_f2x4(u, kf + 4 * j);
-        }
-        // every query slot is scored and reduced: the reduction's
-        // shuffles need the whole warp, and the groups of one warp may hold
-        // different query counts (slots past nq hold zero queries)
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int t = 0; t < NP; t += 2) {
-            a0 = ffma2(qv[qi][t], kf[t], a0);
-            a1 = ffma2(qv[qi][t + 1], kf[t + 1], a1);
-          }
-          sc[qi][i] = (a0.x + a0.y) + (a1.x + a1.y);
-        }
-      }
-#pragma unroll
-      for (int o2 = 1; o2 < G; o2 <<= 1) {
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-#pragma unroll
-          for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
-        }
-      }
-      // online softmax over the RS rows, one rescale per tile.  Every query
-      // slot runs it (no branch on nq in the loop); a slot past nq holds a
-      // zero query, stays finite and is never written out.
-      float pr[NQ][RS];
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-#pragma unroll
-        for (int i = 0; i < RS; ++i) pr[qi][i] = 0.f;
-        {
-          float mt = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < RS; ++i)
-            if (val[i]) mt = fmaxf(mt, sc[qi][i]);
-          if (mt != -INFINITY) {
-            const float mn = fmaxf(m[qi], mt);
-            const float alpha = ex2(m[qi] - mn);
-            float psum = 0.f;
-#pragma unroll
-            for (int i = 0; i < RS; ++i) {
-              pr[qi][i] = val[i] ? ex2(sc[qi][i] - mn) : 0.f;
-              psum += pr[qi][i];
-            }
-            l[qi] = fmaf(l[qi], alpha, psum);
-            m[qi] = mn;
-            const float2 al2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int t = 0; t < NP; ++t) o[qi][t] = fmul2(o[qi][t], al2);
-          }
-        }
-      }
-      // weighted values
-#pragma unroll
-      for (int i = 0; i < RS; ++i) {
-        if (val[i]) {
-          const int row = r + i * R;
-          float2 vf[NP];
+        for (int i = 0; i < RS; ++i) {
+          const int row = r + i * R;  // < tile_rows: always inside the stage buffer
+          val[i] = row < tl.nr;
+          float2 kf[NP];
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
-            const uint4 u = *reinterpret_cast<const uint4*>(tb + row * a.row_elems + a.Hkv * HD +
-                                                            LL::chunk_off(li, j, sw));
-            h8_to_f2x4(u, vf + 4 * j);
+            const uint4 uu = *reinterpret_cast<const uint4*>(tb + row * chunk + LL::chunk_off(li, j, sw));
+            h8_to_f2x4(uu, kf + 4 * j);
           }
+          // every query slot is scored and reduced: the reduction's
+          // shuffles need the whole warp, and the groups of one warp may hold
+          // different query counts (slots past nq hold zero queries)
 #pragma unroll
           for (int qi = 0; qi < NQ; ++qi) {
-            const float2 p2 = make_float2(pr[qi][i], pr[qi][i]);
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < NP; ++t) o[qi][t] = ffma2(p2, vf[t], o[qi][t]);
+            for (int t2 = 0; t2 < NP; t2 += 2) {
+              a0 = ffma2(qv[qi][t2], kf[t2], a0);
+              a1 = ffma2(qv[qi][t2 + 1], kf[t2 + 1], a1);
+            }
+            sc[qi][i] = (a0.x + a0.y) + (a1.x + a1.y);
+          }
+        }
+#pragma unroll
+        for (int o2 = 1; o2 < G; o2 <<= 1) {
+#pragma unroll
+          for (int qi = 0; qi < NQ; ++qi) {
+#pragma unroll
+            for (int i = 0; i < RS; ++i) sc[qi][i] += __shfl_xor_sync(kFull, sc[qi][i], o2);
+          }
+        }
+        // online softmax over the RS rows, one rescale per tile.  Every query
+        // slot runs it (no branch on nq in the loop); a slot past nq holds a
+        // zero query, stays finite and is never written out.
+        float pr[NQ][RS];
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+#pragma unroll
+          for (int i = 0; i < RS; ++i) pr[qi][i] = 0.f;
+          {
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < RS; ++i)
+              if (val[i]) mt = fmaxf(mt, sc[qi][i]);
+            if (mt != -INFINITY) {
+              const float mn = fmaxf(m[qi], mt);
+              const float alpha = ex2(m[qi] - mn);
+              float psum = 0.f;
+#pragma unroll
+              for (int i = 0; i < RS; ++i) {
+                pr[qi][i] = val[i] ? ex2(sc[qi][i] - mn) : 0.f;
+                psum += pr[qi][i];
+              }
+              l[qi] = fmaf(l[qi], alpha, psum);
+              m[qi] = mn;
+              const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+              for (int t2 = 0; t2 < NP; ++t2) o[qi][t2] = fmul2(o[qi][t2], al2);
+            }
+          }
+        }
+        // weighted values
+#pragma unroll
+        for (int i = 0; i < RS; ++i) {
+          if (val[i]) {
+            const int row = r + i * R;
+            float2 vf[NP];
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              const uint4 uu = *reinterpret_cast<const uint4*>(tb + row * chunk + voff +
+                                                               LL::chunk_off(li, j, sw));
+              h8_to_f2x4(uu, vf + 4 * j);
+            }
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+              const float2 p2 = make_float2(pr[qi][i], pr[qi][i]);
+#pragma unroll
+              for (int t2 = 0; t2 < NP; ++t2) o[qi][t2] = ffma2(p2, vf[t2], o[qi][t2]);
+            }
           }
         }
       }
-      // the stage is consumed: hand it back to the producer
+      // the stage is consumed (or abandoned): hand it back to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (tl.last) seg_end(tl.g);
+      if (tl.last) seg_end(tl.u);
     }
   }
 
-  // Appending sources with no cached rows (GQA n_past == 0, self lens == 1):
-  // only the new token; CTA g % P handles source g.
+  // Appending units with no cached rows (GQA n_past == 0, self lens == 1):
+  // only the new token; CTA u % P handles unit u.
   if (a.append) {
-    for (int g = blockIdx.x; g < S; g += P) {
-      if (a.lens[g] == (a.mode == kModeGqa ? 0 : 1)) {
-        seg_begin(g);
-        seg_end(g);
+    for (int u = blockIdx.x; u < a.n_units; u += P) {
+      if (slen[u / HS] == (a.mode == kModeGqa ? 0 : 1)) {
+        seg_begin(u);
+        seg_end(u);
       }
     }
   }
+  // the merges this CTA won (ctl[3] was last written before a barrier)
+  named_bar(1, n_cons);
+  for (int i = 0; i < ctl[3]; ++i) merge_unit(ctl[4 + i]);
   grid_launch_dependents();
 }
 
@@ -899,14 +1047,13 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 struct Variant {
   int NQ, DPL, RS, MAXT;
 };
-static constexpr int kNumVariants = 6;
+static constexpr int kNumVariants = 4;
 static constexpr Variant kVariants[kNumVariants] = {
-    {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256},
-    {1, 16, 2, 384}, {2, 16, 2, 384}};  // the last two: 2 rows per slot (tuning)
+    {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256}};
 
-static int variant_index(int nq, int rs) {
-  if (nq <= 1) return rs == 2 ? 4 : 0;
-  if (nq <= 2) return rs == 2 ? 5 : 1;
+static int variant_index(int nq) {
+  if (nq <= 1) return 0;
+  if (nq <= 2) return 1;
   if (nq <= 4) return 2;
   if (nq <= 8) return 3;
   return -1;
@@ -925,8 +1072,6 @@ static void* kernel_for(int HD, int vi) {
       case 1: return kernel_ptr<64, 1>();
       case 2: return kernel_ptr<64, 2>();
       case 3: return kernel_ptr<64, 3>();
-      case 4: return kernel_ptr<64, 4>();
-      case 5: return kernel_ptr<64, 5>();
     }
   } else if (HD == 128) {
     switch (vi) {
@@ -934,108 +1079,133 @@ static void* kernel_for(int HD, int vi) {
       case 1: return kernel_ptr<128, 1>();
       case 2: return kernel_ptr<128, 2>();
       case 3: return kernel_ptr<128, 3>();
-      case 4: return kernel_ptr<128, 4>();
-      case 5: return kernel_ptr<128, 5>();
     }
   }
   return nullptr;
 }
 
-// Tuning knobs; ASRKV_DECODE_TUNE="tile_kb=80,smem_kb=200,ctas=0,R=0,rs=4,min_kb=64,seg_kb=256,pf_kb=-1,qs=0"
-// overrides them (ctas / R = 0: chosen automatically; rs: rows per slot;
-// qs: queries per thread group when a KV row serves more than two queries,
-// 0 = 2;
-// min_kb: fewest K/V bytes one CTA takes; seg_kb: K/V bytes' worth of
-// virtual rows charged to each source, so CTAs that start or finish more
-// sources take fewer rows; pf_kb: K/V bytes a CTA prefetches into L2 before
-// its grid dependency wait, -1 = the stage ring's size, 0 = none).
-// Defaults (measured on GB300): one CTA per SM with about ten consumer
-// warps and two or more stages of large tiles.
+// Tuning constants (measured on GB300): one CTA per SM with about ten
+// consumer warps and two or more stages of large tiles.
+//   tile_kb: largest K/V tile (bytes of row chunks) one stage holds;
+//   smem_kb: shared memory the stage ring may fill;
+//   min_kb: fewest K/V bytes one CTA takes (bounds the partials per unit);
+//   seg_kb: K/V bytes' worth of virtual rows charged to each unit, so CTAs
+//     that start or finish more units take fewer rows;
+//   qs: queries per thread group when a KV row serves more than two queries;
+//   parts: the number of CTA pieces per unit the head split aims at (a
+//     source is cut into the fewest head groups that bring its expected
+//     pieces to this or below);
+//   min_chunk: fewest bytes of one row a head group streams.
 struct DecodeTune {
-  int tile_kb = 80, smem_kb = 200, ctas = 0, R = 0, rs = 4, min_kb = 64, seg_kb = 256, pf_kb = -1,
-      qs = 0;
+  int tile_kb = 80, smem_kb = 200, min_kb = 64, seg_kb = 256, qs = 2, parts = 6, min_chunk = 512;
 };
 
-static DecodeTune decode_tune() {
-  static DecodeTune t = [] {
-    DecodeTune d;
-    const char* e = getenv("ASRKV_DECODE_TUNE");
-    if (e) {
-      char key[32];
-      int val, n;
-      while (sscanf(e, " %31[A-Za-z_]=%d%n", key, &val, &n) == 2) {
-        if (!strcmp(key, "tile_kb")) d.tile_kb = val;
-        else if (!strcmp(key, "smem_kb")) d.smem_kb = val;
-        else if (!strcmp(key, "ctas")) d.ctas = val;
-        else if (!strcmp(key, "R")) d.R = val;
-        else if (!strcmp(key, "rs")) d.rs = val;
-        else if (!strcmp(key, "min_kb")) d.min_kb = val;
-        else if (!strcmp(key, "seg_kb")) d.seg_kb = val;
-        else if (!strcmp(key, "pf_kb")) d.pf_kb = val;
-        else if (!strcmp(key, "qs")) d.qs = val;
-
-        e += n;
-        if (*e == ',') ++e;
-      }
-    }
-    return d;
-  }();
-  return t;
-}
+static constexpr DecodeTune decode_tune() { return DecodeTune{}; }
 
 struct DecodePlan {
-  int R, tile_rows, stages, stage_elems, threads, smem, min_share, seg_rows, pf_bytes;
+  int vi, MS, HS, hs, R, tile_rows, stages, stage_elems, threads, smem, min_share, seg_rows,
+      pf_bytes;
 };
 
-// Row slots R: the consumer count R * Hkv * G must be a multiple of 32 and
+// Row slots R: the consumer count R * Hv * G must be a multiple of 32 and
 // fit the variant's thread cap (at most 320 consumers); among those, the
-// largest R whose tile fits tile_kb (else the smallest valid R).  Stages: as many as fit smem_kb, 2..8.
-// One CTA takes at least min_kb (64 KB) of rows, so a source splits into a
-// bounded number of partial results.
-static bool plan_decode(int HD, const Variant& v, int Hkv, int row_elems, int n_src, int MS,
-                        DecodePlan& p) {
+// largest R whose tile fits tile_kb (else the smallest valid R).  Stages: as
+// many as fit smem_kb, 2..8.  One CTA takes at least min_kb of rows, so a
+// unit splits into a bounded number of partial results.
+static bool plan_layout(const DecodeArgs& a, int HD, int vi, int MS, int hs, DecodePlan& p) {
+  const int n_src = a.n_src;
   const DecodeTune tune = decode_tune();
+  const Variant& v = kVariants[vi];
   const int G = HD / v.DPL;
-  const int per_slot = MS * Hkv * G;
+  const int per_slot = MS * hs * G;
   const int budget = std::min(v.MAXT - 32, 320);
-  const int row_bytes = row_elems * 2;
+  const int chunk_elems = 2 * hs * HD;
+  const int chunk_bytes = chunk_elems * 2;
   int best = 0, smallest = 0;
   for (int R = 1; R * per_slot <= budget; ++R) {
     if ((R * per_slot) % 32 != 0) continue;
     if (!smallest) smallest = R;
-    if (R * v.RS * row_bytes <= tune.tile_kb * 1024) best = R;
+    if (R * v.RS * chunk_bytes <= tune.tile_kb * 1024) best = R;
   }
-  if (tune.R > 0 && tune.R * per_slot <= budget && (tune.R * per_slot) % 32 == 0) best = tune.R;
   if (!best) best = smallest;
   if (!best) return false;
+  p.vi = vi;
+  p.MS = MS;
+  p.hs = hs;
   p.R = best;
   p.threads = best * per_slot + 32;
   p.tile_rows = best * v.RS;
-  p.stage_elems = dsm_align(p.tile_rows * row_elems, 64);
-  const int cap = std::max(tune.smem_kb, 16) * 1024;
+  p.stage_elems = dsm_align(p.tile_rows * chunk_elems, 64);
+  const int cap = tune.smem_kb * 1024;
   int stages = 8;
   while (stages > 2 &&
-         decode_smem_layout(stages, n_src, p.R, MS * Hkv, v.NQ, HD, p.stage_elems).total > cap)
+         decode_smem_layout(stages, n_src, p.R, MS * hs, v.NQ, HD, p.stage_elems).total > cap)
     --stages;
   p.stages = stages;
-  p.smem = decode_smem_layout(stages, n_src, p.R, MS * Hkv, v.NQ, HD, p.stage_elems).total;
+  p.smem = decode_smem_layout(stages, n_src, p.R, MS * hs, v.NQ, HD, p.stage_elems).total;
   if (p.smem > 227 * 1024) return false;
-  const int min_bytes = std::max(tune.min_kb, 1) * 1024;
-  p.min_share = std::max(p.tile_rows, (min_bytes + row_bytes - 1) / row_bytes);
-  p.seg_rows = std::max(tune.seg_kb, 0) * 1024 / row_bytes;
-  p.pf_bytes = tune.pf_kb < 0 ? stages * p.tile_rows * row_bytes : std::min(tune.pf_kb, 1 << 20) * 1024;
+  p.min_share = std::max(p.tile_rows, (tune.min_kb * 1024 + chunk_bytes - 1) / chunk_bytes);
+  p.seg_rows = tune.seg_kb * 1024 / chunk_bytes;
+  p.pf_bytes = stages * p.tile_rows * chunk_bytes;
   return true;
 }
 
-size_t decode_ws_bytes(int n_src, int max_members, int Hq, int HD, int sms) {
-  const int64_t slots = (int64_t)kMaxCtasPerSm * sms + n_src;
-  const size_t counters = align_up((size_t)n_src * 4, 256);
-  const size_t ml = align_up((size_t)slots * max_members * Hq * 2 * 4, 256);
-  const size_t o = (size_t)slots * max_members * Hq * HD * 4;
-  return counters + ml + o;
+// The variant and query split (more than two queries per KV row, the beams
+// of a group, are split over groups of threads, `qs` queries each: fewer
+// registers per thread, more warps per SM), then the head split: the fewest
+// head groups per source whose expected pieces per unit are at most
+// `parts`.  The expectation takes each source at half its capacity (self,
+// GQA) or at its frames (cross), spread over one CTA per SM.
+static bool plan_decode(const DecodeArgs& a, int HD, int nq_needed, int sms, DecodePlan& p) {
+  const DecodeTune tune = decode_tune();
+  int MS = 1, nq_var = nq_needed;
+  if (tune.qs > 0 && tune.qs < nq_needed) {
+    nq_var = tune.qs;
+    MS = (nq_needed + tune.qs - 1) / tune.qs;
+  }
+  int vi = variant_index(nq_var);
+  if (vi < 0) return false;
+  const double rows = a.mode == kModeCross ? (double)a.fixed_len : 0.5 * a.capacity;
+  const double row_bytes = 2.0 * a.row_elems;
+  const double share = std::max(a.n_src * rows * row_bytes / sms, tune.min_kb * 1024.0);
+  bool found = false;
+  for (int pass = 0; pass < 2 && !found; ++pass) {
+    if (pass == 1) {  // the split's thread layout does not fit: one group per KV head
+      MS = 1;
+      vi = variant_index(nq_needed);
+      if (vi < 0) return false;
+    }
+    // Cross-attention keeps whole rows: its beams already share each row
+    // among several queries, and splitting the heads measured slower there.
+    const int max_hs_split = a.mode == kModeCross ? 1 : a.Hkv;
+    for (int HS = 1; HS <= max_hs_split; ++HS) {
+      if (a.Hkv % HS != 0) continue;
+      const int hs = a.Hkv / HS;
+      if (HS > 1 && 4 * hs * HD < tune.min_chunk) break;
+      DecodePlan c;
+      if (!plan_layout(a, HD, vi, MS, hs, c)) continue;
+      c.HS = HS;
+      p = c;
+      found = true;
+      if (rows * row_bytes / HS / share <= tune.parts) break;
+    }
+  }
+  return found;
 }
 
-static std::once_flag g_attr_once[2][kNumVariants];
+static size_t counter_bytes(int n_src, int Hq) { return align_up((size_t)n_src * Hq * 4, 256); }
+
+size_t decode_counter_bytes(int n_src, int Hq) { return counter_bytes(n_src, Hq); }
+
+// Partial results: one slot per (CTA piece, unit), each with max_members x
+// (query heads of the unit) entries; (P + n_src * HS) * hs * rep <= (P +
+// n_src) * Hq for every head split, so one size serves them all.
+size_t decode_ws_bytes(int n_src, int max_members, int Hq, int HD, int sms) {
+  const int64_t entries = ((int64_t)kMaxCtasPerSm * sms + n_src) * max_members * Hq;
+  const size_t ml = align_up((size_t)entries * 2 * 4, 256);
+  const size_t o = (size_t)entries * HD * 4;
+  return counter_bytes(n_src, Hq) + ml + o;
+}
 
 // CTAs per SM for (kernel, threads, smem) on the current device; the query
 // is slow next to a launch, so results are memoised (small linear table).
@@ -1061,52 +1231,34 @@ static int occupancy_cached(void* fn, int threads, int smem) {
   return occ;
 }
 
+// Test support (asr_debug_stall_next_decode): the next decode launch made by
+// this host thread issues no copies and bounds its waits by this many ns.
+static thread_local uint64_t t_stall_ns = 0;
+
 static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
-  // More than two queries per KV row (the beams of a group) are split over
-  // groups of threads, `split` queries each, instead of one group holding
-  // them all: fewer registers per thread, more warps per SM.
-  const int qs = decode_tune().qs;
-  const int split = qs > 0 ? qs : (nq_needed > 2 ? 2 : 0);
-  int nq_var = nq_needed, MS = 1;
-  if (split > 0 && split < nq_needed) {
-    nq_var = split;
-    MS = (nq_needed + split - 1) / split;
-  }
-  int vi = variant_index(nq_var, decode_tune().rs);
-  if (vi < 0) return ASR_ERR_UNSUPPORTED;
-  DecodePlan p;
-  if (!plan_decode(HD, kVariants[vi], a.Hkv, a.row_elems, a.n_src, MS, p)) {
-    // the split's thread layout does not fit (many heads): one group per head
-    MS = 1;
-    vi = variant_index(nq_needed, decode_tune().rs);
-    if (vi < 0 || !plan_decode(HD, kVariants[vi], a.Hkv, a.row_elems, a.n_src, 1, p))
-      return ASR_ERR_UNSUPPORTED;
-  }
-  const Variant& v = kVariants[vi];
-  (void)v;
-  a.MS = MS;
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
+  DecodePlan p;
+  if (!plan_decode(a, HD, nq_needed, sms, p)) return ASR_ERR_UNSUPPORTED;
   const size_t need = decode_ws_bytes(a.n_src, a.max_members, a.Hq, HD, sms);
   if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < need) return ASR_ERR_WORKSPACE;
-  void* fn = kernel_for(HD, vi);
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(g_attr_once[HD == 64 ? 0 : 1][vi], [&] {
-    attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  });
-  if (attr_err != cudaSuccess) return ASR_ERR_CUDA;
+  void* fn = kernel_for(HD, p.vi);
+  if (ensure_dynamic_smem(fn, 227 * 1024) != cudaSuccess) return ASR_ERR_CUDA;
   int occ = occupancy_cached(fn, p.threads, p.smem);
   if (occ <= 0) return ASR_ERR_CUDA;
-  const int want = decode_tune().ctas;
-  if (want > 0) occ = std::min(occ, want);
   occ = std::max(1, std::min(occ, kMaxCtasPerSm));
+  a.MS = p.MS;
+  a.HS = p.HS;
+  a.hs = p.hs;
+  a.chunk_elems = 2 * p.hs * HD;
+  a.n_units = a.n_src * p.HS;
   char* w = static_cast<char*>(ws);
   a.counters = reinterpret_cast<int*>(w);
-  w += align_up((size_t)a.n_src * 4, 256);
-  const int64_t slots = (int64_t)kMaxCtasPerSm * sms + a.n_src;
+  w += counter_bytes(a.n_src, a.Hq);
+  const int64_t entries = ((int64_t)kMaxCtasPerSm * sms + a.n_src) * a.max_members * a.Hq;
   a.part_ml = reinterpret_cast<float*>(w);
-  w += align_up((size_t)slots * a.max_members * a.Hq * 2 * 4, 256);
+  w += align_up((size_t)entries * 2 * 4, 256);
   a.part_o = reinterpret_cast<float*>(w);
   a.R = p.R;
   a.tile_rows = p.tile_rows;
@@ -1115,6 +1267,26 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
   a.stages = p.stages;
   a.pf_bytes = p.pf_bytes;
   a.stage_elems = p.stage_elems;
+  a.wait_ns = kWaitLimitNs;
+  a.stall = 0;
+  if (t_stall_ns) {
+    a.wait_ns = t_stall_ns;
+    a.stall = 1;
+    t_stall_ns = 0;
+  }
+  if (p.HS > 1) {
+    // rows of every source as {HD, Hkv, 2 (K, V), rows, sources}: a box of
+    // {HD, hs, 2, n, 1} lands as n row chunks [K of the hs heads | V of them]
+    const uint64_t rows = a.mode == kModeCross ? (uint64_t)a.fixed_len : (uint64_t)a.capacity;
+    const uint64_t dims[5] = {(uint64_t)HD, (uint64_t)a.Hkv, 2, rows, (uint64_t)a.n_src};
+    const uint64_t strides[4] = {(uint64_t)HD * 2, (uint64_t)a.Hkv * HD * 2,
+                                 (uint64_t)a.row_elems * 2, (uint64_t)a.src_stride * 2};
+    const uint32_t box_rows[5] = {(uint32_t)HD, (uint32_t)p.hs, 2, (uint32_t)kBoxRows, 1};
+    const uint32_t box_row[5] = {(uint32_t)HD, (uint32_t)p.hs, 2, 1, 1};
+    if (!make_tmap_f16_5d_plain(&a.tmap_rows, a.kv, dims, strides, box_rows) ||
+        !make_tmap_f16_5d_plain(&a.tmap_row, a.kv, dims, strides, box_row))
+      return ASR_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms * occ);
   cfg.blockDim = dim3(p.threads);
@@ -1130,11 +1302,21 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
 }
 
-static bool rows_fit_int(int64_t n_src, int64_t rows) { return n_src * rows < (1LL << 31); }
+// The flattened key axis is int: every source's rows plus its virtual rows,
+// once per head group, must fit.
+static bool rows_fit_int(int64_t n_src, int64_t rows, int64_t kv_heads) {
+  return n_src * (rows + 1024) * kv_heads < (1LL << 31);
+}
 
 }  // namespace asrkv
 
 using namespace asrkv;
+
+extern "C" int asr_debug_stall_next_decode(uint64_t wait_ns) {
+  if (wait_ns == 0 || wait_ns > kWaitLimitNs) return ASR_ERR_INVALID_ARG;
+  t_stall_ns = wait_ns;
+  return ASR_OK;
+}
 
 extern "C" int asr_self_attn_step(const float* q, int64_t q_stride, const uint16_t* cache,
                                   int64_t seq_stride, const int32_t* lens, int B, int heads,
@@ -1150,7 +1332,7 @@ extern "C" int asr_self_attn_step(const float* q, int64_t q_stride, const uint16
   if (!aligned16(q) || !aligned16(cache) || !aligned16(out) || q_stride % 4 != 0 ||
       seq_stride % 8 != 0)
     return ASR_ERR_MISALIGNED;
-  if (!rows_fit_int(B, capacity)) return ASR_ERR_UNSUPPORTED;
+  if (!rows_fit_int(B, capacity, heads)) return ASR_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   a.q = q;
   a.q_stride = q_stride;
@@ -1189,7 +1371,7 @@ extern "C" int asr_self_attn_append_step(const float* q, int64_t q_stride, const
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cache) ||
       !aligned16(out) || q_stride % 4 != 0 || kv_stride % 4 != 0 || seq_stride % 8 != 0)
     return ASR_ERR_MISALIGNED;
-  if (!rows_fit_int(B, capacity)) return ASR_ERR_UNSUPPORTED;
+  if (!rows_fit_int(B, capacity, heads)) return ASR_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   a.q = q;
   a.q_stride = q_stride;
@@ -1234,7 +1416,7 @@ extern "C" int asr_cross_attn_step(const float* q, int64_t q_stride, const uint1
   if (!aligned16(q) || !aligned16(cross) || !aligned16(out) || q_stride % 4 != 0 ||
       group_stride % 8 != 0)
     return ASR_ERR_MISALIGNED;
-  if (!rows_fit_int(G, frames)) return ASR_ERR_UNSUPPORTED;
+  if (!rows_fit_int(G, frames, heads)) return ASR_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   a.q = q;
   a.q_stride = q_stride;
@@ -1280,7 +1462,7 @@ extern "C" int asr_gqa_step(const float* q, int64_t q_stride, const float* k_new
       !aligned16(k_norm_w) || !aligned16(cache) || !aligned16(out) || seq_stride % 8 != 0 ||
       q_stride % 4 != 0 || kv_stride % 4 != 0)
     return ASR_ERR_MISALIGNED;
-  if (!rows_fit_int(B, capacity)) return ASR_ERR_UNSUPPORTED;
+  if (!rows_fit_int(B, capacity, kv_heads)) return ASR_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   a.q = q;
   a.q_stride = q_stride;

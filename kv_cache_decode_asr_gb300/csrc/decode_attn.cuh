@@ -2,6 +2,7 @@
 // (kernel in decode_attn.cu, workspace sizing in abi.cu).
 #pragma once
 
+#include <cuda.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -13,7 +14,15 @@ enum DecodeMode { kModeSelf = 0, kModeCross = 1, kModeGqa = 2 };
 // partial results a workspace must hold.
 constexpr int kMaxCtasPerSm = 4;
 
+// Rows per box of the large tensor-map copy of a head group's row chunks.
+constexpr int kBoxRows = 8;
+
 struct DecodeArgs {
+  // tensor maps of the K/V rows, used when a work unit is a group of KV heads
+  // narrower than the row (HS > 1): dims {HD, Hkv, 2 (K, V), rows, sources},
+  // boxes {HD, hs, 2, kBoxRows or 1, 1}
+  CUtensorMap tmap_rows;
+  CUtensorMap tmap_row;
   // queries: fp32, sequence b at q + b*q_stride, head h at h*HD
   const float* q;
   int64_t q_stride;
@@ -31,21 +40,28 @@ struct DecodeArgs {
   int max_members;       // cross: max sequences per group; else 1
   float qscale;          // scale * log2(e): scores are kept in the log2 domain
   float* out;            // fp32 [B][Hq*HD]
+  // work units: source g is split into HS groups of hs = Hkv / HS KV heads;
+  // unit u = g * HS + hg streams the hs heads' K and V chunks of g's rows
+  int HS, hs;
+  int chunk_elems;  // f16 elements of one row chunk in shared memory (2 * hs * HD)
+  int n_units;      // n_src * HS
   // workspace
-  int* counters;   // [n_src], zero between calls
-  float* part_ml;  // [(P + n_src) * max_members * Hq][2]  (max, sum) per partial
-  float* part_o;   // [(P + n_src) * max_members * Hq][HD] unnormalised output per partial
+  int* counters;   // [n_units], zero between calls
+  float* part_ml;  // [(P + n_units) * max_members * hs * rep][2]  (max, sum) per partial
+  float* part_o;   // [(P + n_units) * max_members * hs * rep][HD] unnormalised output
   int32_t* dev_err;
   // tiling
   int R;            // row slots (groups of the same head working on different rows)
   int MS;           // query splits: groups of one head and row slot, each on NQ of its queries
   int tile_rows;    // rows per pipeline stage (R * rows per slot)
-  int min_share;    // fewest rows one CTA takes (bounds the partials per source)
-  int seg_rows;     // virtual rows charged per source on the flattened key axis
+  int min_share;    // fewest rows one CTA takes (bounds the partials per unit)
+  int seg_rows;     // virtual rows charged per unit on the flattened key axis
   int stages;       // pipeline depth
   int stage_elems;  // f16 elements per stage buffer (128-byte multiple)
   int mode;         // DecodeMode
   int pf_bytes;     // K/V bytes of its share a CTA asks L2 to prefetch before the grid dependency wait
+  uint64_t wait_ns; // bound of every mbarrier wait (ns of %globaltimer)
+  int stall;        // test support: the producer issues no copies, so every wait runs out
   // new-token append (GQA step, fused self step): the call writes row p and
   // folds that key in; p = n_past (GQA) or lens - 1 (self)
   int append;
@@ -61,13 +77,19 @@ struct DecodeArgs {
 };
 
 // Shared-memory layout of one CTA (bytes from the dynamic smem base).
+//   bars: full/empty mbarriers of the stage ring; ctl: control words; off,
+//     mstart: the consumers' source offsets and first sequences; poff: the
+//     producer's offsets; slen: the length entry of each source (self,
+//     GQA); rope, wts: GQA tables; merge: row-slot merge buffer; stage: the
+//     K/V ring.
 struct DecodeSmem {
-  int bars, ctl, off, mstart, poff, rope, wts, merge, stage, total;
+  int bars, ctl, off, mstart, poff, slen, rope, wts, merge, stage, total;
 };
 
 __host__ __device__ inline int dsm_align(int x, int a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, int R, int Hkv,
+// Hv: virtual heads of a unit (query splits x KV heads of the group).
+__host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, int R, int Hv,
                                                          int NQ, int HD, int stage_elems) {
   DecodeSmem s;
   s.bars = 0;
@@ -75,15 +97,22 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.off = dsm_align(s.ctl + 16 * 4, 16);
   s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
   s.poff = dsm_align(s.mstart + (n_src + 1) * 4, 16);
-  s.rope = dsm_align(s.poff + (n_src + 1) * 4, 16);
+  s.slen = dsm_align(s.poff + (n_src + 1) * 4, 16);
+  s.rope = dsm_align(s.slen + (n_src + 1) * 4, 16);
   s.wts = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
   s.merge = dsm_align(s.wts + 2 * HD * 4, 16);
-  s.stage = dsm_align(s.merge + (R > 1 ? (R - 1) : 0) * Hkv * NQ * (HD + 4) * 4, 128);
+  s.stage = dsm_align(s.merge + (R / 2) * Hv * NQ * (HD + 4) * 4, 128);
   s.total = s.stage + stages * stage_elems * 2;
   return s;
 }
 
-// Workspace bytes of a decode call with n_src sources on a device with `sms` SMs.
+// Workspace bytes of a decode call with n_src sources and Hq query heads on a
+// device with `sms` SMs (any head split: a unit of hs KV heads keeps only
+// its own query heads' partials).
 size_t decode_ws_bytes(int n_src, int max_members, int Hq, int HD, int sms);
+
+// Bytes at the start of that workspace that hold the per-unit counters (zero
+// between calls).
+size_t decode_counter_bytes(int n_src, int Hq);
 
 }  // namespace asrkv

@@ -610,8 +610,6 @@ static bool lin_plan(int M, int N, int K, int norm, bool glu, int sms, LinPlan* 
   return false;
 }
 
-static std::once_flag g_lin_attr;
-
 }  // namespace asrkv
 
 using namespace asrkv;
@@ -663,12 +661,8 @@ extern "C" int asr_linear(const float* x, int64_t x_stride, int norm, const floa
   if (p.ws_bytes > 0 &&
       (!ws || ws_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0))
     return ASR_ERR_WORKSPACE;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(g_lin_attr, [] {
-    attr = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kLinSmemMax);
-  });
-  if (attr != cudaSuccess) return ASR_ERR_CUDA;
+  if (ensure_dynamic_smem((const void*)linear_kernel, kLinSmemMax) != cudaSuccess)
+    return ASR_ERR_CUDA;
   CUtensorMap tw;
   if (!make_tmap_f16_3d(&tw, w, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
                         (uint64_t)N * K * 2, 64, 128))

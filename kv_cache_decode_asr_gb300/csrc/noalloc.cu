@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_attn.cuh"
 
 namespace asrkv {
 
@@ -81,11 +82,11 @@ extern "C" int asr_self_attn_step_noalloc(const float* q, int64_t q_stride, cons
   int st = ASR_OK;
   void* scratch = scratch_address(&st);
   if (!scratch) return st;
-  // The kernels expect their per-sequence counters (the first B ints of the
-  // workspace) to start at zero.  Each call leaves them at zero, but clear
-  // them anyway so that nothing depends on an earlier call having finished
-  // normally.  This is a memset, not an allocation.
-  if (cudaMemsetAsync(scratch, 0, align_up((size_t)B * 4, 256), (cudaStream_t)stream) !=
+  // The kernel expects its per-unit counters (at the start of the workspace)
+  // to start at zero.  Each call leaves them at zero, but clear them anyway
+  // so that nothing depends on an earlier call having finished normally.
+  // This is a memset, not an allocation.
+  if (cudaMemsetAsync(scratch, 0, decode_counter_bytes(B, heads), (cudaStream_t)stream) !=
       cudaSuccess)
     return ASR_ERR_CUDA;
   return asr_self_attn_step(q, q_stride, cache, seq_stride, lens, B, heads, head_dim, capacity,

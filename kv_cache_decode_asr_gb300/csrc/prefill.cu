@@ -782,6 +782,23 @@ bool make_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_f16_5d_plain(CUtensorMap* map, const void* base, const uint64_t dims[5],
+                            const uint64_t strides_bytes[4], const uint32_t box[5]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], estr[5];
+  for (int i = 0; i < 5; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    estr[i] = 1;
+  }
+  for (int i = 0; i < 4; ++i) st[i] = strides_bytes[i];
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void*>(base), d, st, bx, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv) {
@@ -793,9 +810,6 @@ size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv) {
 size_t mha_ws_bytes(int B, int T, int H, int HD) {
   return (size_t)B * H * HD * round_up(T, 128) * 2;  // V^T
 }
-
-static std::once_flag g_prefill_attr;
-static std::once_flag g_attn_attr[8];
 
 }  // namespace asrkv
 
@@ -819,12 +833,7 @@ static int prefill_check(int B, int T, int q_heads, int kv_heads, int head_dim, 
 }
 
 static cudaError_t prefill_attrs() {
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(g_prefill_attr, [] {
-    attr = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                100 * 1024);
-  });
-  return attr;
+  return ensure_dynamic_smem((const void*)prefill_prep_kernel, 100 * 1024);
 }
 
 // Launch the tensor-core attention for head dimension HD, causal or not.
@@ -834,12 +843,9 @@ static cudaError_t prefill_attrs() {
 template <int HD, bool CAUSAL, bool VARLEN>
 static int launch_attn_tc_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             PrefillAttnArgs& aa, cudaStream_t stream) {
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(g_attn_attr[(HD == 64 ? 0 : 4) + (CAUSAL ? 0 : 2) + (VARLEN ? 1 : 0)], [] {
-    attr = cudaFuncSetAttribute(attn_tc_kernel<HD, CAUSAL, VARLEN>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<HD>::SMEM);
-  });
-  if (attr != cudaSuccess) return ASR_ERR_CUDA;
+  if (ensure_dynamic_smem((const void*)attn_tc_kernel<HD, CAUSAL, VARLEN>, AttnCfg<HD>::SMEM) !=
+      cudaSuccess)
+    return ASR_ERR_CUDA;
   aa.n_qt = (aa.T + 127) / 128;
   aa.n_pairs = (aa.n_qt + 1) / 2;
   aa.n_items = aa.n_pairs * aa.B * aa.Hq;

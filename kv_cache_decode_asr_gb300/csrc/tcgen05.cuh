@@ -264,6 +264,12 @@ bool make_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
                       uint32_t box1);
 
+// Host: a 5-D f16 tensor map without swizzle (dims innermost first, strides
+// in bytes for dims 1..4) with the given box; out-of-range elements read as
+// zero.  Returns false on failure.
+bool make_tmap_f16_5d_plain(CUtensorMap* map, const void* base, const uint64_t dims[5],
+                            const uint64_t strides_bytes[4], const uint32_t box[5]);
+
 // Workspace bytes of the prefill: q^ [B][T][Hq*128] f16 (1024-byte aligned
 // end), then V^T [B*Hkv][128][T rounded up to 128] f16.
 size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv);

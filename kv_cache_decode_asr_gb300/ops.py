@@ -58,6 +58,7 @@ SIGNATURES = {
     "asr_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int, _int]),
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
+    "asr_debug_stall_next_decode": (_int, [ctypes.c_uint64]),
 }
 
 _LIB = None
@@ -114,6 +115,13 @@ def asr_status_string(status):
 
 def asr_version():
     return load().asr_version()
+
+
+def asr_debug_stall_next_decode(wait_ns):
+    """Test support: the next decode-attention launch from this thread issues
+    no copies, so its waits run out after wait_ns and it reports
+    DEVERR_TIMEOUT (its outputs are undefined)."""
+    _check("asr_debug_stall_next_decode", load().asr_debug_stall_next_decode(int(wait_ns)))
 
 
 def asr_workspace_size(op, B, n_sources, max_beams, q_heads, head_dim, T=0):

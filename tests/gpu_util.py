@@ -9,6 +9,8 @@ and byte paths (append, rearrange, appended V rows) must match bit for bit.
 import numpy as np
 import torch
 
+from kv_cache_decode_asr_gb300 import synthetic as syn
+
 ABS_TOL = 2e-3
 REL_TOL = 1e-2
 
@@ -56,3 +58,16 @@ def f16_ulp(bits):
 
 def new_err():
     return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def lo_plane_inputs(M, N, K, seed):
+    """Activations +-2^e (1 + j 2^-13), e in [-2, 2], j in {3, 5}: the f16
+    high part of each drops exactly 3 2^-13 2^e.  Weights f16 N(0, 1/K)."""
+    r = syn.rng(seed)
+    e = r.integers(-2, 3, (M, K)).astype(np.float64)
+    j = np.where(r.integers(0, 2, (M, K)) == 0, 3.0, 5.0)
+    sgn = np.where(r.integers(0, 2, (M, K)) == 0, -1.0, 1.0)
+    x = (sgn * 2.0 ** e * (1.0 + j * 2.0 ** -13)).astype(np.float32)
+    w = (syn.host_normal_f32((N, K), seed + 1) * np.float32(K ** -0.5)).astype(
+        np.float16).view(np.uint16)
+    return x, w

@@ -296,6 +296,15 @@ def test_cross_attn_bad_groups():
     err = new_err()
     got = _run_cross(q, cross, np.array([1, 0, 0, 1, 2, 2], np.int32), G, 2, H, hd, frames, err=err)
     assert np.all(got == 0) and int(err.item()) == ops.DEVERR_INDEX
+    # a negative group id before the first group: only that sequence is
+    # skipped, and the members of group 0 are the sequences that follow it
+    group = np.array([-1, 0, 0, 1, 2, 2], np.int32)
+    err = new_err()
+    got = _run_cross(q, cross, group, G, 2, H, hd, frames, err=err)
+    ref, _ = oracle.cross_attn_step(q, cross, np.array([0, 0, 0, 1, 2, 2], np.int32), H, hd,
+                                    hd ** -0.5)
+    assert np.all(got[0] == 0) and int(err.item()) == ops.DEVERR_INDEX
+    assert_attn_close(got[1:], ref[1:], "cross after a negative group id")
 
 
 # ----------------------------------------------------------- GQA step ----

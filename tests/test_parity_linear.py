@@ -25,7 +25,8 @@ import oracle  # noqa: E402
 from kv_cache_decode_asr_gb300 import ops  # noqa: E402
 from kv_cache_decode_asr_gb300 import synthetic as syn  # noqa: E402
 
-from gpu_util import assert_attn_close, dev, host, host_u16, new_err  # noqa: E402
+from gpu_util import (assert_attn_close, dev, host, host_u16, lo_plane_inputs,  # noqa: E402
+                      new_err)
 
 GELU_SLOPE = 1.13
 
@@ -78,6 +79,35 @@ CASES = [
     (3, 100, 128, "store", True, False),       # fewer weight rows than one 128-row tile
     (4, 10240, 128, "gelu", True, False),      # 80 weight tiles, K split in two under the norm
 ]
+
+
+# Activations whose low bits matter: each value is +-2^e (1 + j 2^-13), j in
+# {3, 5}, so its f16 high part drops exactly 3 2^-13 2^e, which the f16
+# remainder plane holds exactly.  The two planes together reach the tensor
+# cores with no rounding, and what is left is the fp32 accumulation error
+# (about 2^-22 of sum |a||W| measured on random data).  Without the remainder
+# plane the error would be sum_k lo_k W_nk, about 3.7e-4 |a| sqrt(K) |W|, i.e.
+# 2^-16.6 of sum |a||W| at K = 1280 and more at K = 128: the bound 2^-19
+# sum |a||W| separates the two.
+LO_PLANE_BOUND = 2.0 ** -19
+LO_PLANE_CASES = [(32, 1280, 1280), (16, 2048, 2048), (8, 512, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", LO_PLANE_CASES)
+def test_linear_keeps_the_activation_remainder(M, N, K):
+    """The activation's low bits reach the product: error <= 2^-19 sum|a||W|."""
+    x, w = lo_plane_inputs(M, N, K, 7700 + K)
+    ref = oracle.linear(x, w, None, mode="store")
+    s = np.abs(x.astype(np.float64)) @ np.abs(dec16(w)).T
+    y_d = torch.full((M, N), float("nan"), device="cuda")
+    err = new_err()
+    ops.asr_linear(dev(x), dev(w), y_d, mode="store", ws=ops.linear_workspace(M, N, K),
+                   dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    worst = assert_linear_close(host(y_d), ref, LO_PLANE_BOUND * s + 1e-7, s,
+                                f"remainder plane M={M} N={N} K={K}")
+    print(f"remainder plane M={M} N={N} K={K}: worst err / sum|a||w| = {worst:.2e}")
 
 
 @pytest.mark.parametrize("M,N,K,mode,ln,strided", CASES)

@@ -109,4 +109,10 @@ def test_prefill_full_qwen3_asr_sampled():
         rows = oracle.prefill_attn_rows(qhat[b, ts, h * HD:(h + 1) * HD], ts, ref_cache[b], Hq, Hkv,
                                         HD, h, HD ** -0.5)
         assert_attn_close(got[b, ts, h * HD:(h + 1) * HD], rows, f"prefill b={b} h={h}")
+    # one (sequence, head) pair whole: every one of its 1536 rows, element-wise
+    b, h = 2, 9
+    all_t = np.arange(T, dtype=np.int32)
+    rows = oracle.prefill_attn_rows(qhat[b, :, h * HD:(h + 1) * HD], all_t, ref_cache[b], Hq, Hkv,
+                                    HD, h, HD ** -0.5)
+    assert_attn_close(got[b, :, h * HD:(h + 1) * HD], rows, f"prefill b={b} h={h}, all rows")
     assert np.all(np.isfinite(got))

@@ -5,9 +5,10 @@ for a workspace: a plugin whose host owns every allocation and forbids
 allocating while it enqueues work, or a real-time audio thread that must not
 wait on an allocator.  The library keeps that entry point's scratch in a
 fixed array in device memory.  These tests call it through the C ABI and
-check it against the ordinary entry point (which takes a workspace) on two
-calls in a row with different inputs, so that whatever the first call left in
-the shared array cannot leak into the second.
+check it against the ordinary entry point (which takes a workspace) and
+against the CPU oracle, on two calls in a row with different inputs, so that
+whatever the first call left in the shared array cannot leak into the
+second.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it passes both alone and after the others.
@@ -20,6 +21,7 @@ import pytest
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+import oracle  # noqa: E402
 from kv_cache_decode_asr_gb300 import ops  # noqa: E402
 from kv_cache_decode_asr_gb300 import synthetic as syn  # noqa: E402
 
@@ -33,6 +35,7 @@ def _lib():
     from kv_cache_decode_asr_gb300 import build
     build.build()
     ops.load()
+    oracle.build()
 
 
 def _inputs(B, H, hd, cap, seed):
@@ -58,6 +61,9 @@ def test_noalloc_matches_workspace_entry_on_two_calls(B, H, hd, cap):
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         assert_attn_close(host(got), host(ref), f"no-alloc call seed={seed}")
+        want, skipped = oracle.self_attn_step(qh, ch, lh, H, hd, hd ** -0.5, q_stride=3 * d)
+        assert skipped == 0
+        assert_attn_close(host(got), want, f"no-alloc call seed={seed} vs oracle")
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
