@@ -1090,14 +1090,16 @@ static void* kernel_for(int HD, int vi) {
 //   smem_kb: shared memory the stage ring may fill;
 //   min_kb: fewest K/V bytes one CTA takes (bounds the partials per unit);
 //   seg_kb: K/V bytes' worth of virtual rows charged to each unit, so CTAs
-//     that start or finish more units take fewer rows;
+//     that start or finish more units take fewer rows (gqa_seg_kb for the
+//     GQA step, whose unit start also normalises and rotates its queries);
 //   qs: queries per thread group when a KV row serves more than two queries;
 //   parts: the number of CTA pieces per unit the head split aims at (a
 //     source is cut into the fewest head groups that bring its expected
 //     pieces to this or below);
 //   min_chunk: fewest bytes of one row a head group streams.
 struct DecodeTune {
-  int tile_kb = 80, smem_kb = 200, min_kb = 64, seg_kb = 256, qs = 2, parts = 6, min_chunk = 512;
+  int tile_kb = 80, smem_kb = 200, min_kb = 64, seg_kb = 256, gqa_seg_kb = 384, qs = 2, parts = 6,
+      min_chunk = 512;
 };
 
 static constexpr DecodeTune decode_tune() { return DecodeTune{}; }
@@ -1113,6 +1115,7 @@ struct DecodePlan {
 // many as fit smem_kb, 2..8.  One CTA takes at least min_kb of rows, so a
 // unit splits into a bounded number of partial results.
 static bool plan_layout(const DecodeArgs& a, int HD, int vi, int MS, int hs, DecodePlan& p) {
+  const int seg_kb = a.mode == kModeGqa ? decode_tune().gqa_seg_kb : decode_tune().seg_kb;
   const int n_src = a.n_src;
   const DecodeTune tune = decode_tune();
   const Variant& v = kVariants[vi];
@@ -1145,7 +1148,7 @@ static bool plan_layout(const DecodeArgs& a, int HD, int vi, int MS, int hs, Dec
   p.smem = decode_smem_layout(stages, n_src, p.R, MS * hs, v.NQ, HD, p.stage_elems).total;
   if (p.smem > 227 * 1024) return false;
   p.min_share = std::max(p.tile_rows, (tune.min_kb * 1024 + chunk_bytes - 1) / chunk_bytes);
-  p.seg_rows = tune.seg_kb * 1024 / chunk_bytes;
+  p.seg_rows = seg_kb * 1024 / chunk_bytes;
   p.pf_bytes = stages * p.tile_rows * chunk_bytes;
   return true;
 }
