@@ -58,7 +58,9 @@ cross_fill_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant_
   uint64_t* empty = full + kFillStages;
   uint64_t* acc_full = empty + kFillStages;  // [2]: the accumulator of a tile is complete
   uint64_t* acc_empty = acc_full + 2;        // [2]: the epilogue has read it
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* drain = acc_empty + 2;           // every MMA this CTA issued has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_any = reinterpret_cast<int*>(tslot + 1);  // some wait of this CTA gave up
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -70,6 +72,8 @@ cross_fill_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant_
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
     }
+    mbar_init(drain, 1);
+    *abort_any = 0;
     fence_barrier_init();
   }
   if (warp == 4) {
@@ -86,9 +90,9 @@ cross_fill_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant_
   const int n_tiles_all = a.n_tiles_total;
   bool ok = true;
 
+  int gs = 0;  // ring position (producer: copies issued)
   if (warp == 4) {
     // ======================================================= TMA producer
-    int gs = 0;  // ring position
     for (int tile = blockIdx.x; tile < n_tiles_all && ok; tile += gridDim.x) {
       const int nt = tile % a.n_tiles, mt_all = tile / a.n_tiles;
       const int g = mt_all / a.m_tiles_per_group, mt = mt_all % a.m_tiles_per_group;
@@ -186,7 +190,26 @@ cross_fill_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant_
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
-  if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+  if (!ok && lane == 0) {
+    set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    atomicExch(abort_any, 1);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // After a wait gave up, nothing may still be in flight into this CTA's
+  // shared memory or tensor memory when it frees them and leaves: the
+  // producer waits (bounded) for the copies it issued (only the last ring's
+  // worth can be pending), the MMA warp for every MMA it issued (a commit
+  // tracks all of them).
+  if (*reinterpret_cast<volatile int*>(abort_any)) {
+    if (warp == 4) {
+      for (int i = max(0, gs - kFillStages); i < gs; ++i)
+        mbar_wait_warp(&full[i % kFillStages], (i / kFillStages) & 1);
+    } else if (warp == 5) {
+      mma_commit_warp(drain);
+      mbar_wait_warp(drain, 0);
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 4) {

@@ -191,9 +191,11 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
   uint64_t* xin_full = empty + kLinStages;  // the fp32 activations have landed
   uint64_t* x_full = xin_full + 1;          // the f16 operand is in shared memory
   uint64_t* acc_full = x_full + 1;          // the accumulator is complete
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* drain = acc_full + 1;           // every MMA this CTA issued has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   int* last_flag = reinterpret_cast<int*>(tslot + 1);
   int* abort_flag = last_flag + 1;  // a wait of warps 0-3 gave up
+  int* abort_any = abort_flag + 1;  // some wait of this CTA gave up
   float* s_s1 = reinterpret_cast<float*>(sFb + f32b + 256);
   float* s_s2 = s_s1 + kLinMaxMT;  // LayerNorm sums of this CTA's K range
   float* s_dm = s_s2 + kLinMaxMT;  // mean - x_0 of each row
@@ -216,7 +218,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
     mbar_init(xin_full, 1);
     mbar_init(x_full, kLinStageThreads);
     mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
+    *abort_any = 0;
+    *last_flag = 0;
     fence_barrier_init();
   }
   if (tid < MT) s_s1[tid] = s_s2[tid] = 0.f;
@@ -550,7 +555,26 @@ linear_kernel(const __grid_constant__ CUtensorMap tw, const LinArgs a) {
       }
     }
   }
-  if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+  if (!ok && lane == 0) {
+    set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    atomicExch(abort_any, 1);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // After a wait gave up, nothing may still be in flight into this CTA's
+  // shared memory or tensor memory when it frees them and leaves: the bulk
+  // copies of warp 0 into xin_full (the activations, its first phase, and in
+  // the last CTA of a tile the reloaded sums, its second; bounded waits; the
+  // W producer already waited for its own copies above) and every MMA the
+  // MMA warp issued (a commit tracks all of them).
+  if (*reinterpret_cast<volatile int*>(abort_any)) {
+    if (warp == 0) {
+      mbar_wait_warp(xin_full, *reinterpret_cast<volatile int*>(last_flag) ? 1 : 0);
+    } else if (warp == kLinMmaWarp) {
+      mma_commit_warp(drain);
+      mbar_wait_warp(drain, 0);
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kLinTmaWarp) {

@@ -391,7 +391,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
   uint64_t* p_full = s_full + 2;            // [A0, A1, B0, B1]: half h (keys 64h..) of P of tile g
   uint64_t* o_done = p_full + 4;            // [A, B]: the slot's last PV of an item
   uint64_t* o_free = o_done + 2;            // [A, B]: the softmax has read O of its item
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_free + 2);
+  uint64_t* drain = o_free + 2;             // every MMA this CTA issued has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_any = reinterpret_cast<int*>(tslot + 1);  // some wait of this CTA gave up
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -413,6 +415,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       mbar_init(&o_done[i], 1);
       mbar_init(&o_free[i], 4);
     }
+    mbar_init(drain, 1);
+    *abort_any = 0;
     fence_barrier_init();
   }
   if (warp == 8) {
@@ -430,6 +434,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
   auto tS = [&](int i) { return tbase + 128u * i; };
   auto tO = [&](int i) { return tbase + 256u + 128u * i; };
 
+  int nk = 0, nv = 0, nq = 0;  // producer: K, V tile copies and Q uses issued
   if (warp == 8) {
     // ======================================================= TMA producer
     // The whole warp runs the schedule; one elected lane issues each copy.
@@ -446,6 +451,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       if (c > 0 && !(ok = mbar_wait_warp(&q_empty[u], (c - 1) & 1))) return;
       const bool has = (i == 0 ? x.nA : x.nB) > 0;
       mbar_arrive_expect_tx_warp(&q_full[u], has ? kQTile : 0);
+      ++nq;
       if (has) {
         const int qt = i == 0 ? x.qt_a : x.qt_b;
         unsigned char* qd = sQ + u * kQTile;
@@ -470,18 +476,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         unsigned char* vd = sV + s * kVTile;
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&k_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&k_full[s], kKTile);
+        ++nk;
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
           tma_load_3d_warp(kd + c * kHalfBlock, &tk, x.kvh * HD + 64 * c, j * 128, x.b, &k_full[s]);
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&v_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
+        ++nv;
         tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
         if (j == 0) load_q(k, 1, x);  // the buffer of this item's slot A tile's predecessor
       }
       if (VARLEN && ok && x.n == 0) load_q(k, 1, x);  // an empty item still completes its slot B use
     }
-    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    if (!ok && lane == 0) {
+      set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+      atomicExch(abort_any, 1);
+    }
   } else if (warp == 9) {
     // ======================================================= MMA issuer
     // The whole warp runs the schedule (operand descriptors stay
@@ -602,7 +613,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       ox[1] += x.nB > 0 ? 1 : 0;
       gk += x.n;
     }
-    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    if (!ok && lane == 0) {
+      set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+      atomicExch(abort_any, 1);
+    }
   } else {
     // ======================================================= softmax
     const int i = warp >> 2;                  // 0: slot A, 1: slot B
@@ -737,7 +751,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
       }
     }
-    if (!ok && lane == 0) set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+    if (!ok && lane == 0) {
+      set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+      atomicExch(abort_any, 1);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // After any wait of this CTA gave up, nothing may still be in flight into
+  // its shared memory or tensor memory when it frees them and leaves: the
+  // producer waits (bounded) for the copies it issued (only the last ring's
+  // worth of K and V tiles and the last use of each Q buffer can be
+  // pending), the MMA warp for every MMA it issued (a commit tracks all of
+  // them).
+  if (*reinterpret_cast<volatile int*>(abort_any)) {
+    if (warp == 8) {
+      for (int i = max(0, nk - kKVStages); i < nk; ++i)
+        mbar_wait_warp(&k_full[i % kKVStages], (i / kKVStages) & 1);
+      for (int i = max(0, nv - kKVStages); i < nv; ++i)
+        mbar_wait_warp(&v_full[i % kKVStages], (i / kKVStages) & 1);
+      for (int n = max(0, nq - kQBufs); n < nq; ++n)
+        mbar_wait_warp(&q_full[n % kQBufs], (n / kQBufs) & 1);
+    } else if (warp == 9) {
+      mma_commit_warp(drain);
+      mbar_wait_warp(drain, 0);
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
