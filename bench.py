@@ -218,17 +218,26 @@ class WhisperStep:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 
     separate_append = False
+    # beam reorder fused into each layer's append + self launch (else one
+    # asr_kv_rearrange launch over all layers first)
+    separate_reorder = False
     profile_kernel = "cross"
+
+    def fused_reorder(self):
+        return self.rearrange and not self.separate_reorder
 
     # kernels launched by one step
     def launches(self):
-        return (1 if self.rearrange else 0) + (3 if self.separate_append else 2) * self.L
+        return ((1 if self.rearrange and not self.fused_reorder() else 0) +
+                (3 if self.separate_append and not self.fused_reorder() else 2) * self.L)
 
     def layer_calls(self, l, stream=None):
         ops, d = self.ops, self.d
         cache_l = self.cache[:, l]
         qkv = self.qkv[l]
-        if self.separate_append:
+        if self.fused_reorder():
+            self.reorder_self_call(l, stream)
+        elif self.separate_append:
             ops.asr_kv_append(qkv[:, d:2 * d], qkv[:, 2 * d:], cache_l, self.slot, self.H,
                               self.hd, self.cap, dev_err=self.err, stream=stream)
             ops.asr_self_attn_step(qkv[:, :d], cache_l, self.lens, self.H, self.hd, self.cap,
@@ -242,13 +251,20 @@ class WhisperStep:
                                           stream=stream)
         self.cross_call(l, stream)
 
+    def reorder_self_call(self, l, stream=None):
+        d, qkv = self.d, self.qkv[l]
+        self.ops.asr_self_attn_reorder_append_step(
+            qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:], self.cache_src[:, l], self.cache[:, l],
+            self.idx, self.lens_src, self.lens, self.H, self.hd, self.cap, self.scale,
+            self.out_self[l], self.ws_self, dev_err=self.err, stream=stream)
+
     def cross_call(self, l, stream=None):
         self.ops.asr_cross_attn_step(self.qx[l], self.cross[l], self.group, self.G, self.beam,
                                      self.H, self.hd, self.F, self.scale, self.out_cross[l],
                                      self.ws_cross, dev_err=self.err, stream=stream)
 
     def step(self, stream=None):
-        if self.rearrange:
+        if self.rearrange and not self.fused_reorder():
             self.ops.asr_kv_rearrange(self.cache_src, self.cache, self.idx, self.lens_src,
                                       self.lens, self.L, self.row, self.cap,
                                       layer_stride=self.cap * self.row, dev_err=self.err,
@@ -285,7 +301,9 @@ class WhisperStep:
         return "self+append" if self.profile_kernel == "self" else "cross"
 
     def dominant_call(self, l, stream=None):
-        if self.profile_kernel == "self":
+        if self.profile_kernel == "self" and self.fused_reorder():
+            self.reorder_self_call(l, stream)
+        elif self.profile_kernel == "self":
             ops, d = self.ops, self.d
             qkv = self.qkv[l]
             ops.asr_self_attn_append_step(qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:],
@@ -328,10 +346,20 @@ class WhisperStep:
         out_c, _ = oracle.cross_attn_step(qx, cross_h, self.group_host, self.H, self.hd,
                                           self.scale)
         dt = time.perf_counter() - t0
-        return dt, {"self": out_s, "cross": out_c}
+        ref = {"self": out_s, "cross": out_c}
+        if self.rearrange:
+            # the reordered cache with the appended rows: compared as integers
+            # (0 when every f16 bit pattern matches)
+            ref["cache_bits"] = cache_h.astype(np.float64)
+        return dt, ref
 
     def gpu_layer_outputs(self, l):
-        return {"self": self.out_self[l].cpu().numpy(), "cross": self.out_cross[l].cpu().numpy()}
+        import torch
+        got = {"self": self.out_self[l].cpu().numpy(), "cross": self.out_cross[l].cpu().numpy()}
+        if self.rearrange:
+            got["cache_bits"] = (self.cache[:, l].contiguous().view(torch.int16).cpu().numpy()
+                                 .view(np.uint16).astype(np.float64))
+        return got
 
     def oracle_sample(self, i, oracle):
         """(oracle seconds, fraction of the step, reference, gpu) for layer i."""
@@ -1227,6 +1255,8 @@ def run_ours(args):
     wl = make_workload(args.workload, device, rank, args.layers)
     if args.separate_append:
         wl.separate_append = True
+    if args.separate_reorder:
+        wl.separate_reorder = True
     if args.roofline_kernel != "default":
         wl.profile_kernel = args.roofline_kernel
         wl.dominant_kernel = f"roofline of the {args.roofline_kernel} kernel"
@@ -1428,6 +1458,9 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration measurements of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--separate-reorder", action="store_true",
+                    help="beam workload: one asr_kv_rearrange launch before the layers instead "
+                         "of the reorder fused into each layer's append + self launch")
     ap.add_argument("--separate-append", action="store_true",
                     help="Whisper: launch the K/V append and the self-attention separately")
     ap.add_argument("--roofline-kernel", default="default", choices=["default", "cross", "self"],

@@ -156,6 +156,36 @@ int asr_self_attn_append_step(const float* q, int64_t q_stride, const float* k_n
                               int head_dim, int capacity, float scale, float* out, void* ws,
                               size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
+/* a6 + a1 + a2 fused -- beam reorder of one layer's self cache, append of the
+ * new token and self-attention, in one launch.
+ * Defines: "mlx-bun whisper.ts", WhisperKvCache.rearrange (take along the batch
+ * axis of the self k/v before the step) followed by the append + self step
+ * above.  Equal, byte for byte in cache_dst and lens_dst and in out, to
+ * asr_kv_rearrange over this one layer (n_layers = 1) followed by
+ * asr_self_attn_append_step on cache_dst with lens = lens_dst:
+ *   for beam b with s = idx[b] and L = lens_src[s]:
+ *   rows [0, L-1) of cache_dst[b] = rows [0, L-1) of cache_src[s] (bitwise);
+ *   row L-1 of cache_dst[b] = f16_rne(k_new_b) || f16_rne(v_new_b);
+ *   out_b = self-attention of q_b over rows [0, L) of cache_dst[b];
+ *   lens_dst[b] = L.
+ * The history rows are read once: each tile is attended from shared memory
+ * and stored to cache_dst from there.  idx, lens_src, lens_dst: int32 [B],
+ * device.  idx[b] outside [0, B) (ASR_DEVERR_INDEX) or L outside
+ * [1, capacity] (ASR_DEVERR_LEN) skips beam b: its output row is zeroed,
+ * lens_dst[b] = 0 and cache_dst[b] is left untouched.  cache_src and
+ * cache_dst share seq_stride and must not overlap (ASR_ERR_ALIAS), nor may
+ * lens_dst overlap lens_src or idx.  Rows of cache_dst past L are left
+ * untouched.  Other arguments, alignment and errors as
+ * asr_self_attn_append_step; ws: the ASR_OP_SELF_ATTN size. */
+int asr_self_attn_reorder_append_step(const float* q, int64_t q_stride, const float* k_new,
+                                      const float* v_new, int64_t kv_stride,
+                                      const uint16_t* cache_src, uint16_t* cache_dst,
+                                      int64_t seq_stride, const int32_t* idx,
+                                      const int32_t* lens_src, int32_t* lens_dst, int B,
+                                      int heads, int head_dim, int capacity, float scale,
+                                      float* out, void* ws, size_t ws_bytes, int32_t* dev_err,
+                                      asr_stream_t stream);
+
 /* a3 (+ a4) -- cross-attention of one token per sequence over the encoder's
  * cached K/V, shared by the beams of one audio.
  * Defines: "wavo 0.1.0, src/whisper/decoder.rs", Decoder::record_step
@@ -407,7 +437,8 @@ int asr_version(void);
 
 /* Test support for the bounded waits (no counterpart in the pages).  Arms the
  * next decode-attention launch (asr_self_attn_step, asr_self_attn_append_step,
- * asr_cross_attn_step, asr_gqa_step or asr_self_attn_step_noalloc) made by
+ * asr_self_attn_reorder_append_step, asr_cross_attn_step, asr_gqa_step or
+ * asr_self_attn_step_noalloc) made by
  * the calling host thread: its producer issues no copies, so every pipeline
  * wait of that launch runs out after wait_ns nanoseconds (0 < wait_ns <= 2 s).
  * The kernel then sets ASR_DEVERR_TIMEOUT in dev_err, passes over its

@@ -110,4 +110,4 @@ extern "C" const char* asr_status_string(int status) {
   }
 }
 
-extern "C" int asr_version(void) { return 100; }
+extern "C" int asr_version(void) { return 101; }

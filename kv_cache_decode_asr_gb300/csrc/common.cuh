@@ -151,6 +151,31 @@ __device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint3
       : "memory");
 }
 
+// One bulk (TMA) copy shared -> global in the thread's current bulk group.
+// dst, src 16-byte aligned; bytes a multiple of 16.  The shared memory must
+// not change until bulk_wait_read() says the copy has read it.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+
+// Close the thread's current bulk group of shared -> global copies.
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has read its shared
+// memory (the writes to global memory may still be in flight).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Hint: bring `bytes` of global memory at `src` into L2 (no destination, no
 // completion to wait for).  src 16-byte aligned; bytes a multiple of 16.  A
 // prefetch changes no memory and is never observed by loads, so it is safe

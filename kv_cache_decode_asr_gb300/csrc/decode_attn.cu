@@ -64,9 +64,11 @@ __device__ __forceinline__ int streamed_rows(const DecodeArgs& a, int v) {
 // room.  Cross: a group is streamed when some sequence belongs to it (the
 // flags go through off[] itself, which is then scanned in place); returns -1
 // when the group indices are not sorted.  cg: read the inputs from L2 only
-// (the early, hint-only pass before the grid dependency wait).
+// (the early, hint-only pass before the grid dependency wait).  With a beam
+// reorder, source g takes the length of sequence idx[g] (0, nothing to
+// stream, for an index outside [0, S)) and src_out[g] receives idx[g].
 __device__ int warp_offsets(const DecodeArgs& a, int* off, int S, int lane, bool cg,
-                             int* lens_out = nullptr) {
+                             int* lens_out = nullptr, int* src_out = nullptr) {
   if (a.mode == kModeCross) {
     for (int g = lane; g <= S; g += 32) off[g] = 0;
     __syncwarp();
@@ -87,7 +89,14 @@ __device__ int warp_offsets(const DecodeArgs& a, int* off, int S, int lane, bool
       if (a.mode == kModeCross) {
         keys = off[g] ? a.HS * (a.fixed_len + a.seg_rows) : 0;
       } else {
-        const int v = cg ? __ldcg(a.lens + g) : a.lens[g];
+        int v;
+        if (a.idx) {
+          const int sq = cg ? __ldcg(a.idx + g) : a.idx[g];
+          v = (sq >= 0 && sq < S) ? (cg ? __ldcg(a.lens + sq) : a.lens[sq]) : 0;
+          if (src_out) src_out[g] = sq;
+        } else {
+          v = cg ? __ldcg(a.lens + g) : a.lens[g];
+        }
         if (lens_out) lens_out[g] = v;
         const int k = streamed_rows(a, v);
         keys = k > 0 ? a.HS * (k + a.seg_rows) : 0;
@@ -547,9 +556,10 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   // a load, so the hint cannot change a result.  Its offsets go to the stage
   // ring, which nothing touches before this warp's first copy.
   if (warp == cons_warps && !a.stall && a.pf_bytes > 0 &&
-      (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
+      2 * (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
     int* poff = reinterpret_cast<int*>(stage);
-    const int run = warp_offsets(a, poff, S, lane, true);
+    int* psq = poff + S + 1;  // beam reorder: the sequence each source reads
+    const int run = warp_offsets(a, poff, S, lane, true, nullptr, psq);
     if (run > 0) {
       const int pshare = max((int)((run + gridDim.x - 1) / gridDim.x), a.min_share);
       const int pk0 = (int)min((int64_t)blockIdx.x * pshare, (int64_t)run);
@@ -594,7 +604,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         int left = a.pf_bytes;
         while (left > 0 && it.next(tl)) {
           if (HS == 1) {
-            bulk_prefetch_l2(a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
+            const int sq = a.idx ? psq[tl.g] : tl.g;
+            bulk_prefetch_l2(a.kv + (int64_t)sq * a.src_stride + (int64_t)tl.row0 * a.row_elems,
                              (uint32_t)tl.nr * chunk_bytes);
           } else {
             for (int rr = 0; rr < tl.nr; rr += kBoxRows)
@@ -614,7 +625,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     // computes the offsets itself (the same integers the consumers compute)
     // and starts at once.
     int* toff = poff_region;
-    const int total = warp_offsets(a, toff, S, lane, false);
+    int* tsq = reinterpret_cast<int*>(smem + lay.psrc);
+    const int total = warp_offsets(a, toff, S, lane, false, nullptr, tsq);
     if (total <= 0 || a.stall) {  // nothing to stream, unsorted groups, or the stall test
       grid_launch_dependents();
       return;
@@ -624,22 +636,47 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     const int k1 = min(k0 + share, total);
     if (lane == 0 && k0 < k1) {
       const uint64_t pol = policy_evict_first();
+      // Beam reorder (whole rows, HS == 1): each tile, once it has landed, is
+      // also stored to its destination sequence.  The stores trail the loads
+      // by stages - 1 tiles (a second walker `st` names them), so waiting for
+      // the tile to store never holds back a load the ring has room for; the
+      // store of the tile a stage held has read it before the stage is
+      // loaded again.
+      const bool reorder = a.idx != nullptr;
       TileIter it(toff, S, HS, k0, k1, a.tile_rows, a.seg_rows);
-      Tile tl;
-      int t = 0;
+      TileIter st(toff, S, HS, k0, k1, a.tile_rows, a.seg_rows);
+      Tile tl, ts;
+      int t = 0, stored = 0;
+      bool aborted = false;
+      auto store_next = [&]() -> bool {
+        const int j = stored;
+        if (!st.next(ts) || !mbar_wait(&full[j % a.stages], (j / a.stages) & 1, a.wait_ns))
+          return false;
+        bulk_s2g(a.cache_w + (int64_t)ts.g * a.src_stride + (int64_t)ts.row0 * a.row_elems,
+                 stage + (size_t)(j % a.stages) * a.stage_elems, (uint32_t)ts.nr * chunk_bytes);
+        bulk_commit();
+        ++stored;
+        return true;
+      };
       for (; it.next(tl); ++t) {
         const int s = t % a.stages;
         if (t >= a.stages && !mbar_wait(&empty[s], ((t / a.stages) - 1) & 1, a.wait_ns)) {
-          set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
-          *abort_flag = 1;
+          aborted = true;
           break;
         }
         if (*abort_flag) break;  // the consumers gave up: issue nothing more
+        if (reorder && t >= a.stages) bulk_wait_read();  // tile t - stages is stored
         uint16_t* dst = stage + (size_t)s * a.stage_elems;
         mbar_arrive_expect_tx(&full[s], (uint32_t)tl.nr * chunk_bytes);
         if (HS == 1) {
-          bulk_g2s(dst, a.kv + (int64_t)tl.g * a.src_stride + (int64_t)tl.row0 * a.row_elems,
+          const int sq = reorder ? tsq[tl.g] : tl.g;
+          bulk_g2s(dst, a.kv + (int64_t)sq * a.src_stride + (int64_t)tl.row0 * a.row_elems,
                    (uint32_t)tl.nr * chunk_bytes, &full[s], pol);
+          if (reorder && t >= a.stages - 1 && !store_next()) {
+            ++t;  // tile t was issued: the drain below covers it
+            aborted = true;
+            break;
+          }
         } else {
           const int c1 = tl.hg * hs;
           int rr = 0;
@@ -651,11 +688,26 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
                         pol);
         }
       }
-      // The CTA must not end while a copy into its shared memory is in
-      // flight: wait (bounded) until the last copies issued have landed.
+      // the tiles still to store
+      if (reorder && !aborted && *abort_flag == 0) {
+        while (stored < t) {
+          if (!store_next()) {
+            aborted = true;
+            break;
+          }
+        }
+      }
+      if (aborted) {
+        set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // The CTA must not end while a copy into or out of its shared memory
+      // is in flight: wait (bounded) until the last loads issued have landed,
+      // then for the stores (which read only landed tiles and always finish).
       for (int t2 = max(0, t - a.stages); t2 < t; ++t2)
         if (!mbar_wait(&full[t2 % a.stages], (t2 / a.stages) & 1, a.wait_ns))
           set_dev_err(a.dev_err, ASR_DEVERR_TIMEOUT);
+      if (reorder) bulk_wait_all();
     }
     grid_launch_dependents();
     return;
@@ -701,7 +753,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
         const int v = slen[b];
         const bool ok =
             a.mode == kModeSelf ? (v >= 1 && v <= a.capacity) : (v >= 0 && v < a.capacity);
-        if (!ok) bad = ASR_DEVERR_LEN;
+        if (!ok) bad = (a.idx && (unsigned)a.idx[b] >= (unsigned)S) ? ASR_DEVERR_INDEX : ASR_DEVERR_LEN;
+        if (a.lens_out && lane == 0) a.lens_out[b] = bad ? 0 : v;
       }
       if (bad) {
         for (int i = lane * 4; i < qw; i += 128)
@@ -1180,7 +1233,8 @@ static bool plan_decode(const DecodeArgs& a, int HD, int nq_needed, int sms, Dec
     }
     // Cross-attention keeps whole rows: its beams already share each row
     // among several queries, and splitting the heads measured slower there.
-    const int max_hs_split = a.mode == kModeCross ? 1 : a.Hkv;
+    // The beam reorder stores whole landed rows, so it keeps them too.
+    const int max_hs_split = (a.mode == kModeCross || a.idx) ? 1 : a.Hkv;
     for (int HS = 1; HS <= max_hs_split; ++HS) {
       if (a.Hkv % HS != 0) continue;
       const int hs = a.Hkv / HS;
@@ -1357,34 +1411,50 @@ extern "C" int asr_self_attn_step(const float* q, int64_t q_stride, const uint16
   return launch_decode(a, head_dim, 1, ws, ws_bytes, (cudaStream_t)stream);
 }
 
-extern "C" int asr_self_attn_append_step(const float* q, int64_t q_stride, const float* k_new,
-                                         const float* v_new, int64_t kv_stride, uint16_t* cache,
-                                         int64_t seq_stride, const int32_t* lens, int B, int heads,
-                                         int head_dim, int capacity, float scale, float* out,
-                                         void* ws, size_t ws_bytes, int32_t* dev_err,
-                                         asr_stream_t stream) {
+// The append + self step, with or without a beam reorder (idx != nullptr:
+// kv is the source cache, cache_w the destination, lens the source lengths).
+static int self_append_step(const float* q, int64_t q_stride, const float* k_new,
+                            const float* v_new, int64_t kv_stride, const uint16_t* src,
+                            uint16_t* cache, int64_t seq_stride, const int32_t* idx,
+                            const int32_t* lens, int32_t* lens_out, int B, int heads,
+                            int head_dim, int capacity, float scale, float* out, void* ws,
+                            size_t ws_bytes, int32_t* dev_err, cudaStream_t stream) {
   if (B < 0 || B > ASR_MAX_BATCH || heads < 1 || capacity < 1) return ASR_ERR_INVALID_ARG;
   if ((head_dim != 64 && head_dim != 128) || heads > ASR_MAX_KV_HEADS) return ASR_ERR_UNSUPPORTED;
   if (B == 0) return ASR_OK;
-  if (!q || !k_new || !v_new || !cache || !lens || !out) return ASR_ERR_INVALID_ARG;
+  if (!q || !k_new || !v_new || !src || !cache || !lens || !out) return ASR_ERR_INVALID_ARG;
   const int64_t row = 2LL * heads * head_dim;
   if (q_stride < (int64_t)heads * head_dim || kv_stride < (int64_t)heads * head_dim ||
       seq_stride < (int64_t)capacity * row)
     return ASR_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cache) ||
-      !aligned16(out) || q_stride % 4 != 0 || kv_stride % 4 != 0 || seq_stride % 8 != 0)
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(src) ||
+      !aligned16(cache) || !aligned16(out) || q_stride % 4 != 0 || kv_stride % 4 != 0 ||
+      seq_stride % 8 != 0)
     return ASR_ERR_MISALIGNED;
   if (!rows_fit_int(B, capacity, heads)) return ASR_ERR_UNSUPPORTED;
+  if (idx) {
+    // the destination rows must not overlap the source rows, and lens_out
+    // neither the lengths nor the indices (other CTAs still read them)
+    const uintptr_t bytes = ((uintptr_t)(B - 1) * (uintptr_t)seq_stride +
+                             (uintptr_t)capacity * (uintptr_t)row) * 2;
+    const uintptr_t s0 = (uintptr_t)src, d0 = (uintptr_t)cache;
+    if (s0 < d0 + bytes && d0 < s0 + bytes) return ASR_ERR_ALIAS;
+    const uintptr_t ib = (uintptr_t)B * 4, o0 = (uintptr_t)lens_out;
+    const uintptr_t l0 = (uintptr_t)lens, x0 = (uintptr_t)idx;
+    if ((o0 < l0 + ib && l0 < o0 + ib) || (o0 < x0 + ib && x0 < o0 + ib)) return ASR_ERR_ALIAS;
+  }
   DecodeArgs a = {};
   a.q = q;
   a.q_stride = q_stride;
-  a.kv = cache;
+  a.kv = src;
   a.cache_w = cache;
   a.src_stride = seq_stride;
   a.row_elems = (int)row;
   a.n_src = B;
   a.B = B;
   a.lens = lens;
+  a.idx = idx;
+  a.lens_out = lens_out;
   a.capacity = capacity;
   a.Hq = heads;
   a.Hkv = heads;
@@ -1398,7 +1468,29 @@ extern "C" int asr_self_attn_append_step(const float* q, int64_t q_stride, const
   a.kv_stride = kv_stride;
   a.k_new = k_new;
   a.v_new = v_new;
-  return launch_decode(a, head_dim, 1, ws, ws_bytes, (cudaStream_t)stream);
+  return launch_decode(a, head_dim, 1, ws, ws_bytes, stream);
+}
+
+extern "C" int asr_self_attn_append_step(const float* q, int64_t q_stride, const float* k_new,
+                                         const float* v_new, int64_t kv_stride, uint16_t* cache,
+                                         int64_t seq_stride, const int32_t* lens, int B, int heads,
+                                         int head_dim, int capacity, float scale, float* out,
+                                         void* ws, size_t ws_bytes, int32_t* dev_err,
+                                         asr_stream_t stream) {
+  return self_append_step(q, q_stride, k_new, v_new, kv_stride, cache, cache, seq_stride, nullptr,
+                          lens, nullptr, B, heads, head_dim, capacity, scale, out, ws, ws_bytes,
+                          dev_err, (cudaStream_t)stream);
+}
+
+extern "C" int asr_self_attn_reorder_append_step(
+    const float* q, int64_t q_stride, const float* k_new, const float* v_new, int64_t kv_stride,
+    const uint16_t* cache_src, uint16_t* cache_dst, int64_t seq_stride, const int32_t* idx,
+    const int32_t* lens_src, int32_t* lens_dst, int B, int heads, int head_dim, int capacity,
+    float scale, float* out, void* ws, size_t ws_bytes, int32_t* dev_err, asr_stream_t stream) {
+  if (B > 0 && (!idx || !lens_dst)) return ASR_ERR_INVALID_ARG;
+  return self_append_step(q, q_stride, k_new, v_new, kv_stride, cache_src, cache_dst, seq_stride,
+                          idx, lens_src, lens_dst, B, heads, head_dim, capacity, scale, out, ws,
+                          ws_bytes, dev_err, (cudaStream_t)stream);
 }
 
 extern "C" int asr_cross_attn_step(const float* q, int64_t q_stride, const uint16_t* cross,

@@ -68,6 +68,13 @@ struct DecodeArgs {
   int64_t kv_stride;  // floats between sequences of k_new / v_new
   const float* k_new;
   const float* v_new;
+  // self step with a beam reorder (take along the batch axis, fused): source
+  // g streams the history rows of sequence idx[g] of kv and stores them to
+  // sequence g of cache_w (same strides) as they pass through shared memory;
+  // lens holds the source lengths and lens_out[g] = lens[idx[g]] (0 when
+  // sequence g is skipped).  idx == nullptr: no reorder.
+  const int32_t* idx;
+  int32_t* lens_out;
   // GQA only
   const float* wq;
   const float* wk;
@@ -78,12 +85,13 @@ struct DecodeArgs {
 
 // Shared-memory layout of one CTA (bytes from the dynamic smem base).
 //   bars: full/empty mbarriers of the stage ring; ctl: control words; off,
-//     mstart: the consumers' source offsets and first sequences; poff: the
-//     producer's offsets; slen: the length entry of each source (self,
+//     mstart: the consumers' source offsets and first sequences; poff, psrc:
+//     the producer's offsets and the cache sequence each source reads (beam
+//     reorder); slen: the length entry of each source (self,
 //     GQA); rope, wts: GQA tables; merge: row-slot merge buffer; stage: the
 //     K/V ring.
 struct DecodeSmem {
-  int bars, ctl, off, mstart, poff, slen, rope, wts, merge, stage, total;
+  int bars, ctl, off, mstart, poff, psrc, slen, rope, wts, merge, stage, total;
 };
 
 __host__ __device__ inline int dsm_align(int x, int a) { return (x + a - 1) / a * a; }
@@ -97,7 +105,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.off = dsm_align(s.ctl + 16 * 4, 16);
   s.mstart = dsm_align(s.off + (n_src + 1) * 4, 16);
   s.poff = dsm_align(s.mstart + (n_src + 1) * 4, 16);
-  s.slen = dsm_align(s.poff + (n_src + 1) * 4, 16);
+  s.psrc = dsm_align(s.poff + (n_src + 1) * 4, 16);
+  s.slen = dsm_align(s.psrc + (n_src + 1) * 4, 16);
   s.rope = dsm_align(s.slen + (n_src + 1) * 4, 16);
   s.wts = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
   s.merge = dsm_align(s.wts + 2 * HD * 4, 16);

@@ -33,6 +33,9 @@ SIGNATURES = {
                                   _p, _p]),
     "asr_self_attn_append_step": (_int, [_p, _i64, _p, _p, _i64, _p, _i64, _p, _int, _int, _int,
                                          _int, _f, _p, _p, _sz, _p, _p]),
+    "asr_self_attn_reorder_append_step": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _i64, _p, _p,
+                                                 _p, _int, _int, _int, _int, _f, _p, _p, _sz, _p,
+                                                 _p]),
     "asr_cross_attn_step": (_int, [_p, _i64, _p, _i64, _p, _int, _int, _int, _int, _int, _int, _f,
                                    _p, _p, _sz, _p, _p]),
     "asr_gqa_step": (_int, [_p, _i64, _p, _p, _i64, _p, _p, _f, _f, _p, _p, _i64, _int, _int, _int,
@@ -196,6 +199,32 @@ def asr_self_attn_append_step(q, k_new, v_new, cache, lens, heads, head_dim, cap
                                           _ptr(lens), B, heads, head_dim, capacity, float(scale),
                                           _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
     _check("asr_self_attn_append_step", st)
+
+
+def asr_self_attn_reorder_append_step(q, k_new, v_new, cache_src, cache_dst, idx, lens_src,
+                                      lens_dst, heads, head_dim, capacity, scale, out, ws,
+                                      dev_err=None, stream=None):
+    """Beam reorder + append + self-attention of one layer.  cache_src,
+    cache_dst: f16 caches with one sequence stride; idx, lens_src, lens_dst:
+    int32 [B]; other arguments as asr_self_attn_append_step."""
+    import torch
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (out, "out")):
+        _need(t, torch.float32, n)
+    _need(cache_src, torch.float16, "cache_src")
+    _need(cache_dst, torch.float16, "cache_dst")
+    for t, n in ((idx, "idx"), (lens_src, "lens_src"), (lens_dst, "lens_dst")):
+        _need(t, torch.int32, n)
+    if k_new.stride(0) != v_new.stride(0):
+        raise ValueError("k_new and v_new must share the row stride")
+    if cache_src.stride(0) != cache_dst.stride(0):
+        raise ValueError("cache_src and cache_dst must share the sequence stride")
+    B = idx.shape[0]
+    wp, wn = _ws_ptr(ws)
+    st = load().asr_self_attn_reorder_append_step(
+        _ptr(q), q.stride(0), _ptr(k_new), _ptr(v_new), k_new.stride(0), _ptr(cache_src),
+        _ptr(cache_dst), cache_src.stride(0), _ptr(idx), _ptr(lens_src), _ptr(lens_dst), B, heads,
+        head_dim, capacity, float(scale), _ptr(out), wp, wn, _ptr(dev_err), _stream(stream))
+    _check("asr_self_attn_reorder_append_step", st)
 
 
 def asr_self_attn_step_noalloc(q, cache, lens, heads, head_dim, capacity, scale, out,
