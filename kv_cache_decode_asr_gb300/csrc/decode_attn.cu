@@ -379,66 +379,86 @@ __device__ __forceinline__ void rope_table(float* rope, const float* turns, int 
   }
 }
 
-// Merge the (max, sum, output) states of the R row slots into row slot 0
-// through shared memory, as a tree: at each level the upper half of the
-// remaining slots hands its state to the lower half.  Called by all consumer
-// threads; merge holds R/2 entries of Hv x NQ states.
+// Row-slot states to shared memory: entry (slot r, virtual head hv, query
+// qi) at merge + ((r * Hv + hv) * NQ + qi) * (HD + 4) holds the unnormalised
+// output in dimension order, then (max, sum).  Query slots past nq are not
+// written (combine_slots skips them).
 template <int HD, int NQ, int DPL>
-__device__ __forceinline__ void merge_row_slots(float (&M)[NQ], float (&Ls)[NQ],
-                                                float2 (&O)[NQ][DPL / 2], float* merge, int r,
-                                                int R, int hv, int Hv, int li, int sw, int nq,
-                                                int n_cons) {
+__device__ __forceinline__ void slot_states_out(const float (&M)[NQ], const float (&Ls)[NQ],
+                                                const float2 (&O)[NQ][DPL / 2], float* merge,
+                                                int r, int hv, int Hv, int li, int sw, int nq) {
   using LL = LaneLayout<HD, DPL>;
-  for (int n = R; n > 1;) {
-    const int half = (n + 1) >> 1;
-    named_bar(1, n_cons);  // the previous readers of the buffer are done
-    if (r >= half && r < n) {
 #pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          float* mb = merge + (((r - half) * Hv + hv) * NQ + qi) * (HD + 4);
+  for (int qi = 0; qi < NQ; ++qi) {
+    if (qi < nq) {
+      float* mb = merge + ((r * Hv + hv) * NQ + qi) * (HD + 4);
 #pragma unroll
-          for (int j = 0; j < LL::NCH; ++j) {
-            float4* dst = reinterpret_cast<float4*>(mb + LL::chunk_off(li, j, sw));
-            dst[0] = make_float4(O[qi][4 * j].x, O[qi][4 * j].y, O[qi][4 * j + 1].x,
-                                 O[qi][4 * j + 1].y);
-            dst[1] = make_float4(O[qi][4 * j + 2].x, O[qi][4 * j + 2].y, O[qi][4 * j + 3].x,
-                                 O[qi][4 * j + 3].y);
-          }
-          if (li == 0) {
-            mb[HD] = M[qi];
-            mb[HD + 1] = Ls[qi];
-          }
-        }
+      for (int j = 0; j < LL::NCH; ++j) {
+        float4* dst = reinterpret_cast<float4*>(mb + LL::chunk_off(li, j, sw));
+        dst[0] = make_float4(O[qi][4 * j].x, O[qi][4 * j].y, O[qi][4 * j + 1].x, O[qi][4 * j + 1].y);
+        dst[1] = make_float4(O[qi][4 * j + 2].x, O[qi][4 * j + 2].y, O[qi][4 * j + 3].x,
+                             O[qi][4 * j + 3].y);
+      }
+      if (li == 0) *reinterpret_cast<float2*>(mb + HD) = make_float2(M[qi], Ls[qi]);
+    }
+  }
+}
+
+// Combine the R row-slot states of a CTA's piece of one unit (written by
+// slot_states_out) in one pass: each consumer thread takes a 4-dimension
+// slice of one query, rescales every slot to the common maximum and sums.
+// slot < 0: the unit lies entirely in this CTA and the slice is written
+// normalised to the output; else it is written, unnormalised with its (max,
+// sum), as partial `slot` of the unit.  members: the source's sequences
+// (cross: beams of the group), first at mbase; hg: the unit's head group.
+template <int HD, int NQ>
+__device__ __forceinline__ void combine_slots(const DecodeArgs& a, const float* merge, int R,
+                                              int Hv, int members, int mbase, int hg,
+                                              int64_t slot, int tid, int n_cons) {
+  constexpr int U4 = HD / 4;
+  const int hs = a.hs, rep = a.rep;
+  const int hqu = hs * rep;  // query heads of a unit
+  const int qw = a.Hq * HD;
+  const int n = Hv * NQ * U4;
+  for (int x = tid; x < n; x += n_cons) {
+    const int d0 = (x % U4) * 4;
+    const int e = x / U4;  // entry hv * NQ + qi
+    const int qi = e % NQ, hv = e / NQ;
+    const int ms = Hv == hs ? 0 : hv / hs, hl = hv - ms * hs;  // no query split: no division
+    const int qg = ms * NQ + qi;  // query of the unit's source: member * rep + head offset
+    if (qg >= members * rep) continue;  // a query slot past nq: never written
+    const float* base = merge + e * (HD + 4);
+    const int stride = Hv * NQ * (HD + 4);  // from one row slot's entry to the next
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int r = 0; r < R; ++r) M = fmaxf(M, base[r * stride + HD]);
+    float L = 0.f;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int r = 0; r < R; ++r) {
+        const float* mb = base + r * stride;
+        const float2 ml = *reinterpret_cast<const float2*>(mb + HD);
+        const float4 v = *reinterpret_cast<const float4*>(mb + d0);
+        const float c = ex2(ml.x - M);  // 0 for a slot that saw no rows
+        const float2 c2 = make_float2(c, c);
+        L = fmaf(ml.y, c, L);
+        acc0 = ffma2(c2, make_float2(v.x, v.y), acc0);
+        acc1 = ffma2(c2, make_float2(v.z, v.w), acc1);
       }
     }
-    named_bar(1, n_cons);
-    if (r < n - half) {
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          const float* mb = merge + ((r * Hv + hv) * NQ + qi) * (HD + 4);
-          const float m2 = mb[HD], l2 = mb[HD + 1];
-          const float mn = fmaxf(M[qi], m2);
-          if (mn != -INFINITY) {
-            const float ca = ex2(M[qi] - mn), cb = ex2(m2 - mn);
-            Ls[qi] = Ls[qi] * ca + l2 * cb;
-#pragma unroll
-            for (int j = 0; j < LL::NCH; ++j) {
-              const float4* src = reinterpret_cast<const float4*>(mb + LL::chunk_off(li, j, sw));
-              const float4 u0 = src[0], u1 = src[1];
-              const float2 cb2 = make_float2(cb, cb), ca2 = make_float2(ca, ca);
-              O[qi][4 * j] = ffma2(cb2, make_float2(u0.x, u0.y), fmul2(O[qi][4 * j], ca2));
-              O[qi][4 * j + 1] = ffma2(cb2, make_float2(u0.z, u0.w), fmul2(O[qi][4 * j + 1], ca2));
-              O[qi][4 * j + 2] = ffma2(cb2, make_float2(u1.x, u1.y), fmul2(O[qi][4 * j + 2], ca2));
-              O[qi][4 * j + 3] = ffma2(cb2, make_float2(u1.z, u1.w), fmul2(O[qi][4 * j + 3], ca2));
-            }
-            M[qi] = mn;
-          }
-        }
-      }
+    const int mem = rep == 1 ? qg : qg / rep;
+    const int xq = hl * rep + (qg - mem * rep);  // query head within the unit
+    if (slot < 0) {
+      const float inv = 1.0f / L;
+      *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + xq) * HD + d0) =
+          make_float4(acc0.x * inv, acc0.y * inv, acc1.x * inv, acc1.y * inv);
+    } else {
+      const int64_t pidx = (slot * a.max_members + mem) * hqu + xq;
+      *reinterpret_cast<float4*>(a.part_o + pidx * HD + d0) =
+          make_float4(acc0.x, acc0.y, acc1.x, acc1.y);
+      if (d0 == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(M, L);
     }
-    n = half;
   }
 }
 
@@ -888,21 +908,6 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     if (fold) append_fold(g, kx, vx);
   };
 
-  // Write the normalised output of query qi.  No shuffles: callable per group.
-  auto finalize = [&](int qi, float Ls, float2* O) {
-    const int b = mbase + (qb + qi) / rep;
-    const int hq = h * rep + (qb + qi) % rep;
-    const float inv = 1.0f / Ls;
-    float* dst = a.out + (int64_t)b * qw + hq * HD;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      float4* p = reinterpret_cast<float4*>(dst + LL::chunk_off(li, j, sw));
-      p[0] = make_float4(O[4 * j].x * inv, O[4 * j].y * inv, O[4 * j + 1].x * inv, O[4 * j + 1].y * inv);
-      p[1] = make_float4(O[4 * j + 2].x * inv, O[4 * j + 2].y * inv, O[4 * j + 3].x * inv,
-                         O[4 * j + 3].y * inv);
-    }
-  };
-
   // The merge of unit u's partials by the last CTA to finish it.
   auto merge_unit = [&](int u) {
     const UnitSpan sp = unit_span(off, HS, a.seg_rows, u);
@@ -912,41 +917,23 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
                      mst[g], tid, n_cons);
   };
 
+  // The end of this CTA's piece of unit u: the row slots' states meet in
+  // shared memory and are combined slice by slice (one barrier pair, no
+  // tree), straight into the output when the CTA holds the whole unit, else
+  // into this piece's partial, which the last CTA to finish the unit merges.
   auto seg_end = [&](int u) {
-    merge_row_slots<HD, NQ, DPL>(m, l, o, merge, r, R, hv, Hv, li, sw, nq, n_cons);
+    named_bar(1, n_cons);  // the previous readers of the buffer are done
+    slot_states_out<HD, NQ, DPL>(m, l, o, merge, r, hv, Hv, li, sw, nq);
+    named_bar(1, n_cons);
     // pieces of this unit over the grid
     const UnitSpan sp = unit_span(off, HS, a.seg_rows, u);
     const int first = sp.gl > 0 ? sp.go / share : 0;
     const int lastp = sp.gl > 0 ? (sp.go + sp.gl - 1) / share : 0;
     const int parts = sp.gl > 0 ? lastp - first + 1 : 0;
-    if (parts <= 1) {
-      if (r == 0) {
-#pragma unroll
-        for (int qi = 0; qi < NQ; ++qi)
-          if (qi < nq) finalize(qi, l[qi], o[qi]);
-      }
-      return;
-    }
-    const int hqu = hs * rep;
-    if (r == 0) {
-      const int64_t slot = (int64_t)blockIdx.x + u;
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        if (qi < nq) {
-          const int64_t pidx =
-              (slot * a.max_members + (qb + qi) / rep) * hqu + hl * rep + (qb + qi) % rep;
-          float* po = a.part_o + pidx * HD;
-#pragma unroll
-          for (int j = 0; j < NCH; ++j) {
-            float4* p = reinterpret_cast<float4*>(po + LL::chunk_off(li, j, sw));
-            p[0] = make_float4(o[qi][4 * j].x, o[qi][4 * j].y, o[qi][4 * j + 1].x, o[qi][4 * j + 1].y);
-            p[1] = make_float4(o[qi][4 * j + 2].x, o[qi][4 * j + 2].y, o[qi][4 * j + 3].x,
-                               o[qi][4 * j + 3].y);
-          }
-          if (li == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(m[qi], l[qi]);
-        }
-      }
-    }
+    const int g = u / HS;
+    combine_slots<HD, NQ>(a, merge, R, Hv, min(mst[g + 1] - mst[g], a.max_members), mst[g],
+                          u - g * HS, parts > 1 ? (int64_t)blockIdx.x + u : -1, tid, n_cons);
+    if (parts <= 1) return;
     // ticket: the barrier orders the CTA's partial writes before thread 0's
     // release; the acquire side lets the last CTA read everyone's partials
     named_bar(1, n_cons);
@@ -1163,7 +1150,8 @@ struct DecodePlan {
 };
 
 // Row slots R: the consumer count R * Hv * G must be a multiple of 32 and
-// fit the variant's thread cap (at most 320 consumers); among those, the
+// fit the variant's thread cap (at most 320 consumers), and two stages plus
+// the slots' merge entries must fit in shared memory; among those, the
 // largest R whose tile fits tile_kb (else the smallest valid R).  Stages: as
 // many as fit smem_kb, 2..8.  One CTA takes at least min_kb of rows, so a
 // unit splits into a bounded number of partial results.
@@ -1180,6 +1168,9 @@ static bool plan_layout(const DecodeArgs& a, int HD, int vi, int MS, int hs, Dec
   int best = 0, smallest = 0;
   for (int R = 1; R * per_slot <= budget; ++R) {
     if ((R * per_slot) % 32 != 0) continue;
+    // two stages and the R slots' merge entries must fit a CTA's shared memory
+    const int se = dsm_align(R * v.RS * chunk_elems, 64);
+    if (decode_smem_layout(2, n_src, R, MS * hs, v.NQ, HD, se).total > 227 * 1024) break;
     if (!smallest) smallest = R;
     if (R * v.RS * chunk_bytes <= tune.tile_kb * 1024) best = R;
   }

@@ -88,8 +88,8 @@ struct DecodeArgs {
 //     mstart: the consumers' source offsets and first sequences; poff, psrc:
 //     the producer's offsets and the cache sequence each source reads (beam
 //     reorder); slen: the length entry of each source (self,
-//     GQA); rope, wts: GQA tables; merge: row-slot merge buffer; stage: the
-//     K/V ring.
+//     GQA); rope, wts: GQA tables; merge: the row slots' states (R entries
+//     of Hv x NQ); stage: the K/V ring.
 struct DecodeSmem {
   int bars, ctl, off, mstart, poff, psrc, slen, rope, wts, merge, stage, total;
 };
@@ -110,7 +110,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int stages, int n_src, 
   s.rope = dsm_align(s.slen + (n_src + 1) * 4, 16);
   s.wts = dsm_align(s.rope + (HD > 64 ? HD : 64) * 4, 16);
   s.merge = dsm_align(s.wts + 2 * HD * 4, 16);
-  s.stage = dsm_align(s.merge + (R / 2) * Hv * NQ * (HD + 4) * 4, 128);
+  s.stage = dsm_align(s.merge + R * Hv * NQ * (HD + 4) * 4, 128);
   s.total = s.stage + stages * stage_elems * 2;
   return s;
 }
