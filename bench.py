@@ -295,10 +295,16 @@ class WhisperStep:
 
     def dominant_bytes_per_launch(self):
         b = self.bytes_per_layer()
-        return b["self"] + b["append"] if self.profile_kernel == "self" else b["cross"]
+        if self.profile_kernel != "self":
+            return b["cross"]
+        # the fused reorder also writes the history rows it streams (the
+        # standalone reorder's read of them is the self launch's own read)
+        return b["self"] + b["append"] + (b["rearrange"] // 2 if self.fused_reorder() else 0)
 
     def traffic_key(self):
-        return "self+append" if self.profile_kernel == "self" else "cross"
+        if self.profile_kernel != "self":
+            return "cross"
+        return "self+append+reorder" if self.fused_reorder() else "self+append"
 
     def dominant_call(self, l, stream=None):
         if self.profile_kernel == "self" and self.fused_reorder():
