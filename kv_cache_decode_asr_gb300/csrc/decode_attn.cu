@@ -271,18 +271,16 @@ __device__ __forceinline__ float group_sum(float v) {
 // Lane layout of one head vector: a group of G = HD/DPL lanes covers the
 // head; lane li holds NCH = DPL/8 chunks of 8 dims.  Register slot j holds
 // chunk li + (j ^ sw)*G, i.e. dims (li + (j^sw)*G)*8 .. +8, as 4 float pairs
-// (pair t: slot t/4, dims 2*(t%4), 2*(t%4)+1 of the chunk).  With two or
-// more chunks per lane the NeoX RoPE partner (i, i + HD/2) of every dim is
-// in the same lane, in slot j ^ NCH/2.  When a quarter-warp holds several
-// groups (G < 8), sw = (group index) mod (8/G) rotates their slots, so the
-// quarter-warp's 8 lanes cover all 32 shared-memory banks per load.
+// (pair t: slot t/4, dims 2*(t%4), 2*(t%4)+1 of the chunk).  With two chunks
+// per lane the NeoX RoPE partner (i, i + HD/2) of every dim is in the same
+// lane.  sw (0/1) swaps the slots of odd groups when a quarter-warp holds two
+// groups (G = 4), so its 8 lanes cover all 32 shared-memory banks per load.
 template <int HD, int DPL>
 struct LaneLayout {
   static constexpr int NCH = DPL / 8;
   static constexpr int G = HD / DPL;
   static constexpr int NP = DPL / 2;
-  static constexpr int kSwapMask = G < 8 ? 8 / G - 1 : 0;
-  static_assert(NCH * G * 8 == HD && (G >= 8 || NCH >= 8 / G), "lane layout");
+  static constexpr bool kSwap = NCH == 2 && G < 8;
   static __device__ __forceinline__ int chunk_off(int li, int j, int sw) {
     return (li + (j ^ sw) * G) * 8;
   }
@@ -327,28 +325,20 @@ __device__ __forceinline__ void norm_rope(float2* x, const float* __restrict__ w
     const int d0 = LL::dim(li, t, sw);
     xn[t] = make_float2(w[d0] * (x[t].x * rinv), w[d0 + 1] * (x[t].y * rinv));
   }
-  if constexpr (LL::NCH >= 2) {
-    // slot j holds chunk c = li + (j ^ sw) * G; its partner chunk c +- HD/16
-    // (dims i +- HD/2) is in slot j ^ NCH/2 of the same lane
-    float2 y[NP];
+  if constexpr (LL::NCH == 2) {
+    // chunk li holds dims i < HD/2 (slot sw), chunk li + G their partners
+    // i + HD/2 (slot 1 - sw)
 #pragma unroll
-    for (int j = 0; j < LL::NCH; ++j) {
-      const int c = li + (j ^ sw) * G;
-      const bool lower = c * 8 < HD / 2;
-      const int ib = (lower ? c : c - LL::NCH * G / 2) * 8;
-      const int jp = j ^ (LL::NCH / 2);
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int i0 = ib + 2 * p;
-        const float c0 = rope[i0], s0 = rope[HD / 2 + i0];
-        const float c1 = rope[i0 + 1], s1 = rope[HD / 2 + i0 + 1];
-        const float2 a = xn[4 * j + p], b = xn[4 * jp + p];
-        y[4 * j + p] = lower ? make_float2(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1)
-                             : make_float2(a.x * c0 + b.x * s0, a.y * c1 + b.y * s1);
-      }
+    for (int p = 0; p < 4; ++p) {
+      const int i0 = li * 8 + 2 * p;
+      const float c0 = rope[i0], s0 = rope[HD / 2 + i0];
+      const float c1 = rope[i0 + 1], s1 = rope[HD / 2 + i0 + 1];
+      const float2 lo = sw ? xn[4 + p] : xn[p], hi = sw ? xn[p] : xn[4 + p];
+      const float2 ylo = make_float2(lo.x * c0 - hi.x * s0, lo.y * c1 - hi.y * s1);
+      const float2 yhi = make_float2(hi.x * c0 + lo.x * s0, hi.y * c1 + lo.y * s1);
+      x[p] = sw ? yhi : ylo;
+      x[4 + p] = sw ? ylo : yhi;
     }
-#pragma unroll
-    for (int t = 0; t < NP; ++t) x[t] = y[t];
   } else {
     // one chunk per lane: the partner chunk lives in lane li ^ (G/2)
     const bool lower = li < G / 2;
@@ -814,7 +804,7 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   const int qb = ms * NQ;  // this group's first query of a source
   const int rep = a.rep;
   const int R = a.R;
-  const int sw = grp & LL::kSwapMask;
+  const int sw = LL::kSwap ? (grp & 1) : 0;
   const int hoff = hl * HD;  // element offset of this group's head in a chunk's K (or V) half
   const int voff = hs * HD;  // element offset of the V half of a chunk
 
