@@ -405,24 +405,25 @@ __device__ __forceinline__ void slot_states_out(const float (&M)[NQ], const floa
 }
 
 // Combine the R row-slot states of a CTA's piece of one unit (written by
-// slot_states_out) in one pass: each consumer thread takes a 4-dimension
-// slice of one query, rescales every slot to the common maximum and sums.
-// slot < 0: the unit lies entirely in this CTA and the slice is written
-// normalised to the output; else it is written, unnormalised with its (max,
-// sum), as partial `slot` of the unit.  members: the source's sequences
-// (cross: beams of the group), first at mbase; hg: the unit's head group.
-template <int HD, int NQ>
+// slot_states_out) in one pass: each consumer thread takes a slice of 4 * V4
+// dimensions of one query, rescales every slot to the common maximum and
+// sums.  slot < 0: the unit lies entirely in this CTA and the slice is
+// written normalised to the output; else it is written, unnormalised with
+// its (max, sum), as partial `slot` of the unit.  members: the source's
+// sequences (cross: beams of the group), first at mbase; hg: the unit's
+// head group.  V4 = 2 when slices of 4 would outnumber the threads.
+template <int HD, int NQ, int V4>
 __device__ __forceinline__ void combine_slots(const DecodeArgs& a, const float* merge, int R,
                                               int Hv, int members, int mbase, int hg,
                                               int64_t slot, int tid, int n_cons) {
-  constexpr int U4 = HD / 4;
+  constexpr int US = HD / (4 * V4);
   const int hs = a.hs, rep = a.rep;
   const int hqu = hs * rep;  // query heads of a unit
   const int qw = a.Hq * HD;
-  const int n = Hv * NQ * U4;
+  const int n = Hv * NQ * US;
   for (int x = tid; x < n; x += n_cons) {
-    const int d0 = (x % U4) * 4;
-    const int e = x / U4;  // entry hv * NQ + qi
+    const int d0 = (x % US) * 4 * V4;
+    const int e = x / US;  // entry hv * NQ + qi
     const int qi = e % NQ, hv = e / NQ;
     const int ms = Hv == hs ? 0 : hv / hs, hl = hv - ms * hs;  // no query split: no division
     const int qg = ms * NQ + qi;  // query of the unit's source: member * rep + head offset
@@ -433,30 +434,41 @@ __device__ __forceinline__ void combine_slots(const DecodeArgs& a, const float* 
 #pragma unroll 4
     for (int r = 0; r < R; ++r) M = fmaxf(M, base[r * stride + HD]);
     float L = 0.f;
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    float2 acc[2 * V4];
+#pragma unroll
+    for (int w = 0; w < 2 * V4; ++w) acc[w] = make_float2(0.f, 0.f);
     if (M != -INFINITY) {
 #pragma unroll 4
       for (int r = 0; r < R; ++r) {
         const float* mb = base + r * stride;
         const float2 ml = *reinterpret_cast<const float2*>(mb + HD);
-        const float4 v = *reinterpret_cast<const float4*>(mb + d0);
         const float c = ex2(ml.x - M);  // 0 for a slot that saw no rows
         const float2 c2 = make_float2(c, c);
         L = fmaf(ml.y, c, L);
-        acc0 = ffma2(c2, make_float2(v.x, v.y), acc0);
-        acc1 = ffma2(c2, make_float2(v.z, v.w), acc1);
+#pragma unroll
+        for (int w = 0; w < V4; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(mb + d0 + 4 * w);
+          acc[2 * w] = ffma2(c2, make_float2(v.x, v.y), acc[2 * w]);
+          acc[2 * w + 1] = ffma2(c2, make_float2(v.z, v.w), acc[2 * w + 1]);
+        }
       }
     }
     const int mem = rep == 1 ? qg : qg / rep;
     const int xq = hl * rep + (qg - mem * rep);  // query head within the unit
     if (slot < 0) {
       const float inv = 1.0f / L;
-      *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + xq) * HD + d0) =
-          make_float4(acc0.x * inv, acc0.y * inv, acc1.x * inv, acc1.y * inv);
+      float* dst = a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + xq) * HD + d0;
+#pragma unroll
+      for (int w = 0; w < V4; ++w)
+        *reinterpret_cast<float4*>(dst + 4 * w) =
+            make_float4(acc[2 * w].x * inv, acc[2 * w].y * inv, acc[2 * w + 1].x * inv,
+                        acc[2 * w + 1].y * inv);
     } else {
       const int64_t pidx = (slot * a.max_members + mem) * hqu + xq;
-      *reinterpret_cast<float4*>(a.part_o + pidx * HD + d0) =
-          make_float4(acc0.x, acc0.y, acc1.x, acc1.y);
+#pragma unroll
+      for (int w = 0; w < V4; ++w)
+        *reinterpret_cast<float4*>(a.part_o + pidx * HD + d0 + 4 * w) =
+            make_float4(acc[2 * w].x, acc[2 * w].y, acc[2 * w + 1].x, acc[2 * w + 1].y);
       if (d0 == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(M, L);
     }
   }
@@ -464,36 +476,42 @@ __device__ __forceinline__ void combine_slots(const DecodeArgs& a, const float* 
 
 // The last CTA to finish unit u (source g, head group hg) merges the
 // partials of every piece of it (its own among them): each consumer thread
-// takes 4 consecutive output values of one query and combines that slice
-// over pieces first..lastp, 8 pieces per L2 round trip, then writes it
-// normalised.  The piece of CTA c sits in partial slot c + u.
-template <int HD>
+// takes 4 * V4 consecutive output values of one query and combines that
+// slice over pieces first..lastp, 8 pieces per L2 round trip, then writes
+// it normalised.  The piece of CTA c sits in partial slot c + u.  V4 = 2
+// when slices of 4 would outnumber the threads (beam groups: many queries
+// per unit), so that each thread makes one pass.
+template <int HD, int V4>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int u, int hg, int first,
                                              int lastp, int members, int mbase, int tid,
                                              int n_cons) {
-  constexpr int U4 = HD / 4;
+  constexpr int US = HD / (4 * V4);  // slices per head vector
   constexpr int KB = 8;
   const int hqu = a.hs * a.rep;  // query heads of a unit
   const int qw = a.Hq * HD;
-  const int nunits = members * hqu * U4;
+  const int nunits = members * hqu * US;
   for (int x = tid; x < nunits; x += n_cons) {
-    const int d0 = (x % U4) * 4;
-    const int mj = x / U4;  // member * hqu + query head within the unit
+    const int d0 = (x % US) * 4 * V4;
+    const int mj = x / US;  // member * hqu + query head within the unit
     const int mem = mj / hqu, j = mj - mem * hqu;
     float M = -INFINITY, Lsum = 0.f;
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    float2 acc[2 * V4];
+#pragma unroll
+    for (int w = 0; w < 2 * V4; ++w) acc[w] = make_float2(0.f, 0.f);
     for (int kb = first; kb <= lastp; kb += KB) {
       float2 ml[KB];
-      float4 xv[KB];
+      float4 xv[KB][V4];
 #pragma unroll
       for (int i = 0; i < KB; ++i) {
         if (kb + i <= lastp) {
           const int64_t pidx = ((int64_t)(kb + i + u) * a.max_members + mem) * hqu + j;
           ml[i] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + pidx * 2));
-          xv[i] = ld_cg_f4(a.part_o + pidx * HD + d0);
+#pragma unroll
+          for (int w = 0; w < V4; ++w) xv[i][w] = ld_cg_f4(a.part_o + pidx * HD + d0 + 4 * w);
         } else {
           ml[i] = make_float2(-INFINITY, 0.f);
-          xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < V4; ++w) xv[i][w] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       float mb = M;
@@ -503,21 +521,28 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int u, int hg,
       const float ca = ex2(M - mb);
       const float2 ca2 = make_float2(ca, ca);
       Lsum *= ca;
-      acc0 = fmul2(acc0, ca2);
-      acc1 = fmul2(acc1, ca2);
+#pragma unroll
+      for (int w = 0; w < 2 * V4; ++w) acc[w] = fmul2(acc[w], ca2);
 #pragma unroll
       for (int i = 0; i < KB; ++i) {
         const float c = ex2(ml[i].x - mb);  // 0 for an absent piece
         const float2 c2 = make_float2(c, c);
         Lsum = fmaf(ml[i].y, c, Lsum);
-        acc0 = ffma2(c2, make_float2(xv[i].x, xv[i].y), acc0);
-        acc1 = ffma2(c2, make_float2(xv[i].z, xv[i].w), acc1);
+#pragma unroll
+        for (int w = 0; w < V4; ++w) {
+          acc[2 * w] = ffma2(c2, make_float2(xv[i][w].x, xv[i][w].y), acc[2 * w]);
+          acc[2 * w + 1] = ffma2(c2, make_float2(xv[i][w].z, xv[i][w].w), acc[2 * w + 1]);
+        }
       }
       M = mb;
     }
     const float inv = 1.0f / Lsum;
-    *reinterpret_cast<float4*>(a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + j) * HD + d0) =
-        make_float4(acc0.x * inv, acc0.y * inv, acc1.x * inv, acc1.y * inv);
+    float* dst = a.out + (int64_t)(mbase + mem) * qw + (hg * hqu + j) * HD + d0;
+#pragma unroll
+    for (int w = 0; w < V4; ++w)
+      *reinterpret_cast<float4*>(dst + 4 * w) =
+          make_float4(acc[2 * w].x * inv, acc[2 * w].y * inv, acc[2 * w + 1].x * inv,
+                      acc[2 * w + 1].y * inv);
   }
 }
 
@@ -913,8 +938,14 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     const UnitSpan sp = unit_span(off, HS, a.seg_rows, u);
     const int first = sp.go / share, lastp = (sp.go + sp.gl - 1) / share;
     const int g = u / HS;
-    merge_pieces<HD>(a, u, u - g * HS, first, lastp, min(mst[g + 1] - mst[g], a.max_members),
-                     mst[g], tid, n_cons);
+    const int members = min(mst[g + 1] - mst[g], a.max_members);
+    // wider slices only where several queries share a unit (one query per
+    // KV head always has a thread per slice)
+    if (NQ > 1 && members * hs * rep * (HD / 4) > n_cons)
+      merge_pieces<HD, (NQ > 1 ? 2 : 1)>(a, u, u - g * HS, first, lastp, members, mst[g], tid,
+                                         n_cons);
+    else
+      merge_pieces<HD, 1>(a, u, u - g * HS, first, lastp, members, mst[g], tid, n_cons);
   };
 
   // The end of this CTA's piece of unit u: the row slots' states meet in
@@ -931,8 +962,13 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     const int lastp = sp.gl > 0 ? (sp.go + sp.gl - 1) / share : 0;
     const int parts = sp.gl > 0 ? lastp - first + 1 : 0;
     const int g = u / HS;
-    combine_slots<HD, NQ>(a, merge, R, Hv, min(mst[g + 1] - mst[g], a.max_members), mst[g],
-                          u - g * HS, parts > 1 ? (int64_t)blockIdx.x + u : -1, tid, n_cons);
+    const int64_t pslot = parts > 1 ? (int64_t)blockIdx.x + u : -1;
+    const int members = min(mst[g + 1] - mst[g], a.max_members);
+    if (NQ > 1 && Hv * NQ * (HD / 4) > n_cons)
+      combine_slots<HD, NQ, (NQ > 1 ? 2 : 1)>(a, merge, R, Hv, members, mst[g], u - g * HS, pslot,
+                                              tid, n_cons);
+    else
+      combine_slots<HD, NQ, 1>(a, merge, R, Hv, members, mst[g], u - g * HS, pslot, tid, n_cons);
     if (parts <= 1) return;
     // ticket: the barrier orders the CTA's partial writes before thread 0's
     // release; the acquire side lets the last CTA read everyone's partials
@@ -1087,9 +1123,14 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
 struct Variant {
   int NQ, DPL, RS, MAXT;
 };
-static constexpr int kNumVariants = 4;
+static constexpr int kNumVariants = 5;
 static constexpr Variant kVariants[kNumVariants] = {
-    {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256}};
+    {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256},
+    // the GQA step at head_dim 128 with two query heads per KV head: five
+    // rows per thread and tile (its consumers bound the tiles; measured 1 %
+    // faster than four, which the beam-group cross launches keep)
+    {2, 16, 5, 384}};
+static constexpr int kGqaVariant = 4;
 
 static int variant_index(int nq) {
   if (nq <= 1) return 0;
@@ -1119,6 +1160,7 @@ static void* kernel_for(int HD, int vi) {
       case 1: return kernel_ptr<128, 1>();
       case 2: return kernel_ptr<128, 2>();
       case 3: return kernel_ptr<128, 3>();
+      case kGqaVariant: return kernel_ptr<128, kGqaVariant>();
     }
   }
   return nullptr;
@@ -1212,6 +1254,7 @@ static bool plan_decode(const DecodeArgs& a, int HD, int nq_needed, int sms, Dec
   }
   int vi = variant_index(nq_var);
   if (vi < 0) return false;
+  if (a.mode == kModeGqa && vi == 1 && HD == 128) vi = kGqaVariant;
   const double rows = a.mode == kModeCross ? (double)a.fixed_len : 0.5 * a.capacity;
   const double row_bytes = 2.0 * a.row_elems;
   const double share = std::max(a.n_src * rows * row_bytes / sms, tune.min_kb * 1024.0);
