@@ -276,8 +276,8 @@ int asr_prefill_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      size_t ws_bytes, int32_t* dev_err, asr_stream_t stream);
 
 /* a7 alone -- the prefill preparation of asr_prefill_attn: cache rows [0, T)
- * (roped K, V) and, in the workspace, q^ and V transposed for the tensor
- * cores.  Same arguments and definitions as asr_prefill_attn. */
+ * (roped K, V) and, in the workspace, q^ for the tensor cores.  Same
+ * arguments and definitions as asr_prefill_attn. */
 int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      const float* q_norm_w, const float* k_norm_w, float eps, float rope_base,
                      int B, int T, int q_heads, int kv_heads, int head_dim, uint16_t* cache,
@@ -308,7 +308,7 @@ int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, int head_dim,
  * heads <= ASR_MAX_KV_HEADS.  The softmax weights enter the P.V product as
  * f16 (tensor cores, tcgen05).
  * ws: asr_workspace_size(ASR_OP_MHA_PREFILL, B, heads, 1, heads, head_dim, T)
- * bytes (V transposed); need not be zeroed. */
+ * bytes (V transposed, used when lens is given); need not be zeroed. */
 int asr_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
                     int B, int T, int heads, int head_dim, float scale, uint16_t* cache,
                     int64_t seq_stride, int capacity, float* out, void* ws, size_t ws_bytes,

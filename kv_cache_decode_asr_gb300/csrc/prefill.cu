@@ -9,13 +9,14 @@
 //
 // a7 prep (CUDA cores, memory bound): per position t the query heads become
 //   q^ = f16(RoPE_t(RMSNorm(q) * w_q)) (to the workspace), the key heads
-//   k^ = f16(RoPE_t(RMSNorm(k) * w_k)) (to cache row t), V is copied to cache
-//   row t and also written transposed (keys contiguous, zero-padded to a
-//   multiple of 128) to the workspace, so both matrix products below read
-//   K-major operands.
+//   k^ = f16(RoPE_t(RMSNorm(k) * w_k)) (to cache row t), and V is copied to
+//   cache row t.
 // a8 attention (5th-generation tensor cores): one CTA per (pair of adjacent
-//   128-query tiles, sequence, query head), warp-specialised.  Q, K and V^T tiles
-//   arrive by tiled TMA with the 128-byte swizzle; S = Q K^T (128 x 64 per
+//   128-query tiles, sequence, query head), warp-specialised.  Q, K and V tiles
+//   arrive by tiled TMA with the 128-byte swizzle (V as the cache holds it,
+//   read by the PV product as an MN-major operand; with per-sequence lengths
+//   the MHA path reads a transposed, zero-padded V^T instead, K-major, so that
+//   no key past a sequence's length reaches the product); S = Q K^T (128 x 64 per
 //   key tile) and O += P V are tcgen05.mma kind::f16 (f16 operands, fp32
 //   accumulators in tensor memory).  Two softmax groups of 256 threads (one
 //   per query tile, two threads per query row, each on half of the 64 key
@@ -52,18 +53,16 @@ struct PrepArgs {
   uint16_t* cache;
   int64_t seq_stride;
   uint16_t* qhat;  // [B][T][Hq*128]
-  uint16_t* vt;    // [B*Hkv][128][Tpad]
   float rope_turns[kPrefillHD];  // theta_i / (2 pi) as float pairs (hi, lo), i < 64
 };
 
 // grid (Tpad / kPrepT, B), 256 threads.  Shared: cos/sin of the chunk's
-// positions, then the chunk's V rows for the transpose.
+// positions.
 __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant__ PrepArgs a) {
   constexpr int HD = kPrefillHD, HALF = HD / 2;
   extern __shared__ __align__(16) unsigned char psm[];
   float* cs = reinterpret_cast<float*>(psm);   // [kPrepT][HALF]
   float* sn = cs + kPrepT * HALF;              // [kPrepT][HALF]
-  uint16_t* vsm = reinterpret_cast<uint16_t*>(sn + kPrepT * HALF);  // [kPrepT][Hkv*HD]
   const int tid = threadIdx.x;
   const int b = blockIdx.y;
   const int t0 = blockIdx.x * kPrepT;
@@ -104,7 +103,7 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
     cs[idx] = c;
     sn[idx] = s;
   }
-  // V rows: to the cache, and staged for the transpose
+  // V rows: to the cache
 #pragma unroll
   for (int u = 0; u < kPrepV; ++u) {
     const int idx = tid + u * (int)blockDim.x;
@@ -113,20 +112,17 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
       if (t0 + tt < a.T)
         *reinterpret_cast<uint4*>(a.cache + (int64_t)b * a.seq_stride + (int64_t)(t0 + tt) * 2 * kw +
                                   kw + c * 8) = vval[u];
-      *reinterpret_cast<uint4*>(vsm + tt * kw + c * 8) = vval[u];
     }
   }
   // the rows past the first blockDim * kPrepV vectors (more KV heads than
   // the registers cover) go the plain way
   for (int idx = tid + kPrepV * (int)blockDim.x; idx < nv; idx += blockDim.x) {
     const int tt = idx / vec_per_row, c = idx % vec_per_row;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (t0 + tt < a.T) {
-      val = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t0 + tt) * kw + c * 8);
+      const uint4 val = *reinterpret_cast<const uint4*>(a.v + ((int64_t)b * a.T + t0 + tt) * kw + c * 8);
       *reinterpret_cast<uint4*>(a.cache + (int64_t)b * a.seq_stride + (int64_t)(t0 + tt) * 2 * kw +
                                 kw + c * 8) = val;
     }
-    *reinterpret_cast<uint4*>(vsm + tt * kw + c * 8) = val;
   }
   __syncthreads();
 
@@ -192,17 +188,6 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __grid_constant
       }
     }
   }
-
-  // V^T[b, kvh, d, t0 .. t0+16): 32 bytes per (kvh, d); zero past T
-  for (int idx = tid; idx < kw; idx += blockDim.x) {
-    alignas(16) uint16_t col[kPrepT];
-#pragma unroll
-    for (int tt = 0; tt < kPrepT; ++tt) col[tt] = vsm[tt * kw + idx];
-    const int kvh = idx / HD, d = idx % HD;
-    uint16_t* dst = a.vt + (((int64_t)b * a.Hkv + kvh) * HD + d) * a.Tpad + t0;
-    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(col);
-    *reinterpret_cast<uint4*>(dst + 8) = *reinterpret_cast<const uint4*>(col + 8);
-  }
 }
 
 // --------------------------------------------------------- MHA prep --
@@ -215,15 +200,16 @@ struct MhaPrepArgs {
   uint16_t* cache;  // or null: rows of [K(H*HD) | V(H*HD)], sequence stride seq_stride
   int64_t seq_stride;
   uint16_t* vt;  // [B*H][HD][Tpad]
+  int write_vt;  // with per-sequence lengths: V^T, zero at and past each length
 };
 
 constexpr int kMhaPrepT = 64;  // positions per CTA
 
 // grid (Tpad / 64, H, B), 256 threads: one head of 64 positions of one
-// sequence per CTA.  Its V (and K) vectors are loaded, copied to the cache
-// rows of the real positions, and V is staged in shared memory, then written
-// transposed (64 positions = 128 bytes per dim row), zero at and past the
-// sequence's length.
+// sequence per CTA.  Its V (and K) vectors are loaded and copied to the
+// cache rows of the real positions; with per-sequence lengths V is also
+// staged in shared memory, then written transposed (64 positions = 128 bytes
+// per dim row), zero at and past the sequence's length.
 __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ MhaPrepArgs a) {
   __shared__ __align__(16) uint16_t tile[kMhaPrepT][128 + 8];
   const int tid = threadIdx.x;
@@ -253,8 +239,9 @@ __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ M
     }
     // 16-byte chunk c of position tt goes to chunk c ^ (tt / 8): the
     // column reads below then hit 32 different banks
-    *reinterpret_cast<uint4*>(&tile[tt][(c ^ ((tt >> 3) & 7)) * 8]) = val;
+    if (a.write_vt) *reinterpret_cast<uint4*>(&tile[tt][(c ^ ((tt >> 3) & 7)) * 8]) = val;
   }
+  if (!a.write_vt) return;
   __syncthreads();
   for (int idx = tid; idx < HD * (kMhaPrepT / 8); idx += blockDim.x) {
     const int d = idx / (kMhaPrepT / 8), q8 = idx % (kMhaPrepT / 8);
@@ -270,6 +257,7 @@ __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ M
 
 struct PrefillAttnArgs {
   int B, T, Hq, Hkv, n_qt, n_pairs, n_items;
+  int vcol0;    // without lengths: column of V head 0 in the rows tv maps
   float sl2e;   // scale * log2(e)
   float* out;   // [B][T][Hq*HD] fp32
   const int32_t* lens;  // real positions per sequence (device, [B]), or null: T for all
@@ -281,10 +269,11 @@ constexpr int kStgBytes = 8 * 32 * 32 * 4;  // output staging: 32 rows x 32 fp32
 constexpr int kBarBytes = 1024;           // mbarriers and the TMEM address
 constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: TMA; 9: MMA
 
-// Tile sizes for head dimension HD (64 or 128).  Q and K tiles are 128 rows
-// of HD dims, stored as HD/64 blocks of 128 rows x 128 bytes (the 128-byte
-// swizzle atom); V^T tiles are HD rows (dims) of 128 keys, as two 64-key
-// blocks.  The K/V ring is deeper when the tiles are smaller.
+// Tile sizes for head dimension HD (64 or 128).  Q, K and V tiles are 128
+// rows (queries or keys) of HD dims, stored as HD/64 blocks of 128 rows x
+// 128 bytes (the 128-byte swizzle atom); V^T tiles (with per-sequence
+// lengths) are HD rows (dims) of 128 keys, as two 64-key blocks.  The K/V
+// ring is deeper when the tiles are smaller.
 template <int HD>
 struct AttnCfg {
   static constexpr int QT = 128 * HD * 2, KT = 128 * HD * 2, VT = HD * 128 * 2;
@@ -483,8 +472,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&v_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
         ++nv;
-        tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
-        tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+        if constexpr (VARLEN) {
+          // V^T rows (dims) of 128 keys, as two 64-key blocks
+          tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+          tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+        } else {
+          // V rows as they lie (keys x HD dims, HD/64 blocks of 128 keys x
+          // 128 bytes): the PV product reads them MN-major
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c)
+            tma_load_3d_warp(vd + c * kHalfBlock, &tv, a.vcol0 + x.kvh * HD + 64 * c, j * 128, x.b,
+                             &v_full[s]);
+        }
         if (j == 0) load_q(k, 1, x);  // the buffer of this item's slot A tile's predecessor
       }
       if (VARLEN && ok && x.n == 0) load_q(k, 1, x);  // an empty item still completes its slot B use
@@ -499,6 +498,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     // warp-uniform); one elected lane issues each tcgen05 operation.
     constexpr uint32_t kIdS = mma_idesc_f16_f32(128, 128);   // S = Q K^T: 128 x 128
     constexpr uint32_t kIdO = mma_idesc_f16_f32(128, HD);    // O += P V: 128 x HD
+    constexpr uint32_t kIdOmn = mma_idesc_f16_f32_bmn(128, HD);  // ... with V rows as B
     const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
     int gk = 0;          // K/V tiles consumed so far
     int gx[2] = {0, 0};  // tiles of slot A / B so far (S and P phases)
@@ -539,9 +539,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * h + k4;
-          mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
-                          sw128_kmajor_desc(aV + st * kVTile + h * (kVTile / 2) + k4 * 32),
-                          kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (VARLEN)
+            mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
+                            sw128_kmajor_desc(aV + st * kVTile + h * (kVTile / 2) + k4 * 32),
+                            kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          else  // keys 16kk .. 16kk+15 are rows 16kk.. of each 64-dim block
+            mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
+                            sw128_mnmajor_desc(aV + st * kVTile + kk * 2048, kHalfBlock), kIdOmn,
+                            (j > 0 || kk > 0) ? 1u : 0u);
         }
         if (h == 1 && j == nX[i] - 1) mma_commit_warp(&o_done[i]);  // the item's O is complete
       };
@@ -840,9 +845,8 @@ bool make_tmap_f16_5d_plain(CUtensorMap* map, const void* base, const uint64_t d
 static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv) {
-  const size_t qhat = align_up((size_t)B * T * Hq * kPrefillHD * 2, 1024);
-  const size_t vt = (size_t)B * Hkv * kPrefillHD * round_up(T, 128) * 2;
-  return qhat + vt;
+  (void)Hkv;  // V is read from the cache rows
+  return align_up((size_t)B * T * Hq * kPrefillHD * 2, 1024);
 }
 
 size_t mha_ws_bytes(int B, int T, int H, int HD) {
@@ -904,11 +908,6 @@ static int launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                  : launch_attn_tc_v<HD, CAUSAL, false>(tq, tk, tv, aa, stream);
 }
 
-static uint16_t* ws_vt(void* ws, int B, int T, int q_heads) {
-  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) +
-                                     align_up((size_t)B * T * q_heads * kPrefillHD * 2, 1024));
-}
-
 extern "C" int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const float* q_norm_w, const float* k_norm_w, float eps,
                                 float rope_base, int B, int T, int q_heads, int kv_heads,
@@ -937,15 +936,13 @@ extern "C" int asr_prefill_prep(const uint16_t* q, const uint16_t* k, const uint
   pa.cache = cache;
   pa.seq_stride = seq_stride;
   pa.qhat = static_cast<uint16_t*>(ws);
-  pa.vt = ws_vt(ws, B, T, q_heads);
   for (int i = 0; i < kPrefillHD / 2; ++i) {
     const double t = pow((double)rope_base, -2.0 * i / kPrefillHD) / (2.0 * 3.14159265358979323846);
     const float hi = (float)t;
     pa.rope_turns[2 * i] = hi;
     pa.rope_turns[2 * i + 1] = (float)(t - (double)hi);
   }
-  const size_t prep_smem =
-      2 * kPrepT * (kPrefillHD / 2) * sizeof(float) + (size_t)kPrepT * kv_heads * kPrefillHD * 2;
+  const size_t prep_smem = 2 * kPrepT * (kPrefillHD / 2) * sizeof(float);
   cudaError_t e = launch_pdl(prefill_prep_kernel, dim3(Tpad / kPrepT, B), dim3(256), prep_smem,
                              (cudaStream_t)stream, pa);
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
@@ -961,19 +958,21 @@ extern "C" int asr_prefill_attention(int B, int T, int q_heads, int kv_heads, in
   if (!out) return ASR_ERR_INVALID_ARG;
   if (!aligned16(out)) return ASR_ERR_MISALIGNED;
   if (prefill_attrs() != cudaSuccess) return ASR_ERR_CUDA;
-  const int Tpad = round_up(T, 128);
   const int64_t row = 2LL * kv_heads * kPrefillHD;
-  // tensor maps: q^ (dims: Hq*128, T, B), cache (row, capacity, B), V^T (Tpad, 128, B*Hkv)
+  // tensor maps: q^ (dims: Hq*128, T, B); the cache rows (row, capacity, B)
+  // for K; the same rows cut at T (row, T, B) for V, so that the keys of the
+  // last tile past T read as zero
   CUtensorMap tq, tk, tv;
   if (!make_tmap_f16_3d(&tq, ws, (uint64_t)q_heads * kPrefillHD, T, B,
                         (uint64_t)q_heads * kPrefillHD * 2, (uint64_t)T * q_heads * kPrefillHD * 2,
                         64, 128) ||
       !make_tmap_f16_3d(&tk, cache, (uint64_t)row, capacity, B, (uint64_t)row * 2,
                         (uint64_t)seq_stride * 2, 64, 128) ||
-      !make_tmap_f16_3d(&tv, ws_vt(ws, B, T, q_heads), Tpad, kPrefillHD, (uint64_t)B * kv_heads,
-                        (uint64_t)Tpad * 2, (uint64_t)Tpad * kPrefillHD * 2, 64, 128))
+      !make_tmap_f16_3d(&tv, cache, (uint64_t)row, T, B, (uint64_t)row * 2,
+                        (uint64_t)seq_stride * 2, 64, 128))
     return ASR_ERR_CUDA;
   PrefillAttnArgs aa = {};
+  aa.vcol0 = kv_heads * kPrefillHD;  // V head 0 follows the K heads in a row
   aa.B = B;
   aa.T = T;
   aa.Hq = q_heads;
@@ -998,34 +997,44 @@ static int mha_check(const uint16_t* q, const uint16_t* k, const uint16_t* v, in
   return ASR_OK;
 }
 
-// The MHA prep (V^T, and cache rows when cache is given) then the
-// tensor-core attention with Q and K read where they lie: K from the cache
-// rows (prefill) or from k itself (encoder).
+// The MHA prep (cache rows when cache is given; V^T with per-sequence
+// lengths) then the tensor-core attention with Q and K read where they lie:
+// K from the cache rows (prefill) or from k itself (encoder), and V from v
+// itself (no lengths: the map is cut at T, so keys past T read as zero) or
+// from V^T (lengths: keys past a sequence's length must read as zero, and
+// rows of v past it may hold anything).
 static int mha_run(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* lens,
                    int B, int T, int heads, int head_dim, float scale, bool causal, uint16_t* cache,
                    int64_t seq_stride, float* out, void* ws, int32_t* dev_err,
                    cudaStream_t stream) {
   const int Tpad = round_up(T, 128);
-  MhaPrepArgs pa = {};
-  pa.k = k;
-  pa.v = v;
-  pa.lens = lens;
-  pa.B = B;
-  pa.T = T;
-  pa.Tpad = Tpad;
-  pa.H = heads;
-  pa.HD = head_dim;
-  pa.cache = cache;
-  pa.seq_stride = seq_stride;
-  pa.vt = static_cast<uint16_t*>(ws);
-  if (launch_pdl(mha_prep_kernel, dim3(Tpad / kMhaPrepT, heads, B), dim3(256), 0, stream, pa) !=
-      cudaSuccess)
-    return ASR_ERR_CUDA;
+  const bool use_vt = lens != nullptr;
+  if (use_vt || cache) {
+    MhaPrepArgs pa = {};
+    pa.k = k;
+    pa.v = v;
+    pa.lens = lens;
+    pa.B = B;
+    pa.T = T;
+    pa.Tpad = Tpad;
+    pa.H = heads;
+    pa.HD = head_dim;
+    pa.cache = cache;
+    pa.seq_stride = seq_stride;
+    pa.vt = static_cast<uint16_t*>(ws);
+    pa.write_vt = use_vt ? 1 : 0;
+    if (launch_pdl(mha_prep_kernel, dim3(Tpad / kMhaPrepT, heads, B), dim3(256), 0, stream, pa) !=
+        cudaSuccess)
+      return ASR_ERR_CUDA;
+  }
   const uint64_t rw = (uint64_t)heads * head_dim;
   CUtensorMap tq, tk, tv;
-  bool ok = make_tmap_f16_3d(&tq, q, rw, T, B, rw * 2, (uint64_t)T * rw * 2, 64, 128) &&
-            make_tmap_f16_3d(&tv, ws, Tpad, head_dim, (uint64_t)B * heads, (uint64_t)Tpad * 2,
-                             (uint64_t)Tpad * head_dim * 2, 64, head_dim);
+  bool ok = make_tmap_f16_3d(&tq, q, rw, T, B, rw * 2, (uint64_t)T * rw * 2, 64, 128);
+  if (use_vt)
+    ok = ok && make_tmap_f16_3d(&tv, ws, Tpad, head_dim, (uint64_t)B * heads, (uint64_t)Tpad * 2,
+                                (uint64_t)Tpad * head_dim * 2, 64, head_dim);
+  else
+    ok = ok && make_tmap_f16_3d(&tv, v, rw, T, B, rw * 2, (uint64_t)T * rw * 2, 64, 128);
   if (cache)  // rows of [K | V] of 2*rw elements; K of head h at column h*hd
     ok = ok && make_tmap_f16_3d(&tk, cache, 2 * rw, T, B, 2 * rw * 2, (uint64_t)seq_stride * 2,
                                 64, 128);
@@ -1037,6 +1046,7 @@ static int mha_run(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
   aa.T = T;
   aa.Hq = heads;
   aa.Hkv = heads;
+  aa.vcol0 = 0;
   aa.sl2e = scale * kLog2eP;
   aa.out = out;
   aa.lens = lens;

@@ -58,6 +58,28 @@ __host__ __device__ constexpr uint32_t mma_idesc_f16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
+// As mma_idesc_f16_f32 with the B operand MN-major (its N elements
+// contiguous: B read as rows of K, e.g. V rows of keys for O += P V).
+__host__ __device__ constexpr uint32_t mma_idesc_f16_f32_bmn(int M, int N) {
+  return mma_idesc_f16_f32(M, N) | (1u << 16);  // B MN-major
+}
+
+// Shared-memory matrix descriptor of an MN-major operand stored with the
+// 128-byte swizzle: rows of 128 bytes along MN (64 f16), one row per K, in
+// atoms of 8 K-rows (1024 bytes); consecutive 8-row K groups 1024 bytes
+// apart (stride byte offset) and consecutive 64-element MN blocks mn_bytes
+// apart (leading byte offset).  addr: the first K-row of the slice, 1024-byte
+// aligned.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t addr, uint32_t mn_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address / 16
+  d |= (uint64_t)((mn_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64-element MN block
+  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: next 8 K-rows
+  d |= (uint64_t)1 << 46;                           // descriptor version (fixed 0b001)
+  d |= (uint64_t)2 << 61;                           // swizzle: 128 B
+  return d;
+}
+
 // Shared-memory matrix descriptor of a K-major operand stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes, atoms
 // contiguous along M/N).  addr: byte address in shared memory of the first
@@ -271,7 +293,7 @@ bool make_tmap_f16_5d_plain(CUtensorMap* map, const void* base, const uint64_t d
                             const uint64_t strides_bytes[4], const uint32_t box[5]);
 
 // Workspace bytes of the prefill: q^ [B][T][Hq*128] f16 (1024-byte aligned
-// end), then V^T [B*Hkv][128][T rounded up to 128] f16.
+// end).
 size_t prefill_ws_bytes(int B, int T, int Hq, int Hkv);
 // Workspace bytes of the MHA prefill and encoder attention (V transposed).
 size_t mha_ws_bytes(int B, int T, int H, int HD);
