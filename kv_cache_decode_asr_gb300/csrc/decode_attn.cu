@@ -1127,9 +1127,12 @@ static constexpr int kNumVariants = 5;
 static constexpr Variant kVariants[kNumVariants] = {
     {1, 16, 4, 384}, {2, 16, 4, 384}, {4, 8, 2, 384}, {8, 8, 2, 256},
     // the GQA step at head_dim 128 with two query heads per KV head: five
-    // rows per thread and tile (its consumers bound the tiles; measured 1 %
-    // faster than four, which the beam-group cross launches keep)
-    {2, 16, 5, 384}};
+    // rows per thread and tile, and at most 256 threads (7 row slots), so a
+    // thread may hold 255 registers rather than 168 (the compiler budgets a
+    // launch bound's threads in multiples of 128): its consumers bound the
+    // tiles, and this measured 2 % faster than four rows in 10 slots, which
+    // the beam-group cross launches keep
+    {2, 16, 5, 256}};
 static constexpr int kGqaVariant = 4;
 
 static int variant_index(int nq) {
