@@ -222,6 +222,9 @@ __global__ void __launch_bounds__(256) mha_prep_kernel(const __grid_constant__ M
     L = a.lens[b];
     if (L < 0 || L > a.T) L = 0;
   }
+  // the attention reads V^T up to the end of the sequence's last 128-key
+  // tile (zero past the length) and never beyond it
+  if (t0 >= (L + 127) / 128 * 128) return;
   const int HD = a.HD, vpr = HD / 8;  // 16-byte vectors per head row
   const int64_t rw = (int64_t)a.H * HD;
   for (int idx = tid; idx < kMhaPrepT * vpr; idx += blockDim.x) {
@@ -272,14 +275,23 @@ constexpr int kAttnThreads = 320;  // warps 0-3, 4-7: softmax of slots A, B; 8: 
 // Tile sizes for head dimension HD (64 or 128).  Q, K and V tiles are 128
 // rows (queries or keys) of HD dims, stored as HD/64 blocks of 128 rows x
 // 128 bytes (the 128-byte swizzle atom); V^T tiles (with per-sequence
-// lengths) are HD rows (dims) of 128 keys, as two 64-key blocks.  The K/V
-// ring is deeper when the tiles are smaller.
-template <int HD>
+// lengths) are HD rows (dims) of 128 keys, as two 64-key blocks.  With head
+// pairs (HP) a K or V^T stage holds the tiles of two heads.  The K/V ring is
+// deeper when the tiles are smaller.
+template <int HD, bool HP = false>
 struct AttnCfg {
-  static constexpr int QT = 128 * HD * 2, KT = 128 * HD * 2, VT = HD * 128 * 2;
-  static constexpr int STAGES = HD == 128 ? 2 : 4;
+  static constexpr int QT = 128 * HD * 2, KT = (HP ? 2 : 1) * 128 * HD * 2;
+  static constexpr int VT = (HP ? 2 : 1) * HD * 128 * 2;
+  static constexpr int STAGES = (HD == 128 || HP) ? 2 : 4;
   static constexpr int SMEM = kQBufs * QT + STAGES * (KT + VT) + kStgBytes + kBarBytes + 1024;
 };
+
+// Head-pair items: the short-prompt multi-head prefill (head dim 64, causal,
+// per-sequence lengths).
+template <int HD, bool CAUSAL, bool VARLEN>
+constexpr bool attn_head_pairs() {
+  return HD == 64 && CAUSAL && VARLEN;
+}
 constexpr float kRescaleLog2 = 8.0f;      // rescale O only when the row max grows by > 2^8
 
 // max of three fp32 values in one instruction (sm_100+)
@@ -295,27 +307,43 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// One work item: two adjacent query tiles of one (sequence, head), tile A =
-// 2p in slot A and tile B = 2p+1 in slot B.  Key tiles are 128 keys.
-// Causal: a query tile visits the key tiles up to its own, so slot B visits
-// one tile more than slot A; unmasked: both visit all key tiles of the
-// sequence.  A tile at or past the sequence's real length L (lens[b]) is
+// One work item: two query tiles of one sequence, tile qt_a of head h in
+// slot A and tile qt_b of head hb in slot B.  Usually the two adjacent tiles
+// 2p and 2p+1 of one head (h = hb), which share every K/V tile.  Head pairs
+// (HP) put the same tile t of heads 2p and 2p+1 in the two slots instead
+// (their K and V tiles are loaded together), so that short prompts, whose
+// one or three tiles per head leave an adjacent pair half empty, keep both
+// slots busy.  Key tiles are 128 keys.  Causal: a query tile visits the key
+// tiles up to its own; unmasked: all key tiles of the sequence.  A tile at or
+// past the sequence's real length L (lens[b]), or of a head past the last, is
 // absent (0 tiles); an item with neither tile is empty.
 struct PfItem {
-  int b, h, kvh, qt_a, qt_b, nA, nB, n, L;
+  int b, h, hb, kvh, qt_a, qt_b, nA, nB, n, L;
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, bool VARLEN, bool HP>
 __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
-  const int BH = a.B * a.Hq;
-  const int pair = a.n_pairs - 1 - it / BH;  // items run longest pairs first
-  const int bh = it % BH;
   PfItem x;
-  x.b = bh / a.Hq;
-  x.h = bh % a.Hq;
-  x.kvh = x.h / (a.Hq / a.Hkv);
-  x.qt_a = 2 * pair;
-  x.qt_b = 2 * pair + 1;
+  if constexpr (HP) {
+    // items run longest tiles first
+    const int hpairs = (a.Hq + 1) / 2, BH = a.B * hpairs;
+    const int t = a.n_qt - 1 - it / BH;
+    const int bh = it % BH;
+    x.b = bh / hpairs;
+    x.h = 2 * (bh % hpairs);
+    x.hb = x.h + 1;
+    x.kvh = x.h;  // head pairs only without grouped queries
+    x.qt_a = x.qt_b = t;
+  } else {
+    const int BH = a.B * a.Hq;
+    const int pair = a.n_pairs - 1 - it / BH;  // items run longest pairs first
+    const int bh = it % BH;
+    x.b = bh / a.Hq;
+    x.h = x.hb = bh % a.Hq;
+    x.kvh = x.h / (a.Hq / a.Hkv);
+    x.qt_a = 2 * pair;
+    x.qt_b = 2 * pair + 1;
+  }
   int L = a.T;
   if (VARLEN) {
     L = __ldg(a.lens + x.b);
@@ -323,12 +351,13 @@ __device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
   }
   x.L = L;
   const int nt = (L + 127) / 128;  // query (and key) tiles of the sequence
+  const bool b_ok = x.hb < a.Hq;
   if (CAUSAL) {
     x.nA = x.qt_a < nt ? x.qt_a + 1 : 0;
-    x.nB = x.qt_b < nt ? x.qt_b + 1 : 0;
+    x.nB = b_ok && x.qt_b < nt ? x.qt_b + 1 : 0;
   } else {
     x.nA = x.qt_a < nt ? nt : 0;
-    x.nB = x.qt_b < nt ? nt : 0;
+    x.nB = b_ok && x.qt_b < nt ? nt : 0;
   }
   x.n = x.nA > x.nB ? x.nA : x.nB;
   return x;
@@ -360,9 +389,11 @@ template <int HD, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const PrefillAttnArgs a) {
-  using C = AttnCfg<HD>;
+  constexpr bool HP = attn_head_pairs<HD, CAUSAL, VARLEN>();
+  using C = AttnCfg<HD, HP>;
   constexpr int kQTile = C::QT, kKTile = C::KT, kVTile = C::VT, kKVStages = C::STAGES;
   constexpr int kHalfBlock = 128 * 128;  // bytes of one 64-dim block of a Q or K tile
+  constexpr int kVHead = HD * 128 * 2;   // bytes of one head's V^T tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char* sQ = smem;                                  // kQBufs Q tiles
@@ -442,17 +473,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       mbar_arrive_expect_tx_warp(&q_full[u], has ? kQTile : 0);
       ++nq;
       if (has) {
-        const int qt = i == 0 ? x.qt_a : x.qt_b;
+        const int qt = i == 0 ? x.qt_a : x.qt_b, qh = i == 0 ? x.h : x.hb;
         unsigned char* qd = sQ + u * kQTile;
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d_warp(qd + c * kHalfBlock, &tq, x.h * HD + 64 * c, qt * 128, x.b, &q_full[u]);
+          tma_load_3d_warp(qd + c * kHalfBlock, &tq, qh * HD + 64 * c, qt * 128, x.b, &q_full[u]);
       }
     };
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
       if (VARLEN && x.h == 0 && x.qt_a == 0 && lane == 0) {
         const int v = __ldg(a.lens + x.b);
         if (v < 0 || v > a.T) set_dev_err(a.dev_err, ASR_DEVERR_LEN);
@@ -466,16 +497,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&k_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&k_full[s], kKTile);
         ++nk;
+        // (head pairs: heads kvh and kvh + 1, whose columns are adjacent)
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
+        for (int c = 0; c < kKTile / kHalfBlock; ++c)
           tma_load_3d_warp(kd + c * kHalfBlock, &tk, x.kvh * HD + 64 * c, j * 128, x.b, &k_full[s]);
         if (gk >= kKVStages && !(ok = mbar_wait_warp(&v_empty[s], ph))) break;
         mbar_arrive_expect_tx_warp(&v_full[s], kVTile);
         ++nv;
         if constexpr (VARLEN) {
-          // V^T rows (dims) of 128 keys, as two 64-key blocks
-          tma_load_3d_warp(vd, &tv, j * 128, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
-          tma_load_3d_warp(vd + kVTile / 2, &tv, j * 128 + 64, 0, x.b * a.Hkv + x.kvh, &v_full[s]);
+          // V^T rows (dims) of 128 keys, as two 64-key blocks (head pairs:
+          // of each head)
+#pragma unroll
+          for (int hh = 0; hh < kVTile / kVHead; ++hh) {
+            const int z = x.b * a.Hkv + x.kvh + hh;
+            tma_load_3d_warp(vd + hh * kVHead, &tv, j * 128, 0, z, &v_full[s]);
+            tma_load_3d_warp(vd + hh * kVHead + kVHead / 2, &tv, j * 128 + 64, 0, z, &v_full[s]);
+          }
         } else {
           // V rows as they lie (keys x HD dims, HD/64 blocks of 128 keys x
           // 128 bytes): the PV product reads them MN-major
@@ -508,7 +545,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
       const int nX[2] = {x.nA, x.nB};
       // Q buffer of slot i (use 2k + i) and the wait for its tile
       const int qb[2] = {(2 * k) % kQBufs, (2 * k + 1) % kQBufs};
@@ -524,7 +561,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
           const uint32_t off = (kk >> 2) * kHalfBlock + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * kHalfBlock + (kk & 3) * 32;
           mma_f16_warp(tS(i), sw128_kmajor_desc(aQ + qbuf * kQTile + off),
-                       sw128_kmajor_desc(aK + st * kKTile + koff), kIdS, kk > 0);
+                       sw128_kmajor_desc(aK + st * kKTile + (HP ? i * kHalfBlock : 0) + koff),
+                       kIdS, kk > 0);
         }
         mma_commit_warp(&s_full[i]);
         if (last) mma_commit_warp(&q_empty[qbuf]);  // its Q free once these finish
@@ -541,7 +579,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
           const int kk = 4 * h + k4;
           if constexpr (VARLEN)
             mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
-                            sw128_kmajor_desc(aV + st * kVTile + h * (kVTile / 2) + k4 * 32),
+                            sw128_kmajor_desc(aV + st * kVTile + (HP ? i * kVHead : 0) +
+                                              h * (kVHead / 2) + k4 * 32),
                             kIdO, (j > 0 || kk > 0) ? 1u : 0u);
           else  // keys 16kk .. 16kk+15 are rows 16kk.. of each 64-dim block
             mma_f16_ts_warp(tO(i), tS(i) + kk * 8,
@@ -601,8 +640,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // this item's tile j has left), while slot B's softmax finishes.
         if (ok && j == x.nA - 1 && x.nB > x.nA) {
           const int it2 = pf_item_index(k + 1, a.n_items);
-          if (it2 >= 0 && (!VARLEN || pf_item<CAUSAL, VARLEN>(a, it2).nA > 0)) {
-            const PfItem x2 = pf_item<CAUSAL, VARLEN>(a, it2);
+          if (it2 >= 0 && (!VARLEN || pf_item<CAUSAL, VARLEN, HP>(a, it2).nA > 0)) {
+            const PfItem x2 = pf_item<CAUSAL, VARLEN, HP>(a, it2);
             const int g0 = gk + x.n, n2 = 2 * (k + 1);
             ok = mbar_wait_warp(&k_full[g0 % kKVStages], (g0 / kKVStages) & 1) &&
                  mbar_wait_warp(&q_full[n2 % kQBufs], (n2 / kQBufs) & 1);
@@ -634,7 +673,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     for (int k = 0; ok; ++k) {
       const int it = pf_item_index(k, a.n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
       const int ni = i == 0 ? x.nA : x.nB;
       if (ni == 0) continue;
       const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
@@ -749,7 +788,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 *reinterpret_cast<const float4*>(stg + rr * 32 + ((cc ^ (rr & 7)) * 4));
             if (r0 + rr < x.L)
               *reinterpret_cast<float4*>(
-                  a.out + (((int64_t)x.b * a.T + r0 + rr) * a.Hq + x.h) * HD + pc * 32 + cc * 4) =
+                  a.out + (((int64_t)x.b * a.T + r0 + rr) * a.Hq + (i == 0 ? x.h : x.hb)) * HD +
+                          pc * 32 + cc * 4) =
                   val;
           }
           __syncwarp();
@@ -885,17 +925,19 @@ static cudaError_t prefill_attrs() {
 template <int HD, bool CAUSAL, bool VARLEN>
 static int launch_attn_tc_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             PrefillAttnArgs& aa, cudaStream_t stream) {
-  if (ensure_dynamic_smem((const void*)attn_tc_kernel<HD, CAUSAL, VARLEN>, AttnCfg<HD>::SMEM) !=
-      cudaSuccess)
+  constexpr bool HP = attn_head_pairs<HD, CAUSAL, VARLEN>();
+  constexpr int smem = AttnCfg<HD, HP>::SMEM;
+  if (HP && aa.Hq != aa.Hkv) return ASR_ERR_UNSUPPORTED;  // head pairs share no K/V head
+  if (ensure_dynamic_smem((const void*)attn_tc_kernel<HD, CAUSAL, VARLEN>, smem) != cudaSuccess)
     return ASR_ERR_CUDA;
   aa.n_qt = (aa.T + 127) / 128;
   aa.n_pairs = (aa.n_qt + 1) / 2;
-  aa.n_items = aa.n_pairs * aa.B * aa.Hq;
+  aa.n_items = HP ? aa.n_qt * aa.B * ((aa.Hq + 1) / 2) : aa.n_pairs * aa.B * aa.Hq;
   const int sms = device_sm_count();
   if (sms <= 0) return ASR_ERR_CUDA;
   const int ctas = aa.n_items < sms ? aa.n_items : sms;
   cudaError_t e = launch_pdl(attn_tc_kernel<HD, CAUSAL, VARLEN>, dim3(ctas), dim3(kAttnThreads),
-                             (size_t)AttnCfg<HD>::SMEM, stream, tq, tk, tv, aa);
+                             (size_t)smem, stream, tq, tk, tv, aa);
   return e == cudaSuccess ? ASR_OK : ASR_ERR_CUDA;
 }
 
