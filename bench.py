@@ -775,9 +775,6 @@ class DecoderStep(WhisperStep):
     dominant = "cross"
     dominant_kernel = "decode_attn_kernel<64,1> (asr_cross_attn_step)"
     profile_kernel = "cross"
-    # 256 launches a step: the end-to-end figure replays the captured step
-    # graph (as a caller would) instead of re-issuing every call from Python
-    e2e_via_graph = True
 
     def __init__(self, name, cfg, device, rank=0):
         import torch
@@ -927,7 +924,6 @@ class QwenDecoderStep(GqaStep):
 
     dominant = "gqa"
     dominant_kernel = "decode_attn_kernel<128,2> (asr_gqa_step)"
-    e2e_via_graph = True
 
     def __init__(self, name, cfg, device, rank=0):
         from kv_cache_decode_asr_gb300 import decoder
@@ -1306,10 +1302,7 @@ def run_ours(args):
         for _ in range(e2e_steps):
             for h, t in zip(h_ins, ins):
                 t.copy_(h, non_blocking=True)
-            if getattr(wl, "e2e_via_graph", False):
-                graph.replay()  # the static step graph a caller captures once and replays
-            else:
-                wl.step()
+            graph.replay()  # the static step graph a caller captures once and replays
             for h, t in zip(h_outs, outs):
                 h.copy_(t, non_blocking=True)
     stream.synchronize()
@@ -1388,7 +1381,9 @@ def run_ours(args):
             **extra,
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "step": "the C-ABI calls of one step, captured once as a CUDA graph and "
+                            "replayed between the copies"},
             "gpu_launches": gpu_launches,
             "cpu_baseline": cpu,
             "parity": parity,
