@@ -321,16 +321,23 @@ struct PfItem {
   int b, h, hb, kvh, qt_a, qt_b, nA, nB, n, L;
 };
 
+// Head pairs list only the tiles that exist: tab holds the sequences ordered
+// by their tile count, most first (tab[0 .. B)), then for each tile t the
+// number of sequences that have it (tab[B + t]).  Item it runs tile t of
+// the first tab[B + t] sequences, t from the last down, head pairs fastest.
 template <bool CAUSAL, bool VARLEN, bool HP>
-__device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it) {
+__device__ __forceinline__ PfItem pf_item(const PrefillAttnArgs& a, int it, const int* tab) {
   PfItem x;
   if constexpr (HP) {
     // items run longest tiles first
-    const int hpairs = (a.Hq + 1) / 2, BH = a.B * hpairs;
-    const int t = a.n_qt - 1 - it / BH;
-    const int bh = it % BH;
-    x.b = bh / hpairs;
-    x.h = 2 * (bh % hpairs);
+    const int hpairs = (a.Hq + 1) / 2;
+    int t = a.n_qt - 1;
+    while (t > 0 && it >= tab[a.B + t] * hpairs) {
+      it -= tab[a.B + t] * hpairs;
+      --t;
+    }
+    x.b = tab[it / hpairs];
+    x.h = 2 * (it % hpairs);
     x.hb = x.h + 1;
     x.kvh = x.h;  // head pairs only without grouped queries
     x.qt_a = x.qt_b = t;
@@ -414,6 +421,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
   uint64_t* drain = o_free + 2;             // every MMA this CTA issued has completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_any = reinterpret_cast<int*>(tslot + 1);  // some wait of this CTA gave up
+  // head pairs: the item table (see pf_item), after the barrier block
+  int* tab = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(bar) + kBarBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -445,10 +454,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
   }
   grid_launch_dependents();
   grid_dependency_wait();
+  if constexpr (HP) {
+    if (warp == 0) {
+      // sequences by tile count, most first (one ballot per 32 sequences
+      // and count), and per tile the number of sequences that have it; the
+      // item count last.  A bad length is reported here (its sequence has
+      // no tiles, so no item would).
+      int pos = 0;
+      for (int v = a.n_qt; v >= 1; --v) {
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+          const int b = b0 + lane;
+          int L = 0;
+          if (b < a.B) {
+            L = __ldg(a.lens + b);
+            if (L < 0 || L > a.T) {
+              if (v == a.n_qt && blockIdx.x == 0) set_dev_err(a.dev_err, ASR_DEVERR_LEN);
+              L = 0;
+            }
+          }
+          const bool hit = b < a.B && (L + 127) / 128 == v;
+          const unsigned m = __ballot_sync(0xffffffffu, hit);
+          if (hit) tab[pos + __popc(m & ((1u << lane) - 1u))] = b;
+          pos += __popc(m);
+        }
+        if (lane == 0) tab[a.B + v - 1] = pos;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int items = 0;
+        for (int t = 0; t < a.n_qt; ++t) items += tab[a.B + t];
+        tab[a.B + a.n_qt] = items * ((a.Hq + 1) / 2);
+      }
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tslot;
+  // items of this launch: head pairs count only the tiles that exist
+  const int n_items = HP ? tab[a.B + a.n_qt] : a.n_items;
   // TMEM columns: S/P of slot i at 128*i (P: 128 keys packed two per column
   // over the first 64), O_A at 256, O_B at 384.
   auto tS = [&](int i) { return tbase + 128u * i; };
@@ -481,9 +525,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       }
     };
     for (int k = 0; ok; ++k) {
-      const int it = pf_item_index(k, a.n_items);
+      const int it = pf_item_index(k, n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it, tab);
       if (VARLEN && x.h == 0 && x.qt_a == 0 && lane == 0) {
         const int v = __ldg(a.lens + x.b);
         if (v < 0 || v > a.T) set_dev_err(a.dev_err, ASR_DEVERR_LEN);
@@ -543,9 +587,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     bool ok = true;
     bool a_early = false;  // slot A's first S of this item was issued during the previous one
     for (int k = 0; ok; ++k) {
-      const int it = pf_item_index(k, a.n_items);
+      const int it = pf_item_index(k, n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it, tab);
       const int nX[2] = {x.nA, x.nB};
       // Q buffer of slot i (use 2k + i) and the wait for its tile
       const int qb[2] = {(2 * k) % kQBufs, (2 * k + 1) % kQBufs};
@@ -639,9 +683,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // item now (its Q is already in; its first K tile lands in the stage
         // this item's tile j has left), while slot B's softmax finishes.
         if (ok && j == x.nA - 1 && x.nB > x.nA) {
-          const int it2 = pf_item_index(k + 1, a.n_items);
-          if (it2 >= 0 && (!VARLEN || pf_item<CAUSAL, VARLEN, HP>(a, it2).nA > 0)) {
-            const PfItem x2 = pf_item<CAUSAL, VARLEN, HP>(a, it2);
+          const int it2 = pf_item_index(k + 1, n_items);
+          if (it2 >= 0 && (!VARLEN || pf_item<CAUSAL, VARLEN, HP>(a, it2, tab).nA > 0)) {
+            const PfItem x2 = pf_item<CAUSAL, VARLEN, HP>(a, it2, tab);
             const int g0 = gk + x.n, n2 = 2 * (k + 1);
             ok = mbar_wait_warp(&k_full[g0 % kKVStages], (g0 / kKVStages) & 1) &&
                  mbar_wait_warp(&q_full[n2 % kQBufs], (n2 / kQBufs) & 1);
@@ -671,9 +715,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     bool ok = true;
     float v[128];
     for (int k = 0; ok; ++k) {
-      const int it = pf_item_index(k, a.n_items);
+      const int it = pf_item_index(k, n_items);
       if (it < 0) break;
-      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it);
+      const PfItem x = pf_item<CAUSAL, VARLEN, HP>(a, it, tab);
       const int ni = i == 0 ? x.nA : x.nB;
       if (ni == 0) continue;
       const int q0 = (i == 0 ? x.qt_a : x.qt_b) * 128;
@@ -926,11 +970,14 @@ template <int HD, bool CAUSAL, bool VARLEN>
 static int launch_attn_tc_v(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             PrefillAttnArgs& aa, cudaStream_t stream) {
   constexpr bool HP = attn_head_pairs<HD, CAUSAL, VARLEN>();
-  constexpr int smem = AttnCfg<HD, HP>::SMEM;
   if (HP && aa.Hq != aa.Hkv) return ASR_ERR_UNSUPPORTED;  // head pairs share no K/V head
+  aa.n_qt = (aa.T + 127) / 128;
+  // head pairs: the item table (sequences, tile counts, item count)
+  const int smem =
+      AttnCfg<HD, HP>::SMEM + (HP ? (int)align_up((size_t)(aa.B + aa.n_qt + 1) * 4, 16) : 0);
+  if (smem > 227 * 1024) return ASR_ERR_UNSUPPORTED;
   if (ensure_dynamic_smem((const void*)attn_tc_kernel<HD, CAUSAL, VARLEN>, smem) != cudaSuccess)
     return ASR_ERR_CUDA;
-  aa.n_qt = (aa.T + 127) / 128;
   aa.n_pairs = (aa.n_qt + 1) / 2;
   aa.n_items = HP ? aa.n_qt * aa.B * ((aa.Hq + 1) / 2) : aa.n_pairs * aa.B * aa.Hq;
   const int sms = device_sm_count();

@@ -120,6 +120,22 @@ def test_bad_length_is_flagged_and_skipped():
     assert_attn_close(got[1, :64], ref[1, :64], "encoder beside a bad length")
 
 
+def test_prefill_bad_length_is_flagged_and_skipped():
+    """The prompt prefill with a length past T: flagged, that sequence
+    skipped (no cache rows, output untouched), the other one correct."""
+    B, T, H, hd, cap = 2, 200, 4, 64, 256
+    q, k, v = _inputs(B, T, H, hd, 2993)
+    cache0 = syn.host_normal_f16bits((B, cap, 2 * H * hd), 2994)
+    got, cache_gpu, err = _run_prefill(q, k, v, H, hd, np.array([T + 1, 150], np.int32), cache0)
+    assert err & ops.DEVERR_LEN
+    assert np.all(np.isnan(got[0]))
+    assert np.array_equal(cache_gpu[0], cache0[0])
+    ref_cache = cache0.copy()
+    ref, _ = oracle.mha_attn(q, k, v, H, hd, hd ** -0.5, True, lens=[0, 150], cache=ref_cache)
+    assert_attn_close(got[1, :150], ref[1, :150], "prefill beside a bad length")
+    assert np.array_equal(cache_gpu[1], ref_cache[1])
+
+
 def test_repeat_is_identical():
     B, T, H, hd = 2, 300, 4, 64
     q, k, v = _inputs(B, T, H, hd, 2995)
