@@ -75,6 +75,8 @@ CASES = [
     (2, 384, 4, 128, [384, 250]),          # head_dim 128, three tiles
     (1, 1, 2, 64, None),                   # a single position
     (2, 260, 20, 64, [0, 260]),            # Whisper-large heads; an empty sequence
+    (3, 128, 4, 64, [0, 0, 0]),            # every sequence empty: no work at all
+    (37, 300, 5, 64, [(7 * i * i + 3 * i) % 301 for i in range(37)]),  # > 32 sequences
 ]
 
 
