@@ -1242,7 +1242,10 @@ def config_dict(args, wl, world, kv_bytes):
     return {"workload": args.workload, **{k: v for k, v in wl.cfg.items()},
             "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB touched per step "
                   f"vs {L2_BYTES / 1e6:.0f} MB L2)",
-            "parallelism": f"replicas x{world} (batch per GPU fixed)"}
+            "parallelism": f"replicas x{world} (batch per GPU fixed)",
+            "decode_start": ("after the previous launch" if args.no_history_ready else
+                             "history ready (asr_set_history_ready: the launches before each "
+                             "attention call write none of its lengths or cached rows)")}
 
 
 def run_ours(args):
@@ -1254,6 +1257,12 @@ def run_ours(args):
     oracle.build()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    # The decode-attention calls of every workload here are steady decode
+    # loops: the launches before each one (another layer's attention or a
+    # projection) write none of its lengths, groups or cached rows, so they
+    # may read those before the grid dependency wait (asr_set_history_ready).
+    from kv_cache_decode_asr_gb300 import ops as kops
+    kops.asr_set_history_ready(not args.no_history_ready)
     wl = make_workload(args.workload, device, rank, args.layers)
     if args.separate_append:
         wl.separate_append = True
@@ -1459,6 +1468,9 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration measurements of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-history-ready", action="store_true",
+                    help="decode-attention calls wait for the previous launch before reading "
+                         "their lengths and history (the library's default order)")
     ap.add_argument("--separate-reorder", action="store_true",
                     help="beam workload: one asr_kv_rearrange launch before the layers instead "
                          "of the reorder fused into each layer's append + self launch")

@@ -448,6 +448,29 @@ int asr_version(void);
  * wait_ns out of range (the launch is then not armed). */
 int asr_debug_stall_next_decode(uint64_t wait_ns);
 
+/* A promise that lets the decode-attention launches of the calling host
+ * thread start earlier (no counterpart in the pages).  Every launch of this
+ * library lets the next one on its stream start while it drains, and the
+ * next one waits (griddepcontrol.wait) for it to finish before it reads
+ * anything.  With ready = 1 the decode-attention entry points
+ * (asr_self_attn_step, asr_self_attn_append_step, asr_cross_attn_step,
+ * asr_gqa_step, asr_self_attn_step_noalloc) read their lengths (and cross
+ * groups), norm weights and cached K/V history before that wait: their
+ * producer starts its copies at once and only the queries, the new token,
+ * the outputs and the workspace wait.  The caller promises that none of the
+ * lengths, groups, norm weights or cached rows a call reads was written by
+ * the last few launches before it on the same stream (the one just before
+ * it, and one that launch may have let start before its own predecessor
+ * finished): true in a steady decode loop (the preceding launches are
+ * projections and other layers' attention), false right after a prefill,
+ * an append or a beam reorder of the same cache, or an upload of the
+ * lengths by a kernel.  A broken promise gives wrong results.  The beam-reorder entry point
+ * (asr_self_attn_reorder_append_step) never starts early (it writes a
+ * destination cache).  The setting is kept per host thread and is read when
+ * a call is made (a captured graph keeps the mode of its capture).  ready:
+ * 0 (the default) or 1; ASR_ERR_INVALID_ARG otherwise. */
+int asr_set_history_ready(int ready);
+
 #ifdef __cplusplus
 }
 #endif

@@ -600,7 +600,11 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
   // inside the K/V buffer, and a prefetch writes nothing and is never seen by
   // a load, so the hint cannot change a result.  Its offsets go to the stage
   // ring, which nothing touches before this warp's first copy.
-  if (warp == cons_warps && !a.stall && a.pf_bytes > 0 &&
+  //
+  // With the caller's promise that the lengths and the history are ready
+  // (a.early) the hints are not needed: the producer starts its copies at
+  // once, and the consumers wait only before the queries (below).
+  if (!a.early && warp == cons_warps && !a.stall && a.pf_bytes > 0 &&
       2 * (S + 1) * 4 <= a.stages * a.stage_elems * 2) {
     int* poff = reinterpret_cast<int*>(stage);
     int* psq = poff + S + 1;  // beam reorder: the sequence each source reads
@@ -662,8 +666,8 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
     __syncwarp();
   }
-  grid_dependency_wait();
   __syncthreads();  // barrier initialisation and ctl are visible to every warp
+  if (!a.early) grid_dependency_wait();
 
   if (warp == cons_warps) {
     // ======================= producer warp: one lane issues the copies.  It
@@ -782,6 +786,9 @@ __global__ void __launch_bounds__(MAXT, 1) decode_attn_kernel(const __grid_const
     }
   }
   named_bar(1, n_cons);
+  // the queries, the new token, the outputs and the workspace belong to
+  // earlier grids: with the caller's promise, the wait comes only now
+  if (a.early) grid_dependency_wait();
   const bool unsorted = a.mode == kModeCross && ctl[2] != 0;
 
   // ---- CTA 0 zeroes the outputs of sequences that are skipped
@@ -1329,6 +1336,10 @@ static int occupancy_cached(void* fn, int threads, int smem) {
 // this host thread issues no copies and bounds its waits by this many ns.
 static thread_local uint64_t t_stall_ns = 0;
 
+// asr_set_history_ready: the decode launches of this host thread read the
+// lengths and the cached history before the grid dependency wait.
+static thread_local int t_history_ready = 0;
+
 static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
   const int sms = device_sm_count();
@@ -1368,6 +1379,8 @@ static int launch_decode(DecodeArgs& a, int HD, int nq_needed, void* ws, size_t 
     a.stall = 1;
     t_stall_ns = 0;
   }
+  // never for a beam reorder (it writes a destination cache) or the stall test
+  a.early = t_history_ready && a.idx == nullptr && !a.stall ? 1 : 0;
   if (p.HS > 1) {
     // rows of every source as {HD, Hkv, 2 (K, V), rows, sources}: a box of
     // {HD, hs, 2, n, 1} lands as n row chunks [K of the hs heads | V of them]
@@ -1405,6 +1418,12 @@ static bool rows_fit_int(int64_t n_src, int64_t rows, int64_t kv_heads) {
 }  // namespace asrkv
 
 using namespace asrkv;
+
+extern "C" int asr_set_history_ready(int ready) {
+  if (ready != 0 && ready != 1) return ASR_ERR_INVALID_ARG;
+  t_history_ready = ready;
+  return ASR_OK;
+}
 
 extern "C" int asr_debug_stall_next_decode(uint64_t wait_ns) {
   if (wait_ns == 0 || wait_ns > kWaitLimitNs) return ASR_ERR_INVALID_ARG;

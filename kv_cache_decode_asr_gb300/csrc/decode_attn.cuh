@@ -62,6 +62,7 @@ struct DecodeArgs {
   int pf_bytes;     // K/V bytes of its share a CTA asks L2 to prefetch before the grid dependency wait
   uint64_t wait_ns; // bound of every mbarrier wait (ns of %globaltimer)
   int stall;        // test support: the producer issues no copies, so every wait runs out
+  int early;        // the caller promised the lengths and history are ready (asr_set_history_ready)
   // new-token append (GQA step, fused self step): the call writes row p and
   // folds that key in; p = n_past (GQA) or lens - 1 (self)
   int append;

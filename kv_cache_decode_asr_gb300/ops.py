@@ -62,6 +62,7 @@ SIGNATURES = {
     "asr_status_string": (ctypes.c_char_p, [_int]),
     "asr_version": (_int, []),
     "asr_debug_stall_next_decode": (_int, [ctypes.c_uint64]),
+    "asr_set_history_ready": (_int, [_int]),
 }
 
 _LIB = None
@@ -118,6 +119,13 @@ def asr_status_string(status):
 
 def asr_version():
     return load().asr_version()
+
+
+def asr_set_history_ready(ready):
+    """Promise (ready=True) that the launch just before each decode-attention
+    call of this thread writes none of its lengths, groups, norm weights or
+    cached rows, so the call reads them before the grid dependency wait."""
+    _check("asr_set_history_ready", load().asr_set_history_ready(1 if ready else 0))
 
 
 def asr_debug_stall_next_decode(wait_ns):

@@ -389,3 +389,45 @@ def test_gqa_bad_positions():
     assert np.all(got[:2] == 0)
     assert_attn_close(got, ref, "gqa with bad positions")
     assert np.array_equal(cache_gpu[:2], cache0[:2])
+
+
+def test_history_ready_gives_the_same_bits():
+    """asr_set_history_ready(1): self, self + append, cross and GQA calls read
+    their lengths, groups and history before the grid dependency wait.  Here
+    the launch before each call is a fill of its output or workspace, which
+    the promise allows, and every result must equal the default order's bit
+    for bit (the beam-reorder entry never starts early; its own tests run
+    with the default)."""
+    B, H, hd, cap = 24, 6, 64, 300
+    qkv, cache, lens = _self_case(B, H, hd, cap, None, 4100)
+    q, cross = _cross_case(20, 4, H, hd, 1500, 4110)
+    group = np.array([i // 5 for i in range(20)], np.int32)
+    gq = _gqa_case(16, 16, 8, 128, 512, 4120)
+    n_past = syn.lens_uniform(16, 1, 500, 4130)
+    d = H * hd
+
+    def self_append():
+        qd = dev(qkv)
+        c = dev(cache)
+        out = torch.full((B, d), float("nan"), device="cuda")
+        ws = ops.workspace(ops.OP_SELF_ATTN, B, B, 1, H, hd)
+        ops.asr_self_attn_append_step(qd[:, :d], qd[:, d:2 * d], qd[:, 2 * d:], c, dev(lens), H,
+                                      hd, cap, hd ** -0.5, out, ws)
+        torch.cuda.synchronize()
+        return host(out), host_u16(c)
+
+    def run_all():
+        return (_run_self(qkv, cache, lens, H, hd, cap), self_append(),
+                _run_cross(q, cross, group, 4, 5, H, hd, 1500),
+                _run_gqa(*gq[:5], n_past, gq[5], 512, 16, 8, 128))
+
+    base = run_all()
+    try:
+        ops.asr_set_history_ready(True)
+        early = run_all()
+    finally:
+        ops.asr_set_history_ready(False)
+    flat = lambda r: [np.asarray(x) for x in (r[0], *r[1], r[2], *r[3])]
+    for a, b in zip(flat(base), flat(early)):
+        assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    assert ops.load().asr_set_history_ready(2) != 0  # 0 or 1 only
